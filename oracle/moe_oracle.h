@@ -1,0 +1,108 @@
+/*
+ * moe_oracle.h -- plain fp64 CPU oracle of the MoE-layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code with the GPU path.
+ *
+ * Every function is the plain definition of its step, written as sequential
+ * loops in double precision (compiled with -ffp-contract=off, no SIMD
+ * intrinsics).  Inputs are read-only host arrays owned by the caller; outputs
+ * are caller-allocated host arrays.  Functions return 0 on success and a
+ * negative code on bad arguments (-1) or a missing expert record (-2).
+ *
+ * Sources (page title, section):
+ *   LazyLoRA README, "The engine": top-16 routing over 896 routed experts,
+ *     MXFP4 experts, fp32 (here: fp64) expert accumulation;
+ *   LazyLoRA README, "File map": the router (top-16 gating with a
+ *     score-correction bias) and SiTU 4*tanh(g/4)*sigmoid(g) x 25*tanh(u/25);
+ *   WASTE README, "3 bits per expert weight": RVQ with 3 stages of 256-entry
+ *     codebooks over 8-dim vectors;
+ *   "Running a 2.78-Trillion-Parameter Model Across Two Desks", Act II: the
+ *     MoE layer returns the gate-weighted sum of the selected experts' outputs.
+ *   MXFP4 element and scale encodings (E2M1, E8M0, blocks of 32) follow the OCP
+ *   Microscaling Formats (MX) v1.0 specification; the pages only name MXFP4.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_ACT_SWIGLU = 0, OR_ACT_SITU = 1 };
+
+/* ---- element decodes ---------------------------------------------------- */
+double or_e2m1(int code);            /* E2M1 code 0..15 -> value (code 8 is -0.0) */
+double or_e8m0(int byte);            /* 2^(byte-127); byte 255 -> NaN            */
+double or_bf16(uint16_t bits);       /* bfloat16 bit pattern -> value           */
+double or_f16(uint16_t bits);        /* IEEE binary16 bit pattern -> value      */
+
+/* ---- weight decodes ----------------------------------------------------- */
+/* MXFP4 matrix [rows][K]: codes [rows][K/2] (low nibble = even column),
+ * scales [rows][K/32] (one E8M0 per 32 consecutive columns).  Row r -> w[K]. */
+void or_mxfp4_row(const uint8_t* codes, const uint8_t* scales, int K, int r, double* w);
+/* RVQ3 matrix [rows][K]: codes [3][rows][K/8] stage-planar, codebooks cb fp16
+ * [3][256][8]; w[r][8v+i] = sum over stages s of cb[s][code_s[r][v]][i]. */
+void or_rvq3_row(const uint8_t* codes, const uint16_t* cb, int rows, int K, int r, double* w);
+
+/* Byte offsets of the three matrices inside one expert record. */
+size_t or_mxfp4_record_bytes(int d, int ff);
+size_t or_rvq3_record_bytes(int d, int ff);
+
+/* ---- router --------------------------------------------------------------
+ * l[t][e] = sum_i W[e][i] x[t][i] (ascending i) + bias[e];
+ * top-k by (l descending, e ascending); g_j = exp(l_j - l_max) / sum_sel exp(.)
+ * logits (nullable) [T][E]; topk_idx [T][k]; gates [T][k]. */
+int or_router(const void* x, int x_dtype, const void* w, int w_dtype, const float* bias, int T, int d, int E,
+              int k, double* logits, int32_t* topk_idx, double* gates);
+/* The top-k/gate step alone, on given fp64 logits [T][E]. */
+int or_topk_gates(const double* logits, int T, int E, int k, int32_t* topk_idx, double* gates);
+
+/* ---- bucketing -----------------------------------------------------------
+ * Stable counting sort of pair ids p = t*k + j by expert topk_idx[p]:
+ * counts [E], offsets [E+1] (exclusive scan), pair_ids [T*k]. */
+int or_bucket(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+              int32_t* pair_ids);
+
+/* ---- one expert FFN for one token ---------------------------------------
+ * g = Wg x, u = Wu x, h = act(g, u), y = Wd h; x [d] and y [d] in fp64. */
+int or_expert_mxfp4(const double* x, const uint8_t* rec, int d, int ff, int act, double* y);
+int or_expert_rvq3(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
+                   const uint16_t* cb_down, int d, int ff, int act, double* y);
+double or_act(double g, double u, int act);
+
+/* ---- combine ------------------------------------------------------------
+ * out[t] = x[t] + sum_{j ascending, g[t][j] != 0} g[t][j] * y_pairs[t*k + j];
+ * x_resid nullable (then out is the MoE delta alone). */
+int or_combine(const double* x_resid, const double* y_pairs, const double* gates, int T, int k, int d,
+               double* out);
+
+/* ---- whole layer ---------------------------------------------------------
+ * quant 0 = MXFP4, 1 = RVQ3.  records: array [E] of host pointers (NULL = the
+ * expert's record is absent; routing a pair to it is an error, -2).
+ * Outputs (each nullable): topk_idx [T][k], gates [T][k], y_delta [T][d] (the
+ * MoE delta, combine with no residual) and out [T][d] (= x + delta).
+ * Only tokens with token_mask[t] != 0 get expert outputs (token_mask nullable =
+ * all tokens); rows of y_delta/out for other tokens are left untouched.
+ * nthreads > 1 runs the independent (token, slot) pairs on that many OpenMP
+ * threads; the arithmetic of each pair is unchanged. */
+int or_layer_forward(const void* x, int x_dtype, const void* router_w, int w_dtype, const float* bias, int T,
+                     int d, int ff, int E, int k, int act, int quant, const uint8_t* const* records,
+                     const uint16_t* cb_gate, const uint16_t* cb_up, const uint16_t* cb_down,
+                     const uint8_t* token_mask, int nthreads, int32_t* topk_idx, double* gates, double* y_delta,
+                     double* out);
+
+/* Expert-parallel partial: like or_layer_forward's delta but summing only the
+ * pairs whose expert lies in [e_begin, e_end), given the routing. */
+int or_partial_delta(const void* x, int x_dtype, const int32_t* topk_idx, const double* gates, int T, int d,
+                     int ff, int k, int act, int quant, const uint8_t* const* records, const uint16_t* cb_gate,
+                     const uint16_t* cb_up, const uint16_t* cb_down, int e_begin, int e_end, double* delta);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ORACLE_H */

@@ -1,0 +1,361 @@
+"""Pins the CPU oracle to facts that do not come from the oracle itself.
+
+Each test names the mistake it is meant to catch.  CPU only.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from tests import npref
+
+GOLDEN = npref.GOLDEN
+
+
+# ----------------------------------------------------------------------------- element decodes
+
+def test_e2m1_all_codes_match_ocp_table():
+    # catches a wrong exponent bias, a swapped sign bit or a wrong subnormal rule
+    for c in range(16):
+        v = oracle.e2m1(c)
+        assert v == npref.E2M1_TABLE[c]
+        assert math.copysign(1.0, v) == math.copysign(1.0, npref.E2M1_TABLE[c])  # -0.0 for code 8
+
+
+def test_e8m0_all_bytes_and_products():
+    # all 16 codes x 256 scale bytes against 2^(b-127) from math.ldexp
+    for b in range(256):
+        s = oracle.e8m0(b)
+        if b == 255:
+            assert math.isnan(s)
+            continue
+        assert s == math.ldexp(1.0, b - 127)
+        for c in range(16):
+            codes = np.full(1, c | (c << 4), dtype=np.uint8)
+            w = oracle.mxfp4_row(np.tile(codes, 16), np.full(1, b, dtype=np.uint8), 32, 0)
+            assert np.all(w == npref.E2M1_TABLE[c] * math.ldexp(1.0, b - 127))
+
+
+def test_bf16_f16_decodes_match_numpy():
+    bits = np.arange(0, 65536, 7, dtype=np.uint16)
+    for b in bits:
+        f = npref.f16_to_f64(np.array([b]))[0]
+        o = oracle.f16(int(b))
+        assert (np.isnan(f) and np.isnan(o)) or f == o
+    for b in bits[::5]:
+        f = npref.bf16_to_f64(np.array([b]))[0]
+        o = oracle.bf16(int(b))
+        assert (np.isnan(f) and np.isnan(o)) or f == o
+
+
+def test_mxfp4_row_nibble_order_and_block_scales():
+    # catches low/high nibble swaps and a scale block applied to the wrong columns
+    rng = np.random.default_rng(7)
+    rows, K = 5, 128
+    codes = rng.integers(0, 256, size=rows * K // 2, dtype=np.uint8)
+    scales = rng.integers(100, 140, size=rows * K // 32, dtype=np.uint8)
+    ref = npref.unpack_mxfp4(codes, scales, rows, K)
+    got = oracle.mxfp4_matrix(codes, scales, rows, K)
+    np.testing.assert_array_equal(got, ref)
+    # column 0 is the low nibble of byte 0
+    codes2 = np.zeros(K // 2, dtype=np.uint8)
+    codes2[0] = 0x72  # col0 = code 2 (1.0), col1 = code 7 (6.0)
+    w = oracle.mxfp4_row(codes2, np.full(K // 32, 127, dtype=np.uint8), K, 0)
+    assert w[0] == 1.0 and w[1] == 6.0 and np.all(w[2:] == 0.0)
+
+
+def test_rvq3_is_sum_of_three_codewords():
+    rng = np.random.default_rng(3)
+    rows, K = 6, 64
+    codes = rng.integers(0, 256, size=3 * rows * K // 8, dtype=np.uint8)
+    cb = si.normal(11, 16, 0.02, 3 * 256 * 8, "f16").reshape(3, 256, 8)
+    got = oracle.rvq3_matrix(codes, cb, rows, K)
+    np.testing.assert_array_equal(got, npref.unpack_rvq3(codes, cb, rows, K))
+    # stages 2 and 3 zeroed: a plain vector-quantisation table lookup
+    cb0 = cb.copy()
+    cb0[1:] = 0
+    got0 = oracle.rvq3_matrix(codes, cb0, rows, K)
+    c0 = codes.reshape(3, rows, K // 8)[0]
+    for r in range(rows):
+        for v in range(K // 8):
+            for i in range(8):
+                assert got0[r, 8 * v + i] == npref.f16_to_f64(np.array([cb[0, c0[r, v], i]]))[0]
+
+
+def test_record_sizes_match_page_figures():
+    with open(os.path.join(GOLDEN, "page_figures.json")) as f:
+        pf = json.load(f)
+    d, ff = pf["latent_shape"]["d"], pf["latent_shape"]["ff"]
+    b = oracle.mxfp4_record_bytes(d, ff)
+    assert b == 17_547_264
+    assert round(b / 1e6, 2) == pf["mxfp4_expert_mb"]["value"]
+    assert round(b / 1e6, 1) == pf["mxfp4_expert_mb_lazylora"]["value"]
+    assert round(b * pf["mxfp4_layer_gb"]["experts"] / 1e9, 1) == pf["mxfp4_layer_gb"]["value"]
+    assert pf["routed_experts_total"]["layers"] * pf["routed_experts_total"]["experts_per_layer"] == \
+        pf["routed_experts_total"]["value"]
+    rv = oracle.rvq3_record_bytes(d, ff)
+    assert rv * 8 / (3 * d * ff) == pf["rvq3_bits_per_weight"]["value"]
+    assert rv == 12_386_304
+    # the generator's record layout agrees with the oracle's
+    assert si.mxfp4_record_size(d, ff) == b and si.rvq3_record_size(d, ff) == rv
+
+
+# ----------------------------------------------------------------------------- router
+
+def _tiny_xw(T=12, d=64, E=24, seed=5, dt="bf16"):
+    x = si.normal(seed, 1, 1.0, T * d, dt).reshape(T, d)
+    W = si.normal(seed, 2, 1 / math.sqrt(d), E * d, dt).reshape(E, d)
+    return x, W
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_router_logits_match_numpy_matmul(dt):
+    # catches a transposed W or a dropped bias
+    x, W = _tiny_xw(dt=dt)
+    bias = si.normal(9, 3, 0.5, W.shape[0], "f32")
+    logits, idx, g = oracle.router(x, W, bias, 5)
+    ref = npref.to_f64(x) @ npref.to_f64(W).T + bias.astype(np.float64)[None]
+    scale = np.abs(npref.to_f64(x)) @ np.abs(npref.to_f64(W)).T
+    assert np.all(np.abs(logits - ref) <= 1e-13 * (scale + 1))
+
+
+def test_router_one_hot_rows_select_coordinates():
+    # W = identity rows: logit e is exactly x[e]
+    T, d = 4, 32
+    x = si.normal(2, 1, 1.0, T * d, "f32").reshape(T, d)
+    W = np.eye(d, dtype=np.float32)
+    logits, idx, g = oracle.router(x, W, None, 3)
+    np.testing.assert_array_equal(logits, x.astype(np.float64))
+    np.testing.assert_array_equal(idx, npref.topk_sorted(x.astype(np.float64), 3))
+
+
+def test_topk_matches_full_sort_every_token():
+    x, W = _tiny_xw(T=64, E=40)
+    logits, idx, g = oracle.router(x, W, None, 7)
+    np.testing.assert_array_equal(idx, npref.topk_sorted(logits, 7))
+
+
+def test_topk_exact_ties_go_to_lower_index():
+    logits = np.array([[1.0, 3.0, 3.0, 2.0, 3.0, 0.0],
+                       [5.0, 5.0, 5.0, 5.0, 5.0, 5.0],
+                       [0.0, -1.0, 0.0, 7.0, 7.0, -1.0]])
+    idx, g = oracle.topk_gates(logits, 4)
+    np.testing.assert_array_equal(idx, [[1, 2, 4, 3], [0, 1, 2, 3], [3, 4, 0, 2]])
+    np.testing.assert_array_equal(idx, npref.topk_sorted(logits, 4))
+    assert np.all(g[1] == 0.25)
+
+
+def test_gates_sum_to_one_and_equal_renormalised_full_softmax():
+    x, W = _tiny_xw(T=32, E=40)
+    bias = si.zipf_bias(40)
+    logits, idx, g = oracle.router(x, W, bias, 6)
+    assert np.all(np.abs(g.sum(axis=1) - 1.0) <= 4e-16 * 6)
+    ref = npref.gates_full_softmax(logits, idx)
+    assert np.all(np.abs(g - ref) <= 1e-14 * ref)
+    assert np.all(np.diff(g, axis=1) <= 0)  # ordered with the logits
+
+
+# ----------------------------------------------------------------------------- bucketing
+
+def test_bucket_matches_brute_force_scan():
+    rng = np.random.default_rng(1)
+    T, k, E = 37, 5, 23
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, pair_ids = oracle.bucket(idx, E)
+    flat = idx.reshape(-1)
+    exp_ids = []
+    for e in range(E):  # O(E * T * k) scan, ascending pair id within each expert
+        ids = [p for p in range(T * k) if flat[p] == e]
+        assert counts[e] == len(ids)
+        exp_ids += ids
+    assert counts.sum() == T * k and offsets[0] == 0 and offsets[-1] == T * k
+    np.testing.assert_array_equal(pair_ids, exp_ids)
+    assert sorted(pair_ids.tolist()) == list(range(T * k))
+    assert npref.fnv1a64(pair_ids) == npref.fnv1a64(np.array(exp_ids, dtype=np.int32))
+
+
+def test_bucket_rejects_out_of_range_expert():
+    idx = np.array([[0, 5]], dtype=np.int32)
+    with pytest.raises(RuntimeError):
+        oracle.bucket(idx, 4)
+
+
+# ----------------------------------------------------------------------------- expert FFN
+
+def _const_record(d, ff, gate_code, gate_scale, rng):
+    """Gate and up matrices constant (one code, one scale byte); down random."""
+    cbytes, sbytes = ff * d // 2, ff * d // 32
+    rec = []
+    for _ in range(2):
+        rec.append(np.full(cbytes, gate_code | (gate_code << 4), dtype=np.uint8))
+        rec.append(np.full(sbytes, gate_scale, dtype=np.uint8))
+    rec.append(rng.integers(0, 256, size=d * ff // 2, dtype=np.uint8))
+    rec.append(rng.integers(118, 126, size=d * ff // 32, dtype=np.uint8))
+    return np.concatenate(rec)
+
+
+def test_expert_closed_form_constant_gate_up():
+    # Wg = Wu = c * ones: g = u = c * sum(x); h = silu(g) * u for every row;
+    # y_i = rowsum(Wd)_i * h.  Catches a transposed down matrix or act mix-up.
+    d, ff = 64, 96
+    rng = np.random.default_rng(0)
+    rec = _const_record(d, ff, 2, 124, rng)  # code 2 = 1.0, c = 2^-3
+    x = npref.to_f64(si.normal(4, 1, 1.0, d, "bf16"))
+    c = 2.0 ** -3
+    s = c * x.sum()
+    h = s / (1.0 + math.exp(-s)) * s
+    wd = npref.mxfp4_record_mats(rec, d, ff)[2]
+    y = oracle.expert_mxfp4(x, rec, d, ff)
+    ref = wd.sum(axis=1) * h
+    assert np.all(np.abs(y - ref) <= 1e-12 * (np.abs(wd).sum(axis=1) * abs(h) + 1e-300))
+
+
+def test_expert_all_zero_codes_give_zero():
+    d, ff = 64, 64
+    rec = np.zeros(oracle.mxfp4_record_bytes(d, ff), dtype=np.uint8)
+    rec[:] = 0
+    x = npref.to_f64(si.normal(1, 1, 1.0, d, "bf16"))
+    assert np.all(oracle.expert_mxfp4(x, rec, d, ff) == 0.0)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "situ"])
+def test_expert_mxfp4_matches_numpy(act):
+    d, ff = 96, 64
+    rec = si.mxfp4_record(3, 2, d, ff, 119, 125)
+    x = npref.to_f64(si.normal(3, 1, 1.0, d, "bf16"))
+    y = oracle.expert_mxfp4(x, rec, d, ff, act)
+    ref = npref.expert(x, npref.mxfp4_record_mats(rec, d, ff), act)
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_expert_rvq3_matches_numpy():
+    d, ff = 64, 96
+    rec = si.rvq3_record(3, 4, d, ff)
+    cb = [si.normal(3, 16 + s, 0.02 / (s + 1), 256 * 8, "f16") for s in range(3)]
+    cbs = np.stack(cb).reshape(3, 256, 8)
+    x = npref.to_f64(si.normal(3, 1, 1.0, d, "bf16"))
+    y = oracle.expert_rvq3(x, rec, cbs, cbs, cbs, d, ff)
+    ref = npref.expert(x, npref.rvq3_record_mats(rec, [cbs, cbs, cbs], d, ff))
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_situ_limits():
+    # small arguments: SiTU -> silu(g) * u (tanh(z) ~ z); saturated gate: -> 100 tanh(u/25)
+    for g, u in [(1e-3, 2e-3), (-2e-3, 1e-3)]:
+        sw = oracle.act(g, u, "swiglu")
+        st = oracle.act(g, u, "situ")
+        assert abs(st - sw) <= 1e-6 * abs(sw)
+    for u in (-30.0, 1.0, 80.0):
+        assert abs(oracle.act(200.0, u, "situ") - 100.0 * math.tanh(u / 25.0)) <= 1e-12 * 100
+    assert oracle.act(-200.0, 3.0, "situ") == pytest.approx(0.0, abs=1e-80)
+    # SwiGLU against scipy's logistic
+    from scipy.special import expit
+    for g, u in [(0.3, -1.2), (-4.0, 2.0), (9.0, 0.5)]:
+        assert oracle.act(g, u) == pytest.approx(g * expit(g) * u, rel=1e-15)
+
+
+# ----------------------------------------------------------------------------- combine / whole layer
+
+def _tiny_layer(seed=0, T=6, d=64, ff=64, E=12, k=3, quant="mxfp4"):
+    r = si.LayerRecipe("t", d=d, ff=ff, E=E, k=k, T=T, x_dtype="f32", w_dtype="f32", seed=seed, scale_lo=119,
+                       scale_hi=125, quant=quant)
+    x = si.layer_x(r)
+    W = si.layer_router_w(r)
+    recs = [si.layer_record(r, e) for e in range(E)]
+    return r, x, W, recs
+
+
+def test_layer_matches_numpy_chain():
+    r, x, W, recs = _tiny_layer()
+    idx, g, y, out = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs)
+    logits, idx_ref, g_ref, delta_ref = npref.layer(x, W, None, r.k,
+                                                    lambda e: npref.mxfp4_record_mats(recs[e], r.d, r.ff))
+    np.testing.assert_array_equal(idx, idx_ref)
+    assert np.all(np.abs(g - g_ref) <= 1e-14 * g_ref)
+    assert np.max(np.abs(y - delta_ref)) <= 1e-12 * np.max(np.abs(delta_ref))
+    np.testing.assert_allclose(out, x.astype(np.float64) + y, rtol=0, atol=1e-12 * np.max(np.abs(out)))
+
+
+def test_layer_rvq3_matches_numpy_chain():
+    r, x, W, recs = _tiny_layer(quant="rvq3", seed=4)
+    cbs = si.layer_codebooks(r)
+    idx, g, y, out = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs, quant="rvq3",
+                                          codebooks=(cbs, cbs, cbs))
+    _, idx_ref, g_ref, delta_ref = npref.layer(x, W, None, r.k,
+                                               lambda e: npref.rvq3_record_mats(recs[e], [cbs] * 3, r.d, r.ff))
+    np.testing.assert_array_equal(idx, idx_ref)
+    assert np.max(np.abs(y - delta_ref)) <= 1e-12 * np.max(np.abs(delta_ref))
+
+
+def test_one_hot_gate_reproduces_single_expert():
+    # a bias that puts one expert 2000 above the rest: its gate is exactly 1 and
+    # every other selected gate underflows to exactly 0 in fp64
+    r, x, W, recs = _tiny_layer()
+    bias = np.zeros(r.E, dtype=np.float32)
+    bias[7] = 2000.0
+    idx, g, y, out = oracle.layer_forward(x, W, bias, r.d, r.ff, r.E, r.k, recs)
+    assert np.all(idx[:, 0] == 7) and np.all(g[:, 0] == 1.0) and np.all(g[:, 1:] == 0.0)
+    for t in range(r.T):
+        np.testing.assert_array_equal(y[t], oracle.expert_mxfp4(x[t].astype(np.float64), recs[7], r.d, r.ff))
+
+
+def test_zero_weight_experts_contribute_nothing_even_if_nan():
+    r, x, W, recs = _tiny_layer()
+    bias = np.zeros(r.E, dtype=np.float32)
+    bias[7] = 2000.0
+    idx, g, y, out = oracle.layer_forward(x, W, bias, r.d, r.ff, r.E, r.k, recs)
+    poisoned = list(recs)
+    for e in set(idx[:, 1:].reshape(-1).tolist()) - {7}:
+        rec = recs[e].copy()
+        cbytes, sbytes = r.ff * r.d // 2, r.ff * r.d // 32
+        rec[cbytes:cbytes + sbytes] = 255  # NaN scales
+        poisoned[e] = rec
+    idx2, g2, y2, out2 = oracle.layer_forward(x, W, bias, r.d, r.ff, r.E, r.k, poisoned)
+    assert np.all(np.isfinite(y2))
+    np.testing.assert_array_equal(y2, y)
+
+
+def test_combine_without_residual_is_the_weighted_sum():
+    rng = np.random.default_rng(2)
+    T, k, d = 3, 4, 8
+    yp = rng.standard_normal((T * k, d))
+    g = rng.random((T, k))
+    g[1, 2] = 0.0
+    yp[1 * k + 2] = np.nan  # skipped because its gate is 0
+    out = oracle.combine(None, yp, g, k)
+    for t in range(T):
+        ref = sum(g[t, j] * yp[t * k + j] for j in range(k) if g[t, j] != 0)
+        np.testing.assert_allclose(out[t], ref, rtol=1e-15, atol=1e-15)
+    xr = rng.standard_normal((T, d))
+    np.testing.assert_allclose(oracle.combine(xr, yp, g, k) - xr, out, rtol=1e-14, atol=1e-14)
+
+
+def test_missing_routed_expert_is_an_error():
+    r, x, W, recs = _tiny_layer()
+    idx, g, y, out = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs)
+    missing = list(recs)
+    missing[int(idx[0, 0])] = None
+    with pytest.raises(RuntimeError):
+        oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, missing)
+
+
+def test_token_mask_and_threads_do_not_change_results():
+    r, x, W, recs = _tiny_layer(T=8)
+    idx, g, y, out = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs)
+    mask = np.array([1, 0, 1, 0, 0, 1, 0, 0], dtype=np.uint8)
+    idx2, g2, y2, out2 = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs, token_mask=mask, nthreads=4)
+    np.testing.assert_array_equal(idx2, idx)
+    np.testing.assert_array_equal(y2[mask == 1], y[mask == 1])
+    assert np.all(np.isnan(y2[mask == 0]))
+
+
+def test_partial_deltas_over_expert_ranges_sum_to_full():
+    r, x, W, recs = _tiny_layer(T=8, E=12)
+    idx, g, y, out = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs)
+    a = oracle.partial_delta(x, idx, g, r.d, r.ff, r.k, recs, 0, 5)
+    b = oracle.partial_delta(x, idx, g, r.d, r.ff, r.k, recs, 5, 12)
+    np.testing.assert_allclose(a + b, y, rtol=0, atol=1e-12 * np.max(np.abs(y)))
