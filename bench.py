@@ -1,0 +1,337 @@
+#!/usr/bin/env python
+"""MoE-layer forward benchmark on one (or N independent) GB300.
+
+Workload (default): the Kimi-K3-shaped MoE layer at decode batch 1 -- d = 3584,
+ff = 3072, 896 MXFP4 experts resident in HBM (15.7 GB), top-16 renormalised
+gates, bf16 activations; every step routes one new token (64 distinct seeded
+tokens cycled), so each step streams 16 fresh experts (287 MB) from HBM.  L2 is
+flushed (a 512 MiB write) between timed steps, outside the timed events.
+
+  value        tokens/s from CUDA events around each moe_layer_forward call,
+               inputs resident in HBM
+  e2e          tokens/s through the same C-ABI call with the token copied in
+               from pinned host memory and the layer output copied back, per step
+  roofline     the dominant kernel (mxfp4_gate_up): algorithmic bytes per launch
+               / its mean launch time (per-launch events from the library's
+               profiler in a second pass over the same steps) vs the measured
+               HBM copy bandwidth
+  cpu_baseline the fp64 C oracle on a bounded sample of the same workload, on
+               this machine's host cores
+
+`--impl reference` times the oracle itself as the reference arm.  Under torchrun
+(N > 1) the ranks run independent replicas (the layer does not shard across
+GPUs here), value = all ranks' tokens / the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; achieved HBM GB/s (decode) / TC util vs peak"
+DEFAULT_WORKLOAD = "k3_mxfp4_decode"
+X_POOL = 64
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work for the oracle sample")
+    return ap.parse_args()
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(r, target_s, max_tokens=64, token_offset=1000):
+    """Times the fp64 oracle on whole tokens of recipe r until ~target_s of wall
+    time; returns (tokens, seconds, threads).  Record generation is excluded."""
+    import numpy as np
+
+    import oracle
+    import seeded_inputs as si
+    threads = host_cores()
+    W = si.layer_router_w(r)
+    b = si.layer_bias(r)
+    cb = si.layer_codebooks(r) if r.quant == "rvq3" else None
+    done, spent = 0, 0.0
+    while done < max_tokens and spent < target_s:
+        x = si.layer_x(r, T=1, token_offset=token_offset + done)
+        _, idx, _ = oracle.router(x, W, b, r.k)
+        recs = [si.layer_record(r, e) if e in set(idx.reshape(-1).tolist()) else None for e in range(r.E)]
+        t0 = time.perf_counter()
+        oracle.layer_forward(x, W, b, r.d, r.ff, r.E, r.k, recs, quant=r.quant, act_kind=r.act,
+                             codebooks=None if cb is None else (cb, cb, cb), nthreads=threads)
+        spent += time.perf_counter() - t0
+        done += 1
+        del recs
+    np.asarray(0)
+    return done, spent, threads
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_max(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import seeded_inputs as si
+    r = si.get_workload(args.workload)
+    per_step = max(1.0, 60.0 / max(1, args.steps))  # whole run within a few minutes
+    oracle_sample(r, target_s=0.0, max_tokens=min(args.warmup, 1))
+    tokens, secs, threads = 0, 0.0, host_cores()
+    for i in range(args.steps):
+        t, s, threads = oracle_sample(r, target_s=per_step, max_tokens=1, token_offset=2000 + i)
+        tokens += t
+        secs += s
+    value = tokens * r.T / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": args.workload, "tokens_per_step": r.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{tokens} tokens of {args.workload}, one token per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import seeded_inputs as si
+    from quantized_expert_ffn_score_gb300 import moe, synthetic
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    r = si.get_workload(args.workload)
+    T = r.T
+    ctx = moe.Context(local)
+    layer = synthetic.device_layer(r, device=dev)
+    x_pool = synthetic.device_x(r, T=X_POOL * T, device=dev).view(X_POOL, T, r.d)
+    out = torch.empty((T, r.d), dtype=torch.float32, device=dev)
+    counts = torch.empty(r.E, dtype=torch.int32, device=dev)
+    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T), device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, counts_out=None):
+        moe.moe_layer_forward(ctx, layer, x_pool[i % X_POOL], out, ws, counts_out=counts_out)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step(i)
+    ctx.check()
+
+    # ---- timed region: device events around each layer call -----------------
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step(i)
+        stops[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    dist_barrier(world)
+    ctx.check()
+    dev_ms = sum(s.elapsed_time(e) for s, e in zip(starts, stops))
+    dev_ms_max = dist_max(dev_ms, world, dev)
+
+    # ---- per-kernel pass (same steps, library profiler) ------------------------
+    ctx.profile(16 * K + 64)
+    distinct = []
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        step(i, counts_out=counts)
+        distinct.append(int((counts > 0).sum().item()))
+    prof = ctx.profile_read()
+    ctx.profile(0)
+    launches_per_step = sum(n for n, _ in prof.values()) / K
+
+    # ---- end to end through the ABI with host buffers --------------------------
+    x_host = torch.empty((X_POOL, T, r.d), dtype=x_pool.dtype, pin_memory=True)
+    x_host.copy_(x_pool.cpu())
+    out_host = torch.empty((T, r.d), dtype=torch.float32, pin_memory=True)
+    x_dev = torch.empty((T, r.d), dtype=x_pool.dtype, device=dev)
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e_starts[i].record(stream)
+        x_dev.copy_(x_host[i % X_POOL], non_blocking=True)
+        moe.moe_layer_forward(ctx, layer, x_dev, out, ws)
+        out_host.copy_(out, non_blocking=True)
+        e_stops[i].record(stream)
+    torch.cuda.synchronize()
+    ctx.check()
+    e2e_ms = dist_max(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_stops)), world, dev)
+
+    tokens_total = world * K * T
+    value = tokens_total / (dev_ms_max / 1e3)
+    peaks = measured_peaks()
+    rec_bytes = si.mxfp4_record_size(r.d, r.ff) if r.quant == "mxfp4" else si.rvq3_record_size(r.d, r.ff)
+    # dominant kernel: the gate/up expert kernel streams the gate and up thirds of
+    # every routed expert's record once per launch
+    dom = "mxfp4_gate_up" if r.quant == "mxfp4" else "rvq3_gate_up"
+    mean_distinct = float(np.mean(distinct))
+    dom_bytes = mean_distinct * (2 * rec_bytes / 3) + T * r.d * 2 + T * r.k * r.ff * 4
+    roofline = None
+    if dom in prof:
+        n, ms = prof[dom]
+        achieved = dom_bytes / (ms / n / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                    "bytes_per_launch": dom_bytes, "mean_launch_us": 1e3 * ms / n, "traffic": None}
+    step_bytes = mean_distinct * rec_bytes + r.E * r.d * 2 + T * r.d * 2
+    kernels = {k: {"launches": n, "mean_us": 1e3 * ms / n} for k, (n, ms) in prof.items()}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded counter-based generator; random-init weights)",
+            "config": {"workload": args.workload, "d": r.d, "ff": r.ff, "E": r.E, "k": r.k, "tokens_per_step": T,
+                       "quant": r.quant, "experts_resident_gb": round(r.E * rec_bytes / 1e9, 2),
+                       "l2": "flushed between steps (512 MiB write outside the timed events)",
+                       "x_pool": X_POOL, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "layer_hbm_gbs": step_bytes / (dev_ms_max / K / 1e3) / 1e9,
+            "roofline": roofline, "kernels": kernels,
+            "e2e": {"value": tokens_total / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * r.d * x_pool.element_size(), "d2h_bytes_per_step": T * r.d * 4},
+            "gpu_launches": int(round(launches_per_step * K)), "clocks": clk, "wall_s": wall}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tokens, secs, threads = oracle_sample(r, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tokens * T / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{tokens} tokens of {args.workload} (one token per call, pairs on "
+                                          f"{threads} OpenMP threads), {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,261 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE-layer forward library, libmoe_gb300.so.
+ *
+ * The layer (Kimi-K3 shape: d = 3584 latent, ff = 3072, E = 896 routed experts,
+ * top-16) runs in five steps, each one entry point below:
+ *
+ *   moe_route_topk       router logits, top-k selection, renormalised gates
+ *   moe_bucket_tokens    group the (token, slot) pairs by expert
+ *   moe_expert_ffn_mxfp4 / moe_expert_ffn_rvq3
+ *                        decode each selected expert's gate/up/down matrices
+ *                        from their compressed form inside the kernel and run
+ *                        the SwiGLU (or SiTU) FFN with fp32 accumulation
+ *   moe_combine          gate-weighted sum of the expert outputs, added to the
+ *                        residual
+ *   moe_layer_forward    the four steps chained on one stream
+ *   moe_stack_forward    several layers chained, bf16 activations in between
+ *
+ * Sources (page title, section):
+ *   - "Running a 2.78-Trillion-Parameter Model Across Two Desks", Act II: one
+ *     activation vector per MoE layer goes in and the weighted sum of the
+ *     selected experts' outputs comes back; 17.55 MB per MXFP4 expert; fp32
+ *     compute with bf16 storage after a bf16 path failed its tolerance gate.
+ *   - LazyLoRA README, "The engine": 896 routed experts per layer, top-16
+ *     routing, MXFP4 expert weights, a fused decode-and-dot that never widens
+ *     the packed weights, expert sums accumulated in fp32; "File map": the
+ *     router's top-16 gating with a score-correction bias, and SiTU.
+ *   - WASTE README, "3 bits per expert weight": residual vector quantisation
+ *     with 3 stages of 256-entry codebooks over 8-dim vectors; "How it works":
+ *     gate, up and down of one expert adjacent in one record; "What is this":
+ *     an embeddable C API with an init-able config and status codes.
+ *   - MXFP4 encodings follow the OCP Microscaling Formats (MX) v1.0
+ *     specification (E2M1 elements, E8M0 scale per 32 elements).
+ *
+ * Conventions that hold for every call:
+ *   - Every data pointer is a DEVICE pointer owned by the caller unless a
+ *     comment says otherwise.  The library allocates nothing per call: scratch
+ *     memory is the caller's workspace `ws` of `ws_bytes` bytes (256-byte
+ *     aligned), sized with the matching moe_*_ws_bytes query.
+ *   - Calls are asynchronous on `stream` and do not synchronise the host.
+ *     They must be made with the context's device current.
+ *   - Arguments are validated on the host first; a bad argument returns a
+ *     status at once and launches nothing.  Problems only visible on the device
+ *     (an out-of-range expert index in caller-supplied routing, a NULL record
+ *     for an expert that tokens were routed to, a pipeline wait that timed out)
+ *     set the context's device error word; the affected work is skipped, the
+ *     call's outputs are then undefined, and moe_ctx_check reports the error.
+ *     No weight is ever replaced by zeros or random values.
+ *   - Activations (x, out), router weights and fp32 pair buffers must be
+ *     16-byte aligned (they are read with vector loads); records and codebooks
+ *     too.  A misaligned pointer is MOE_ERR_INVALID_ARG.
+ *   - T = 0 is valid and launches nothing.
+ *   - Limits: d and ff multiples of 32, 32 <= d, ff <= 4096; 1 <= k <= 32,
+ *     k <= E <= 2048; T * k <= 2^24.  Larger shapes return MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,      /* NULL pointer, bad shape, bad enum        */
+  MOE_ERR_UNSUPPORTED = 2,      /* shape outside the limits above           */
+  MOE_ERR_WORKSPACE = 3,        /* ws NULL, misaligned or too small         */
+  MOE_ERR_CUDA = 4,             /* a CUDA runtime call failed               */
+  MOE_ERR_BAD_EXPERT_INDEX = 5, /* routing named an expert outside [0, E)   */
+  MOE_ERR_MISSING_EXPERT = 6,   /* a routed expert's record pointer is NULL */
+  MOE_ERR_TIMEOUT = 7           /* a bounded device-side wait gave up       */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SITU = 1 } moe_act;
+typedef enum { MOE_QUANT_MXFP4 = 0, MOE_QUANT_RVQ3 = 1 } moe_quant;
+
+typedef struct moe_ctx moe_ctx;
+
+/*
+ * MXFP4 expert bank.  records: device array [E] of device pointers, one per
+ * expert (NULL = absent), each 16-byte aligned, pointing at one contiguous
+ * record of moe_mxfp4_record_bytes(d, ff) bytes laid out as
+ *   gate.codes [ff][d/2] | gate.scales [ff][d/32] | up.codes [ff][d/2] |
+ *   up.scales [ff][d/32] | down.codes [d][ff/2]   | down.scales [d][ff/32]
+ * Matrices are row-major with the contraction axis contiguous: column c of a
+ * row is the low nibble of byte c/2 when c is even and the high nibble when c
+ * is odd; scale byte c/32 of the row (E8M0, value 2^(byte-127), 0xFF = NaN)
+ * multiplies the 32 columns of that block.  Gate and up map d -> ff, down maps
+ * ff -> d.  For d = 3584, ff = 3072 a record is 17,547,264 bytes and every
+ * region starts on a 4 KiB multiple.
+ */
+typedef struct {
+  const uint8_t* const* records;
+  int d, ff, E;
+} moe_mxfp4_experts;
+
+/*
+ * RVQ3 expert bank.  records: as above, each record moe_rvq3_record_bytes(d, ff)
+ * bytes laid out stage-planar and position-major:
+ *   gate.codes [3][d/8][ff] | up.codes [3][d/8][ff] | down.codes [3][ff/8][d]
+ * i.e. code[s][v][r] is stage s's codebook index for weights r, 8v..8v+7 of
+ * the matrix (rows contiguous for a fixed vector position).  codebooks[m] for
+ * m = gate, up, down: device fp16 [3][256][8] (stage, entry, component).  The
+ * weight is the sum of the three stages' codewords:
+ *   w[r][8v+i] = cb[0][code[0][v][r]][i] + cb[1][code[1][v][r]][i] + cb[2][code[2][v][r]][i].
+ * The three pointers may be equal (one codebook set per layer).
+ */
+typedef struct {
+  const uint8_t* const* records;
+  const uint16_t* codebooks[3];
+  int d, ff, E;
+} moe_rvq3_experts;
+
+/* One MoE layer: router (W [E][d] row-major, optional additive fp32 logit bias
+ * [E]) and its expert bank. */
+typedef struct {
+  int d, ff, E, k;
+  moe_act act;
+  moe_quant quant;
+  const void* router_w;
+  moe_dtype router_w_dtype;
+  const float* router_bias; /* nullable */
+  moe_mxfp4_experts mxfp4;  /* used when quant == MOE_QUANT_MXFP4 */
+  moe_rvq3_experts rvq3;    /* used when quant == MOE_QUANT_RVQ3  */
+} moe_layer;
+
+/* ---- context ------------------------------------------------------------- */
+
+MOE_API const char* moe_status_str(moe_status s);
+
+/* Creates a context on `device` (allocates a 16-byte device error word; this and
+ * moe_ctx_destroy are the only calls that allocate).  The caller's current
+ * device is left unchanged. */
+MOE_API moe_status moe_ctx_create(moe_ctx** ctx, int device);
+MOE_API void moe_ctx_destroy(moe_ctx* ctx);
+
+/* Synchronises `stream`, reads and clears the device error word.  Returns
+ * MOE_OK or the first device-detected error since the last check; *detail (if
+ * non-NULL) receives its detail (the offending expert index, or -1). */
+MOE_API moe_status moe_ctx_check(moe_ctx* ctx, cudaStream_t stream, int* detail);
+
+/* Per-launch timing, a diagnostic for benchmarks.  moe_ctx_profile(ctx, n)
+ * with n > 0 creates 2n CUDA events (this allocates) and from then on every
+ * kernel the context's calls launch is bracketed by an event pair on its
+ * stream, up to n launches between reads; n = 0 turns it off and frees the
+ * events.  moe_ctx_profile_read synchronises `stream`, then writes, per kernel
+ * name in order of first launch, the name (NUL-terminated, 32 bytes per entry
+ * in `names`), the launch count and the summed milliseconds, for at most
+ * max_entries names; it clears the records and returns the number of entries
+ * written, or minus a moe_status on error.  The event records sit between
+ * launches, so the timed launches do not overlap their neighbours. */
+MOE_API moe_status moe_ctx_profile(moe_ctx* ctx, int n);
+MOE_API int moe_ctx_profile_read(moe_ctx* ctx, cudaStream_t stream, int max_entries, char* names, int* launches,
+                                 double* total_ms);
+
+/* Library version string and the SM count the context sizes its grids for. */
+MOE_API const char* moe_version(void);
+MOE_API int moe_ctx_num_sms(const moe_ctx* ctx);
+
+/* ---- sizes ----------------------------------------------------------------- */
+
+MOE_API size_t moe_mxfp4_record_bytes(int d, int ff);
+MOE_API size_t moe_rvq3_record_bytes(int d, int ff);
+
+/* Workspace bytes each call needs (0 if the shape is invalid). */
+MOE_API size_t moe_route_topk_ws_bytes(int T, int d, int E, int k);
+MOE_API size_t moe_bucket_tokens_ws_bytes(int T, int k, int E);
+MOE_API size_t moe_expert_ffn_ws_bytes(int T, int k, int d, int ff, int E, moe_quant quant);
+MOE_API size_t moe_layer_forward_ws_bytes(const moe_layer* L, int T);
+MOE_API size_t moe_stack_forward_ws_bytes(const moe_layer* layers, int n_layers, int T);
+
+/* ---- the steps ----------------------------------------------------------- */
+
+/*
+ * Router and top-k.  x [T][d] (x_dtype), router_w [E][d] (w_dtype), bias [E]
+ * fp32 or NULL.  Writes topk_idx [T][k] (int32) and gates [T][k] (fp32).
+ *   l[t][e] = sum_i W[e][i] * x[t][i] + bias[e]
+ *   topk_idx[t][0..k) = the k largest l[t][.] ordered by (l descending, e
+ *   ascending): an exact tie goes to the lower expert index;
+ *   gates[t][j] = exp(l_j - l_0) / sum_j' exp(l_j' - l_0)  (softmax over all E
+ *   experts restricted to the selected ones and renormalised).
+ * Logits are accumulated in fp32 with a rigorous error bound per logit; where
+ * the bound leaves the order of the selected experts or the k-th/(k+1)-th
+ * boundary undecided, the candidates are recomputed in fp64 (and, if still
+ * undecided, by a sequential fp64 sum in ascending i), so the selection equals
+ * the one made on exact fp64 logits summed in ascending i.
+ */
+MOE_API moe_status moe_route_topk(moe_ctx* ctx, const void* x, moe_dtype x_dtype, const void* router_w, moe_dtype w_dtype,
+                          const float* bias, int T, int d, int E, int k, int32_t* topk_idx, float* gates, void* ws,
+                          size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Bucketing: a stable counting sort of the pairs p = t*k + j by expert
+ * topk_idx[p].  Writes counts [E] (pairs per expert), offsets [E+1] (exclusive
+ * prefix sum, offsets[E] = T*k) and pair_ids [T*k] (pair ids grouped by expert
+ * in ascending expert order, ascending p within an expert).  Counts come from
+ * warp-aggregated shared-memory atomics; the slot order is deterministic.
+ */
+MOE_API moe_status moe_bucket_tokens(moe_ctx* ctx, const int32_t* topk_idx, int T, int k, int E, int32_t* counts,
+                             int32_t* offsets, int32_t* pair_ids, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Expert FFN for every routed pair.  x [T][d] (x_dtype); offsets/pair_ids as
+ * written by moe_bucket_tokens.  For the pair in slot s of expert e (token
+ * t = pair_ids[s] / k):  g = Wg_e x_t, u = Wu_e x_t, h = act(g, u),
+ * y = Wd_e h, written to y_pairs [T*k][d] (fp32) at row pair_ids[s].
+ * act: SwiGLU h = silu(g) * u; SiTU h = 4 tanh(g/4) sigmoid(g) * 25 tanh(u/25).
+ * Weights are decoded in registers / shared memory and never written back;
+ * products and sums are fp32.
+ */
+MOE_API moe_status moe_expert_ffn_mxfp4(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k,
+                                const moe_mxfp4_experts* experts, moe_act act, const int32_t* offsets,
+                                const int32_t* pair_ids, float* y_pairs, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+MOE_API moe_status moe_expert_ffn_rvq3(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k,
+                               const moe_rvq3_experts* experts, moe_act act, const int32_t* offsets,
+                               const int32_t* pair_ids, float* y_pairs, void* ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/*
+ * Combine: out[t][i] = x_resid[t][i] + sum over j ascending with gates[t][j] != 0
+ * of gates[t][j] * y_pairs[t*k + j][i].  x_resid [T][d] (x_dtype) may be NULL
+ * (out is then the MoE delta alone).  out [T][d] in out_dtype (bf16: the fp32
+ * sum rounded to nearest even).  A pair with gate 0 is never read.
+ */
+MOE_API moe_status moe_combine(moe_ctx* ctx, const void* x_resid, moe_dtype x_dtype, const float* y_pairs,
+                       const float* gates, int T, int k, int d, void* out, moe_dtype out_dtype, cudaStream_t stream);
+
+/*
+ * The whole layer: route, bucket, expert FFN, combine (with x as residual).
+ * x [T][d] (x_dtype), out [T][d] (out_dtype; may not alias x).  The optional
+ * outputs topk_idx_out [T][k], gates_out [T][k], counts_out [E] receive the
+ * routing when non-NULL.
+ */
+MOE_API moe_status moe_layer_forward(moe_ctx* ctx, const moe_layer* L, const void* x, moe_dtype x_dtype, int T, void* out,
+                             moe_dtype out_dtype, int32_t* topk_idx_out, float* gates_out, int32_t* counts_out,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Several layers in sequence: layer l's output, rounded to bf16 (nearest
+ * even), is layer l+1's input.  x [T][d] (x_dtype) feeds layer 0; out [T][d]
+ * receives the last layer's output in out_dtype.  All layers share d.
+ */
+MOE_API moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers, const void* x, moe_dtype x_dtype,
+                             int T, void* out, moe_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

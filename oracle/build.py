@@ -2,6 +2,7 @@
 
 TEST INFRASTRUCTURE ONLY.
 """
+import fcntl
 import os
 import subprocess
 
@@ -11,12 +12,21 @@ SRC = [os.path.join(HERE, "moe_oracle.c")]
 HDR = [os.path.join(HERE, "moe_oracle.h")]
 
 
+def _stale():
+    return not os.path.exists(LIB) or any(os.path.getmtime(s) > os.path.getmtime(LIB) for s in SRC + HDR)
+
+
 def build(force=False):
-    stale = not os.path.exists(LIB) or any(os.path.getmtime(s) > os.path.getmtime(LIB) for s in SRC + HDR)
-    if force or stale:
-        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
-               "-o", LIB] + SRC + ["-lm"]
-        subprocess.check_call(cmd)
+    if not (force or _stale()):
+        return LIB
+    with open(os.path.join(HERE, ".build.lock"), "w") as lk:
+        fcntl.flock(lk, fcntl.LOCK_EX)  # one builder at a time; others reuse its result
+        if force or _stale():
+            tmp = LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
+                   "-o", tmp] + SRC + ["-lm"]
+            subprocess.check_call(cmd)
+            os.replace(tmp, LIB)
     return LIB
 
 

@@ -72,7 +72,7 @@ void or_rvq3_row(const uint8_t* codes, const uint16_t* cb, int rows, int K, int 
     for (int i = 0; i < 8; ++i) {
       double acc = 0.0;
       for (int s = 0; s < 3; ++s) {
-        int c = codes[((size_t)s * rows + r) * nv + v];
+        int c = codes[((size_t)s * nv + v) * rows + r];
         acc += or_f16(cb[((size_t)s * 256 + c) * 8 + i]);
       }
       w[8 * v + i] = acc;

@@ -45,8 +45,9 @@ double or_f16(uint16_t bits);        /* IEEE binary16 bit pattern -> value      
 /* MXFP4 matrix [rows][K]: codes [rows][K/2] (low nibble = even column),
  * scales [rows][K/32] (one E8M0 per 32 consecutive columns).  Row r -> w[K]. */
 void or_mxfp4_row(const uint8_t* codes, const uint8_t* scales, int K, int r, double* w);
-/* RVQ3 matrix [rows][K]: codes [3][rows][K/8] stage-planar, codebooks cb fp16
- * [3][256][8]; w[r][8v+i] = sum over stages s of cb[s][code_s[r][v]][i]. */
+/* RVQ3 matrix [rows][K]: codes [3][K/8][rows] (stage-planar, position-major:
+ * code[s][v][r]), codebooks cb fp16 [3][256][8];
+ * w[r][8v+i] = sum over stages s of cb[s][code[s][v][r]][i]. */
 void or_rvq3_row(const uint8_t* codes, const uint16_t* cb, int rows, int K, int r, double* w);
 
 /* Byte offsets of the three matrices inside one expert record. */

@@ -1,0 +1,175 @@
+// bucket.cu -- group the (token, slot) pairs by expert: a stable counting sort
+// of pair ids p = t*k + j by topk_idx[p] (the grouping step that precedes the
+// expert FFN; "Running a 2.78-Trillion-Parameter Model Across Two Desks", Act II
+// computes each selected expert once per layer for the tokens routed to it).
+//
+// One CTA.  Warp w owns the contiguous pair range [w*P/W, (w+1)*P/W).
+//   1. per-warp histograms hist[w][e] with warp-aggregated shared atomics
+//      (__match_any_sync groups lanes holding the same expert; the group's
+//      leader adds the group size);
+//   2. per expert, an exclusive scan over warps gives each warp's base inside
+//      the expert's bucket; a block scan over experts gives offsets;
+//   3. each warp re-walks its range in order and writes pair ids: the rank of a
+//      lane inside its match group plus the running per-(warp, expert) count.
+// Ascending p within every bucket, independent of timing.
+#include <utility>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBucketMaxWarps = 32;
+
+// Exclusive scan of v over the block (all threads participate); returns the
+// prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) scratch[lane] = s;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  int base = warp > 0 ? scratch[warp - 1] : 0;
+  *total = scratch[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void bucket_kernel(BucketArgs a) {
+  extern __shared__ int bsm[];
+  const int E = a.E, P = a.T * a.k;
+  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* hist = bsm;                 // [nw][E]: counts, then running slot positions
+  int* scan_scratch = hist + nw * E;  // [32]
+  __shared__ int s_carry;
+  pdl_wait();
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  pdl_launch_dependents();
+  const int per = (P + nw - 1) / nw;
+  const int p_begin = min(P, warp * per), p_end = min(P, p_begin + per);
+  // 1. histograms
+  for (int base = p_begin; base < p_end; base += 32) {
+    const int p = base + lane;
+    int e = p < p_end ? a.topk_idx[p] : -1;
+    if (p < p_end && (e < 0 || e >= E)) {
+      dev_error(a.err, MOE_ERR_BAD_EXPERT_INDEX, e);
+      e = -1;
+    }
+    const unsigned act = __ballot_sync(0xffffffffu, e >= 0);
+    if (e >= 0) {
+      const unsigned grp = __match_any_sync(act, e);
+      if (lane == __ffs(grp) - 1) atomicAdd(&hist[warp * E + e], __popc(grp));
+    }
+  }
+  __syncthreads();
+  // 2. per expert: counts and per-warp bases; block scan over experts
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    int cnt = 0;
+    if (e < E) {
+      for (int w = 0; w < nw; ++w) {
+        int c = hist[w * E + e];
+        hist[w * E + e] = cnt;  // exclusive base of warp w inside expert e's bucket
+        cnt += c;
+      }
+    }
+    int total;
+    int off = block_exclusive_scan(cnt, scan_scratch, &total) + carry;
+    if (e < E) {
+      a.counts[e] = cnt;
+      a.offsets[e] = off;
+      for (int w = 0; w < nw; ++w) hist[w * E + e] += off;  // absolute running position
+    }
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    a.offsets[E] = carry;
+    s_carry = 0;
+  }
+  __syncthreads();
+  // active expert list (ascending expert id)
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    const int f = (e < E && a.offsets[e + 1] > a.offsets[e]) ? 1 : 0;
+    int total;
+    const int pos = block_exclusive_scan(f, scan_scratch, &total) + s_carry;
+    if (f) a.active[1 + pos] = e;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.active[0] = s_carry;
+  // 3. stable scatter, walking each warp's range in ascending p
+  for (int base = p_begin; base < p_end; base += 32) {
+    const int p = base + lane;
+    int e = p < p_end ? a.topk_idx[p] : -1;
+    if (e >= E) e = -1;
+    const unsigned act = __ballot_sync(0xffffffffu, e >= 0);
+    if (e >= 0) {
+      const unsigned grp = __match_any_sync(act, e);
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      const int pos = hist[warp * E + e] + rank;
+      a.pair_ids[pos] = p;
+      __syncwarp(grp);
+      if (lane == __ffs(grp) - 1) hist[warp * E + e] += __popc(grp);
+    }
+    __syncwarp();
+  }
+}
+
+// Active expert list from offsets alone (used when the expert FFN is called on
+// its own): active[0] = count, active[1..] = experts with a non-empty bucket.
+__global__ void active_kernel(const int32_t* offsets, int E, int32_t* active) {
+  __shared__ int scratch[32];
+  __shared__ int s_carry;
+  pdl_wait();
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    const int f = (e < E && offsets[e + 1] > offsets[e]) ? 1 : 0;
+    int total;
+    const int pos = block_exclusive_scan(f, scratch, &total) + s_carry;
+    if (f) active[1 + pos] = e;
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) active[0] = s_carry;
+}
+
+}  // namespace
+
+cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s) {
+  const int P = a.T * a.k;
+  int nw = (P + 255) / 256;  // ~8 rounds of 32 pairs per warp
+  nw = nw < 1 ? 1 : (nw > kBucketMaxWarps ? kBucketMaxWarps : nw);
+  if (nw < 4) nw = 4;
+  const int nw_smem = (200 * 1024 / 4 - 32) / a.E;  // per-warp histograms must fit in shared memory
+  if (nw > nw_smem) nw = nw_smem;
+  size_t smem = ((size_t)nw * a.E + 32) * sizeof(int);
+  cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch("bucket", bucket_kernel, dim3(1), dim3(nw * 32), smem, s, pdl, a);
+}
+
+cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s) {
+  return launch("active_list", active_kernel, dim3(1), dim3(256), 0, s, pdl, offsets, E, active);
+}
+
+}  // namespace moe

@@ -1,0 +1,208 @@
+// moe_internal.cuh -- device helpers and kernel launcher declarations shared by
+// the translation units of libmoe_gb300.so.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxK = 32;          // top-k limit
+constexpr int kMaxE = 2048;        // expert-count limit
+constexpr int kMaxDim = 4096;      // d, ff limit
+constexpr int kRowsPerHalf = 16;   // GEMV tile: rows per half-warp
+constexpr int kTokChunk = 2;       // GEMV: tokens per pass over a weight tile
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded device waits: 2 s
+
+// ---------------------------------------------------------------- error word
+// err[0] = first status code, err[1] = its detail.  First error wins.
+__device__ __forceinline__ void dev_error(int* err, int code, int detail) {
+  if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, detail);
+}
+
+// ---------------------------------------------------------------- PDL
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- timers
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete, for at most
+// kWaitLimitNs.  Returns false (and records MOE_ERR_TIMEOUT) if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      dev_error(err, MOE_ERR_TIMEOUT, -1);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Named barrier among `nthreads` threads (a multiple of 32) with id `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- numeric helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// E8M0 scale byte -> 2^(b-127) as fp32 (0 -> 2^-127 subnormal, 255 -> NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  if (b == 255u) return __uint_as_float(0x7FC00000u);
+  if (b == 0u) return __uint_as_float(0x00400000u);
+  return __uint_as_float(b << 23);
+}
+
+__device__ __forceinline__ float act_fn(float g, float u, int act) {
+  float sig = 1.0f / (1.0f + expf(-g));
+  if (act == MOE_ACT_SITU) return 4.0f * tanhf(g * 0.25f) * sig * 25.0f * tanhf(u * 0.04f);
+  return g * sig * u;
+}
+
+__device__ __forceinline__ float load_act(const void* p, int dtype, size_t i) {
+  if (dtype == MOE_BF16) return bf16_bits_to_f32(static_cast<const uint16_t*>(p)[i]);
+  return static_cast<const float*>(p)[i];
+}
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.  All pointers are device pointers.
+
+struct RouteArgs {
+  const void* x;
+  int x_dtype;
+  const void* w;
+  int w_dtype;
+  const float* bias;
+  int T, d, E, k;
+  float* logits;  // [T][E]   workspace
+  float* nrm_w;   // [E]      workspace: ||W_e||_2
+  float* nrm_x;   // [T]      workspace: ||x_t||_2
+  float gamma;    // relative error-bound coefficient of the fp32 sums
+  int32_t* topk_idx;
+  float* gates;
+  int* err;
+};
+cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s);
+
+struct BucketArgs {
+  const int32_t* topk_idx;
+  int T, k, E;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* pair_ids;
+  int32_t* active;  // [E+1] workspace: active[0] = n_active, active[1..] = experts in ascending order
+  int* err;
+};
+cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s);
+
+struct FfnArgs {
+  const uint8_t* const* records;
+  const uint16_t* cb[3];  // RVQ3 codebooks
+  int d, ff, E, k, T;
+  int act;
+  const void* x;
+  int x_dtype;
+  const int32_t* offsets;
+  const int32_t* pair_ids;
+  const int32_t* active;  // active[0] = n_active, then the expert ids
+  float* h;               // [T*k][ff] workspace, slot order
+  float* y_pairs;         // [T*k][d] by pair id
+  float* partial;         // RVQ3 only: K-slice partial sums (workspace)
+  int* err;
+};
+cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s);
+cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
+cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
+size_t rvq3_partial_floats(int T, int k, int d, int ff);
+
+struct CombineArgs {
+  const void* x;
+  int x_dtype;
+  const float* y_pairs;
+  const float* gates;
+  int T, k, d;
+  void* out;
+  int out_dtype;
+};
+cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
+
+// Per-launch event timing, active while an entry point of a context with
+// profiling enabled runs (set by the ABI layer for the calling thread).
+struct Profiler;
+extern thread_local Profiler* tl_profiler;
+void profiler_begin(Profiler* p, const char* name, cudaStream_t s);
+void profiler_end(Profiler* p, cudaStream_t s);
+
+// Launch helper: optional programmatic dependent launch; `name` labels the
+// launch for the profiler.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   bool pdl, Args&&... args) {
+  Profiler* prof = tl_profiler;
+  if (prof) profiler_begin(prof, name, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (prof) profiler_end(prof, s);
+  return err;
+}
+
+}  // namespace moe

@@ -1,0 +1,295 @@
+"""Thin ctypes binding of libmoe_gb300.so (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch supplies device memory and
+streams); integer arguments are passed through.  If the library has not been
+built this module raises on first use -- there is no fallback path.
+"""
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_BAD_EXPERT_INDEX", 6: "MOE_ERR_MISSING_EXPERT", 7: "MOE_ERR_TIMEOUT"}
+MOE_F32, MOE_BF16 = 0, 1
+ACT = {"swiglu": 0, "situ": 1}
+QUANT = {"mxfp4": 0, "rvq3": 1}
+
+# every symbol include/moe.h declares
+EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy", "moe_ctx_check", "moe_ctx_num_sms",
+           "moe_ctx_profile", "moe_ctx_profile_read",
+           "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
+           "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
+           "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
+           "moe_stack_forward"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, what, detail=None):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        self.detail = detail
+        super().__init__(f"{what}: {self.name}" + (f" (detail {detail})" if detail is not None else ""))
+
+
+class MxExperts(ctypes.Structure):
+    _fields_ = [("records", ctypes.c_void_p), ("d", ctypes.c_int), ("ff", ctypes.c_int), ("E", ctypes.c_int)]
+
+
+class RvqExperts(ctypes.Structure):
+    _fields_ = [("records", ctypes.c_void_p), ("codebooks", ctypes.c_void_p * 3), ("d", ctypes.c_int),
+                ("ff", ctypes.c_int), ("E", ctypes.c_int)]
+
+
+class LayerStruct(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("ff", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
+                ("act", ctypes.c_int), ("quant", ctypes.c_int), ("router_w", ctypes.c_void_p),
+                ("router_w_dtype", ctypes.c_int), ("router_bias", ctypes.c_void_p), ("mxfp4", MxExperts),
+                ("rvq3", RvqExperts)]
+
+
+_lib = None
+
+
+def lib():
+    """Loads the in-tree CUDA library; raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with quantized_expert_ffn_score_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_status_str.argtypes, L.moe_status_str.restype = [i32], ctypes.c_char_p
+        L.moe_version.restype = ctypes.c_char_p
+        L.moe_ctx_create.argtypes = [ctypes.POINTER(vp), i32]
+        L.moe_ctx_destroy.argtypes = [vp]
+        L.moe_ctx_destroy.restype = None
+        L.moe_ctx_check.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        L.moe_ctx_num_sms.argtypes = [vp]
+        L.moe_ctx_profile.argtypes, L.moe_ctx_profile.restype = [vp, i32], i32
+        L.moe_ctx_profile_read.argtypes = [vp, vp, i32, ctypes.c_char_p, ctypes.POINTER(i32),
+                                           ctypes.POINTER(ctypes.c_double)]
+        L.moe_ctx_profile_read.restype = i32
+        L.moe_mxfp4_record_bytes.argtypes, L.moe_mxfp4_record_bytes.restype = [i32, i32], sz
+        L.moe_rvq3_record_bytes.argtypes, L.moe_rvq3_record_bytes.restype = [i32, i32], sz
+        L.moe_route_topk_ws_bytes.argtypes, L.moe_route_topk_ws_bytes.restype = [i32, i32, i32, i32], sz
+        L.moe_bucket_tokens_ws_bytes.argtypes, L.moe_bucket_tokens_ws_bytes.restype = [i32, i32, i32], sz
+        L.moe_expert_ffn_ws_bytes.argtypes, L.moe_expert_ffn_ws_bytes.restype = [i32, i32, i32, i32, i32, i32], sz
+        L.moe_layer_forward_ws_bytes.argtypes = [ctypes.POINTER(LayerStruct), i32]
+        L.moe_layer_forward_ws_bytes.restype = sz
+        L.moe_stack_forward_ws_bytes.argtypes = [ctypes.POINTER(LayerStruct), i32, i32]
+        L.moe_stack_forward_ws_bytes.restype = sz
+        L.moe_route_topk.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.moe_bucket_tokens.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.moe_expert_ffn_mxfp4.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(MxExperts), i32, vp, vp, vp, vp, sz,
+                                           vp]
+        L.moe_expert_ffn_rvq3.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(RvqExperts), i32, vp, vp, vp, vp, sz,
+                                          vp]
+        L.moe_combine.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i32, vp]
+        L.moe_layer_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), vp, i32, i32, vp, i32, vp, vp, vp, vp, sz,
+                                        vp]
+        L.moe_stack_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), i32, vp, i32, i32, vp, i32, vp, sz, vp]
+        for f in ("moe_ctx_create", "moe_ctx_check", "moe_route_topk", "moe_bucket_tokens", "moe_expert_ffn_mxfp4",
+                  "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward", "moe_stack_forward"):
+            getattr(L, f).restype = i32
+        L.moe_ctx_num_sms.restype = i32
+        _lib = L
+    return _lib
+
+
+def version():
+    return lib().moe_version().decode()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dt(t):
+    if t.dtype == torch.float32:
+        return MOE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream if hasattr(s, "cuda_stream") else s
+
+
+def _check(rc, what):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+class Context:
+    """Owns a moe_ctx (its device error word)."""
+
+    def __init__(self, device=None):
+        dev = torch.cuda.current_device() if device is None else device
+        h = ctypes.c_void_p()
+        _check(lib().moe_ctx_create(ctypes.byref(h), dev), "moe_ctx_create")
+        self.handle = h
+        self.device = dev
+
+    @property
+    def num_sms(self):
+        return lib().moe_ctx_num_sms(self.handle)
+
+    def check(self, stream=None):
+        """Synchronises the stream; raises MoeError if a kernel flagged an error."""
+        detail = ctypes.c_int(-1)
+        rc = lib().moe_ctx_check(self.handle, _stream(stream), ctypes.byref(detail))
+        if rc != MOE_OK:
+            raise MoeError(rc, "device error", detail.value)
+
+    def profile(self, capacity):
+        """Turns per-launch event timing on (capacity launches between reads) or off (0)."""
+        _check(lib().moe_ctx_profile(self.handle, capacity), "moe_ctx_profile")
+
+    def profile_read(self, stream=None, max_entries=32):
+        """{kernel name: (launches, total ms)} since the last read."""
+        names = ctypes.create_string_buffer(32 * max_entries)
+        launches = (ctypes.c_int * max_entries)()
+        ms = (ctypes.c_double * max_entries)()
+        n = lib().moe_ctx_profile_read(self.handle, _stream(stream), max_entries, names, launches, ms)
+        if n < 0:
+            raise MoeError(-n, "moe_ctx_profile_read")
+        raw = names.raw
+        return {raw[32 * i:32 * i + 32].split(b"\0")[0].decode(): (launches[i], ms[i]) for i in range(n)}
+
+    def close(self):
+        if self.handle:
+            lib().moe_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ----------------------------------------------------------------------------- sizes
+
+def mxfp4_record_bytes(d, ff):
+    return int(lib().moe_mxfp4_record_bytes(d, ff))
+
+
+def rvq3_record_bytes(d, ff):
+    return int(lib().moe_rvq3_record_bytes(d, ff))
+
+
+def route_topk_ws_bytes(T, d, E, k):
+    return int(lib().moe_route_topk_ws_bytes(T, d, E, k))
+
+
+def bucket_tokens_ws_bytes(T, k, E):
+    return int(lib().moe_bucket_tokens_ws_bytes(T, k, E))
+
+
+def expert_ffn_ws_bytes(T, k, d, ff, E, quant="mxfp4"):
+    return int(lib().moe_expert_ffn_ws_bytes(T, k, d, ff, E, QUANT[quant]))
+
+
+def layer_forward_ws_bytes(layer, T):
+    return int(lib().moe_layer_forward_ws_bytes(ctypes.byref(layer.struct), T))
+
+
+def stack_forward_ws_bytes(layers, T):
+    arr = (LayerStruct * len(layers))(*[l.struct for l in layers])
+    return int(lib().moe_stack_forward_ws_bytes(arr, len(layers), T))
+
+
+def workspace(nbytes, device=None):
+    """A 256-byte aligned uint8 CUDA buffer (torch allocations are 512-byte aligned)."""
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+# ----------------------------------------------------------------------------- experts / layer
+
+class Layer:
+    """A moe_layer: keeps the tensors it points at alive."""
+
+    def __init__(self, d, ff, E, k, router_w, records, quant="mxfp4", act="swiglu", router_bias=None,
+                 codebooks=None, keep=()):
+        self.d, self.ff, self.E, self.k = d, ff, E, k
+        self.quant, self.act = quant, act
+        self.router_w, self.router_bias, self.records, self.codebooks = router_w, router_bias, records, codebooks
+        self._keep = list(keep)
+        s = LayerStruct()
+        s.d, s.ff, s.E, s.k = d, ff, E, k
+        s.act, s.quant = ACT[act], QUANT[quant]
+        s.router_w = _ptr(router_w)
+        s.router_w_dtype = _dt(router_w)
+        s.router_bias = _ptr(router_bias)
+        s.mxfp4 = MxExperts(_ptr(records), d, ff, E)
+        cbs = (ctypes.c_void_p * 3)(*([_ptr(c) for c in codebooks] if codebooks is not None else [None] * 3))
+        s.rvq3 = RvqExperts(_ptr(records), cbs, d, ff, E)
+        self.struct = s
+
+    def mx_experts(self):
+        return MxExperts(_ptr(self.records), self.d, self.ff, self.E)
+
+    def rvq_experts(self):
+        cbs = (ctypes.c_void_p * 3)(*[_ptr(c) for c in self.codebooks])
+        return RvqExperts(_ptr(self.records), cbs, self.d, self.ff, self.E)
+
+
+# ----------------------------------------------------------------------------- the steps
+
+def moe_route_topk(ctx, x, router_w, bias, k, topk_idx, gates, ws, stream=None):
+    T, d = x.shape
+    E = router_w.shape[0]
+    _check(lib().moe_route_topk(ctx.handle, _ptr(x), _dt(x), _ptr(router_w), _dt(router_w), _ptr(bias), T, d, E, k,
+                                _ptr(topk_idx), _ptr(gates), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_route_topk")
+
+
+def moe_bucket_tokens(ctx, topk_idx, E, counts, offsets, pair_ids, ws, stream=None):
+    T, k = topk_idx.shape
+    _check(lib().moe_bucket_tokens(ctx.handle, _ptr(topk_idx), T, k, E, _ptr(counts), _ptr(offsets), _ptr(pair_ids),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_bucket_tokens")
+
+
+def moe_expert_ffn_mxfp4(ctx, x, k, layer, offsets, pair_ids, y_pairs, ws, stream=None):
+    T = x.shape[0]
+    ex = layer.mx_experts()
+    _check(lib().moe_expert_ffn_mxfp4(ctx.handle, _ptr(x), _dt(x), T, k, ctypes.byref(ex), ACT[layer.act],
+                                      _ptr(offsets), _ptr(pair_ids), _ptr(y_pairs), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "moe_expert_ffn_mxfp4")
+
+
+def moe_expert_ffn_rvq3(ctx, x, k, layer, offsets, pair_ids, y_pairs, ws, stream=None):
+    T = x.shape[0]
+    ex = layer.rvq_experts()
+    _check(lib().moe_expert_ffn_rvq3(ctx.handle, _ptr(x), _dt(x), T, k, ctypes.byref(ex), ACT[layer.act],
+                                     _ptr(offsets), _ptr(pair_ids), _ptr(y_pairs), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "moe_expert_ffn_rvq3")
+
+
+def moe_combine(ctx, x_resid, y_pairs, gates, k, out, stream=None, x_dtype=None):
+    T, d = out.shape
+    xdt = _dt(x_resid) if x_resid is not None else (MOE_F32 if x_dtype is None else x_dtype)
+    _check(lib().moe_combine(ctx.handle, _ptr(x_resid), xdt, _ptr(y_pairs), _ptr(gates), T, k, d, _ptr(out),
+                             _dt(out), _stream(stream)), "moe_combine")
+
+
+def moe_layer_forward(ctx, layer, x, out, ws, topk_idx_out=None, gates_out=None, counts_out=None, stream=None):
+    T = x.shape[0]
+    _check(lib().moe_layer_forward(ctx.handle, ctypes.byref(layer.struct), _ptr(x), _dt(x), T, _ptr(out), _dt(out),
+                                   _ptr(topk_idx_out), _ptr(gates_out), _ptr(counts_out), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "moe_layer_forward")
+
+
+def moe_stack_forward(ctx, layers, x, out, ws, stream=None):
+    T = x.shape[0]
+    arr = (LayerStruct * len(layers))(*[l.struct for l in layers])
+    _check(lib().moe_stack_forward(ctx.handle, arr, len(layers), _ptr(x), _dt(x), T, _ptr(out), _dt(out), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "moe_stack_forward")

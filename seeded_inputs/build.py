@@ -3,6 +3,7 @@
 libseeded_inputs_host.so  -- gcc, always built (the CPU tests need it).
 libseeded_inputs_cuda.so  -- nvcc for sm_103a, built when nvcc is present.
 """
+import fcntl
 import os
 import shutil
 import subprocess
@@ -27,22 +28,31 @@ def _nvcc():
     return cand if os.path.exists(cand) else None
 
 
+def _locked_build(out, srcs, make_cmd, force):
+    if not (force or _stale(out, srcs)):
+        return out
+    with open(os.path.join(HERE, ".build.lock"), "w") as lk:
+        fcntl.flock(lk, fcntl.LOCK_EX)  # one builder at a time; others reuse its result
+        if force or _stale(out, srcs):
+            tmp = out + f".tmp{os.getpid()}"
+            subprocess.check_call(make_cmd(tmp))
+            os.replace(tmp, out)
+    return out
+
+
 def build_host(force=False):
-    if force or _stale(HOST_LIB, _HOST_SRC + _HDR):
-        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", HOST_LIB] + _HOST_SRC
-        subprocess.check_call(cmd)
-    return HOST_LIB
+    return _locked_build(HOST_LIB, _HOST_SRC + _HDR, lambda o: ["gcc", "-O2", "-std=c11", "-ffp-contract=off",
+                                                                 "-fPIC", "-shared", "-o", o] + _HOST_SRC, force)
 
 
 def build_cuda(force=False):
     nvcc = _nvcc()
     if nvcc is None:
         return None
-    if force or _stale(CUDA_LIB, _CUDA_SRC + _HDR):
-        cmd = [nvcc, "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-               "-fmad=false", "-Xcompiler", "-fPIC", "-shared", "-o", CUDA_LIB] + _CUDA_SRC
-        subprocess.check_call(cmd)
-    return CUDA_LIB
+    return _locked_build(CUDA_LIB, _CUDA_SRC + _HDR,
+                         lambda o: [nvcc, "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
+                                    "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC", "-shared", "-o", o]
+                         + _CUDA_SRC, force)
 
 
 def build(force=False):

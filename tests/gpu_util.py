@@ -1,0 +1,83 @@
+"""Helpers for the GPU parity tests: run a layer through the C ABI, run the
+oracle on the same seeded inputs, compare.
+
+Tolerance: max |y_gpu - y_ref| <= 2e-3 * RMS(y_ref) on the MoE delta y (the
+layer output minus the residual), the bound the fp32-accumulating path must
+meet; routing indices and bucket contents are compared bit for bit.
+"""
+import os
+
+import numpy as np
+
+import oracle
+import seeded_inputs as si
+
+TOL = 2e-3
+NTHREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def rms_err(y_gpu, y_ref):
+    rms = float(np.sqrt(np.mean(np.asarray(y_ref, dtype=np.float64) ** 2)))
+    err = float(np.max(np.abs(np.asarray(y_gpu, dtype=np.float64) - y_ref)))
+    return err, rms
+
+
+def assert_rms_close(y_gpu, y_ref, tol=TOL, what="output"):
+    err, rms = rms_err(y_gpu, y_ref)
+    assert np.all(np.isfinite(y_gpu)), f"{what}: non-finite values"
+    assert err <= tol * rms, f"{what}: max|err| {err:.3e} > {tol} x RMS {rms:.3e} ({err / rms:.2e})"
+    return err / rms
+
+
+def x_host_f64(x):
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def oracle_layer(r, x_host, tokens=None, nthreads=NTHREADS, records=None):
+    """(logits, topk, gates, y_delta, out) of the oracle; only `tokens` (default
+    all) get expert outputs, and only their experts' records are generated."""
+    W = si.layer_router_w(r)
+    b = si.layer_bias(r)
+    logits, idx, g = oracle.router(x_host, W, b, r.k)
+    T = x_host.shape[0]
+    mask = None
+    sel = np.arange(T) if tokens is None else np.asarray(tokens)
+    if tokens is not None:
+        mask = np.zeros(T, dtype=np.uint8)
+        mask[sel] = 1
+    if records is None:
+        needed = set(int(e) for e in idx[sel].reshape(-1))
+        records = [si.layer_record(r, e) if e in needed else None for e in range(r.E)]
+    cbs = None
+    if r.quant == "rvq3":
+        cb = si.layer_codebooks(r)
+        cbs = (cb, cb, cb)
+    idx2, g2, y, out = oracle.layer_forward(x_host, W, b, r.d, r.ff, r.E, r.k, records, quant=r.quant, act_kind=r.act,
+                                            codebooks=cbs, token_mask=mask, nthreads=nthreads)
+    assert np.array_equal(idx2, idx)
+    return logits, idx, g, y, out
+
+
+def gate_tolerance(r, x_host, logits_ref):
+    """Bound on |g_gpu - g_ref| / g_ref from the fp32 logit error bound used by
+    the router (gamma * ||W_e|| * ||x_t|| + 2^-23 |l|), applied to the logit
+    differences inside the softmax, plus fp32 rounding of the gates."""
+    W = x_host_f64(si.layer_router_w(r))
+    xs = x_host_f64(x_host)
+    nw = np.sqrt((W ** 2).sum(axis=1))
+    nx = np.sqrt((xs ** 2).sum(axis=1))
+    N = 8 if r.w_dtype == "bf16" else 4
+    h = -(-r.d // (32 * N)) + (3 if N == 8 else 2) + 5 + (0 if (r.x_dtype == "bf16" and r.w_dtype == "bf16") else 1)
+    u = 2.0 ** -24
+    gamma = h * u / (1 - h * u) * 1.002 + 1e-12
+    beta = gamma * nx[:, None] * nw[None, :] + 1.2e-7 * np.abs(logits_ref)
+    return 2 * beta.max(axis=1) * 2 + 1e-6  # per token, relative
+
+
+def check_routing(topk_gpu, gates_gpu, idx_ref, g_ref, rel_tol):
+    np.testing.assert_array_equal(topk_gpu, idx_ref)
+    rel = np.abs(gates_gpu.astype(np.float64) - g_ref) / g_ref
+    assert np.all(rel <= np.asarray(rel_tol)[:, None]), f"gate error {rel.max():.3e}"

@@ -43,7 +43,7 @@ def unpack_mxfp4(codes, scales, rows, K):
 
 
 def unpack_rvq3(codes, cb, rows, K):
-    codes = np.asarray(codes, dtype=np.uint8).reshape(3, rows, K // 8)
+    codes = np.asarray(codes, dtype=np.uint8).reshape(3, K // 8, rows).transpose(0, 2, 1)  # -> [s][r][v]
     cbf = f16_to_f64(np.asarray(cb).reshape(3, 256, 8))
     w = cbf[0][codes[0]] + cbf[1][codes[1]] + cbf[2][codes[2]]  # [rows][K/8][8]
     return w.reshape(rows, K)

@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.  Routing indices and bucket contents must be identical;
+outputs within 2e-3 x RMS of the oracle's."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_expert_ffn_score_gb300 import build, moe
+    build.build()
+    return moe
+
+
+@pytest.fixture(scope="module")
+def ctx(lib):
+    c = lib.Context(0)
+    yield c
+    c.close()
+
+
+def run_layer(moe, ctx, layer, x, out_dtype=torch.float32):
+    T = x.shape[0]
+    r = layer.recipe
+    out = torch.empty((T, r.d), dtype=out_dtype, device="cuda")
+    topk = torch.full((T, r.k), -1, dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, r.k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(r.E, dtype=torch.int32, device="cuda")
+    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T))
+    moe.moe_layer_forward(ctx, layer, x, out, ws, topk_idx_out=topk, gates_out=gates, counts_out=counts)
+    ctx.check()
+    return out.float().cpu().numpy(), topk.cpu().numpy(), gates.cpu().numpy(), counts.cpu().numpy()
+
+
+MID_MX = si.LayerRecipe("mid_mxfp4", d=1024, ff=576, E=40, k=6, T=37, seed=11, scale_lo=118, scale_hi=121)
+MID_RVQ = si.LayerRecipe("mid_rvq3", d=1024, ff=576, E=24, k=4, T=11, seed=12, quant="rvq3")
+
+
+def full_check(moe, ctx, r, tokens=None):
+    from quantized_expert_ffn_score_gb300 import synthetic
+    layer = synthetic.device_layer(r)
+    x = synthetic.device_x(r)
+    out, topk, gates, counts = run_layer(moe, ctx, layer, x)
+    xh = si.layer_x(r)
+    logits, idx, g, y, o = gu.oracle_layer(r, xh, tokens=tokens)
+    gu.check_routing(topk, gates, idx, g, gu.gate_tolerance(r, xh, logits))
+    np.testing.assert_array_equal(counts, np.bincount(idx.reshape(-1), minlength=r.E))
+    sel = np.arange(r.T) if tokens is None else np.asarray(tokens)
+    delta = out[sel].astype(np.float64) - gu.x_host_f64(xh)[sel]
+    rel = gu.assert_rms_close(delta, y[sel], what=r.name)
+    return rel
+
+
+def test_tiny_layer(lib, ctx):
+    full_check(lib, ctx, si.get_workload("tiny"))
+
+
+def test_mid_mxfp4_spans_tiles_and_ragged_tail(lib, ctx):
+    full_check(lib, ctx, MID_MX)
+
+
+def test_mid_mxfp4_situ_fp32_router(lib, ctx):
+    full_check(lib, ctx, MID_MX.with_(act="situ", x_dtype="f32", w_dtype="f32", seed=13))
+
+
+def test_mid_mxfp4_bf16_x_fp32_router(lib, ctx):
+    full_check(lib, ctx, MID_MX.with_(w_dtype="f32", seed=14, T=5, k=1))
+
+
+def test_mid_mxfp4_all_experts_selected(lib, ctx):
+    full_check(lib, ctx, MID_MX.with_(E=8, k=8, T=3, seed=15))
+
+
+def test_mid_rvq3(lib, ctx):
+    full_check(lib, ctx, MID_RVQ)
+
+
+def test_mid_rvq3_situ(lib, ctx):
+    full_check(lib, ctx, MID_RVQ.with_(act="situ", seed=16, T=3))
+
+
+@pytest.mark.slow
+def test_k3_mxfp4_decode_b1(lib, ctx):
+    full_check(lib, ctx, si.get_workload("k3_mxfp4_decode"))
+
+
+@pytest.mark.slow
+def test_k3_rvq3_decode_b1(lib, ctx):
+    full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b1"))
+
+
+@pytest.mark.slow
+def test_k3_rvq3_decode_b8(lib, ctx):
+    full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b8"), tokens=[0, 3, 7])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["k3_mxfp4_prefill_zipf", "k3_mxfp4_prefill_uniform"])
+def test_k3_prefill_routing_all_tokens_outputs_sampled(lib, ctx, name):
+    full_check(lib, ctx, si.get_workload(name), tokens=[0, 201, 511])
+
+
+def test_route_topk_and_bucket_standalone_match_oracle(lib, ctx):
+    # the K3 router on 512 tokens, with and without the Zipf bias, then bucketing
+    moe = lib
+    from quantized_expert_ffn_score_gb300 import synthetic
+    for name in ("k3_mxfp4_prefill_zipf", "k3_mxfp4_prefill_uniform"):
+        r = si.get_workload(name)
+        W = torch.empty((r.E, r.d), dtype=torch.bfloat16, device="cuda")
+        si.dev_layer_router_w(r, W.data_ptr())
+        b = si.layer_bias(r)
+        bias = None if b is None else torch.from_numpy(b).cuda()
+        x = synthetic.device_x(r)
+        topk = torch.empty((r.T, r.k), dtype=torch.int32, device="cuda")
+        gates = torch.empty((r.T, r.k), dtype=torch.float32, device="cuda")
+        ws = moe.workspace(moe.route_topk_ws_bytes(r.T, r.d, r.E, r.k))
+        moe.moe_route_topk(ctx, x, W, bias, r.k, topk, gates, ws)
+        counts = torch.empty(r.E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(r.E + 1, dtype=torch.int32, device="cuda")
+        pairs = torch.empty(r.T * r.k, dtype=torch.int32, device="cuda")
+        wsb = moe.workspace(moe.bucket_tokens_ws_bytes(r.T, r.k, r.E))
+        moe.moe_bucket_tokens(ctx, topk, r.E, counts, offsets, pairs, wsb)
+        ctx.check()
+        xh = si.layer_x(r)
+        logits, idx, g = oracle.router(xh, si.layer_router_w(r), b, r.k)
+        gu.check_routing(topk.cpu().numpy(), gates.cpu().numpy(), idx, g, gu.gate_tolerance(r, xh, logits))
+        c_ref, o_ref, p_ref = oracle.bucket(idx, r.E)
+        np.testing.assert_array_equal(counts.cpu().numpy(), c_ref)
+        np.testing.assert_array_equal(offsets.cpu().numpy(), o_ref)
+        np.testing.assert_array_equal(pairs.cpu().numpy(), p_ref)
+
+
+def test_router_certifies_exact_ties_and_near_ties(lib, ctx):
+    # duplicated router rows give exactly equal logits (ties must go to the lower
+    # index); rows differing in one low bit give near-ties the fp32 bound cannot
+    # separate, forcing the fp64 and sequential-fp64 recomputation paths
+    moe = lib
+    d, E, k, T = 256, 64, 8, 16
+    rng = np.random.default_rng(0)
+    Wf = (rng.standard_normal((E, d)) / 16).astype(np.float32)
+    Wb = torch.from_numpy(Wf).to(torch.bfloat16)
+    Wb[10] = Wb[3]
+    Wb[40] = Wb[3]
+    Wb[20] = Wb[7]
+    w16 = Wb.view(torch.int16)
+    w16[21] = w16[7]
+    w16[21, 5] += 1  # one ulp apart in one weight
+    x = torch.from_numpy(rng.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16)
+    x[:, :] = x[0]  # every token the same: the tied experts appear in many top-k sets
+    x[1:, 0] += torch.arange(1, T, dtype=torch.bfloat16) * 0.01
+    Wd, xd = Wb.cuda(), x.cuda()
+    topk = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.route_topk_ws_bytes(T, d, E, k))
+    moe.moe_route_topk(ctx, xd, Wd, None, k, topk, gates, ws)
+    ctx.check()
+    xh = x.view(torch.int16).numpy().view(np.uint16)
+    Wh = Wb.view(torch.int16).numpy().view(np.uint16)
+    logits, idx, g = oracle.router(xh, Wh, None, k)
+    np.testing.assert_array_equal(topk.cpu().numpy(), idx)
+
+
+def test_stack_layers_individually_and_chained(lib, ctx):
+    """Six K3-shaped... reduced to a mid shape here; the full-size stack is in
+    test_k3_stack.  Each layer on its own seeded input, then the chain."""
+    moe = lib
+    from quantized_expert_ffn_score_gb300 import synthetic
+    recipes = [MID_MX.with_(seed=200 + l, T=9) for l in range(3)]
+    layers = [synthetic.device_layer(r) for r in recipes]
+    x0 = synthetic.device_x(recipes[0])
+    out = torch.empty((9, MID_MX.d), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.stack_forward_ws_bytes(layers, 9))
+    moe.moe_stack_forward(ctx, layers, x0, out, ws)
+    ctx.check()
+    # the chain by hand through moe_layer_forward must give the same bits
+    x = x0
+    for i, (r, layer) in enumerate(zip(recipes, layers)):
+        last = i == len(recipes) - 1
+        o = torch.empty((9, r.d), dtype=torch.float32 if last else torch.bfloat16, device="cuda")
+        w = moe.workspace(moe.layer_forward_ws_bytes(layer, 9))
+        moe.moe_layer_forward(ctx, layer, x, o, w)
+        x = o
+    ctx.check()
+    assert torch.equal(x, out)
+
+
+def test_combine_bf16_output_rounds_fp32_sum(lib, ctx):
+    moe = lib
+    T, k, d = 5, 3, 64
+    g = torch.rand((T, k), device="cuda")
+    g[2, 1] = 0.0
+    y = torch.randn((T * k, d), device="cuda")
+    y[2 * k + 1] = float("nan")  # gate 0: never read
+    xr = torch.randn((T, d), device="cuda").to(torch.bfloat16)
+    out32 = torch.empty((T, d), device="cuda")
+    out16 = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_combine(ctx, xr, y, g, k, out32)
+    moe.moe_combine(ctx, xr, y, g, k, out16)
+    ctx.check()
+    assert torch.isfinite(out32).all()
+    assert torch.equal(out32.to(torch.bfloat16), out16)
+    ref = oracle.combine(xr.float().cpu().numpy().astype(np.float64), torch.nan_to_num(y).cpu().double().numpy(),
+                         g.cpu().double().numpy(), k)
+    np.testing.assert_allclose(out32.cpu().numpy(), ref, rtol=1e-5, atol=1e-5)

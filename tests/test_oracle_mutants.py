@@ -31,6 +31,7 @@ MUTANTS = [
     ("combine uses wrong slot", "y_pairs[((size_t)t * k + j) * d + i]", "y_pairs[((size_t)t * k + (k - 1 - j)) * d + i]"),
     ("RVQ stage dropped", "for (int s = 0; s < 3; ++s) {\n        int c", "for (int s = 0; s < 2; ++s) {\n        int c"),
     ("RVQ codebook stride", "cb[((size_t)s * 256 + c) * 8 + i]", "cb[((size_t)s * 256 + c) + i]"),
+    ("RVQ codes read row-major", "codes[((size_t)s * nv + v) * rows + r]", "codes[((size_t)s * rows + r) * nv + v]"),
     ("SiTU cap", "25.0 * tanh(u / 25.0)", "25.0 * tanh(u / 20.0)"),
     ("f16 exponent bias", "ldexp(1024.0 + m, e - 25)", "ldexp(1024.0 + m, e - 24)"),
 ]

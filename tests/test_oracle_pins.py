@@ -79,7 +79,7 @@ def test_rvq3_is_sum_of_three_codewords():
     cb0 = cb.copy()
     cb0[1:] = 0
     got0 = oracle.rvq3_matrix(codes, cb0, rows, K)
-    c0 = codes.reshape(3, rows, K // 8)[0]
+    c0 = codes.reshape(3, K // 8, rows)[0].T  # code[0][v][r] -> [r][v]
     for r in range(rows):
         for v in range(K // 8):
             for i in range(8):
