@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work for the oracle sample")
+    ap.add_argument("--only", choices=["route_topk"], default=None,
+                    help="time one step of the layer alone (a small case for profiler captures)")
     return ap.parse_args()
 
 
@@ -247,6 +249,7 @@ def run_ours(args):
     clk = clocks.stop()
     dist_barrier(world)
     ctx.check()
+    fp64_tokens, seq_logits = ctx.stats()
     dev_ms = sum(s.elapsed_time(e) for s, e in zip(starts, stops))
     dev_ms_max = dist_max(dev_ms, world, dev)
 
@@ -310,7 +313,8 @@ def run_ours(args):
             "roofline": roofline, "kernels": kernels,
             "e2e": {"value": tokens_total / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": T * r.d * x_pool.element_size(), "d2h_bytes_per_step": T * r.d * 4},
-            "gpu_launches": int(round(launches_per_step * K)), "clocks": clk, "wall_s": wall}
+            "gpu_launches": int(round(launches_per_step * K)), "clocks": clk, "wall_s": wall,
+            "router_fp64_recheck": {"tokens": fp64_tokens, "sequential_logits": seq_logits, "of_tokens": K * T}}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tokens, secs, threads = oracle_sample(r, target_s=args.cpu_seconds)
@@ -326,8 +330,34 @@ def run_ours(args):
     return 0
 
 
+def run_only_route(args):
+    """moe_route_topk alone on the workload's router and tokens (no expert bank)."""
+    import torch
+
+    import seeded_inputs as si
+    from quantized_expert_ffn_score_gb300 import moe, synthetic
+    r = si.get_workload(args.workload)
+    ctx = moe.Context(0)
+    W = torch.empty((r.E, r.d), dtype=torch.bfloat16 if r.w_dtype == "bf16" else torch.float32, device="cuda")
+    si.dev_layer_router_w(r, W.data_ptr())
+    b = si.layer_bias(r)
+    bias = None if b is None else torch.from_numpy(b).cuda()
+    x_pool = synthetic.device_x(r, T=X_POOL * r.T).view(X_POOL, r.T, r.d)
+    topk = torch.empty((r.T, r.k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((r.T, r.k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.route_topk_ws_bytes(r.T, r.d, r.E, r.k))
+    for i in range(args.warmup + args.steps):
+        moe.moe_route_topk(ctx, x_pool[i % X_POOL], W, bias, r.k, topk, gates, ws)
+    ctx.check()
+    print(json.dumps({"only": "route_topk", "workload": args.workload, "steps": args.steps,
+                      "fp64_recheck": ctx.stats()}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.only == "route_topk":
+        return run_only_route(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

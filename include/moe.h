@@ -150,6 +150,11 @@ MOE_API void moe_ctx_destroy(moe_ctx* ctx);
  * non-NULL) receives its detail (the offending expert index, or -1). */
 MOE_API moe_status moe_ctx_check(moe_ctx* ctx, cudaStream_t stream, int* detail);
 
+/* Router diagnostics: synchronises `stream` and returns (then clears) the
+ * number of tokens whose top-k needed the fp64 recheck and the number of
+ * logits that were recomputed by the sequential fp64 sum since the last call. */
+MOE_API moe_status moe_ctx_stats(moe_ctx* ctx, cudaStream_t stream, long long* fp64_tokens, long long* seq_logits);
+
 /* Per-launch timing, a diagnostic for benchmarks.  moe_ctx_profile(ctx, n)
  * with n > 0 creates 2n CUDA events (this allocates) and from then on every
  * kernel the context's calls launch is bracketed by an event pair on its

@@ -7,6 +7,8 @@
 
 #include "moe_internal.cuh"
 
+#include <map>
+#include <mutex>
 #include <vector>
 
 namespace moe {
@@ -25,6 +27,20 @@ struct Profiler {
 };
 
 thread_local Profiler* tl_profiler = nullptr;
+
+cudaError_t ensure_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = done[{dev, kernel}];
+  if (bytes <= cur) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (err == cudaSuccess) cur = bytes;
+  return err;
+}
 
 void profiler_begin(Profiler* p, const char* name, cudaStream_t s) {
   p->open = -1;
@@ -126,17 +142,57 @@ float router_gamma(int d, moe_dtype x_dtype, moe_dtype w_dtype) {
   return (float)(g * 1.0001);
 }
 
+// Small token counts (decode) compute the router logits with compensated sums:
+// the logit kernel is memory-bound there, and the much tighter bound lets the
+// top-k certify almost every token without the fp64 recheck.
+constexpr int kCompensatedMaxT = 16;
+
+// Bound coefficient of the compensated logits: |l32 - l_ref| <= K * sum|w x| +
+// 4u |l32| with K = (gamma_n^2 (1 + gamma_n) + gamma64_{d+1}) * 1.01, n = d + 32.
+float router_gamma_comp(int d) {
+  const double u = 5.9604644775390625e-8, u64 = 1.1102230246251565e-16;
+  const double n = d + 32.0, gn = n * u / (1.0 - n * u), g64 = (d + 1.0) * u64 / (1.0 - (d + 1.0) * u64);
+  return (float)((gn * gn * (1.0 + gn) + g64) * 1.01);
+}
+
 struct RouteWs {
   float* logits;
   float* nrm_w;
   float* nrm_x;
+  float* absdot;
 };
 RouteWs carve_route(Carver& c, int T, int E) {
   RouteWs r;
   r.logits = c.take<float>((size_t)T * E);
   r.nrm_w = c.take<float>(E);
   r.nrm_x = c.take<float>(T > 0 ? T : 1);
+  r.absdot = c.take<float>(T <= kCompensatedMaxT ? (size_t)T * E : 1);
   return r;
+}
+
+moe::RouteArgs route_args(const void* x, moe_dtype x_dtype, const void* w, moe_dtype w_dtype, const float* bias,
+                          int T, int d, int E, int k, const RouteWs& ws, int32_t* topk, float* gates, int* err) {
+  moe::RouteArgs ra;
+  std::memset(&ra, 0, sizeof ra);
+  ra.x = x;
+  ra.x_dtype = x_dtype;
+  ra.w = w;
+  ra.w_dtype = w_dtype;
+  ra.bias = bias;
+  ra.T = T;
+  ra.d = d;
+  ra.E = E;
+  ra.k = k;
+  ra.logits = ws.logits;
+  ra.nrm_w = ws.nrm_w;
+  ra.nrm_x = ws.nrm_x;
+  ra.absdot = ws.absdot;
+  ra.comp = T <= kCompensatedMaxT ? 1 : 0;
+  ra.gamma = ra.comp ? router_gamma_comp(d) : router_gamma(d, x_dtype, w_dtype);
+  ra.topk_idx = topk;
+  ra.gates = gates;
+  ra.err = err;
+  return ra;
 }
 
 struct FfnWs {
@@ -226,10 +282,8 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   const int32_t* topk = topk_out ? topk_out : w.topk;
   const float* gates = gates_out ? gates_out : w.gates;
   int32_t* counts = counts_out ? counts_out : w.counts;
-  moe::RouteArgs ra{x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, T, L->d, L->E, L->k,
-                    w.route.logits, w.route.nrm_w, w.route.nrm_x,
-                    router_gamma(L->d, x_dtype, L->router_w_dtype), const_cast<int32_t*>(topk),
-                    const_cast<float*>(gates), ctx->err};
+  moe::RouteArgs ra = route_args(x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, T, L->d, L->E, L->k,
+                                 w.route, const_cast<int32_t*>(topk), const_cast<float*>(gates), ctx->err);
   moe_status st = cuda_status(moe::launch_route_topk(ra, ctx->num_sms, s));
   if (st != MOE_OK) return st;
   moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, ctx->err};
@@ -369,9 +423,21 @@ moe_status moe_ctx_check(moe_ctx* ctx, cudaStream_t stream, int* detail) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
   int h[2] = {0, 0};
   if (cudaMemcpy(h, ctx->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (h[0] != 0 && cudaMemset(ctx->err, 0, 4 * sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h[0] != 0 && cudaMemset(ctx->err, 0, 2 * sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   if (detail) *detail = h[0] ? h[1] : -1;
   return static_cast<moe_status>(h[0]);
+}
+
+moe_status moe_ctx_stats(moe_ctx* ctx, cudaStream_t stream, long long* fp64_tokens, long long* seq_logits) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, ctx->err + 2, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ctx->err + 2, 0, 2 * sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fp64_tokens) *fp64_tokens = h[0];
+  if (seq_logits) *seq_logits = h[1];
+  return MOE_OK;
 }
 
 size_t moe_mxfp4_record_bytes(int d, int ff) {
@@ -436,8 +502,7 @@ moe_status moe_route_topk(moe_ctx* ctx, const void* x, moe_dtype x_dtype, const 
   if ((st = ws_check(ws, ws_bytes, moe_route_topk_ws_bytes(T, d, E, k))) != MOE_OK) return st;
   Carver c(ws);
   RouteWs w = carve_route(c, T, E);
-  moe::RouteArgs ra{x, x_dtype, router_w, w_dtype, bias, T, d, E, k, w.logits, w.nrm_w, w.nrm_x,
-                    router_gamma(d, x_dtype, w_dtype), topk_idx, gates, ctx->err};
+  moe::RouteArgs ra = route_args(x, x_dtype, router_w, w_dtype, bias, T, d, E, k, w, topk_idx, gates, ctx->err);
   return cuda_status(moe::launch_route_topk(ra, ctx->num_sms, stream));
 }
 

@@ -49,19 +49,21 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   return base + x - v;
 }
 
-__global__ void bucket_kernel(BucketArgs a) {
+// The first nw warps own the pairs; all blockDim threads take part in the
+// per-expert scans (blockDim is sized from E, nw from T*k).
+__global__ void bucket_kernel(BucketArgs a, int nw) {
   extern __shared__ int bsm[];
   const int E = a.E, P = a.T * a.k;
-  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* hist = bsm;                 // [nw][E]: counts, then running slot positions
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* hist = bsm;                    // [nw][E]: counts, then running slot positions
   int* scan_scratch = hist + nw * E;  // [32]
-  __shared__ int s_carry;
   pdl_wait();
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   pdl_launch_dependents();
   const int per = (P + nw - 1) / nw;
-  const int p_begin = min(P, warp * per), p_end = min(P, p_begin + per);
+  const int p_begin = warp < nw ? min(P, warp * per) : P;
+  const int p_end = warp < nw ? min(P, p_begin + per) : P;
   // 1. histograms
   for (int base = p_begin; base < p_end; base += 32) {
     const int p = base + lane;
@@ -77,44 +79,37 @@ __global__ void bucket_kernel(BucketArgs a) {
     }
   }
   __syncthreads();
-  // 2. per expert: counts and per-warp bases; block scan over experts
-  int carry = 0;
+  // 2. per expert: counts and per-warp bases; block scans over experts give
+  //    the offsets and the active-expert list (experts with a non-empty bucket)
+  int carry = 0, acarry = 0;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
     int cnt = 0;
     if (e < E) {
       for (int w = 0; w < nw; ++w) {
-        int c = hist[w * E + e];
+        const int c = hist[w * E + e];
         hist[w * E + e] = cnt;  // exclusive base of warp w inside expert e's bucket
         cnt += c;
       }
     }
-    int total;
-    int off = block_exclusive_scan(cnt, scan_scratch, &total) + carry;
+    int total, atotal;
+    const int off = block_exclusive_scan(cnt, scan_scratch, &total) + carry;
+    const int f = cnt > 0 ? 1 : 0;
+    const int apos = block_exclusive_scan(f, scan_scratch, &atotal) + acarry;
     if (e < E) {
       a.counts[e] = cnt;
       a.offsets[e] = off;
+      if (f) a.active[1 + apos] = e;
       for (int w = 0; w < nw; ++w) hist[w * E + e] += off;  // absolute running position
     }
     carry += total;
+    acarry += atotal;
   }
   if (threadIdx.x == 0) {
     a.offsets[E] = carry;
-    s_carry = 0;
+    a.active[0] = acarry;
   }
   __syncthreads();
-  // active expert list (ascending expert id)
-  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
-    const int e = e0 + threadIdx.x;
-    const int f = (e < E && a.offsets[e + 1] > a.offsets[e]) ? 1 : 0;
-    int total;
-    const int pos = block_exclusive_scan(f, scan_scratch, &total) + s_carry;
-    if (f) a.active[1 + pos] = e;
-    __syncthreads();
-    if (threadIdx.x == 0) s_carry += total;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) a.active[0] = s_carry;
   // 3. stable scatter, walking each warp's range in ascending p
   for (int base = p_begin; base < p_end; base += 32) {
     const int p = base + lane;
@@ -158,14 +153,16 @@ __global__ void active_kernel(const int32_t* offsets, int E, int32_t* active) {
 
 cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s) {
   const int P = a.T * a.k;
-  int nw = (P + 255) / 256;  // ~8 rounds of 32 pairs per warp
+  int nw = (P + 255) / 256;  // pair warps: ~8 rounds of 32 pairs each
   nw = nw < 1 ? 1 : (nw > kBucketMaxWarps ? kBucketMaxWarps : nw);
-  if (nw < 4) nw = 4;
   const int nw_smem = (200 * 1024 / 4 - 32) / a.E;  // per-warp histograms must fit in shared memory
   if (nw > nw_smem) nw = nw_smem;
-  size_t smem = ((size_t)nw * a.E + 32) * sizeof(int);
-  cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  return launch("bucket", bucket_kernel, dim3(1), dim3(nw * 32), smem, s, pdl, a);
+  int nthreads = 32 * ((a.E + 31) / 32);  // one scan element per thread where possible
+  if (nthreads > 1024) nthreads = 1024;
+  if (nthreads < 32 * nw) nthreads = 32 * nw;
+  const size_t smem = ((size_t)nw * a.E + 32) * sizeof(int);
+  ensure_smem(bucket_kernel, smem);
+  return launch("bucket", bucket_kernel, dim3(1), dim3(nthreads), smem, s, pdl, a, nw);
 }
 
 cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s) {

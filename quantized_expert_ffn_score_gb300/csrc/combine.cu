@@ -19,15 +19,25 @@ __global__ void combine_kernel(const CombineArgs a) {
   const int t = blockIdx.y;
   const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (4 * i4 >= a.d) return;
+  // groups of 16 slots: the gates, then all 16 y loads (independent of each
+  // other), then the fma chain in ascending j
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < a.k; ++j) {
-    const float g = a.gates[(size_t)t * a.k + j];
-    if (g == 0.f) continue;
-    const float4 y = reinterpret_cast<const float4*>(a.y_pairs + ((size_t)t * a.k + j) * a.d)[i4];
-    acc.x = fmaf(g, y.x, acc.x);
-    acc.y = fmaf(g, y.y, acc.y);
-    acc.z = fmaf(g, y.z, acc.z);
-    acc.w = fmaf(g, y.w, acc.w);
+  for (int j0 = 0; j0 < a.k; j0 += 16) {
+    float g[16];
+    float4 y[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) g[u] = j0 + u < a.k ? a.gates[(size_t)t * a.k + j0 + u] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (g[u] != 0.f) y[u] = reinterpret_cast<const float4*>(a.y_pairs + ((size_t)t * a.k + j0 + u) * a.d)[i4];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (g[u] == 0.f) continue;
+      acc.x = fmaf(g[u], y[u].x, acc.x);
+      acc.y = fmaf(g[u], y[u].y, acc.y);
+      acc.z = fmaf(g[u], y[u].z, acc.z);
+      acc.w = fmaf(g[u], y[u].w, acc.w);
+    }
   }
   const size_t o = (size_t)t * a.d + 4 * (size_t)i4;
   if (a.x) {

@@ -127,7 +127,9 @@ struct RouteArgs {
   float* logits;  // [T][E]   workspace
   float* nrm_w;   // [E]      workspace: ||W_e||_2
   float* nrm_x;   // [T]      workspace: ||x_t||_2
-  float gamma;    // relative error-bound coefficient of the fp32 sums
+  float* absdot;  // [T][E]   workspace: sum_i |W[e][i] x[t][i]| (compensated logits only)
+  int comp;       // logits by compensated (Dot2) sums; bounds from absdot
+  float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
   int32_t* topk_idx;
   float* gates;
   int* err;
@@ -175,6 +177,14 @@ struct CombineArgs {
   int out_dtype;
 };
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
+
+// Raises a kernel's dynamic shared memory limit on the current device once,
+// instead of before every launch (the driver call costs microseconds).
+cudaError_t ensure_smem(const void* kernel, size_t bytes);
+template <typename... KArgs>
+cudaError_t ensure_smem(void (*kernel)(KArgs...), size_t bytes) {
+  return ensure_smem(reinterpret_cast<const void*>(kernel), bytes);
+}
 
 // Per-launch event timing, active while an entry point of a context with
 // profiling enabled runs (set by the ABI layer for the calling thread).

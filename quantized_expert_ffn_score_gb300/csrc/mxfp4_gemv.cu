@@ -8,15 +8,25 @@
 //   MODE 0  gate/up: tile = rows [r0, r0+16) of Wg and of Wu; the epilogue
 //           applies the activation and writes h[slot][r] (fp32).
 //   MODE 1  down:    tile = rows [r0, r0+32) of Wd; writes y_pairs[pair][r].
+// Each CTA owns a contiguous range of the (expert, row tile) list, so it meets
+// at most a few experts and keeps an expert's input vectors in registers
+// across that expert's tiles.
 // Data movement: one producer lane streams each tile (codes and E8M0 scales of
 // both halves, 4 contiguous byte ranges of the expert record) into a ring of
 // shared-memory stages with 1-D bulk async copies completing on an mbarrier.
-// Compute: consumer warp w, lane l owns the 32-column block b = 16w + (l & 15)
-// of the contraction axis for half (l >> 4) of the tile, keeps that block of
-// the input vector in registers, and for each of the tile's 16 rows decodes its
-// 16 code bytes (cvt e2m1x2 -> f16x2 -> f32) and accumulates in fp32; the block
-// sum is multiplied by 2^(scale-127).  A 16-lane reduce-scatter leaves row
-// (l & 15) on lane l; warps are summed through shared memory.
+// Compute: two groups of consumer warps split each half tile's 16 rows (8
+// each); in a group, warp w, lane l owns the 32-column block b = 16w + (l & 15)
+// of the contraction axis for half (l >> 4) of the tile.  For each of its 8
+// rows it converts its 16 code bytes with cvt.e2m1x2 (two E2M1 codes -> f16x2,
+// exact) and accumulates the block in fp32:
+//   * bf16 activations: converted once to f16 after an exact power-of-two
+//     rescale (x * 2^-s with max|x| * 2^-s < 2^15), then fma.f32.f16 -- the
+//     product of two f16 values is exact in fp32 and the sum is fp32;
+//   * fp32 inputs (fp32 x, and h for the down projection): the f16 weights are
+//     widened to fp32 and multiplied in fp32.
+// The block sum is multiplied by 2^(scale-127) (and 2^s).  A reduce-scatter
+// over the 16 lanes of a half leaves each row on one lane; warps are summed
+// through a double-buffered shared-memory array, one named barrier per tile.
 #include <utility>
 
 #include "moe_internal.cuh"
@@ -26,14 +36,15 @@ namespace {
 
 constexpr int kMaxStages = 4;
 constexpr int kSmemBudget = 220 * 1024;
+constexpr int kNT = kTokChunk;  // tokens per pass over a tile (and cached per expert)
 
 struct Geom {
-  int K;                // contraction length
-  int nblk;             // K / 32
-  int warps;            // consumer warps: ceil(nblk / 16)
-  int tpe;              // tiles per expert
-  uint32_t half_codes;  // bytes of codes per half tile: 16 * K / 2
-  uint32_t half_scales; // bytes of scales per half tile: 16 * K / 32
+  int K;                 // contraction length
+  int nblk;              // K / 32
+  int warps;             // consumer warps: ceil(nblk / 16)
+  int tpe;               // tiles per expert
+  uint32_t half_codes;   // bytes of codes per half tile: 16 * K / 2
+  uint32_t half_scales;  // bytes of scales per half tile: 16 * K / 32
   uint32_t stage_bytes;
   int stages;
   size_t smem;
@@ -47,13 +58,27 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
       : "r"(w));
 }
 
-__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
-  __half2 v = *reinterpret_cast<__half2*>(&h);
-  return __half22float2(v);
+// Block dot products: 32 codes q (low nibble = even column) against the lane's
+// 32 input values.  f16 inputs: fma.f32.f16 on each half of the converted code
+// pair (exact products, fp32 sums); fp32 inputs: the f16 pair widened to fp32.
+__device__ __forceinline__ float dot32_f16(const uint4 q, const unsigned short* x) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2(w[i], h);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2;\n"
+          " fma.rn.f32.f16 %0, lo, %3, %0;\n fma.rn.f32.f16 %1, hi, %4, %1; }"
+          : "+f"(s0), "+f"(s1)
+          : "r"(h[j]), "h"(x[8 * i + 2 * j]), "h"(x[8 * i + 2 * j + 1]));
+  }
+  return s0 + s1;
 }
 
-// sum over the 32 columns of one block: codes q (low nibble = even column) times x.
-__device__ __forceinline__ float dot32(const uint4 q, const float* x) {
+__device__ __forceinline__ float dot32_f32(const uint4 q, const float* x) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -62,7 +87,7 @@ __device__ __forceinline__ float dot32(const uint4 q, const float* x) {
     e2m1x8_to_f16x2(w[i], h);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 f = h2_to_f2(h[j]);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
       s0 = fmaf(f.x, x[8 * i + 2 * j], s0);
       s1 = fmaf(f.y, x[8 * i + 2 * j + 1], s1);
     }
@@ -70,11 +95,12 @@ __device__ __forceinline__ float dot32(const uint4 q, const float* x) {
   return s0 + s1;
 }
 
-// 16 rows x NT values per lane -> lane (l & 15) holds the half-warp sum of row (l & 15).
-template <int NT>
-__device__ __forceinline__ void reduce_scatter16(float (&v)[16][NT], int lane) {
+// RPG (8 or 16) rows x NT values per lane -> the half-warp sum of row
+// (l & (RPG-1)) ends on lane l (for RPG = 8 on the lanes with (l & 8) == 0).
+template <int RPG, int NT>
+__device__ __forceinline__ void reduce_rows(float (&v)[RPG][NT], int lane) {
 #pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) {
+  for (int m = RPG / 2; m >= 1; m >>= 1) {
     const bool upper = (lane & m) != 0;
 #pragma unroll
     for (int i = 0; i < m; ++i) {
@@ -86,10 +112,14 @@ __device__ __forceinline__ void reduce_scatter16(float (&v)[16][NT], int lane) {
       }
     }
   }
+  if (RPG == 8) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) v[0][n] += __shfl_xor_sync(0xffffffffu, v[0][n], 8);
+  }
 }
 
 template <int MODE>
-__device__ __forceinline__ void tile_sources(const FfnArgs& a, const uint8_t* rec, int rt, const Geom& g,
+__device__ __forceinline__ void tile_sources(const FfnArgs& a, const uint8_t* rec, int rt,
                                              const uint8_t* (&src)[4]) {
   const size_t d = a.d, ff = a.ff;
   const size_t mat = ff * d / 2 + ff * d / 32;
@@ -118,47 +148,170 @@ __device__ __forceinline__ bool record_ok(const uint8_t* rec) {
   return rec != nullptr && ((reinterpret_cast<uintptr_t>(rec) & 15u) == 0);
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(9 * 32) mxfp4_gemv_kernel(const FfnArgs a, const Geom g) {
+// 2^s as fp32 for |s| <= 126.
+__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
+
+// The lane's inputs (its 32-column block) for up to kNT tokens (slots s_begin ..):
+// f16 values after a per-token power-of-two rescale (XF16), or fp32.
+template <int MODE, bool XF16>
+struct Inputs {
+  unsigned short xh[XF16 ? kNT : 1][32];
+  float xf[XF16 ? 1 : kNT][32];
+  float pw[kNT];  // 2^s per token (XF16), else 1
+
+  // All consumer threads call this together (it has named barriers when XF16).
+  __device__ void load(const FfnArgs& a, int s_begin, int count, int b, bool vb, float* xmax_smem, int cw,
+                       int lane, int nthreads) {
+#pragma unroll
+    for (int q = 0; q < kNT; ++q) {
+      pw[q] = 1.f;
+      float v[32];
+      if (q < count && vb) {
+        const int slot = s_begin + q;
+        if (MODE == 0) {
+          const size_t base = (size_t)(a.pair_ids[slot] / a.k) * a.d + (size_t)b * 32;
+          if (a.x_dtype == MOE_BF16) {
+            const uint4* px = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + base);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint4 w = px[u];
+              const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                v[8 * u + 2 * j] = __uint_as_float(w4[j] << 16);
+                v[8 * u + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+              }
+            }
+          } else {
+            const float4* px = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + base);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 f = px[u];
+              v[4 * u] = f.x;
+              v[4 * u + 1] = f.y;
+              v[4 * u + 2] = f.z;
+              v[4 * u + 3] = f.w;
+            }
+          }
+        } else {
+          const float4* ph = reinterpret_cast<const float4*>(a.h + (size_t)slot * a.ff + (size_t)b * 32);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 f = ph[u];
+            v[4 * u] = f.x;
+            v[4 * u + 1] = f.y;
+            v[4 * u + 2] = f.z;
+            v[4 * u + 3] = f.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      if (XF16) {
+        // per-token max |x| over the whole row: lane -> warp -> CTA
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) xmax_smem[cw * kNT + q] = m;
+        named_bar_sync(2, nthreads);
+        float mx = 0.f;
+        for (int w = 0; w < nthreads / 32; ++w) mx = fmaxf(mx, xmax_smem[w * kNT + q]);
+        named_bar_sync(2, nthreads);
+        int s = 0;
+        if (mx > 0.f && mx < INFINITY) s = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 - 14;
+        s = max(-100, min(100, s));
+        pw[q] = pow2f(s);
+        const float inv = pow2f(-s);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xh[XF16 ? q : 0][j] = __half_as_ushort(__float2half_rn(v[j] * inv));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xf[XF16 ? 0 : q][j] = v[j];
+      }
+    }
+  }
+};
+
+// The RPG rows of one warp group of a staged half tile, NT tokens: block
+// partial sums scaled by the rows' E8M0 scales (and 2^s).
+template <int RPG, int NT, bool XF16, int MODE>
+__device__ __forceinline__ void group_rows(const uint8_t* codes, const uint8_t* scales, int K,
+                                           const Inputs<MODE, XF16>& in, bool vb, float (&acc)[RPG][kNT]) {
+#pragma unroll
+  for (int r = 0; r < RPG; ++r) {
+#pragma unroll
+    for (int q = 0; q < kNT; ++q) acc[r][q] = 0.f;
+    if (vb) {
+      const uint4 q4 = *reinterpret_cast<const uint4*>(codes + (size_t)r * (K / 2));
+      const float sc = e8m0_to_f32(scales[(size_t)r * (K / 32)]);
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        if (XF16)
+          acc[r][q] = dot32_f16(q4, in.xh[XF16 ? q : 0]) * (sc * in.pw[q]);
+        else
+          acc[r][q] = dot32_f32(q4, in.xf[XF16 ? 0 : q]) * sc;
+      }
+    }
+  }
+}
+
+// Warps: G*W consumers (group grp = cw / W takes rows RPG*grp .. of each half
+// tile, RPG = 16 / G; wk = cw % W is the lane blocks' K group), then one
+// producer warp.  At most 16 warps, so every thread may hold 128 registers.
+template <int MODE, bool XF16, int G>
+__global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a, const Geom g) {
+  constexpr int RPG = 16 / G;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)g.stages * g.stage_bytes);
   uint64_t* empty = full + kMaxStages;
-  float* red = reinterpret_cast<float*>(empty + kMaxStages);  // [warps][2][16][kTokChunk]
-  __shared__ int abort_flag;
+  float* red = reinterpret_cast<float*>(empty + kMaxStages);  // [2][W][2][16][kNT]
+  float* xmax = red + 2 * g.warps * 2 * 16 * kNT;             // [2W][kNT]
+  // Tile index (1-based) at which a consumer wait first timed out; consumers
+  // compare it with their current tile after the per-pass barrier, so all of
+  // them leave at the same tile even if another wait times out later.
+  __shared__ int abort_tile;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = g.warps;
+  const int NC = G * W;  // consumer warps
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], W);
+      mbar_init(&empty[s], NC);
     }
-    abort_flag = 0;
+    abort_tile = 0x7fffffff;
     fence_mbar_init();
   }
   __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
 
-  const int n_act = a.active[0];
-  const int total = n_act * g.tpe;
+  const long long total = (long long)a.active[0] * g.tpe;
+  const int t_begin = (int)(total * blockIdx.x / gridDim.x);
+  const int t_end = (int)(total * (blockIdx.x + 1) / gridDim.x);
 
-  if (warp == W) {
+  if (warp == NC) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int it = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const int e = a.active[1 + tile / g.tpe];
-        const uint8_t* rec = a.records[e];
-        if (!record_ok(rec)) {
-          dev_error(a.err, rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG, e);
-          continue;
+      int it = 0, cur_a = -1, e = -1;
+      const uint8_t* rec = nullptr;
+      for (int tile = t_begin; tile < t_end; ++tile) {
+        const int ai = tile / g.tpe;
+        if (ai != cur_a) {
+          cur_a = ai;
+          e = a.active[1 + ai];
+          rec = a.records[e];
+          if (!record_ok(rec)) dev_error(a.err, rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG, e);
         }
+        if (!record_ok(rec)) continue;
         const int stage = it % g.stages, n = it / g.stages;
         if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) break;  // consumers time out too
-        if (*(volatile int*)&abort_flag) break;
+        if (*(volatile int*)&abort_tile != 0x7fffffff) break;
         const uint8_t* src[4];
-        tile_sources<MODE>(a, rec, tile % g.tpe, g, src);
+        tile_sources<MODE>(a, rec, tile % g.tpe, src);
         uint8_t* dst = smem + (size_t)stage * g.stage_bytes;
         mbar_arrive_expect_tx(&full[stage], 2 * (g.half_codes + g.half_scales));
         bulk_g2s(dst, src[0], g.half_codes, &full[stage]);
@@ -175,102 +328,64 @@ __global__ void __launch_bounds__(9 * 32) mxfp4_gemv_kernel(const FfnArgs a, con
   }
 
   // -------------------------------------------------------------- consumers
+  const int cw = warp, grp = cw / W, wk = cw % W;
   const int half = lane >> 4;
-  const int b = warp * 16 + (lane & 15);
+  const int b = wk * 16 + (lane & 15);
   const bool vb = b < g.nblk;
   const int K = g.K;
-  const int nthreads = W * 32;
-  int it = 0;
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const int e = a.active[1 + tile / g.tpe];
-    if (!record_ok(a.records[e])) continue;
+  const int nthreads = NC * 32;
+  Inputs<MODE, XF16> in;
+  int it = 0, buf = 0, cur_a = -1, s0 = 0, ne = 0;
+  bool rec_good = false;
+  for (int tile = t_begin; tile < t_end; ++tile) {
+    const int ai = tile / g.tpe;
+    if (ai != cur_a) {  // a new expert: its slots, and its inputs if they fit the register cache
+      cur_a = ai;
+      const int e = a.active[1 + ai];
+      rec_good = record_ok(a.records[e]);
+      s0 = a.offsets[e];
+      ne = a.offsets[e + 1] - s0;
+      if (rec_good && ne <= kNT) in.load(a, s0, ne, b, vb, xmax, cw, lane, nthreads);
+    }
+    if (!rec_good) continue;
     const int rt = tile % g.tpe;
     const int stage = it % g.stages, n = it / g.stages;
     ++it;
-    // A timed-out wait is recorded before the barrier, so every consumer warp
-    // reads the same flag after it and they leave the loop together (the
-    // producer never writes this flag).
-    if (!mbar_wait(&full[stage], n & 1, a.err)) atomicExch(&abort_flag, 1);
-    named_bar_sync(1, nthreads);
-    if (*(volatile int*)&abort_flag) break;
+    if (!mbar_wait(&full[stage], n & 1, a.err)) atomicMin(&abort_tile, it);
     const uint8_t* st = smem + (size_t)stage * g.stage_bytes;
-    const uint8_t* codes = st + half * g.half_codes + b * 16;
-    const uint8_t* scales = st + 2 * g.half_codes + half * g.half_scales + b;
-    const int s0 = a.offsets[e];
-    const int ne = a.offsets[e + 1] - s0;
-    for (int c0 = 0; c0 < ne; c0 += kTokChunk) {
-      const int nt = min(kTokChunk, ne - c0);
-      float xin[kTokChunk][32];
+    const uint8_t* codes = st + half * g.half_codes + (size_t)(RPG * grp) * (K / 2) + b * 16;
+    const uint8_t* scales = st + 2 * g.half_codes + half * g.half_scales + (size_t)(RPG * grp) * (K / 32) + b;
+    bool stop = false;
+    for (int c0 = 0; c0 < ne; c0 += kNT) {
+      const int nt = min(kNT, ne - c0);
+      if (ne > kNT) in.load(a, s0 + c0, nt, b, vb, xmax, cw, lane, nthreads);
+      float acc[RPG][kNT];
+      if (nt == 1)
+        group_rows<RPG, 1, XF16, MODE>(codes, scales, K, in, vb, acc);
+      else
+        group_rows<RPG, kNT, XF16, MODE>(codes, scales, K, in, vb, acc);
+      reduce_rows<RPG, kNT>(acc, lane);
+      float* rb = red + buf * (W * 2 * 16 * kNT);
+      if (RPG == 16 || (lane & 8) == 0) {
 #pragma unroll
-      for (int q = 0; q < kTokChunk; ++q) {
-        if (q < nt && vb) {
-          const int slot = s0 + c0 + q;
-          if (MODE == 0) {
-            const size_t base = (size_t)(a.pair_ids[slot] / a.k) * a.d + (size_t)b * 32;
-            if (a.x_dtype == MOE_BF16) {
-              const uint4* px = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + base);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const uint4 u = px[v];
-                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  xin[q][8 * v + 2 * j] = __uint_as_float(w4[j] << 16);
-                  xin[q][8 * v + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
-                }
-              }
-            } else {
-              const float4* px = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + base);
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 f = px[v];
-                xin[q][4 * v] = f.x;
-                xin[q][4 * v + 1] = f.y;
-                xin[q][4 * v + 2] = f.z;
-                xin[q][4 * v + 3] = f.w;
-              }
-            }
-          } else {
-            const float4* ph = reinterpret_cast<const float4*>(a.h + (size_t)slot * a.ff + (size_t)b * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 f = ph[v];
-              xin[q][4 * v] = f.x;
-              xin[q][4 * v + 1] = f.y;
-              xin[q][4 * v + 2] = f.z;
-              xin[q][4 * v + 3] = f.w;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) xin[q][j] = 0.f;
-        }
+        for (int q = 0; q < kNT; ++q)
+          rb[(((wk * 2 + half) * 16) + RPG * grp + (lane & (RPG - 1))) * kNT + q] = acc[0][q];
       }
-      float acc[16][kTokChunk];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        if (vb) {
-          const uint4 q4 = *reinterpret_cast<const uint4*>(codes + (size_t)r * (K / 2));
-          const float sc = e8m0_to_f32(scales[(size_t)r * (K / 32)]);
-#pragma unroll
-          for (int q = 0; q < kTokChunk; ++q) acc[r][q] = dot32(q4, xin[q]) * sc;
-        } else {
-#pragma unroll
-          for (int q = 0; q < kTokChunk; ++q) acc[r][q] = 0.f;
-        }
-      }
-      reduce_scatter16<kTokChunk>(acc, lane);
-#pragma unroll
-      for (int q = 0; q < kTokChunk; ++q) red[(((warp * 2 + half) * 16) + (lane & 15)) * kTokChunk + q] = acc[0][q];
+      // one barrier per pass: it publishes rb, and a timed-out wait recorded
+      // before it makes every consumer warp leave together
       named_bar_sync(1, nthreads);
+      if (*(volatile int*)&abort_tile <= it) {
+        stop = true;
+        break;
+      }
       const int tid = threadIdx.x;
       if (MODE == 0) {
         for (int idx = tid; idx < 16 * nt; idx += nthreads) {
           const int r = idx & 15, q = idx >> 4;
           float gsum = 0.f, usum = 0.f;
           for (int w = 0; w < W; ++w) {
-            gsum += red[(((w * 2 + 0) * 16) + r) * kTokChunk + q];
-            usum += red[(((w * 2 + 1) * 16) + r) * kTokChunk + q];
+            gsum += rb[(((w * 2 + 0) * 16) + r) * kNT + q];
+            usum += rb[(((w * 2 + 1) * 16) + r) * kNT + q];
           }
           a.h[(size_t)(s0 + c0 + q) * a.ff + (size_t)rt * 16 + r] = act_fn(gsum, usum, a.act);
         }
@@ -278,13 +393,14 @@ __global__ void __launch_bounds__(9 * 32) mxfp4_gemv_kernel(const FfnArgs a, con
         for (int idx = tid; idx < 32 * nt; idx += nthreads) {
           const int r = idx & 15, hf = (idx >> 4) & 1, q = idx >> 5;
           float ysum = 0.f;
-          for (int w = 0; w < W; ++w) ysum += red[(((w * 2 + hf) * 16) + r) * kTokChunk + q];
+          for (int w = 0; w < W; ++w) ysum += rb[(((w * 2 + hf) * 16) + r) * kNT + q];
           const int pair = a.pair_ids[s0 + c0 + q];
           a.y_pairs[(size_t)pair * a.d + (size_t)rt * 32 + hf * 16 + r] = ysum;
         }
       }
-      named_bar_sync(1, nthreads);
+      buf ^= 1;  // the next pass writes the other buffer; this one is read-safe until the barrier after it
     }
+    if (stop) break;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -299,11 +415,24 @@ Geom make_geom(int mode, int d, int ff) {
   g.half_codes = 16u * (uint32_t)g.K / 2u;
   g.half_scales = 16u * (uint32_t)g.K / 32u;
   g.stage_bytes = 2u * (g.half_codes + g.half_scales);
-  const size_t fixed = 2 * kMaxStages * sizeof(uint64_t) + (size_t)g.warps * 2 * 16 * kTokChunk * sizeof(float);
+  const size_t fixed = 2 * kMaxStages * sizeof(uint64_t) + (size_t)2 * g.warps * 2 * 16 * kNT * sizeof(float) +
+                       (size_t)2 * g.warps * kNT * sizeof(float);
   g.stages = (int)((kSmemBudget - fixed) / g.stage_bytes);
   if (g.stages > kMaxStages) g.stages = kMaxStages;
   g.smem = (size_t)g.stages * g.stage_bytes + fixed;
   return g;
+}
+
+template <int MODE, bool XF16>
+cudaError_t launch_one(const FfnArgs& a, const Geom& g, int num_sms, bool pdl, cudaStream_t s, const char* name) {
+  if (2 * g.warps + 1 <= 16) {  // two row groups (K <= 3584)
+    ensure_smem(mxfp4_gemv_kernel<MODE, XF16, 2>, g.smem);
+    return launch(name, mxfp4_gemv_kernel<MODE, XF16, 2>, dim3(num_sms), dim3((2 * g.warps + 1) * 32), g.smem, s,
+                  pdl, a, g);
+  }
+  ensure_smem(mxfp4_gemv_kernel<MODE, XF16, 1>, g.smem);
+  return launch(name, mxfp4_gemv_kernel<MODE, XF16, 1>, dim3(num_sms), dim3((g.warps + 1) * 32), g.smem, s, pdl, a,
+                g);
 }
 
 }  // namespace
@@ -312,11 +441,10 @@ cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream
   if (a.T == 0) return cudaSuccess;
   const Geom g0 = make_geom(0, a.d, a.ff), g1 = make_geom(1, a.d, a.ff);
   if (g0.stages < 2 || g1.stages < 2) return cudaErrorInvalidValue;
-  cudaFuncSetAttribute(mxfp4_gemv_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g0.smem);
-  cudaFuncSetAttribute(mxfp4_gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g1.smem);
-  cudaError_t err = launch("mxfp4_gate_up", mxfp4_gemv_kernel<0>, dim3(num_sms), dim3((g0.warps + 1) * 32), g0.smem, s, pdl, a, g0);
+  cudaError_t err = a.x_dtype == MOE_BF16 ? launch_one<0, true>(a, g0, num_sms, pdl, s, "mxfp4_gate_up")
+                                          : launch_one<0, false>(a, g0, num_sms, pdl, s, "mxfp4_gate_up");
   if (err != cudaSuccess) return err;
-  return launch("mxfp4_down", mxfp4_gemv_kernel<1>, dim3(num_sms), dim3((g1.warps + 1) * 32), g1.smem, s, true, a, g1);
+  return launch_one<1, false>(a, g1, num_sms, true, s, "mxfp4_down");
 }
 
 }  // namespace moe

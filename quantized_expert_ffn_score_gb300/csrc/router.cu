@@ -19,15 +19,15 @@ namespace {
 
 constexpr int kLogitWarps = 8;
 constexpr int kTokTile = 4;
+constexpr int kLoadBatch = 16;  // 16-byte chunks each lane has in flight
 
 template <typename T>
-struct Vec16;  // 16 bytes of weights as floats
+struct Vec16;  // 16 bytes of router weights as floats
 template <>
 struct Vec16<uint16_t> {
   static constexpr int N = 8;
-  __device__ static void load(const void* base, size_t elem, float* out) {
-    uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem));
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  __device__ static void unpack(const uint4 v, float* out) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       out[2 * i] = __uint_as_float(w[i] << 16);
@@ -38,18 +38,47 @@ struct Vec16<uint16_t> {
 template <>
 struct Vec16<float> {
   static constexpr int N = 4;
-  __device__ static void load(const void* base, size_t elem, float* out) {
-    float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem));
-    out[0] = v.x;
-    out[1] = v.y;
-    out[2] = v.z;
-    out[3] = v.w;
+  __device__ static void unpack(const uint4 v, float* out) {
+    out[0] = __uint_as_float(v.x);
+    out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z);
+    out[3] = __uint_as_float(v.w);
   }
 };
 
+// Stages x[t0 .. t0+nt) into shared memory as fp32, 8 (bf16) or 4 (fp32)
+// elements per 16-byte load.
+__device__ __forceinline__ void stage_x(const RouteArgs& a, int t0, int nt, float* xs) {
+  const int d = a.d;
+  if (a.x_dtype == MOE_BF16) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)t0 * d);
+    for (int i = threadIdx.x; i < nt * d / 8; i += blockDim.x) {
+      const uint4 v = src[i];
+      float4* dst = reinterpret_cast<float4*>(xs + 8 * i);
+      dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+      dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                           __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t0 * d);
+    for (int i = threadIdx.x; i < nt * d / 4; i += blockDim.x) reinterpret_cast<float4*>(xs)[i] = src[i];
+  }
+}
+
+// Error-free transformation (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
 // One warp per expert row, up to kTokTile tokens per CTA (x staged in shared
-// memory as fp32).  Each lane keeps one accumulator per element position of
-// its 16-byte chunk; the depth of the summation tree is d/(32N) + log2(N) + 5.
+// memory as fp32).  Lane chunk c covers columns (32c + lane) * N .. + N, and
+// the lane keeps one accumulator per element position of its chunk, so the
+// depth of the summation tree is ceil(d/(32N)) + log2(N) + 5.  The weights do
+// not depend on the previous kernel, so a lane issues the loads of its first
+// kLoadBatch chunks before waiting for it.
 template <typename WT>
 __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteArgs a) {
   extern __shared__ float xs[];  // [kTokTile][d]
@@ -58,9 +87,16 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   const int t0 = blockIdx.y * kTokTile;
   const int nt = min(kTokTile, a.T - t0);
   const int d = a.d;
+  const int e = blockIdx.x * kLogitWarps + warp;
+  const int nch = d / (32 * N);        // whole warp-wide chunk rows
+  const int rem = d - nch * 32 * N;    // columns left over (a multiple of N)
+  uint4 wv[kLoadBatch];
+  const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)(e < a.E ? e : 0) * d);
+#pragma unroll
+  for (int u = 0; u < kLoadBatch; ++u)
+    if (e < a.E && u < nch) wv[u] = __ldg(wrow + u * 32 + lane);
   pdl_wait();
-  for (int i = threadIdx.x; i < nt * d; i += blockDim.x)
-    xs[i] = load_act(a.x, a.x_dtype, (size_t)t0 * d + i);
+  stage_x(a, t0, nt, xs);
   __syncthreads();
   if (blockIdx.x == 0 && warp < nt) {  // ||x_t||_2
     float s = 0.f;
@@ -69,7 +105,6 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) a.nrm_x[t0 + warp] = sqrtf(s);
   }
-  const int e = blockIdx.x * kLogitWarps + warp;
   if (e >= a.E) return;
   float acc[kTokTile][N];
 #pragma unroll
@@ -77,10 +112,9 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
 #pragma unroll
     for (int m = 0; m < N; ++m) acc[t][m] = 0.f;
   float sq = 0.f;
-  const size_t row = (size_t)e * d;
-  for (int c = lane * N; c < d; c += 32 * N) {
+  auto consume = [&](const uint4 raw, int c) {
     float w[N];
-    Vec16<WT>::load(a.w, row + c, w);
+    Vec16<WT>::unpack(raw, w);
 #pragma unroll
     for (int m = 0; m < N; ++m) sq = fmaf(w[m], w[m], sq);
 #pragma unroll
@@ -89,7 +123,7 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
         const float4* xv = reinterpret_cast<const float4*>(xs + t * d + c);  // d, c multiples of 4
 #pragma unroll
         for (int q = 0; q < N / 4; ++q) {
-          float4 x4 = xv[q];
+          const float4 x4 = xv[q];
           acc[t][4 * q + 0] = fmaf(w[4 * q + 0], x4.x, acc[t][4 * q + 0]);
           acc[t][4 * q + 1] = fmaf(w[4 * q + 1], x4.y, acc[t][4 * q + 1]);
           acc[t][4 * q + 2] = fmaf(w[4 * q + 2], x4.z, acc[t][4 * q + 2]);
@@ -97,12 +131,25 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
         }
       }
     }
+  };
+#pragma unroll
+  for (int u = 0; u < kLoadBatch; ++u)
+    if (u < nch) consume(wv[u], (u * 32 + lane) * N);
+  for (int cb = kLoadBatch; cb < nch; cb += kLoadBatch) {
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (cb + u < nch) wv[u] = __ldg(wrow + (cb + u) * 32 + lane);
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (cb + u < nch) consume(wv[u], ((cb + u) * 32 + lane) * N);
   }
+  if (lane * N < rem) consume(__ldg(wrow + nch * 32 + lane), (nch * 32 + lane) * N);
   if (blockIdx.y == 0) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
     if (lane == 0) a.nrm_w[e] = sqrtf(sq);
   }
+  pdl_launch_dependents();
   const float b = a.bias ? a.bias[e] : 0.f;
 #pragma unroll
   for (int t = 0; t < kTokTile; ++t) {
@@ -118,13 +165,91 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   }
 }
 
-// ---------------------------------------------------------------- top-k
-constexpr int kTopkThreads = 128;
+// Compensated variant (used for small T): per lane and token a running sum s,
+// the exact rounding errors of the products and of the sums accumulated in c
+// (Dot2 of Ogita, Rump and Oishi), and sum|p|; lanes merge with TwoSum.  Writes
+// logits = fl(fl(s + c) + bias) and absdot = sum|p|.
+template <typename WT>
+__global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(RouteArgs a) {
+  extern __shared__ float xs[];  // [kTokTile][d]
+  constexpr int N = Vec16<WT>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.y * kTokTile;
+  const int nt = min(kTokTile, a.T - t0);
+  const int d = a.d;
+  const int e = blockIdx.x * kLogitWarps + warp;
+  const int nch = d / (32 * N);
+  const int rem = d - nch * 32 * N;
+  uint4 wv[kLoadBatch];
+  const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)(e < a.E ? e : 0) * d);
+#pragma unroll
+  for (int u = 0; u < kLoadBatch; ++u)
+    if (e < a.E && u < nch) wv[u] = __ldg(wrow + u * 32 + lane);
+  pdl_wait();
+  stage_x(a, t0, nt, xs);
+  __syncthreads();
+  if (e >= a.E) return;
+  float s[kTokTile], c[kTokTile], sa[kTokTile];
+#pragma unroll
+  for (int t = 0; t < kTokTile; ++t) s[t] = c[t] = sa[t] = 0.f;
+  auto consume = [&](const uint4 raw, int col) {
+    float w[N];
+    Vec16<WT>::unpack(raw, w);
+#pragma unroll
+    for (int t = 0; t < kTokTile; ++t) {
+      if (t < nt) {
+        const float* xr = xs + t * d + col;
+#pragma unroll
+        for (int m = 0; m < N; ++m) {
+          const float p = __fmul_rn(w[m], xr[m]);
+          const float ep = __fmaf_rn(w[m], xr[m], -p);
+          float t2, es;
+          two_sum(s[t], p, t2, es);
+          s[t] = t2;
+          c[t] = __fadd_rn(c[t], __fadd_rn(es, ep));
+          sa[t] = __fadd_rn(sa[t], fabsf(p));
+        }
+      }
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < kLoadBatch; ++u)
+    if (u < nch) consume(wv[u], (u * 32 + lane) * N);
+  for (int cb = kLoadBatch; cb < nch; cb += kLoadBatch) {
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (cb + u < nch) wv[u] = __ldg(wrow + (cb + u) * 32 + lane);
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (cb + u < nch) consume(wv[u], ((cb + u) * 32 + lane) * N);
+  }
+  if (lane * N < rem) consume(__ldg(wrow + nch * 32 + lane), (nch * 32 + lane) * N);
+  pdl_launch_dependents();
+  const float b = a.bias ? a.bias[e] : 0.f;
+#pragma unroll
+  for (int t = 0; t < kTokTile; ++t) {
+    if (t >= nt) break;
+    float st = s[t], ct = c[t], at = sa[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float s2 = __shfl_xor_sync(0xffffffffu, st, o);
+      const float c2 = __shfl_xor_sync(0xffffffffu, ct, o);
+      at = __fadd_rn(at, __shfl_xor_sync(0xffffffffu, at, o));
+      float t2, es;
+      two_sum(st, s2, t2, es);
+      st = t2;
+      ct = __fadd_rn(__fadd_rn(ct, c2), es);
+    }
+    if (lane == 0) {
+      a.logits[(size_t)(t0 + t) * a.E + e] = __fadd_rn(__fadd_rn(st, ct), b);
+      a.absdot[(size_t)(t0 + t) * a.E + e] = at;
+    }
+  }
+}
 
-struct Key {  // ordering (value descending, index ascending)
-  double v;
-  int e;
-};
+// ---------------------------------------------------------------- top-k
+constexpr int kTopkThreads = 256;
+
 __device__ __forceinline__ bool better(double v1, int e1, double v2, int e2) {
   return v1 > v2 || (v1 == v2 && e1 < e2);
 }
@@ -134,32 +259,119 @@ __device__ __forceinline__ double load_d(const void* p, int dtype, size_t i) {
   return (double)static_cast<const float*>(p)[i];
 }
 
-// fp64 logit by one warp: lanes take i = lane, lane+32, ... sequentially, then
-// a shuffle tree.  Returns the value and sum |w_i x_i| (both on every lane).
-__device__ void logit_fp64_warp(const RouteArgs& a, int t, int e, double* val, double* abs_sum) {
+// Eight consecutive elements i0 .. i0+7 (i0 a multiple of 8) of a bf16 or fp32
+// row as doubles, with one or two 16-byte loads.
+__device__ __forceinline__ void load8_d(const void* p, int dtype, size_t i0, double (&v)[8]) {
+  if (dtype == MOE_BF16) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + i0));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = (double)__uint_as_float(w[j] << 16);
+      v[2 * j + 1] = (double)__uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i0);
+    const float4 f0 = __ldg(q), f1 = __ldg(q + 1);
+    v[0] = f0.x, v[1] = f0.y, v[2] = f0.z, v[3] = f0.w;
+    v[4] = f1.x, v[5] = f1.y, v[6] = f1.z, v[7] = f1.w;
+  }
+}
+
+// The same eight elements as fp32 (exact for bf16 and fp32 inputs).
+__device__ __forceinline__ void load8_f(const void* p, int dtype, size_t i0, float (&v)[8]) {
+  if (dtype == MOE_BF16) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + i0));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i0);
+    const float4 f0 = __ldg(q), f1 = __ldg(q + 1);
+    v[0] = f0.x, v[1] = f0.y, v[2] = f0.z, v[3] = f0.w;
+    v[4] = f1.x, v[5] = f1.y, v[6] = f1.z, v[7] = f1.w;
+  }
+}
+
+constexpr int kGroupsInFlight = 4;  // 8-element groups a lane loads before summing them
+
+// Compensated fp32 logit by one warp (the Dot2 scheme of Ogita, Rump and Oishi,
+// "Accurate sum and dot product", 2005): every rounding error of the products
+// and of the running sums is captured exactly and summed separately, lanes are
+// merged with TwoSum.  With n = d terms, the result val (returned in fp64 with
+// the bias added) satisfies |val - exact| <= u|val| + gamma_n^2 sum|w_i x_i|;
+// abs_sum receives that sum in fp32 (relative error <= gamma_n).
+__device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, double* abs_sum) {
   const int lane = threadIdx.x & 31;
-  double s = 0.0, sa = 0.0;
+  float s = 0.f, c = 0.f, sa = 0.f;
   const size_t xr = (size_t)t * a.d, wr = (size_t)e * a.d;
-  for (int i = lane; i < a.d; i += 32) {
-    double p = load_d(a.w, a.w_dtype, wr + i) * load_d(a.x, a.x_dtype, xr + i);
-    s += p;
-    sa += fabs(p);
+  const int ng = a.d / 8;
+  for (int g0 = lane; g0 < ng; g0 += 32 * kGroupsInFlight) {
+    float w[kGroupsInFlight][8], x[kGroupsInFlight][8];
+#pragma unroll
+    for (int u = 0; u < kGroupsInFlight; ++u) {
+      const int g = g0 + 32 * u;
+      if (g < ng) {
+        load8_f(a.w, a.w_dtype, wr + 8 * (size_t)g, w[u]);
+        load8_f(a.x, a.x_dtype, xr + 8 * (size_t)g, x[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroupsInFlight; ++u) {
+      if (g0 + 32 * u >= ng) break;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wf = w[u][j], xf = x[u][j];
+        const float p = __fmul_rn(wf, xf);
+        const float ep = __fmaf_rn(wf, xf, -p);  // p + ep == wf * xf exactly
+        float t2, es;
+        two_sum(s, p, t2, es);
+        s = t2;
+        c = __fadd_rn(c, __fadd_rn(es, ep));
+        sa = __fadd_rn(sa, fabsf(p));
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    s += __shfl_xor_sync(0xffffffffu, s, o);
-    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+    sa = __fadd_rn(sa, __shfl_xor_sync(0xffffffffu, sa, o));
+    float t2, es;
+    two_sum(s, s2, t2, es);
+    s = t2;
+    c = __fadd_rn(__fadd_rn(c, c2), es);
   }
-  *val = s + (a.bias ? (double)a.bias[e] : 0.0);
+  *val = (double)s + (double)c + (a.bias ? (double)a.bias[e] : 0.0);
   *abs_sum = sa;
 }
 
 // The reference arithmetic itself: sequential fp64 sum in ascending i, then the
-// bias.  Every product is exact in fp64, so fma equals multiply-then-add.
+// bias.  Every product is exact in fp64, so fma equals multiply-then-add.  The
+// loads run ahead of the sum in 8-element groups.
 __device__ double logit_fp64_sequential(const RouteArgs& a, int t, int e) {
   double s = 0.0;
   const size_t xr = (size_t)t * a.d, wr = (size_t)e * a.d;
-  for (int i = 0; i < a.d; ++i) s = fma(load_d(a.w, a.w_dtype, wr + i), load_d(a.x, a.x_dtype, xr + i), s);
+  const int ng = a.d / 8;
+  for (int g0 = 0; g0 < ng; g0 += kGroupsInFlight) {
+    double w[kGroupsInFlight][8], x[kGroupsInFlight][8];
+#pragma unroll
+    for (int u = 0; u < kGroupsInFlight; ++u) {
+      if (g0 + u < ng) {
+        load8_d(a.w, a.w_dtype, wr + 8 * (size_t)(g0 + u), w[u]);
+        load8_d(a.x, a.x_dtype, xr + 8 * (size_t)(g0 + u), x[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroupsInFlight; ++u) {
+      if (g0 + u >= ng) break;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s = fma(w[u][j], x[u][j], s);
+    }
+  }
   if (a.bias) s += (double)a.bias[e];
   return s;
 }
@@ -169,192 +381,289 @@ __device__ __forceinline__ double gamma64(int n) {
   return n * u / (1.0 - n * u);
 }
 
-// One CTA per token.
-// Dynamic shared memory layout for E experts (topk_smem_bytes).
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kSlicePerLane = (kMaxE + kTopkThreads - 1) / kTopkThreads;  // logits per thread
+
+// Dynamic shared memory for E experts.
 __host__ __device__ inline size_t topk_smem_bytes(int E) {
-  size_t e8 = ((size_t)E + 7) / 8 * 8;
-  return e8 * (2 * sizeof(double) + 3 * sizeof(float) + 2);
+  const size_t e8 = ((size_t)E + 7) / 8 * 8;
+  return e8 * (2 * sizeof(double) + 2 * sizeof(float) + sizeof(int) + 2);
 }
 
+// (v1, e1) before (v2, e2): larger value first, then lower index.
+__device__ __forceinline__ bool before(float v1, int e1, float v2, int e2) {
+  return v1 > v2 || (v1 == v2 && e1 < e2);
+}
+
+// Order-preserving unsigned image of an fp32 value (larger value, larger key).
+__device__ __forceinline__ uint32_t ord_bits(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ float block_max(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  float m = -INFINITY;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, scratch[w]);
+  __syncthreads();
+  return m;
+}
+
+// One CTA per token: a radix select finds the (k+1)-th largest fp32 logit,
+// the k+1 experts at or above it are ordered by counting, and the bounds then
+// certify the selection or send the CTA down the recheck path.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
-  extern __shared__ double dsm[];
-  const size_t e8 = ((size_t)a.E + 7) / 8 * 8;
-  double* clo = dsm;                                              // rare path: candidate bounds
+  extern __shared__ double tsm[];
+  const int E = a.E, k = a.k;
+  const size_t e8 = ((size_t)E + 7) / 8 * 8;
+  double* clo = tsm;  // recheck path: candidate bounds
   double* chi = clo + e8;
-  float* sv = reinterpret_cast<float*>(chi + e8);                 // fp32 logits
-  float* sb = sv + e8;                                            // their error bounds
-  int* cand = reinterpret_cast<int*>(sb + e8);                    // rare path: candidate experts
-  unsigned char* taken = reinterpret_cast<unsigned char*>(cand + e8);
-  unsigned char* cflag = taken + e8;
+  float* sv = reinterpret_cast<float*>(chi + e8);  // fp32 logits
+  float* sb = sv + e8;                             // their error bounds
+  int* cand = reinterpret_cast<int*>(sb + e8);     // recheck path: candidate experts
+  unsigned char* insel = reinterpret_cast<unsigned char*>(cand + e8);
+  unsigned char* cflag = insel + e8;
   __shared__ int sel[kMaxK + 1];
+  __shared__ int candA[kMaxK + 1];
+  __shared__ int hist[256];
+  __shared__ int s_digit, s_need, s_na, s_nb;
   __shared__ int n_cand, certified;
+  __shared__ float scratch[kTopkWarps];
   __shared__ int order[kMaxK];
   __shared__ double oval[kMaxK];
 
   const int t = blockIdx.x;
-  const int E = a.E, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
-  const float nx = a.nrm_x[t];
-  for (int e = tid; e < E; e += blockDim.x) {
-    float v = a.logits[(size_t)t * E + e];
-    sv[e] = v;
-    sb[e] = a.gamma * a.nrm_w[e] * nx + 1.2e-7f * fabsf(v) + 1e-30f;
-    taken[e] = 0;
+  const float nx = a.comp ? 0.f : a.nrm_x[t];
+  // load: thread tid holds experts e = tid + 256 i as order-preserving keys
+  uint32_t key[kSlicePerLane];
+#pragma unroll
+  for (int i = 0; i < kSlicePerLane; ++i) {
+    const int e = tid + kTopkThreads * i;
+    key[i] = 0u;
+    if (e < E) {
+      const float v = a.logits[(size_t)t * E + e];
+      sv[e] = v;
+      sb[e] = a.comp ? a.gamma * a.absdot[(size_t)t * E + e] + 2.4e-7f * fabsf(v) + 1e-30f
+                     : a.gamma * a.nrm_w[e] * nx + 1.2e-7f * fabsf(v) + 1e-30f;
+      insel[e] = 0;
+      key[i] = ord_bits(v);
+    }
   }
-  __syncthreads();
   pdl_launch_dependents();
   const int nsel = min(k + 1, E);
-  if (warp == 0) {
-    for (int j = 0; j < nsel; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-      for (int e = lane; e < E; e += 32)
-        if (!taken[e] && (sv[e] > bv || (sv[e] == bv && e < be))) {
-          bv = sv[e];
-          be = e;
+  // radix select of the nsel-th largest key, 8 bits per pass from the top
+  uint32_t prefix = 0u, mask = 0u;
+  int need = nsel;  // how many keys >= the threshold still to account for at this digit
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kSlicePerLane; ++i)
+      if (tid + kTopkThreads * i < E && (key[i] & mask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+    __syncthreads();
+    if (warp == 0) {  // lane l scans bins 255-8l .. 248-8l, top down
+      int c[8], lsum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        lsum += c[j];
+      }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - lsum;
+      if (excl < need && need <= incl) {
+        int run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= need) {
+            s_digit = 255 - 8 * lane - j;
+            s_need = need - run;
+            break;
+          }
+          run += c[j];
         }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)s_digit << shift;
+    mask |= 255u << shift;
+    need = s_need;
+  }
+  // the selection: every key above the threshold, then the `need` lowest-index
+  // experts whose key equals it
+  if (tid == 0) {
+    s_na = 0;
+    s_nb = 0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kSlicePerLane; ++i) {
+    const int e = tid + kTopkThreads * i;
+    if (e < E) {
+      if (key[i] > prefix) candA[atomicAdd(&s_na, 1)] = e;
+      else if (key[i] == prefix) cand[atomicAdd(&s_nb, 1)] = e;
+    }
+  }
+  __syncthreads();
+  const int na = s_na, nb = s_nb;
+  for (int c = tid; c < nb; c += blockDim.x) {
+    int r = 0;
+    for (int c2 = 0; c2 < nb; ++c2) r += cand[c2] < cand[c];
+    if (r < need) candA[na + r] = cand[c];
+  }
+  __syncthreads();
+  if (tid < nsel) {  // order by (logit descending, index ascending): rank by counting
+    const int e = candA[tid];
+    const float v = sv[e];
+    int r = 0;
+    for (int c2 = 0; c2 < nsel; ++c2) {
+      const int e2 = candA[c2];
+      r += before(sv[e2], e2, v, e);
+    }
+    sel[r] = e;
+  }
+  __syncthreads();
+  if (tid < k) insel[sel[tid]] = 1;
+  __syncthreads();
+  // certification: every outsider's upper bound below the lowest selected lower
+  // bound, and strict separation of consecutive selected experts
+  float hi_out = -INFINITY;
+  for (int e = tid; e < E; e += blockDim.x)
+    if (!insel[e]) hi_out = fmaxf(hi_out, sv[e] + sb[e]);
+  hi_out = block_max(hi_out, scratch);
+  float lo_neg = -INFINITY;  // max of -lo_j: the lowest selected lower bound, negated
+  bool bad = false;
+  if (tid < k) {
+    const int e = sel[tid];
+    const float lo = sv[e] - sb[e];
+    lo_neg = -lo;
+    if (tid + 1 < k) bad = !(lo > sv[sel[tid + 1]] + sb[sel[tid + 1]]);
+  }
+  const float m = -block_max(lo_neg, scratch);
+  const int nbad = __syncthreads_or(bad ? 1 : 0);
+  if (tid == 0) certified = (!nbad && hi_out < m) ? 1 : 0;
+  __syncthreads();
+  if (certified) {
+    if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum
+      const float v0 = sv[sel[0]];
+      const float g = lane < k ? expf(sv[sel[lane]] - v0) : 0.f;
+      float den = g;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (lane < k) {
+        a.topk_idx[(size_t)t * k + lane] = sel[lane];
+        a.gates[(size_t)t * k + lane] = g / den;
+      }
+    }
+    return;
+  }
+
+  // ---- recheck path: every expert that could be in the top k ----------------
+  if (tid == 0) {
+    atomicAdd(a.err + 2, 1);
+    n_cand = 0;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    if (insel[e] || sv[e] + sb[e] >= m) {
+      const int c = atomicAdd(&n_cand, 1);  // list order is irrelevant: the ordering below is total
+      cand[c] = e;
+      clo[c] = (double)sv[e] - (double)sb[e];
+      chi[c] = (double)sv[e] + (double)sb[e];
+    }
+  }
+  __syncthreads();
+  const int n = n_cand;
+  // pass 1: candidates whose interval meets another one's get a compensated value
+  for (int c = tid; c < n; c += blockDim.x) {
+    unsigned char f = 0;
+    for (int c2 = 0; c2 < n; ++c2)
+      if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
+    cflag[c] = f;
+  }
+  __syncthreads();
+  // bound of the compensated sum: gamma_n^2 * sum|p| (sum|p| itself within
+  // gamma_n), u |val|, and the fp64 reference's own error gamma64_d * sum|p|
+  const double u32 = 5.9604644775390625e-8;
+  const double gn = (a.d + 32) * u32 / (1.0 - (a.d + 32) * u32);
+  const double bound_scale = (gn * gn * (1.0 + gn) + gamma64(a.d + 1)) * 1.01;
+  for (int c = warp; c < n; c += kTopkThreads / 32) {
+    if (!cflag[c] || a.comp) continue;  // compensated logits: this level would add nothing
+    double val, sa;
+    logit_dot2_warp(a, t, cand[c], &val, &sa);
+    if (lane == 0) {
+      const double bd = bound_scale * (double)sa + 1.2e-7 * fabs(val) + 1e-30;
+      clo[c] = val - bd;
+      chi[c] = val + bd;
+    }
+  }
+  __syncthreads();
+  // pass 2: still undecided -> the reference's own sequential fp64 sum
+  for (int c = tid; c < n; c += blockDim.x) {
+    unsigned char f = 0;
+    for (int c2 = 0; c2 < n; ++c2)
+      if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
+    cflag[c] = f;
+  }
+  __syncthreads();
+  for (int c = tid; c < n; c += blockDim.x) {
+    if (!cflag[c]) continue;
+    atomicAdd(a.err + 3, 1);
+    const double val = logit_fp64_sequential(a, t, cand[c]);
+    clo[c] = val;
+    chi[c] = val;
+  }
+  __syncthreads();
+  // order the candidates: disjoint intervals order by midpoint; overlapping
+  // ones are now exact and order by value, ties by expert index
+  if (warp == 0) {
+    for (int j = 0; j < k; ++j) {
+      double bvv = -INFINITY;
+      int be = 0x7fffffff, bc = -1;
+      for (int c = lane; c < n; c += 32) {
+        if (cflag[c] == 2) continue;
+        const double mid = 0.5 * (clo[c] + chi[c]);
+        if (bc < 0 || better(mid, cand[c], bvv, be)) {
+          bvv = mid;
+          be = cand[c];
+          bc = c;
+        }
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
+        const double ov = __shfl_xor_sync(0xffffffffu, bvv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (oc >= 0 && (bc < 0 || better(ov, oe, bvv, be))) {
+          bvv = ov;
           be = oe;
+          bc = oc;
         }
       }
       if (lane == 0) {
-        sel[j] = be;
-        taken[be] = 1;
+        order[j] = be;
+        oval[j] = bvv;
+        cflag[bc] = 2;
       }
       __syncwarp();
     }
-    // certification: strict separation of consecutive selected experts, and
-    // every outsider's upper bound below the lowest selected lower bound
-    int ok = 1;
-    float m = INFINITY;
-    for (int j = 0; j < k; ++j) {
-      float lo = sv[sel[j]] - sb[sel[j]];
-      m = fminf(m, lo);
-      if (j + 1 < k && !(lo > sv[sel[j + 1]] + sb[sel[j + 1]])) ok = 0;
-    }
-    float hi_out = -INFINITY;
-    for (int e = lane; e < E; e += 32) {
-      bool in = false;
-      for (int j = 0; j < k; ++j) in |= (sel[j] == e);
-      if (!in) hi_out = fmaxf(hi_out, sv[e] + sb[e]);
-    }
+    const float g = lane < k ? expf((float)(oval[lane] - oval[0])) : 0.f;
+    float den = g;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) hi_out = fmaxf(hi_out, __shfl_xor_sync(0xffffffffu, hi_out, o));
-    if (!(hi_out < m)) ok = 0;
-    if (lane == 0) {
-      certified = ok;
-      for (int j = 0; j < k; ++j) {
-        order[j] = sel[j];
-        oval[j] = (double)sv[sel[j]];
-      }
-    }
-  }
-  __syncthreads();
-
-  if (!certified) {
-    // ---- rare path: candidates that could be in the top-k ----------------
-    if (tid == 0) {
-      float m = INFINITY;
-      for (int j = 0; j < k; ++j) m = fminf(m, sv[sel[j]] - sb[sel[j]]);
-      int n = 0;
-      for (int e = 0; e < E; ++e) {
-        bool in = false;
-        for (int j = 0; j < k; ++j) in |= (sel[j] == e);
-        if (in || sv[e] + sb[e] >= m) {
-          cand[n] = e;
-          clo[n] = (double)sv[e] - (double)sb[e];
-          chi[n] = (double)sv[e] + (double)sb[e];
-          ++n;
-        }
-      }
-      n_cand = n;
-    }
-    __syncthreads();
-    const int n = n_cand;
-    // pass 1: candidates whose interval meets another one's get an fp64 value
-    for (int c = tid; c < n; c += blockDim.x) {
-      unsigned char f = 0;
-      for (int c2 = 0; c2 < n; ++c2)
-        if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
-      cflag[c] = f;
-    }
-    __syncthreads();
-    const double bound_scale = (gamma64(a.d / 32 + 6) + gamma64(a.d + 1)) * 1.001;
-    for (int c = warp; c < n; c += kTopkThreads / 32) {
-      if (!cflag[c]) continue;
-      double v, sa;
-      logit_fp64_warp(a, t, cand[c], &v, &sa);
-      if (lane == 0) {
-        double bd = bound_scale * sa + 4.5e-16 * fabs(v) + 1e-300;
-        clo[c] = v - bd;
-        chi[c] = v + bd;
-      }
-    }
-    __syncthreads();
-    // pass 2: still undecided -> the reference's own sequential fp64 sum
-    for (int c = tid; c < n; c += blockDim.x) {
-      unsigned char f = 0;
-      for (int c2 = 0; c2 < n; ++c2)
-        if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
-      cflag[c] = f;
-    }
-    __syncthreads();
-    for (int c = tid; c < n; c += blockDim.x) {
-      if (!cflag[c]) continue;
-      double v = logit_fp64_sequential(a, t, cand[c]);
-      clo[c] = v;
-      chi[c] = v;
-    }
-    __syncthreads();
-    // order the candidates: disjoint intervals order by midpoint; overlapping
-    // ones are now exact and order by value, ties by expert index
-    if (warp == 0) {
-      for (int j = 0; j < k; ++j) {
-        double bv = -INFINITY;
-        int be = 0x7fffffff, bc = -1;
-        for (int c = lane; c < n; c += 32) {
-          if (cflag[c] == 2) continue;
-          double mid = 0.5 * (clo[c] + chi[c]);
-          if (bc < 0 || better(mid, cand[c], bv, be)) {
-            bv = mid;
-            be = cand[c];
-            bc = c;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-          if (oc >= 0 && (bc < 0 || better(ov, oe, bv, be))) {
-            bv = ov;
-            be = oe;
-            bc = oc;
-          }
-        }
-        if (lane == 0) {
-          order[j] = be;
-          oval[j] = bv;
-          cflag[bc] = 2;
-        }
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-  }
-
-  if (tid == 0) {
-    double den = 0.0;
-    for (int j = 0; j < k; ++j) den += exp(oval[j] - oval[0]);
-    for (int j = 0; j < k; ++j) {
-      a.topk_idx[(size_t)t * k + j] = order[j];
-      a.gates[(size_t)t * k + j] = (float)(exp(oval[j] - oval[0]) / den);
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane < k) {
+      a.topk_idx[(size_t)t * k + lane] = order[lane];
+      a.gates[(size_t)t * k + lane] = g / den;
     }
   }
 }
@@ -364,19 +673,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
 cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s) {
   (void)num_sms;
   if (a.T == 0) return cudaSuccess;
-  dim3 grid((a.E + kLogitWarps - 1) / kLogitWarps, (a.T + kTokTile - 1) / kTokTile);
-  size_t smem = (size_t)kTokTile * a.d * sizeof(float);
+  const dim3 grid((a.E + kLogitWarps - 1) / kLogitWarps, (a.T + kTokTile - 1) / kTokTile);
+  const size_t smem = (size_t)kTokTile * a.d * sizeof(float);
   cudaError_t err;
-  if (a.w_dtype == MOE_BF16) {
-    cudaFuncSetAttribute(router_logits_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (a.comp) {
+    if (a.w_dtype == MOE_BF16) {
+      ensure_smem(router_logits_comp_kernel<uint16_t>, smem);
+      err = launch("router_logits", router_logits_comp_kernel<uint16_t>, grid, dim3(kLogitWarps * 32), smem, s,
+                   false, a);
+    } else {
+      ensure_smem(router_logits_comp_kernel<float>, smem);
+      err = launch("router_logits", router_logits_comp_kernel<float>, grid, dim3(kLogitWarps * 32), smem, s, false,
+                   a);
+    }
+  } else if (a.w_dtype == MOE_BF16) {
+    ensure_smem(router_logits_kernel<uint16_t>, smem);
     err = launch("router_logits", router_logits_kernel<uint16_t>, grid, dim3(kLogitWarps * 32), smem, s, false, a);
   } else {
-    cudaFuncSetAttribute(router_logits_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    ensure_smem(router_logits_kernel<float>, smem);
     err = launch("router_logits", router_logits_kernel<float>, grid, dim3(kLogitWarps * 32), smem, s, false, a);
   }
   if (err != cudaSuccess) return err;
-  size_t tsm = topk_smem_bytes(a.E);
-  cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsm);
+  const size_t tsm = topk_smem_bytes(a.E);
+  ensure_smem(topk_kernel, tsm);
   return launch("topk", topk_kernel, dim3(a.T), dim3(kTopkThreads), tsm, s, true, a);
 }
 

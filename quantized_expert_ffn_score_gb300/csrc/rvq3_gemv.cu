@@ -193,8 +193,8 @@ cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_
   if (a.T == 0) return cudaSuccess;
   const int P = a.T * a.k;
   const RGeom g0 = make_rgeom(0, a.d, a.ff), g1 = make_rgeom(1, a.d, a.ff);
-  cudaFuncSetAttribute(rvq3_unit_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRvqSmem);
-  cudaFuncSetAttribute(rvq3_unit_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRvqSmem);
+  ensure_smem(rvq3_unit_kernel<0>, kRvqSmem);
+  ensure_smem(rvq3_unit_kernel<1>, kRvqSmem);
   const dim3 grid(2 * num_sms);
   cudaError_t err = launch("rvq3_gate_up", rvq3_unit_kernel<0>, grid, dim3(kRvqThreads), kRvqSmem, s, pdl, a, g0);
   if (err != cudaSuccess) return err;

@@ -22,7 +22,7 @@ QUANT = {"mxfp4": 0, "rvq3": 1}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy", "moe_ctx_check", "moe_ctx_num_sms",
-           "moe_ctx_profile", "moe_ctx_profile_read",
+           "moe_ctx_profile", "moe_ctx_profile_read", "moe_ctx_stats",
            "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
            "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
@@ -72,6 +72,8 @@ def lib():
         L.moe_ctx_check.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.moe_ctx_num_sms.argtypes = [vp]
         L.moe_ctx_profile.argtypes, L.moe_ctx_profile.restype = [vp, i32], i32
+        L.moe_ctx_stats.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]
+        L.moe_ctx_stats.restype = i32
         L.moe_ctx_profile_read.argtypes = [vp, vp, i32, ctypes.c_char_p, ctypes.POINTER(i32),
                                            ctypes.POINTER(ctypes.c_double)]
         L.moe_ctx_profile_read.restype = i32
@@ -148,6 +150,12 @@ class Context:
         rc = lib().moe_ctx_check(self.handle, _stream(stream), ctypes.byref(detail))
         if rc != MOE_OK:
             raise MoeError(rc, "device error", detail.value)
+
+    def stats(self, stream=None):
+        """(tokens that needed the fp64 top-k recheck, logits recomputed sequentially) since the last call."""
+        a, b = ctypes.c_longlong(0), ctypes.c_longlong(0)
+        _check(lib().moe_ctx_stats(self.handle, _stream(stream), ctypes.byref(a), ctypes.byref(b)), "moe_ctx_stats")
+        return a.value, b.value
 
     def profile(self, capacity):
         """Turns per-launch event timing on (capacity launches between reads) or off (0)."""

@@ -159,8 +159,11 @@ def test_router_certifies_exact_ties_and_near_ties(lib, ctx):
     topk = torch.empty((T, k), dtype=torch.int32, device="cuda")
     gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
     ws = moe.workspace(moe.route_topk_ws_bytes(T, d, E, k))
+    ctx.stats()
     moe.moe_route_topk(ctx, xd, Wd, None, k, topk, gates, ws)
     ctx.check()
+    fp64_tokens, seq_logits = ctx.stats()
+    assert fp64_tokens > 0 and seq_logits > 0  # both recheck passes ran
     xh = x.view(torch.int16).numpy().view(np.uint16)
     Wh = Wb.view(torch.int16).numpy().view(np.uint16)
     logits, idx, g = oracle.router(xh, Wh, None, k)
