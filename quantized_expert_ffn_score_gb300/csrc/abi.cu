@@ -159,6 +159,7 @@ struct RouteWs {
   float* logits;
   float* nrm_w;
   float* nrm_x;
+  float* max_x;
   float* absdot;
 };
 RouteWs carve_route(Carver& c, int T, int E) {
@@ -166,6 +167,7 @@ RouteWs carve_route(Carver& c, int T, int E) {
   r.logits = c.take<float>((size_t)T * E);
   r.nrm_w = c.take<float>(E);
   r.nrm_x = c.take<float>(T > 0 ? T : 1);
+  r.max_x = c.take<float>(T > 0 ? T : 1);
   r.absdot = c.take<float>(T <= kCompensatedMaxT ? (size_t)T * E : 1);
   return r;
 }
@@ -186,6 +188,7 @@ moe::RouteArgs route_args(const void* x, moe_dtype x_dtype, const void* w, moe_d
   ra.logits = ws.logits;
   ra.nrm_w = ws.nrm_w;
   ra.nrm_x = ws.nrm_x;
+  ra.max_x = ws.max_x;
   ra.absdot = ws.absdot;
   ra.comp = T <= kCompensatedMaxT ? 1 : 0;
   ra.gamma = ra.comp ? router_gamma_comp(d) : router_gamma(d, x_dtype, w_dtype);
@@ -197,12 +200,14 @@ moe::RouteArgs route_args(const void* x, moe_dtype x_dtype, const void* w, moe_d
 
 struct FfnWs {
   int32_t* active;
+  float* max_x;
   float* h;
   float* partial;
 };
 FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   FfnWs f;
   f.active = c.take<int32_t>((size_t)E + 1);
+  f.max_x = c.take<float>(T > 0 ? T : 1);
   f.h = c.take<float>((size_t)T * k * ff);
   f.partial = q == MOE_QUANT_RVQ3 ? c.take<float>(moe::rvq3_partial_floats(T, k, d, ff)) : nullptr;
   return f;
@@ -268,6 +273,7 @@ moe::FfnArgs ffn_args(const moe_ctx* ctx, const void* x, moe_dtype x_dtype, int 
   a.offsets = offsets;
   a.pair_ids = pair_ids;
   a.active = w.active;
+  a.max_x = w.max_x;
   a.h = w.h;
   a.partial = w.partial;
   a.y_pairs = y_pairs;
@@ -291,6 +297,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   if (st != MOE_OK) return st;
   moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, L->k, L->d, L->ff, L->E, L->act, w.offsets, w.pairs, w.y_pairs,
                              w.ffn);
+  fa.max_x = w.route.max_x;  // computed by the router kernel
   if (L->quant == MOE_QUANT_MXFP4) {
     fa.records = L->mxfp4.records;
     st = cuda_status(moe::launch_mxfp4_ffn(fa, ctx->num_sms, true, s));
@@ -555,6 +562,8 @@ moe_status moe_expert_ffn_mxfp4(moe_ctx* ctx, const void* x, moe_dtype x_dtype, 
   a.records = experts->records;
   st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), false,
                                                    stream));
+  if (st != MOE_OK) return st;
+  st = cuda_status(moe::launch_token_absmax(x, x_dtype, T, experts->d, const_cast<float*>(a.max_x), true, stream));
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_mxfp4_ffn(a, ctx->num_sms, true, stream));
 }

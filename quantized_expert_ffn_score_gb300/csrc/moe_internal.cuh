@@ -127,6 +127,7 @@ struct RouteArgs {
   float* logits;  // [T][E]   workspace
   float* nrm_w;   // [E]      workspace: ||W_e||_2
   float* nrm_x;   // [T]      workspace: ||x_t||_2
+  float* max_x;   // [T]      workspace: max_i |x_t[i]|
   float* absdot;  // [T][E]   workspace: sum_i |W[e][i] x[t][i]| (compensated logits only)
   int comp;       // logits by compensated (Dot2) sums; bounds from absdot
   float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
@@ -157,6 +158,7 @@ struct FfnArgs {
   const int32_t* offsets;
   const int32_t* pair_ids;
   const int32_t* active;  // active[0] = n_active, then the expert ids
+  const float* max_x;     // [T] max_i |x_t[i]| (bf16 activations are rescaled by a power of two from it)
   float* h;               // [T*k][ff] workspace, slot order
   float* y_pairs;         // [T*k][d] by pair id
   float* partial;         // RVQ3 only: K-slice partial sums (workspace)
@@ -164,6 +166,7 @@ struct FfnArgs {
 };
 cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s);
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
+cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float* max_x, bool pdl, cudaStream_t s);
 cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 size_t rvq3_partial_floats(int T, int k, int d, int ff);
 

@@ -63,7 +63,7 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
 // pair (exact products, fp32 sums); fp32 inputs: the f16 pair widened to fp32.
 __device__ __forceinline__ float dot32_f16(const uint4 q, const unsigned short* x) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float s0 = 0.f, s1 = 0.f;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t h[4];
@@ -72,15 +72,15 @@ __device__ __forceinline__ float dot32_f16(const uint4 q, const unsigned short* 
     for (int j = 0; j < 4; ++j)
       asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2;\n"
           " fma.rn.f32.f16 %0, lo, %3, %0;\n fma.rn.f32.f16 %1, hi, %4, %1; }"
-          : "+f"(s0), "+f"(s1)
+          : "+f"(s[2 * (j & 1)]), "+f"(s[2 * (j & 1) + 1])
           : "r"(h[j]), "h"(x[8 * i + 2 * j]), "h"(x[8 * i + 2 * j + 1]));
   }
-  return s0 + s1;
+  return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 __device__ __forceinline__ float dot32_f32(const uint4 q, const float* x) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float s0 = 0.f, s1 = 0.f;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t h[4];
@@ -88,11 +88,11 @@ __device__ __forceinline__ float dot32_f32(const uint4 q, const float* x) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
-      s0 = fmaf(f.x, x[8 * i + 2 * j], s0);
-      s1 = fmaf(f.y, x[8 * i + 2 * j + 1], s1);
+      s[2 * (j & 1)] = fmaf(f.x, x[8 * i + 2 * j], s[2 * (j & 1)]);
+      s[2 * (j & 1) + 1] = fmaf(f.y, x[8 * i + 2 * j + 1], s[2 * (j & 1) + 1]);
     }
   }
-  return s0 + s1;
+  return (s[0] + s[1]) + (s[2] + s[3]);
 }
 
 // RPG (8 or 16) rows x NT values per lane -> the half-warp sum of row
@@ -159,9 +159,7 @@ struct Inputs {
   float xf[XF16 ? 1 : kNT][32];
   float pw[kNT];  // 2^s per token (XF16), else 1
 
-  // All consumer threads call this together (it has named barriers when XF16).
-  __device__ void load(const FfnArgs& a, int s_begin, int count, int b, bool vb, float* xmax_smem, int cw,
-                       int lane, int nthreads) {
+  __device__ void load(const FfnArgs& a, int s_begin, int count, int b, bool vb) {
 #pragma unroll
     for (int q = 0; q < kNT; ++q) {
       pw[q] = 1.f;
@@ -209,17 +207,9 @@ struct Inputs {
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
       if (XF16) {
-        // per-token max |x| over the whole row: lane -> warp -> CTA
-        float m = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) xmax_smem[cw * kNT + q] = m;
-        named_bar_sync(2, nthreads);
+        // exact power-of-two rescale from the token's max |x| (router kernel)
         float mx = 0.f;
-        for (int w = 0; w < nthreads / 32; ++w) mx = fmaxf(mx, xmax_smem[w * kNT + q]);
-        named_bar_sync(2, nthreads);
+        if (q < count) mx = a.max_x[a.pair_ids[s_begin + q] / a.k];
         int s = 0;
         if (mx > 0.f && mx < INFINITY) s = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 - 14;
         s = max(-100, min(100, s));
@@ -235,15 +225,18 @@ struct Inputs {
   }
 };
 
-// The RPG rows of one warp group of a staged half tile, NT tokens: block
-// partial sums scaled by the rows' E8M0 scales (and 2^s).
+// One pass over the RPG rows of one warp group of a staged half tile for NT
+// tokens: block partial sums scaled by the rows' E8M0 scales (and 2^s),
+// reduced over the half-warp, written to the pass's reduction buffer rb.
 template <int RPG, int NT, bool XF16, int MODE>
-__device__ __forceinline__ void group_rows(const uint8_t* codes, const uint8_t* scales, int K,
-                                           const Inputs<MODE, XF16>& in, bool vb, float (&acc)[RPG][kNT]) {
+__device__ __forceinline__ void pass_rows(const uint8_t* codes, const uint8_t* scales, int K,
+                                          const Inputs<MODE, XF16>& in, bool vb, float* rb, int wk, int half, int grp,
+                                          int lane) {
+  float acc[RPG][NT];
 #pragma unroll
   for (int r = 0; r < RPG; ++r) {
 #pragma unroll
-    for (int q = 0; q < kNT; ++q) acc[r][q] = 0.f;
+    for (int q = 0; q < NT; ++q) acc[r][q] = 0.f;
     if (vb) {
       const uint4 q4 = *reinterpret_cast<const uint4*>(codes + (size_t)r * (K / 2));
       const float sc = e8m0_to_f32(scales[(size_t)r * (K / 32)]);
@@ -256,23 +249,30 @@ __device__ __forceinline__ void group_rows(const uint8_t* codes, const uint8_t* 
       }
     }
   }
+  reduce_rows<RPG, NT>(acc, lane);
+  if (RPG == 16 || (lane & 8) == 0) {
+#pragma unroll
+    for (int q = 0; q < NT; ++q) rb[(((wk * 2 + half) * 16) + RPG * grp + (lane & (RPG - 1))) * kNT + q] = acc[0][q];
+  }
 }
 
 // Warps: G*W consumers (group grp = cw / W takes rows RPG*grp .. of each half
 // tile, RPG = 16 / G; wk = cw % W is the lane blocks' K group), then one
 // producer warp.  At most 16 warps, so every thread may hold 128 registers.
+// Consumers never meet at a CTA-wide barrier: each pass's partial sums go to a
+// double-buffered shared array whose fill is counted by an mbarrier, and
+// consumer warp 0 alone waits for it and writes the pass's outputs.  Every wait
+// is bounded; a warp whose wait runs out records MOE_ERR_TIMEOUT and leaves,
+// and the others then run out of their own waits and leave too.
 template <int MODE, bool XF16, int G>
 __global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a, const Geom g) {
   constexpr int RPG = 16 / G;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)g.stages * g.stage_bytes);
   uint64_t* empty = full + kMaxStages;
-  float* red = reinterpret_cast<float*>(empty + kMaxStages);  // [2][W][2][16][kNT]
-  float* xmax = red + 2 * g.warps * 2 * 16 * kNT;             // [2W][kNT]
-  // Tile index (1-based) at which a consumer wait first timed out; consumers
-  // compare it with their current tile after the per-pass barrier, so all of
-  // them leave at the same tile even if another wait times out later.
-  __shared__ int abort_tile;
+  uint64_t* red_full = empty + kMaxStages;  // [2]
+  uint64_t* red_empty = red_full + 2;       // [2]
+  float* red = reinterpret_cast<float*>(red_empty + 2);  // [2][W][2][16][kNT]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = g.warps;
@@ -282,7 +282,10 @@ __global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a,
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NC);
     }
-    abort_tile = 0x7fffffff;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&red_full[b], NC);
+      mbar_init(&red_empty[b], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -308,8 +311,7 @@ __global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a,
         }
         if (!record_ok(rec)) continue;
         const int stage = it % g.stages, n = it / g.stages;
-        if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) break;  // consumers time out too
-        if (*(volatile int*)&abort_tile != 0x7fffffff) break;
+        if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) break;
         const uint8_t* src[4];
         tile_sources<MODE>(a, rec, tile % g.tpe, src);
         uint8_t* dst = smem + (size_t)stage * g.stage_bytes;
@@ -333,9 +335,8 @@ __global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a,
   const int b = wk * 16 + (lane & 15);
   const bool vb = b < g.nblk;
   const int K = g.K;
-  const int nthreads = NC * 32;
   Inputs<MODE, XF16> in;
-  int it = 0, buf = 0, cur_a = -1, s0 = 0, ne = 0;
+  int it = 0, pc = 0, cur_a = -1, s0 = 0, ne = 0;
   bool rec_good = false;
   for (int tile = t_begin; tile < t_end; ++tile) {
     const int ai = tile / g.tpe;
@@ -345,62 +346,54 @@ __global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a,
       rec_good = record_ok(a.records[e]);
       s0 = a.offsets[e];
       ne = a.offsets[e + 1] - s0;
-      if (rec_good && ne <= kNT) in.load(a, s0, ne, b, vb, xmax, cw, lane, nthreads);
+      if (rec_good && ne <= kNT) in.load(a, s0, ne, b, vb);
     }
     if (!rec_good) continue;
     const int rt = tile % g.tpe;
-    const int stage = it % g.stages, n = it / g.stages;
+    const int stage = it % g.stages;
+    if (!mbar_wait(&full[stage], (it / g.stages) & 1, a.err)) return;
     ++it;
-    if (!mbar_wait(&full[stage], n & 1, a.err)) atomicMin(&abort_tile, it);
     const uint8_t* st = smem + (size_t)stage * g.stage_bytes;
     const uint8_t* codes = st + half * g.half_codes + (size_t)(RPG * grp) * (K / 2) + b * 16;
     const uint8_t* scales = st + 2 * g.half_codes + half * g.half_scales + (size_t)(RPG * grp) * (K / 32) + b;
-    bool stop = false;
     for (int c0 = 0; c0 < ne; c0 += kNT) {
       const int nt = min(kNT, ne - c0);
-      if (ne > kNT) in.load(a, s0 + c0, nt, b, vb, xmax, cw, lane, nthreads);
-      float acc[RPG][kNT];
+      if (ne > kNT) in.load(a, s0 + c0, nt, b, vb);
+      const int bi = pc & 1, use = pc >> 1;
+      ++pc;
+      if (use > 0 && !mbar_wait(&red_empty[bi], (use - 1) & 1, a.err)) return;
+      float* rb = red + bi * (W * 2 * 16 * kNT);
       if (nt == 1)
-        group_rows<RPG, 1, XF16, MODE>(codes, scales, K, in, vb, acc);
+        pass_rows<RPG, 1, XF16, MODE>(codes, scales, K, in, vb, rb, wk, half, grp, lane);
       else
-        group_rows<RPG, kNT, XF16, MODE>(codes, scales, K, in, vb, acc);
-      reduce_rows<RPG, kNT>(acc, lane);
-      float* rb = red + buf * (W * 2 * 16 * kNT);
-      if (RPG == 16 || (lane & 8) == 0) {
-#pragma unroll
-        for (int q = 0; q < kNT; ++q)
-          rb[(((wk * 2 + half) * 16) + RPG * grp + (lane & (RPG - 1))) * kNT + q] = acc[0][q];
-      }
-      // one barrier per pass: it publishes rb, and a timed-out wait recorded
-      // before it makes every consumer warp leave together
-      named_bar_sync(1, nthreads);
-      if (*(volatile int*)&abort_tile <= it) {
-        stop = true;
-        break;
-      }
-      const int tid = threadIdx.x;
-      if (MODE == 0) {
-        for (int idx = tid; idx < 16 * nt; idx += nthreads) {
-          const int r = idx & 15, q = idx >> 4;
-          float gsum = 0.f, usum = 0.f;
-          for (int w = 0; w < W; ++w) {
-            gsum += rb[(((w * 2 + 0) * 16) + r) * kNT + q];
-            usum += rb[(((w * 2 + 1) * 16) + r) * kNT + q];
+        pass_rows<RPG, kNT, XF16, MODE>(codes, scales, K, in, vb, rb, wk, half, grp, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_full[bi]);
+      if (cw == 0) {  // the pass's outputs, once every consumer warp has published
+        if (!mbar_wait(&red_full[bi], use & 1, a.err)) return;
+        if (MODE == 0) {
+          for (int idx = lane; idx < 16 * nt; idx += 32) {
+            const int r = idx & 15, q = idx >> 4;
+            float gsum = 0.f, usum = 0.f;
+            for (int w = 0; w < W; ++w) {
+              gsum += rb[(((w * 2 + 0) * 16) + r) * kNT + q];
+              usum += rb[(((w * 2 + 1) * 16) + r) * kNT + q];
+            }
+            a.h[(size_t)(s0 + c0 + q) * a.ff + (size_t)rt * 16 + r] = act_fn(gsum, usum, a.act);
           }
-          a.h[(size_t)(s0 + c0 + q) * a.ff + (size_t)rt * 16 + r] = act_fn(gsum, usum, a.act);
+        } else {
+          for (int idx = lane; idx < 32 * nt; idx += 32) {
+            const int r = idx & 15, hf = (idx >> 4) & 1, q = idx >> 5;
+            float ysum = 0.f;
+            for (int w = 0; w < W; ++w) ysum += rb[(((w * 2 + hf) * 16) + r) * kNT + q];
+            const int pair = a.pair_ids[s0 + c0 + q];
+            a.y_pairs[(size_t)pair * a.d + (size_t)rt * 32 + hf * 16 + r] = ysum;
+          }
         }
-      } else {
-        for (int idx = tid; idx < 32 * nt; idx += nthreads) {
-          const int r = idx & 15, hf = (idx >> 4) & 1, q = idx >> 5;
-          float ysum = 0.f;
-          for (int w = 0; w < W; ++w) ysum += rb[(((w * 2 + hf) * 16) + r) * kNT + q];
-          const int pair = a.pair_ids[s0 + c0 + q];
-          a.y_pairs[(size_t)pair * a.d + (size_t)rt * 32 + hf * 16 + r] = ysum;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_empty[bi]);
       }
-      buf ^= 1;  // the next pass writes the other buffer; this one is read-safe until the barrier after it
     }
-    if (stop) break;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -415,8 +408,7 @@ Geom make_geom(int mode, int d, int ff) {
   g.half_codes = 16u * (uint32_t)g.K / 2u;
   g.half_scales = 16u * (uint32_t)g.K / 32u;
   g.stage_bytes = 2u * (g.half_codes + g.half_scales);
-  const size_t fixed = 2 * kMaxStages * sizeof(uint64_t) + (size_t)2 * g.warps * 2 * 16 * kNT * sizeof(float) +
-                       (size_t)2 * g.warps * kNT * sizeof(float);
+  const size_t fixed = (2 * kMaxStages + 4) * sizeof(uint64_t) + (size_t)2 * g.warps * 2 * 16 * kNT * sizeof(float);
   g.stages = (int)((kSmemBudget - fixed) / g.stage_bytes);
   if (g.stages > kMaxStages) g.stages = kMaxStages;
   g.smem = (size_t)g.stages * g.stage_bytes + fixed;
@@ -435,7 +427,29 @@ cudaError_t launch_one(const FfnArgs& a, const Geom& g, int num_sms, bool pdl, c
                 g);
 }
 
+// max_i |x_t[i]| per token, one CTA per token (for the standalone expert call).
+__global__ void token_absmax_kernel(const void* x, int x_dtype, int d, float* max_x) {
+  __shared__ float part[32];
+  pdl_wait();
+  const int t = blockIdx.x;
+  float m = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) m = fmaxf(m, fabsf(load_act(x, x_dtype, (size_t)t * d + i)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, part[w]);
+    max_x[t] = m;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float* max_x, bool pdl, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  return launch("token_absmax", token_absmax_kernel, dim3(T), dim3(256), 0, s, pdl, x, x_dtype, d, max_x);
+}
 
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;

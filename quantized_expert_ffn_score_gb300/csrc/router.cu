@@ -66,6 +66,25 @@ __device__ __forceinline__ void stage_x(const RouteArgs& a, int t0, int nt, floa
   }
 }
 
+// ||x_t||_2 and max_i |x_t[i]| of one staged token, by one warp.
+__device__ __forceinline__ void token_stats(const RouteArgs& a, const float* xt, int t) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f, m = 0.f;
+  for (int i = lane; i < a.d; i += 32) {
+    s = fmaf(xt[i], xt[i], s);
+    m = fmaxf(m, fabsf(xt[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  }
+  if (lane == 0) {
+    a.nrm_x[t] = sqrtf(s);
+    a.max_x[t] = m;
+  }
+}
+
 // Error-free transformation (Knuth's TwoSum): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
@@ -98,13 +117,7 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   pdl_wait();
   stage_x(a, t0, nt, xs);
   __syncthreads();
-  if (blockIdx.x == 0 && warp < nt) {  // ||x_t||_2
-    float s = 0.f;
-    for (int i = lane; i < d; i += 32) s = fmaf(xs[warp * d + i], xs[warp * d + i], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) a.nrm_x[t0 + warp] = sqrtf(s);
-  }
+  if (blockIdx.x == 0 && warp < nt) token_stats(a, xs + warp * d, t0 + warp);
   if (e >= a.E) return;
   float acc[kTokTile][N];
 #pragma unroll
@@ -188,25 +201,40 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(Ro
   pdl_wait();
   stage_x(a, t0, nt, xs);
   __syncthreads();
+  if (blockIdx.x == 0 && warp < nt) token_stats(a, xs + warp * d, t0 + warp);
   if (e >= a.E) return;
-  float s[kTokTile], c[kTokTile], sa[kTokTile];
+  // two independent compensated chains per token (even / odd element of each
+  // chunk) for instruction-level parallelism; merged with TwoSum below
+  float s[kTokTile][2], c[kTokTile][2], sa[kTokTile];
 #pragma unroll
-  for (int t = 0; t < kTokTile; ++t) s[t] = c[t] = sa[t] = 0.f;
+  for (int t = 0; t < kTokTile; ++t) {
+    s[t][0] = s[t][1] = c[t][0] = c[t][1] = sa[t] = 0.f;
+  }
   auto consume = [&](const uint4 raw, int col) {
     float w[N];
     Vec16<WT>::unpack(raw, w);
 #pragma unroll
     for (int t = 0; t < kTokTile; ++t) {
       if (t < nt) {
-        const float* xr = xs + t * d + col;
+        const float4* xv = reinterpret_cast<const float4*>(xs + t * d + col);  // d, col multiples of 4
+        float xr[N];
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+          const float4 x4 = xv[q];
+          xr[4 * q] = x4.x;
+          xr[4 * q + 1] = x4.y;
+          xr[4 * q + 2] = x4.z;
+          xr[4 * q + 3] = x4.w;
+        }
 #pragma unroll
         for (int m = 0; m < N; ++m) {
+          const int ch = m & 1;
           const float p = __fmul_rn(w[m], xr[m]);
           const float ep = __fmaf_rn(w[m], xr[m], -p);
           float t2, es;
-          two_sum(s[t], p, t2, es);
-          s[t] = t2;
-          c[t] = __fadd_rn(c[t], __fadd_rn(es, ep));
+          two_sum(s[t][ch], p, t2, es);
+          s[t][ch] = t2;
+          c[t][ch] = __fadd_rn(c[t][ch], __fadd_rn(es, ep));
           sa[t] = __fadd_rn(sa[t], fabsf(p));
         }
       }
@@ -229,7 +257,12 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(Ro
 #pragma unroll
   for (int t = 0; t < kTokTile; ++t) {
     if (t >= nt) break;
-    float st = s[t], ct = c[t], at = sa[t];
+    float st, ct, at = sa[t];
+    {
+      float es;
+      two_sum(s[t][0], s[t][1], st, es);
+      ct = __fadd_rn(__fadd_rn(c[t][0], c[t][1]), es);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float s2 = __shfl_xor_sync(0xffffffffu, st, o);
