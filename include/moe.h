@@ -234,6 +234,29 @@ MOE_API moe_status moe_expert_ffn_rvq3(moe_ctx* ctx, const void* x, moe_dtype x_
                                cudaStream_t stream);
 
 /*
+ * moe_expert_ffn_mxfp4 without a workspace, for callers that cannot allocate
+ * device memory (an embedding framework or server that owns the allocator,
+ * or code that must not allocate after start-up).  Same arguments, same
+ * kernels and the same results as moe_expert_ffn_mxfp4, except that the
+ * scratch those kernels keep between launches (the active-expert list, a
+ * per-token scale and the hidden activations h, T*k*ff floats) lives in a
+ * static device array inside the library, moe_expert_ffn_mxfp4_static_max_bytes()
+ * bytes (4 MiB) that every GPU using the library reserves until the process
+ * exits.  Calls whose scratch would not fit (about T*k*ff > 1,040,000; at
+ * ff = 3072 up to T*k = 340 pairs) return MOE_ERR_UNSUPPORTED.  This call
+ * allocates nothing: the first call on a device looks up the array's device
+ * address (once per device), so make that first call before any stream
+ * capture.  Every call, on every stream of a device, shares the one array and
+ * it keeps the last call's contents: calls that overlap on the GPU race and
+ * give undefined results; serialise them.  The source pages have no
+ * counterpart to this entry point.
+ */
+MOE_API moe_status moe_expert_ffn_mxfp4_static(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k,
+                                               const moe_mxfp4_experts* experts, moe_act act, const int32_t* offsets,
+                                               const int32_t* pair_ids, float* y_pairs, cudaStream_t stream);
+MOE_API size_t moe_expert_ffn_mxfp4_static_max_bytes(void);
+
+/*
  * Combine: out[t][i] = x_resid[t][i] + sum over j ascending with gates[t][j] != 0
  * of gates[t][j] * y_pairs[t*k + j][i].  x_resid [T][d] (x_dtype) may be NULL
  * (out is then the MoE delta alone).  out [T][d] in out_dtype (bf16: the fp32

@@ -531,6 +531,30 @@ moe_status moe_bucket_tokens(moe_ctx* ctx, const int32_t* topk_idx, int T, int k
   return cuda_status(moe::launch_bucket(ba, false, stream));
 }
 
+}  // extern "C"
+
+namespace moe {
+
+moe_status check_expert_ffn_call(const moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k, int d, int ff,
+                                 int E, moe_act act, const int32_t* offsets, const int32_t* pair_ids,
+                                 const float* y_pairs) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  if ((st = check_route_shape(T, d, E, k)) != MOE_OK) return st;
+  if (!dims_ok(d, ff)) return MOE_ERR_UNSUPPORTED;
+  if (!dtype_ok(x_dtype) || (act != MOE_ACT_SWIGLU && act != MOE_ACT_SITU)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !offsets || !pair_ids || !y_pairs) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(y_pairs)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int* ctx_error_word(const moe_ctx* ctx) { return ctx->err; }
+
+}  // namespace moe
+
+extern "C" {
+
 static moe_status expert_ffn_common(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k, int d, int ff,
                                     int E, moe_act act, moe_quant q, const int32_t* offsets, const int32_t* pair_ids,
                                     float* y_pairs, void* ws, size_t ws_bytes, moe::FfnArgs* out_args) {

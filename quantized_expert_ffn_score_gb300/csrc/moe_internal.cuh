@@ -181,6 +181,12 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 
+// ABI-layer helpers (abi.cu) shared with other translation units' entry points.
+moe_status check_expert_ffn_call(const moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k, int d, int ff,
+                                 int E, moe_act act, const int32_t* offsets, const int32_t* pair_ids,
+                                 const float* y_pairs);
+int* ctx_error_word(const moe_ctx* ctx);
+
 // Raises a kernel's dynamic shared memory limit on the current device once,
 // instead of before every launch (the driver call costs microseconds).
 cudaError_t ensure_smem(const void* kernel, size_t bytes);

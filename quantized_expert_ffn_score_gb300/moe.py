@@ -26,7 +26,7 @@ EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy",
            "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
            "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
-           "moe_stack_forward"]
+           "moe_stack_forward", "moe_expert_ffn_mxfp4_static", "moe_expert_ffn_mxfp4_static_max_bytes"]
 
 
 class MoeError(RuntimeError):
@@ -93,6 +93,10 @@ def lib():
         L.moe_expert_ffn_rvq3.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(RvqExperts), i32, vp, vp, vp, vp, sz,
                                           vp]
         L.moe_combine.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, vp, i32, vp]
+        L.moe_expert_ffn_mxfp4_static.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(MxExperts), i32, vp, vp, vp,
+                                                  vp]
+        L.moe_expert_ffn_mxfp4_static.restype = i32
+        L.moe_expert_ffn_mxfp4_static_max_bytes.restype = sz
         L.moe_layer_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), vp, i32, i32, vp, i32, vp, vp, vp, vp, sz,
                                         vp]
         L.moe_stack_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), i32, vp, i32, i32, vp, i32, vp, sz, vp]
@@ -272,6 +276,19 @@ def moe_expert_ffn_mxfp4(ctx, x, k, layer, offsets, pair_ids, y_pairs, ws, strea
     _check(lib().moe_expert_ffn_mxfp4(ctx.handle, _ptr(x), _dt(x), T, k, ctypes.byref(ex), ACT[layer.act],
                                       _ptr(offsets), _ptr(pair_ids), _ptr(y_pairs), _ptr(ws), ws.numel(),
                                       _stream(stream)), "moe_expert_ffn_mxfp4")
+
+
+def moe_expert_ffn_mxfp4_static(ctx, x, k, layer, offsets, pair_ids, y_pairs, stream=None):
+    """moe_expert_ffn_mxfp4 with the library's static scratch instead of a workspace."""
+    T = x.shape[0]
+    ex = layer.mx_experts()
+    _check(lib().moe_expert_ffn_mxfp4_static(ctx.handle, _ptr(x), _dt(x), T, k, ctypes.byref(ex), ACT[layer.act],
+                                             _ptr(offsets), _ptr(pair_ids), _ptr(y_pairs), _stream(stream)),
+           "moe_expert_ffn_mxfp4_static")
+
+
+def expert_ffn_static_max_bytes():
+    return int(lib().moe_expert_ffn_mxfp4_static_max_bytes())
 
 
 def moe_expert_ffn_rvq3(ctx, x, k, layer, offsets, pair_ids, y_pairs, ws, stream=None):
