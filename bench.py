@@ -61,6 +61,24 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel's sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if rec is None:
+        return None
+    h = hashlib.sha256()
+    for src in ("mxfp4_gemv.cu", "moe_internal.cuh"):
+        with open(os.path.join(ROOT, "quantized_expert_ffn_score_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -297,7 +315,8 @@ def run_ours(args):
         achieved = dom_bytes / (ms / n / 1e3) / 1e9
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                    "bytes_per_launch": dom_bytes, "mean_launch_us": 1e3 * ms / n, "traffic": None}
+                    "bytes_per_launch": dom_bytes, "mean_launch_us": 1e3 * ms / n,
+                    "traffic": ncu_traffic(dom) if r.quant == "mxfp4" else None}
     step_bytes = mean_distinct * rec_bytes + r.E * r.d * 2 + T * r.d * 2
     kernels = {k: {"launches": n, "mean_us": 1e3 * ms / n} for k, (n, ms) in prof.items()}
 
