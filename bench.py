@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-min", type=int, default=None,
+                    help="experts with at least this many tokens take the tensor-core GEMM path (library default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work for the oracle sample")
     ap.add_argument("--only", choices=["route_topk"], default=None,
                     help="time one step of the layer alone (a small case for profiler captures)")
@@ -231,6 +233,8 @@ def run_ours(args):
     r = si.get_workload(args.workload)
     T = r.T
     ctx = moe.Context(local)
+    if args.gemm_min is not None:
+        ctx.gemm_min_tokens = args.gemm_min
     layer = synthetic.device_layer(r, device=dev)
     x_pool = synthetic.device_x(r, T=X_POOL * T, device=dev).view(X_POOL, T, r.d)
     out = torch.empty((T, r.d), dtype=torch.float32, device=dev)

@@ -173,6 +173,20 @@ MOE_API int moe_ctx_profile_read(moe_ctx* ctx, cudaStream_t stream, int max_entr
 MOE_API const char* moe_version(void);
 MOE_API int moe_ctx_num_sms(const moe_ctx* ctx);
 
+/* Expert FFN path selection (MXFP4 only; LazyLoRA README, "Batching is the
+ * lever"): in one call, an expert routed at least `min_tokens` tokens runs as a
+ * grouped GEMM on the tensor cores (its weights decoded once per 128 tokens),
+ * the others as the streaming GEMV.  The GEMM path needs bf16 activations and
+ * d, ff multiples of 128; otherwise every expert takes the GEMV path.
+ * min_tokens = 0 turns the GEMM path off; the default is 2.  Negative values
+ * return MOE_ERR_INVALID_ARG.  The setting belongs to the context; calls
+ * already enqueued keep the value they were enqueued with.  Both paths compute
+ * the same sums in fp32 (products exact; the GEMM path feeds h to the down
+ * projection as a bf16 hi + lo pair), so results agree to rounding.
+ * moe_ctx_gemm_min_tokens returns the setting, or -1 for a NULL context. */
+MOE_API moe_status moe_ctx_set_gemm_min_tokens(moe_ctx* ctx, int min_tokens);
+MOE_API int moe_ctx_gemm_min_tokens(const moe_ctx* ctx);
+
 /* ---- sizes ----------------------------------------------------------------- */
 
 MOE_API size_t moe_mxfp4_record_bytes(int d, int ff);

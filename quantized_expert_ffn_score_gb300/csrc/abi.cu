@@ -63,6 +63,7 @@ void profiler_end(Profiler* p, cudaStream_t s) {
 struct moe_ctx {
   int device;
   int num_sms;
+  int gemm_min;  // experts with at least this many tokens take the tensor-core GEMM path (0: never)
   int* err;  // device: [0] status, [1] detail, [2..3] spare
   moe::Profiler* prof;
 };
@@ -147,6 +148,10 @@ float router_gamma(int d, moe_dtype x_dtype, moe_dtype w_dtype) {
 // top-k certify almost every token without the fp64 recheck.
 constexpr int kCompensatedMaxT = 16;
 
+// Experts with at least this many tokens in a call take the tensor-core GEMM
+// path by default (moe_ctx_set_gemm_min_tokens changes it).
+constexpr int kDefaultGemmMinTokens = 2;
+
 // Bound coefficient of the compensated logits: |l32 - l_ref| <= K * sum|w x| +
 // 4u |l32| with K = (gamma_n^2 (1 + gamma_n) + gamma64_{d+1}) * 1.01, n = d + 32.
 float router_gamma_comp(int d) {
@@ -203,6 +208,12 @@ struct FfnWs {
   float* max_x;
   float* h;
   float* partial;
+  int32_t* hot;      // GEMM path (MXFP4, d and ff multiples of 128): expert list,
+  int32_t* hot_blk;  // its token-block prefix,
+  uint16_t* xs;      // the activations in slot order (f16, rescaled per token)
+  float* xscale;     // the per-slot scales of the activations and of h,
+  float* hscale;
+  float* u;          // and the up projections (the gate's go to h)
 };
 FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   FfnWs f;
@@ -210,7 +221,52 @@ FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   f.max_x = c.take<float>(T > 0 ? T : 1);
   f.h = c.take<float>((size_t)T * k * ff);
   f.partial = q == MOE_QUANT_RVQ3 ? c.take<float>(moe::rvq3_partial_floats(T, k, d, ff)) : nullptr;
+  f.hot = f.hot_blk = nullptr;
+  f.xs = nullptr;
+  f.xscale = f.hscale = f.u = nullptr;
+  if (q == MOE_QUANT_MXFP4 && moe::mxfp4_gemm_supported(d, ff, MOE_BF16)) {
+    f.hot = c.take<int32_t>((size_t)E + 1);
+    f.hot_blk = c.take<int32_t>((size_t)E + 1);
+    f.xs = c.take<uint16_t>((size_t)T * k * d > 0 ? (size_t)T * k * d : 1);
+    f.xscale = c.take<float>((size_t)T * k > 0 ? (size_t)T * k : 1);
+    f.hscale = c.take<float>((size_t)T * k > 0 ? (size_t)T * k : 1);
+    f.u = c.take<float>((size_t)T * k * ff > 0 ? (size_t)T * k * ff : 1);
+  }
   return f;
+}
+
+// The GEMM-path split for one call: experts with at least ctx->gemm_min tokens
+// (an expert has at most T), when the shapes and the activation type allow it.
+moe::HotSplit gemm_split(const moe_ctx* ctx, const FfnWs& w, int T, int d, int ff, moe_dtype x_dtype) {
+  moe::HotSplit sp{0, nullptr, nullptr};
+  if (w.hot != nullptr && ctx->gemm_min > 0 && T >= ctx->gemm_min && moe::mxfp4_gemm_supported(d, ff, x_dtype))
+    sp = moe::HotSplit{ctx->gemm_min, w.hot, w.hot_blk};
+  return sp;
+}
+
+moe::GemmArgs gemm_args(const moe::FfnArgs& f, const FfnWs& w) {
+  moe::GemmArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.records = f.records;
+  g.d = f.d;
+  g.ff = f.ff;
+  g.k = f.k;
+  g.T = f.T;
+  g.act = f.act;
+  g.x = f.x;
+  g.max_x = f.max_x;
+  g.offsets = f.offsets;
+  g.pair_ids = f.pair_ids;
+  g.hot = w.hot;
+  g.hot_blk = w.hot_blk;
+  g.xs = w.xs;
+  g.xscale = w.xscale;
+  g.hscale = w.hscale;
+  g.h = f.h;
+  g.u = w.u;
+  g.y_pairs = f.y_pairs;
+  g.err = f.err;
+  return g;
 }
 
 struct LayerWs {
@@ -292,7 +348,9 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
                                  w.route, const_cast<int32_t*>(topk), const_cast<float*>(gates), ctx->err);
   moe_status st = cuda_status(moe::launch_route_topk(ra, ctx->num_sms, s));
   if (st != MOE_OK) return st;
-  moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, ctx->err};
+  const moe::HotSplit split =
+      L->quant == MOE_QUANT_MXFP4 ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype) : moe::HotSplit{0, nullptr, nullptr};
+  moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
   st = cuda_status(moe::launch_bucket(ba, true, s));
   if (st != MOE_OK) return st;
   moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, L->k, L->d, L->ff, L->E, L->act, w.offsets, w.pairs, w.y_pairs,
@@ -300,6 +358,10 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   fa.max_x = w.route.max_x;  // computed by the router kernel
   if (L->quant == MOE_QUANT_MXFP4) {
     fa.records = L->mxfp4.records;
+    if (split.hot != nullptr) {
+      st = cuda_status(moe::launch_mxfp4_gemm(gemm_args(fa, w.ffn), ctx->num_sms, true, s));
+      if (st != MOE_OK) return st;
+    }
     st = cuda_status(moe::launch_mxfp4_ffn(fa, ctx->num_sms, true, s));
   } else {
     fa.records = L->rvq3.records;
@@ -343,6 +405,7 @@ moe_status moe_ctx_create(moe_ctx** ctx, int device) {
     st = MOE_ERR_CUDA;
   } else {
     c->device = device;
+    c->gemm_min = kDefaultGemmMinTokens;
     if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         cudaMalloc(&c->err, 4 * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, 4 * sizeof(int)) != cudaSuccess) {
       if (c->err) cudaFree(c->err);
@@ -368,6 +431,14 @@ void moe_ctx_destroy(moe_ctx* ctx) {
 }
 
 int moe_ctx_num_sms(const moe_ctx* ctx) { return ctx ? ctx->num_sms : 0; }
+
+moe_status moe_ctx_set_gemm_min_tokens(moe_ctx* ctx, int min_tokens) {
+  if (ctx == nullptr || min_tokens < 0) return MOE_ERR_INVALID_ARG;
+  ctx->gemm_min = min_tokens;
+  return MOE_OK;
+}
+
+int moe_ctx_gemm_min_tokens(const moe_ctx* ctx) { return ctx ? ctx->gemm_min : -1; }
 
 moe_status moe_ctx_profile(moe_ctx* ctx, int capacity) {
   if (ctx == nullptr || capacity < 0) return MOE_ERR_INVALID_ARG;
@@ -527,7 +598,8 @@ moe_status moe_bucket_tokens(moe_ctx* ctx, const int32_t* topk_idx, int T, int k
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  moe::BucketArgs ba{topk_idx, T, k, E, counts, offsets, pair_ids, static_cast<int32_t*>(ws), ctx->err};
+  moe::BucketArgs ba{topk_idx, T, k, E, counts, offsets, pair_ids, static_cast<int32_t*>(ws),
+                     moe::HotSplit{0, nullptr, nullptr}, ctx->err};
   return cuda_status(moe::launch_bucket(ba, false, stream));
 }
 
@@ -557,7 +629,8 @@ extern "C" {
 
 static moe_status expert_ffn_common(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k, int d, int ff,
                                     int E, moe_act act, moe_quant q, const int32_t* offsets, const int32_t* pair_ids,
-                                    float* y_pairs, void* ws, size_t ws_bytes, moe::FfnArgs* out_args) {
+                                    float* y_pairs, void* ws, size_t ws_bytes, moe::FfnArgs* out_args,
+                                    FfnWs* out_ws) {
   moe_status st = ctx_ok(ctx);
   if (st != MOE_OK) return st;
   if ((st = check_route_shape(T, d, E, k)) != MOE_OK) return st;
@@ -570,6 +643,7 @@ static moe_status expert_ffn_common(moe_ctx* ctx, const void* x, moe_dtype x_dty
   Carver c(ws);
   FfnWs w = carve_ffn(c, T, k, d, ff, E, q);
   *out_args = ffn_args(ctx, x, x_dtype, T, k, d, ff, E, act, offsets, pair_ids, y_pairs, w);
+  *out_ws = w;
   return MOE_OK;
 }
 
@@ -580,15 +654,21 @@ moe_status moe_expert_ffn_mxfp4(moe_ctx* ctx, const void* x, moe_dtype x_dtype, 
   if (experts == nullptr || experts->records == nullptr) return MOE_ERR_INVALID_ARG;
   ProfScope prof_scope(ctx);
   moe::FfnArgs a;
+  FfnWs w;
   moe_status st = expert_ffn_common(ctx, x, x_dtype, T, k, experts->d, experts->ff, experts->E, act,
-                                    MOE_QUANT_MXFP4, offsets, pair_ids, y_pairs, ws, ws_bytes, &a);
+                                    MOE_QUANT_MXFP4, offsets, pair_ids, y_pairs, ws, ws_bytes, &a, &w);
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
-  st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), false,
+  const moe::HotSplit split = gemm_split(ctx, w, T, experts->d, experts->ff, x_dtype);
+  st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), split, false,
                                                    stream));
   if (st != MOE_OK) return st;
   st = cuda_status(moe::launch_token_absmax(x, x_dtype, T, experts->d, const_cast<float*>(a.max_x), true, stream));
   if (st != MOE_OK) return st;
+  if (split.hot != nullptr) {
+    st = cuda_status(moe::launch_mxfp4_gemm(gemm_args(a, w), ctx->num_sms, true, stream));
+    if (st != MOE_OK) return st;
+  }
   return cuda_status(moe::launch_mxfp4_ffn(a, ctx->num_sms, true, stream));
 }
 
@@ -602,13 +682,14 @@ moe_status moe_expert_ffn_rvq3(moe_ctx* ctx, const void* x, moe_dtype x_dtype, i
       return MOE_ERR_INVALID_ARG;
   ProfScope prof_scope(ctx);
   moe::FfnArgs a;
+  FfnWs w;
   moe_status st = expert_ffn_common(ctx, x, x_dtype, T, k, experts->d, experts->ff, experts->E, act, MOE_QUANT_RVQ3,
-                                    offsets, pair_ids, y_pairs, ws, ws_bytes, &a);
+                                    offsets, pair_ids, y_pairs, ws, ws_bytes, &a, &w);
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
   for (int m = 0; m < 3; ++m) a.cb[m] = experts->codebooks[m];
-  st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), false,
-                                                   stream));
+  st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active),
+                                                   moe::HotSplit{0, nullptr, nullptr}, false, stream));
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_rvq3_ffn(a, ctx->num_sms, true, stream));
 }

@@ -49,6 +49,42 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   return base + x - v;
 }
 
+// Running totals of the expert lists across chunks of the expert range.
+struct SplitCarry {
+  int cold = 0, hot = 0, blk = 0;
+};
+
+// One chunk of experts (one per thread, cnt = bucket size, 0 past E): appends
+// the GEMV-path experts to active[] and the GEMM-path experts to hot[] with
+// their token-block prefix.  Every thread of the block calls it.
+__device__ void split_step(int e, int cnt, int32_t* active, const HotSplit& sp, int* scratch, SplitCarry& c) {
+  const bool is_hot = sp.hot != nullptr && sp.gemm_min > 0 && cnt >= sp.gemm_min;
+  const int f_cold = (cnt > 0 && !is_hot) ? 1 : 0;
+  int t_cold, t_hot, t_blk;
+  const int pos_cold = block_exclusive_scan(f_cold, scratch, &t_cold) + c.cold;
+  if (f_cold) active[1 + pos_cold] = e;
+  if (sp.hot != nullptr) {
+    const int nblk = is_hot ? (cnt + 127) / 128 : 0;
+    const int pos_hot = block_exclusive_scan(is_hot ? 1 : 0, scratch, &t_hot) + c.hot;
+    const int pos_blk = block_exclusive_scan(nblk, scratch, &t_blk) + c.blk;
+    if (is_hot) {
+      sp.hot[1 + pos_hot] = e;
+      sp.hot_blk[pos_hot] = pos_blk;
+    }
+    c.hot += t_hot;
+    c.blk += t_blk;
+  }
+  c.cold += t_cold;
+}
+
+__device__ void split_finish(int32_t* active, const HotSplit& sp, const SplitCarry& c) {
+  active[0] = c.cold;
+  if (sp.hot != nullptr) {
+    sp.hot[0] = c.hot;
+    sp.hot_blk[c.hot] = c.blk;
+  }
+}
+
 // The first nw warps own the pairs; all blockDim threads take part in the
 // per-expert scans (blockDim is sized from E, nw from T*k).
 __global__ void bucket_kernel(BucketArgs a, int nw) {
@@ -80,8 +116,9 @@ __global__ void bucket_kernel(BucketArgs a, int nw) {
   }
   __syncthreads();
   // 2. per expert: counts and per-warp bases; block scans over experts give
-  //    the offsets and the active-expert list (experts with a non-empty bucket)
-  int carry = 0, acarry = 0;
+  //    the offsets and the expert lists (GEMV-path and GEMM-path experts)
+  int carry = 0;
+  SplitCarry sc;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
     int cnt = 0;
@@ -92,22 +129,19 @@ __global__ void bucket_kernel(BucketArgs a, int nw) {
         cnt += c;
       }
     }
-    int total, atotal;
+    int total;
     const int off = block_exclusive_scan(cnt, scan_scratch, &total) + carry;
-    const int f = cnt > 0 ? 1 : 0;
-    const int apos = block_exclusive_scan(f, scan_scratch, &atotal) + acarry;
+    split_step(e, e < E ? cnt : 0, a.active, a.split, scan_scratch, sc);
     if (e < E) {
       a.counts[e] = cnt;
       a.offsets[e] = off;
-      if (f) a.active[1 + apos] = e;
       for (int w = 0; w < nw; ++w) hist[w * E + e] += off;  // absolute running position
     }
     carry += total;
-    acarry += atotal;
   }
   if (threadIdx.x == 0) {
     a.offsets[E] = carry;
-    a.active[0] = acarry;
+    split_finish(a.active, a.split, sc);
   }
   __syncthreads();
   // 3. stable scatter, walking each warp's range in ascending p
@@ -128,25 +162,19 @@ __global__ void bucket_kernel(BucketArgs a, int nw) {
   }
 }
 
-// Active expert list from offsets alone (used when the expert FFN is called on
-// its own): active[0] = count, active[1..] = experts with a non-empty bucket.
-__global__ void active_kernel(const int32_t* offsets, int E, int32_t* active) {
+// Expert lists from offsets alone (used when the expert FFN is called on its
+// own): active[0] = count, active[1..] = GEMV-path experts with a non-empty
+// bucket; the GEMM-path experts go to split.hot.
+__global__ void active_kernel(const int32_t* offsets, int E, int32_t* active, HotSplit split) {
   __shared__ int scratch[32];
-  __shared__ int s_carry;
   pdl_wait();
-  if (threadIdx.x == 0) s_carry = 0;
-  __syncthreads();
+  SplitCarry sc;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
-    const int f = (e < E && offsets[e + 1] > offsets[e]) ? 1 : 0;
-    int total;
-    const int pos = block_exclusive_scan(f, scratch, &total) + s_carry;
-    if (f) active[1 + pos] = e;
-    __syncthreads();
-    if (threadIdx.x == 0) s_carry += total;
-    __syncthreads();
+    const int cnt = e < E ? offsets[e + 1] - offsets[e] : 0;
+    split_step(e, cnt, active, split, scratch, sc);
   }
-  if (threadIdx.x == 0) active[0] = s_carry;
+  if (threadIdx.x == 0) split_finish(active, split, sc);
 }
 
 }  // namespace
@@ -165,8 +193,9 @@ cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s) {
   return launch("bucket", bucket_kernel, dim3(1), dim3(nthreads), smem, s, pdl, a, nw);
 }
 
-cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s) {
-  return launch("active_list", active_kernel, dim3(1), dim3(256), 0, s, pdl, offsets, E, active);
+cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, const HotSplit& split, bool pdl,
+                                       cudaStream_t s) {
+  return launch("active_list", active_kernel, dim3(1), dim3(256), 0, s, pdl, offsets, E, active, split);
 }
 
 }  // namespace moe

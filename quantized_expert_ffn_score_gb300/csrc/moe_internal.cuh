@@ -2,6 +2,7 @@
 // the translation units of libmoe_gb300.so.  Not part of the public ABI.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -103,6 +104,16 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
   return __uint_as_float(b << 23);
 }
 
+// Four bytes of packed E2M1 codes (low nibble = even column) -> four f16x2
+// (exact: every E2M1 value is an f16), byte b -> h[b], even column in the low half.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
 __device__ __forceinline__ float act_fn(float g, float u, int act) {
   float sig = 1.0f / (1.0f + expf(-g));
   if (act == MOE_ACT_SITU) return 4.0f * tanhf(g * 0.25f) * sig * 25.0f * tanhf(u * 0.04f);
@@ -137,6 +148,15 @@ struct RouteArgs {
 };
 cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s);
 
+// Split of the experts with tokens: those with at least `gemm_min` tokens go
+// to the tensor-core GEMM path (hot list), the others to the GEMV path
+// (active list).  gemm_min <= 0 or hot == nullptr: every expert is GEMV.
+struct HotSplit {
+  int gemm_min;
+  int32_t* hot;      // [E+1]: hot[0] = n_hot, hot[1..] = experts in ascending order
+  int32_t* hot_blk;  // [E+1]: exclusive prefix over hot experts of ceil(N_e / 128); hot_blk[n_hot] = total
+};
+
 struct BucketArgs {
   const int32_t* topk_idx;
   int T, k, E;
@@ -144,6 +164,7 @@ struct BucketArgs {
   int32_t* offsets;
   int32_t* pair_ids;
   int32_t* active;  // [E+1] workspace: active[0] = n_active, active[1..] = experts in ascending order
+  HotSplit split;
   int* err;
 };
 cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s);
@@ -164,11 +185,34 @@ struct FfnArgs {
   float* partial;         // RVQ3 only: K-slice partial sums (workspace)
   int* err;
 };
-cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s);
+cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, const HotSplit& split, bool pdl,
+                                       cudaStream_t s);
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float* max_x, bool pdl, cudaStream_t s);
 cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 size_t rvq3_partial_floats(int T, int k, int d, int ff);
+
+// Tensor-core path for the hot experts (mxfp4_gemm.cu): gathers their
+// activations into slot order, then gate/up and down grouped GEMMs.
+struct GemmArgs {
+  const uint8_t* const* records;
+  int d, ff, k, T, act;
+  const void* x;        // [T][d] bf16
+  const float* max_x;   // [T] max_i |x_t[i]|
+  const int32_t* offsets;
+  const int32_t* pair_ids;
+  const int32_t* hot;
+  const int32_t* hot_blk;
+  uint16_t* xs;         // [T*k][d] f16 workspace, slot order (hot slots): x * 2^-s_t
+  float* xscale;        // [T*k] 2^s_t per hot slot
+  float* h;             // [T*k][ff] workspace; a hot slot's row holds g (fp32), then f16 hi[ff] | lo[ff] of h * 2^-s
+  float* u;             // [T*k][ff] workspace: u of the hot slots (fp32)
+  float* hscale;        // [T*k] that 2^s per hot slot
+  float* y_pairs;       // [T*k][d] by pair id
+  int* err;
+};
+bool mxfp4_gemm_supported(int d, int ff, int x_dtype);
+cudaError_t launch_mxfp4_gemm(const GemmArgs& a, int num_sms, bool pdl, cudaStream_t s);
 
 struct CombineArgs {
   const void* x;

@@ -50,14 +50,6 @@ struct Geom {
   size_t smem;
 };
 
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
-}
-
 // Block dot products: 32 codes q (low nibble = even column) against the lane's
 // 32 input values.  f16 inputs: fma.f32.f16 on each half of the converted code
 // pair (exact products, fp32 sums); fp32 inputs: the f16 pair widened to fp32.

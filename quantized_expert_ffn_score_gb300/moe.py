@@ -22,6 +22,7 @@ QUANT = {"mxfp4": 0, "rvq3": 1}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy", "moe_ctx_check", "moe_ctx_num_sms",
+           "moe_ctx_set_gemm_min_tokens", "moe_ctx_gemm_min_tokens",
            "moe_ctx_profile", "moe_ctx_profile_read", "moe_ctx_stats",
            "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
@@ -104,6 +105,8 @@ def lib():
                   "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward", "moe_stack_forward"):
             getattr(L, f).restype = i32
         L.moe_ctx_num_sms.restype = i32
+        L.moe_ctx_set_gemm_min_tokens.argtypes, L.moe_ctx_set_gemm_min_tokens.restype = [vp, i32], i32
+        L.moe_ctx_gemm_min_tokens.argtypes, L.moe_ctx_gemm_min_tokens.restype = [vp], i32
         _lib = L
     return _lib
 
@@ -160,6 +163,15 @@ class Context:
         a, b = ctypes.c_longlong(0), ctypes.c_longlong(0)
         _check(lib().moe_ctx_stats(self.handle, _stream(stream), ctypes.byref(a), ctypes.byref(b)), "moe_ctx_stats")
         return a.value, b.value
+
+    @property
+    def gemm_min_tokens(self):
+        """Experts with at least this many tokens take the tensor-core GEMM path (0: never)."""
+        return lib().moe_ctx_gemm_min_tokens(self.handle)
+
+    @gemm_min_tokens.setter
+    def gemm_min_tokens(self, n):
+        _check(lib().moe_ctx_set_gemm_min_tokens(self.handle, int(n)), "moe_ctx_set_gemm_min_tokens")
 
     def profile(self, capacity):
         """Turns per-launch event timing on (capacity launches between reads) or off (0)."""

@@ -69,6 +69,12 @@ WORKLOADS = {
     # K3 prefill, 512 tokens: Zipf-skewed routing and the uniform control
     "k3_mxfp4_prefill_zipf": LayerRecipe("k3_mxfp4_prefill_zipf", T=512, seed=3, bias="zipf", **K3),
     "k3_mxfp4_prefill_uniform": LayerRecipe("k3_mxfp4_prefill_uniform", T=512, seed=3, **K3),
+    # small cases of the prefill kernels for detailed profiler captures (64
+    # experts, 1.1 GB): Zipf-skewed buckets of up to ~500 tokens, and 40 tokens
+    # (about 10 per expert, the size of a uniform 512-token bucket over 896)
+    "k3_mxfp4_prefill_zipf_e64": LayerRecipe("k3_mxfp4_prefill_zipf_e64", T=512, seed=3, bias="zipf",
+                                             **dict(K3, E=64)),
+    "k3_mxfp4_prefill_b40_e64": LayerRecipe("k3_mxfp4_prefill_b40_e64", T=40, seed=3, **dict(K3, E=64)),
 }
 
 STACK_LAYERS = 6

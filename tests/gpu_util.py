@@ -81,3 +81,33 @@ def check_routing(topk_gpu, gates_gpu, idx_ref, g_ref, rel_tol):
     np.testing.assert_array_equal(topk_gpu, idx_ref)
     rel = np.abs(gates_gpu.astype(np.float64) - g_ref) / g_ref
     assert np.all(rel <= np.asarray(rel_tol)[:, None]), f"gate error {rel.max():.3e}"
+
+
+def run_layer(moe, ctx, layer, x, out_dtype=None):
+    import torch
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    T = x.shape[0]
+    r = layer.recipe
+    out = torch.empty((T, r.d), dtype=out_dtype, device="cuda")
+    topk = torch.full((T, r.k), -1, dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, r.k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(r.E, dtype=torch.int32, device="cuda")
+    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T))
+    moe.moe_layer_forward(ctx, layer, x, out, ws, topk_idx_out=topk, gates_out=gates, counts_out=counts)
+    ctx.check()
+    return out.float().cpu().numpy(), topk.cpu().numpy(), gates.cpu().numpy(), counts.cpu().numpy()
+
+
+def full_check(moe, ctx, r, tokens=None):
+    from quantized_expert_ffn_score_gb300 import synthetic
+    layer = synthetic.device_layer(r)
+    x = synthetic.device_x(r)
+    out, topk, gates, counts = run_layer(moe, ctx, layer, x)
+    xh = si.layer_x(r)
+    logits, idx, g, y, o = oracle_layer(r, xh, tokens=tokens)
+    check_routing(topk, gates, idx, g, gate_tolerance(r, xh, logits))
+    np.testing.assert_array_equal(counts, np.bincount(idx.reshape(-1), minlength=r.E))
+    sel = np.arange(r.T) if tokens is None else np.asarray(tokens)
+    delta = out[sel].astype(np.float64) - x_host_f64(xh)[sel]
+    rel = assert_rms_close(delta, y[sel], what=r.name)
+    return rel, counts

@@ -26,85 +26,57 @@ def ctx(lib):
     c.close()
 
 
-def run_layer(moe, ctx, layer, x, out_dtype=torch.float32):
-    T = x.shape[0]
-    r = layer.recipe
-    out = torch.empty((T, r.d), dtype=out_dtype, device="cuda")
-    topk = torch.full((T, r.k), -1, dtype=torch.int32, device="cuda")
-    gates = torch.empty((T, r.k), dtype=torch.float32, device="cuda")
-    counts = torch.empty(r.E, dtype=torch.int32, device="cuda")
-    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T))
-    moe.moe_layer_forward(ctx, layer, x, out, ws, topk_idx_out=topk, gates_out=gates, counts_out=counts)
-    ctx.check()
-    return out.float().cpu().numpy(), topk.cpu().numpy(), gates.cpu().numpy(), counts.cpu().numpy()
-
-
 MID_MX = si.LayerRecipe("mid_mxfp4", d=1024, ff=576, E=40, k=6, T=37, seed=11, scale_lo=118, scale_hi=121)
 MID_RVQ = si.LayerRecipe("mid_rvq3", d=1024, ff=576, E=24, k=4, T=11, seed=12, quant="rvq3")
 
 
-def full_check(moe, ctx, r, tokens=None):
-    from quantized_expert_ffn_score_gb300 import synthetic
-    layer = synthetic.device_layer(r)
-    x = synthetic.device_x(r)
-    out, topk, gates, counts = run_layer(moe, ctx, layer, x)
-    xh = si.layer_x(r)
-    logits, idx, g, y, o = gu.oracle_layer(r, xh, tokens=tokens)
-    gu.check_routing(topk, gates, idx, g, gu.gate_tolerance(r, xh, logits))
-    np.testing.assert_array_equal(counts, np.bincount(idx.reshape(-1), minlength=r.E))
-    sel = np.arange(r.T) if tokens is None else np.asarray(tokens)
-    delta = out[sel].astype(np.float64) - gu.x_host_f64(xh)[sel]
-    rel = gu.assert_rms_close(delta, y[sel], what=r.name)
-    return rel
-
-
 def test_tiny_layer(lib, ctx):
-    full_check(lib, ctx, si.get_workload("tiny"))
+    gu.full_check(lib, ctx, si.get_workload("tiny"))
 
 
 def test_mid_mxfp4_spans_tiles_and_ragged_tail(lib, ctx):
-    full_check(lib, ctx, MID_MX)
+    gu.full_check(lib, ctx, MID_MX)
 
 
 def test_mid_mxfp4_situ_fp32_router(lib, ctx):
-    full_check(lib, ctx, MID_MX.with_(act="situ", x_dtype="f32", w_dtype="f32", seed=13))
+    gu.full_check(lib, ctx, MID_MX.with_(act="situ", x_dtype="f32", w_dtype="f32", seed=13))
 
 
 def test_mid_mxfp4_bf16_x_fp32_router(lib, ctx):
-    full_check(lib, ctx, MID_MX.with_(w_dtype="f32", seed=14, T=5, k=1))
+    gu.full_check(lib, ctx, MID_MX.with_(w_dtype="f32", seed=14, T=5, k=1))
 
 
 def test_mid_mxfp4_all_experts_selected(lib, ctx):
-    full_check(lib, ctx, MID_MX.with_(E=8, k=8, T=3, seed=15))
+    gu.full_check(lib, ctx, MID_MX.with_(E=8, k=8, T=3, seed=15))
 
 
 def test_mid_rvq3(lib, ctx):
-    full_check(lib, ctx, MID_RVQ)
+    gu.full_check(lib, ctx, MID_RVQ)
 
 
 def test_mid_rvq3_situ(lib, ctx):
-    full_check(lib, ctx, MID_RVQ.with_(act="situ", seed=16, T=3))
+    gu.full_check(lib, ctx, MID_RVQ.with_(act="situ", seed=16, T=3))
 
 
 @pytest.mark.slow
 def test_k3_mxfp4_decode_b1(lib, ctx):
-    full_check(lib, ctx, si.get_workload("k3_mxfp4_decode"))
+    gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_decode"))
 
 
 @pytest.mark.slow
 def test_k3_rvq3_decode_b1(lib, ctx):
-    full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b1"))
+    gu.full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b1"))
 
 
 @pytest.mark.slow
 def test_k3_rvq3_decode_b8(lib, ctx):
-    full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b8"), tokens=[0, 3, 7])
+    gu.full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b8"), tokens=[0, 3, 7])
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["k3_mxfp4_prefill_zipf", "k3_mxfp4_prefill_uniform"])
 def test_k3_prefill_routing_all_tokens_outputs_sampled(lib, ctx, name):
-    full_check(lib, ctx, si.get_workload(name), tokens=[0, 201, 511])
+    gu.full_check(lib, ctx, si.get_workload(name), tokens=[0, 201, 511])
 
 
 def test_route_topk_and_bucket_standalone_match_oracle(lib, ctx):
