@@ -177,7 +177,7 @@ MOE_API int moe_ctx_num_sms(const moe_ctx* ctx);
  * lever"): in one call, an expert routed at least `min_tokens` tokens runs as a
  * grouped GEMM on the tensor cores (its weights decoded once per 128 tokens),
  * the others as the streaming GEMV.  The GEMM path needs bf16 activations and
- * d, ff multiples of 128; otherwise every expert takes the GEMV path.
+ * d, ff multiples of 256; otherwise every expert takes the GEMV path.
  * min_tokens = 0 turns the GEMM path off; the default is 2.  Negative values
  * return MOE_ERR_INVALID_ARG.  The setting belongs to the context; calls
  * already enqueued keep the value they were enqueued with.  Both paths compute

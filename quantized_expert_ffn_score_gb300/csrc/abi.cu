@@ -208,12 +208,12 @@ struct FfnWs {
   float* max_x;
   float* h;
   float* partial;
-  int32_t* hot;      // GEMM path (MXFP4, d and ff multiples of 128): expert list,
+  int32_t* hot;      // GEMM path (MXFP4, d and ff multiples of 256): expert list,
   int32_t* hot_blk;  // its token-block prefix,
   uint16_t* xs;      // the activations in slot order (f16, rescaled per token)
   float* xscale;     // the per-slot scales of the activations and of h,
   float* hscale;
-  float* u;          // and the up projections (the gate's go to h)
+  uint8_t* row_ref;  // and each hot expert row's largest scale byte
 };
 FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   FfnWs f;
@@ -223,14 +223,15 @@ FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   f.partial = q == MOE_QUANT_RVQ3 ? c.take<float>(moe::rvq3_partial_floats(T, k, d, ff)) : nullptr;
   f.hot = f.hot_blk = nullptr;
   f.xs = nullptr;
-  f.xscale = f.hscale = f.u = nullptr;
+  f.xscale = f.hscale = nullptr;
+  f.row_ref = nullptr;
   if (q == MOE_QUANT_MXFP4 && moe::mxfp4_gemm_supported(d, ff, MOE_BF16)) {
     f.hot = c.take<int32_t>((size_t)E + 1);
     f.hot_blk = c.take<int32_t>((size_t)E + 1);
     f.xs = c.take<uint16_t>((size_t)T * k * d > 0 ? (size_t)T * k * d : 1);
     f.xscale = c.take<float>((size_t)T * k > 0 ? (size_t)T * k : 1);
     f.hscale = c.take<float>((size_t)T * k > 0 ? (size_t)T * k : 1);
-    f.u = c.take<float>((size_t)T * k * ff > 0 ? (size_t)T * k * ff : 1);
+    f.row_ref = c.take<uint8_t>((size_t)E * (2 * (size_t)ff + d));
   }
   return f;
 }
@@ -262,8 +263,8 @@ moe::GemmArgs gemm_args(const moe::FfnArgs& f, const FfnWs& w) {
   g.xs = w.xs;
   g.xscale = w.xscale;
   g.hscale = w.hscale;
+  g.row_ref = w.row_ref;
   g.h = f.h;
-  g.u = w.u;
   g.y_pairs = f.y_pairs;
   g.err = f.err;
   return g;

@@ -205,9 +205,9 @@ struct GemmArgs {
   const int32_t* hot_blk;
   uint16_t* xs;         // [T*k][d] f16 workspace, slot order (hot slots): x * 2^-s_t
   float* xscale;        // [T*k] 2^s_t per hot slot
-  float* h;             // [T*k][ff] workspace; a hot slot's row holds g (fp32), then f16 hi[ff] | lo[ff] of h * 2^-s
-  float* u;             // [T*k][ff] workspace: u of the hot slots (fp32)
+  float* h;             // [T*k][ff] workspace; a hot slot's row holds h (fp32), then f16 hi[ff] | lo[ff] of h * 2^-s
   float* hscale;        // [T*k] that 2^s per hot slot
+  uint8_t* row_ref;     // [E][2 ff + d] workspace: largest scale byte per row of the hot experts' Wg, Wu, Wd
   float* y_pairs;       // [T*k][d] by pair id
   int* err;
 };

@@ -137,6 +137,10 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  mma_bf16_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
 // Arrives once on the mbarrier when every MMA this thread issued before has
 // completed (and its shared-memory and TMEM operands may be reused).
 __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
@@ -165,6 +169,15 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(saddr(dst)), "l"(src) : "memory");
+}
+// Arrives on the mbarrier once every cp.async this thread issued before has
+// completed, without incrementing its pending count (the barrier's expected
+// count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(saddr(mbar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>

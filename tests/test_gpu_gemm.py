@@ -17,8 +17,8 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-# d, ff multiples of 128 (the GEMM path's tiling); Zipf(1) bias over 24 experts
-ZIPF = si.LayerRecipe("gemm_zipf", d=512, ff=384, E=24, k=4, T=300, seed=41, bias="zipf", scale_lo=118, scale_hi=121)
+# d, ff multiples of 256 (the GEMM path's tiling); Zipf(1) bias over 24 experts
+ZIPF = si.LayerRecipe("gemm_zipf", d=512, ff=512, E=24, k=4, T=300, seed=41, bias="zipf", scale_lo=118, scale_hi=121)
 # 8 experts, 2 of them per token: every bucket ~50 tokens, the last one hot too
 UNIFORM = si.LayerRecipe("gemm_uniform", d=256, ff=256, E=8, k=2, T=203, seed=42)
 
