@@ -188,6 +188,9 @@ struct FfnArgs {
 cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, const HotSplit& split, bool pdl,
                                        cudaStream_t s);
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
+// The same FFN with the inner products on mma.sync (mxfp4_mma_gemv.cu); bf16 activations.
+bool mxfp4_mma_gemv_supported(int d, int ff, int x_dtype);
+cudaError_t launch_mxfp4_ffn_mma(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float* max_x, bool pdl, cudaStream_t s);
 cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 size_t rvq3_partial_floats(int T, int k, int d, int ff);

@@ -445,6 +445,7 @@ cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float*
 
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
+  if (mxfp4_mma_gemv_supported(a.d, a.ff, a.x_dtype)) return launch_mxfp4_ffn_mma(a, num_sms, pdl, s);
   const Geom g0 = make_geom(0, a.d, a.ff), g1 = make_geom(1, a.d, a.ff);
   if (g0.stages < 2 || g1.stages < 2) return cudaErrorInvalidValue;
   cudaError_t err = a.x_dtype == MOE_BF16 ? launch_one<0, true>(a, g0, num_sms, pdl, s, "mxfp4_gate_up")

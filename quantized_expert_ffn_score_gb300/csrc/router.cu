@@ -178,17 +178,18 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   }
 }
 
-// Compensated variant (used for small T): per lane and token a running sum s,
+// Compensated variant (used for small T; TT tokens per CTA, 1 when T = 1 so
+// that the unrolled code stays small): per lane and token a running sum s,
 // the exact rounding errors of the products and of the sums accumulated in c
 // (Dot2 of Ogita, Rump and Oishi), and sum|p|; lanes merge with TwoSum.  Writes
 // logits = fl(fl(s + c) + bias) and absdot = sum|p|.
-template <typename WT>
+template <typename WT, int TT>
 __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(RouteArgs a) {
-  extern __shared__ float xs[];  // [kTokTile][d]
+  extern __shared__ float xs[];  // [TT][d]
   constexpr int N = Vec16<WT>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.y * kTokTile;
-  const int nt = min(kTokTile, a.T - t0);
+  const int t0 = blockIdx.y * TT;
+  const int nt = min(TT, a.T - t0);
   const int d = a.d;
   const int e = blockIdx.x * kLogitWarps + warp;
   const int nch = d / (32 * N);
@@ -205,16 +206,16 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(Ro
   if (e >= a.E) return;
   // two independent compensated chains per token (even / odd element of each
   // chunk) for instruction-level parallelism; merged with TwoSum below
-  float s[kTokTile][2], c[kTokTile][2], sa[kTokTile];
+  float s[TT][2], c[TT][2], sa[TT];
 #pragma unroll
-  for (int t = 0; t < kTokTile; ++t) {
+  for (int t = 0; t < TT; ++t) {
     s[t][0] = s[t][1] = c[t][0] = c[t][1] = sa[t] = 0.f;
   }
   auto consume = [&](const uint4 raw, int col) {
     float w[N];
     Vec16<WT>::unpack(raw, w);
 #pragma unroll
-    for (int t = 0; t < kTokTile; ++t) {
+    for (int t = 0; t < TT; ++t) {
       if (t < nt) {
         const float4* xv = reinterpret_cast<const float4*>(xs + t * d + col);  // d, col multiples of 4
         float xr[N];
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(Ro
   pdl_launch_dependents();
   const float b = a.bias ? a.bias[e] : 0.f;
 #pragma unroll
-  for (int t = 0; t < kTokTile; ++t) {
+  for (int t = 0; t < TT; ++t) {
     if (t >= nt) break;
     float st, ct, at = sa[t];
     {
@@ -709,15 +710,27 @@ cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s) {
   const dim3 grid((a.E + kLogitWarps - 1) / kLogitWarps, (a.T + kTokTile - 1) / kTokTile);
   const size_t smem = (size_t)kTokTile * a.d * sizeof(float);
   cudaError_t err;
-  if (a.comp) {
+  if (a.comp && a.T == 1) {
+    const dim3 g1((a.E + kLogitWarps - 1) / kLogitWarps, 1);
+    const size_t sm1 = (size_t)a.d * sizeof(float);
     if (a.w_dtype == MOE_BF16) {
-      ensure_smem(router_logits_comp_kernel<uint16_t>, smem);
-      err = launch("router_logits", router_logits_comp_kernel<uint16_t>, grid, dim3(kLogitWarps * 32), smem, s,
+      ensure_smem(router_logits_comp_kernel<uint16_t, 1>, sm1);
+      err = launch("router_logits", router_logits_comp_kernel<uint16_t, 1>, g1, dim3(kLogitWarps * 32), sm1, s,
                    false, a);
     } else {
-      ensure_smem(router_logits_comp_kernel<float>, smem);
-      err = launch("router_logits", router_logits_comp_kernel<float>, grid, dim3(kLogitWarps * 32), smem, s, false,
+      ensure_smem(router_logits_comp_kernel<float, 1>, sm1);
+      err = launch("router_logits", router_logits_comp_kernel<float, 1>, g1, dim3(kLogitWarps * 32), sm1, s, false,
                    a);
+    }
+  } else if (a.comp) {
+    if (a.w_dtype == MOE_BF16) {
+      ensure_smem(router_logits_comp_kernel<uint16_t, kTokTile>, smem);
+      err = launch("router_logits", router_logits_comp_kernel<uint16_t, kTokTile>, grid, dim3(kLogitWarps * 32), smem,
+                   s, false, a);
+    } else {
+      ensure_smem(router_logits_comp_kernel<float, kTokTile>, smem);
+      err = launch("router_logits", router_logits_comp_kernel<float, kTokTile>, grid, dim3(kLogitWarps * 32), smem, s,
+                   false, a);
     }
   } else if (a.w_dtype == MOE_BF16) {
     ensure_smem(router_logits_kernel<uint16_t>, smem);
