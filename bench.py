@@ -63,19 +63,20 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def ncu_traffic(kernel):
+def ncu_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel's sources changed since that capture."""
+    when the capture was not of this workload's launch shape or one of the
+    kernel's sources (listed in the record) changed since that capture."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if rec is None:
+    if rec is None or "sources" not in rec or workload not in rec.get("workloads", ()):
         return None
     h = hashlib.sha256()
-    for src in ("mxfp4_gemv.cu", "moe_internal.cuh"):
+    for src in rec["sources"]:
         with open(os.path.join(ROOT, "quantized_expert_ffn_score_gb300", "csrc", src), "rb") as f:
             h.update(f.read())
     return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
@@ -277,11 +278,11 @@ def run_ours(args):
 
     # ---- per-kernel pass (same steps, library profiler) ------------------------
     ctx.profile(16 * K + 64)
-    distinct = []
+    step_counts = []
     for i in range(K):
         flush.fill_(i & 0xFF)
         step(i, counts_out=counts)
-        distinct.append(int((counts > 0).sum().item()))
+        step_counts.append(counts.cpu().numpy().copy())
     prof = ctx.profile_read()
     ctx.profile(0)
     launches_per_step = sum(n for n, _ in prof.values()) / K
@@ -308,19 +309,37 @@ def run_ours(args):
     value = tokens_total / (dev_ms_max / 1e3)
     peaks = measured_peaks()
     rec_bytes = si.mxfp4_record_size(r.d, r.ff) if r.quant == "mxfp4" else si.rvq3_record_size(r.d, r.ff)
-    # dominant kernel: the gate/up expert kernel streams the gate and up thirds of
-    # every routed expert's record once per launch
-    dom = "mxfp4_gate_up" if r.quant == "mxfp4" else "rvq3_gate_up"
-    mean_distinct = float(np.mean(distinct))
-    dom_bytes = mean_distinct * (2 * rec_bytes / 3) + T * r.d * 2 + T * r.k * r.ff * 4
-    roofline = None
-    if dom in prof:
-        n, ms = prof[dom]
-        achieved = dom_bytes / (ms / n / 1e3) / 1e9
-        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                    "bytes_per_launch": dom_bytes, "mean_launch_us": 1e3 * ms / n,
-                    "traffic": ncu_traffic(dom) if r.quant == "mxfp4" else None}
+    # The expert kernels' algorithmic work per launch.  Experts with at least
+    # gemm_min tokens run on the tensor-core GEMM path when it ran at all; the
+    # others stream through the GEMV path.
+    gemm_ran = "mxfp4_gemm_gate_up" in prof
+    gmin = ctx.gemm_min_tokens if gemm_ran else 1 << 30
+    cnts = np.stack(step_counts)
+    mean_distinct = float(np.mean((cnts > 0).sum(axis=1)))
+    cold_distinct = float(np.mean(((cnts > 0) & (cnts < gmin)).sum(axis=1)))
+    hot_pairs = float(np.mean(np.where(cnts >= gmin, cnts, 0).sum(axis=1)))
+    cold_pairs = float(np.mean(np.where(cnts < gmin, cnts, 0).sum(axis=1)))
+    gemv = "mxfp4_gate_up" if r.quant == "mxfp4" else "rvq3_gate_up"
+    gemv_bytes = cold_distinct * (2 * rec_bytes / 3) + cold_pairs * (r.d * 2 + r.ff * 4)
+    gemm_flops = 2.0 * 2 * r.ff * r.d * hot_pairs
+    rooflines = {}
+    if gemv in prof:
+        n, ms = prof[gemv]
+        ach = gemv_bytes / (ms / n / 1e3) / 1e9
+        rooflines[gemv] = {"bound": "hbm", "kernel": gemv, "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": ach / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                           "bytes_per_launch": gemv_bytes, "mean_launch_us": 1e3 * ms / n,
+                           "traffic": ncu_traffic(gemv, args.workload)}
+    if gemm_ran:
+        n, ms = prof["mxfp4_gemm_gate_up"]
+        ach = gemm_flops / (ms / n / 1e3) / 1e12
+        rooflines["mxfp4_gemm_gate_up"] = {
+            "bound": "tensor", "kernel": "mxfp4_gemm_gate_up", "achieved": ach, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "peak_source": peaks["source"] + " (f16 = bf16 rate)",
+            "flops_per_launch": gemm_flops, "mean_launch_us": 1e3 * ms / n,
+            "traffic": ncu_traffic("mxfp4_gemm_gate_up", args.workload)}
+    # the dominant kernel: the expert kernel with the longest launches
+    roofline = max(rooflines.values(), key=lambda v: v["mean_launch_us"]) if rooflines else None
     step_bytes = mean_distinct * rec_bytes + r.E * r.d * 2 + T * r.d * 2
     kernels = {k: {"launches": n, "mean_us": 1e3 * ms / n} for k, (n, ms) in prof.items()}
 
@@ -333,7 +352,9 @@ def run_ours(args):
                        "l2": "flushed between steps (512 MiB write outside the timed events)",
                        "x_pool": X_POOL, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "layer_hbm_gbs": step_bytes / (dev_ms_max / K / 1e3) / 1e9,
-            "roofline": roofline, "kernels": kernels,
+            "roofline": roofline, "rooflines": rooflines, "kernels": kernels,
+            "experts": {"distinct_per_step": mean_distinct, "gemm_path_pairs": hot_pairs, "gemv_path_experts": cold_distinct,
+                        "gemm_min_tokens": ctx.gemm_min_tokens},
             "e2e": {"value": tokens_total / (e2e_ms / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": T * r.d * x_pool.element_size(), "d2h_bytes_per_step": T * r.d * 4},
             "gpu_launches": int(round(launches_per_step * K)), "clocks": clk, "wall_s": wall,

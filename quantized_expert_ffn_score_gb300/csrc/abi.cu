@@ -347,13 +347,19 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   int32_t* counts = counts_out ? counts_out : w.counts;
   moe::RouteArgs ra = route_args(x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, T, L->d, L->E, L->k,
                                  w.route, const_cast<int32_t*>(topk), const_cast<float*>(gates), ctx->err);
-  moe_status st = cuda_status(moe::launch_route_topk(ra, ctx->num_sms, s));
-  if (st != MOE_OK) return st;
   const moe::HotSplit split =
       L->quant == MOE_QUANT_MXFP4 ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype) : moe::HotSplit{0, nullptr, nullptr};
   moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
-  st = cuda_status(moe::launch_bucket(ba, true, s));
+  if (T == 1) {  // one token: the top-k kernel buckets its pairs itself
+    ra.fuse_bucket = 1;
+    ra.bucket = ba;
+  }
+  moe_status st = cuda_status(moe::launch_route_topk(ra, ctx->num_sms, s));
   if (st != MOE_OK) return st;
+  if (T != 1) {
+    st = cuda_status(moe::launch_bucket(ba, true, s));
+    if (st != MOE_OK) return st;
+  }
   moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, L->k, L->d, L->ff, L->E, L->act, w.offsets, w.pairs, w.y_pairs,
                              w.ffn);
   fa.max_x = w.route.max_x;  // computed by the router kernel

@@ -120,6 +120,13 @@ __device__ __forceinline__ float act_fn(float g, float u, int act) {
   return g * sig * u;
 }
 
+// The activation with the hardware exponential and an approximate divide
+// (relative error about 1e-6, far inside the fp32 path's error budget).
+__device__ __forceinline__ float act_fast(float g, float u, int act) {
+  if (act == MOE_ACT_SITU) return act_fn(g, u, act);
+  return __fdividef(g * u, 1.0f + __expf(-g));
+}
+
 __device__ __forceinline__ float load_act(const void* p, int dtype, size_t i) {
   if (dtype == MOE_BF16) return bf16_bits_to_f32(static_cast<const uint16_t*>(p)[i]);
   return static_cast<const float*>(p)[i];
@@ -128,25 +135,7 @@ __device__ __forceinline__ float load_act(const void* p, int dtype, size_t i) {
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  All pointers are device pointers.
 
-struct RouteArgs {
-  const void* x;
-  int x_dtype;
-  const void* w;
-  int w_dtype;
-  const float* bias;
-  int T, d, E, k;
-  float* logits;  // [T][E]   workspace
-  float* nrm_w;   // [E]      workspace: ||W_e||_2
-  float* nrm_x;   // [T]      workspace: ||x_t||_2
-  float* max_x;   // [T]      workspace: max_i |x_t[i]|
-  float* absdot;  // [T][E]   workspace: sum_i |W[e][i] x[t][i]| (compensated logits only)
-  int comp;       // logits by compensated (Dot2) sums; bounds from absdot
-  float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
-  int32_t* topk_idx;
-  float* gates;
-  int* err;
-};
-cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s);
+
 
 // Split of the experts with tokens: those with at least `gemm_min` tokens go
 // to the tensor-core GEMM path (hot list), the others to the GEMV path
@@ -168,6 +157,28 @@ struct BucketArgs {
   int* err;
 };
 cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s);
+
+struct RouteArgs {
+  const void* x;
+  int x_dtype;
+  const void* w;
+  int w_dtype;
+  const float* bias;
+  int T, d, E, k;
+  float* logits;  // [T][E]   workspace
+  float* nrm_w;   // [E]      workspace: ||W_e||_2
+  float* nrm_x;   // [T]      workspace: ||x_t||_2
+  float* max_x;   // [T]      workspace: max_i |x_t[i]|
+  float* absdot;  // [T][E]   workspace: sum_i |W[e][i] x[t][i]| (compensated logits only)
+  int comp;       // logits by compensated (Dot2) sums; bounds from absdot
+  float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
+  int32_t* topk_idx;
+  float* gates;
+  int* err;
+  int fuse_bucket;    // one token: the top-k kernel also buckets the pairs (with `bucket`)
+  BucketArgs bucket;
+};
+cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s);
 
 struct FfnArgs {
   const uint8_t* const* records;

@@ -161,13 +161,6 @@ __device__ __forceinline__ void dequant_block(const uint4 q, uint32_t mult, uint
   }
 }
 
-// The activation with the hardware exponential and an approximate divide
-// (relative error about 1e-6, far inside the fp32 path's error budget).
-__device__ __forceinline__ float act_fast(float g, float u, int act) {
-  if (act == MOE_ACT_SITU) return act_fn(g, u, act);
-  return __fdividef(g * u, 1.0f + __expf(-g));
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap map0,

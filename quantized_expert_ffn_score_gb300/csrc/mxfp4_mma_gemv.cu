@@ -400,7 +400,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
               us += rbase[((size_t)w * kRows + 16 + r) * kTok + n];
             }
             const float pw = tok_f[n];
-            a.h[(size_t)tok_i[n] * a.ff + (size_t)rt * 16 + r] = act_fn(gs * pw, us * pw, a.act);
+            a.h[(size_t)tok_i[n] * a.ff + (size_t)rt * 16 + r] = act_fast(gs * pw, us * pw, a.act);
           }
         } else {
           for (int idx = lane; idx < kRows * nt; idx += 32) {

@@ -12,7 +12,7 @@
 // l_ref exactly (bf16 x bf16 and fp32 x fp32 products are exact in fp64).
 #include <utility>
 
-#include "moe_internal.cuh"
+#include "bucket_body.cuh"
 
 namespace moe {
 namespace {
@@ -447,10 +447,10 @@ __device__ float block_max(float v, float* scratch) {
   return m;
 }
 
-// One CTA per token: a radix select finds the (k+1)-th largest fp32 logit,
+// One CTA per token (the body of the top-k kernel): a radix select finds the (k+1)-th largest fp32 logit,
 // the k+1 experts at or above it are ordered by counting, and the bounds then
 // certify the selection or send the CTA down the recheck path.
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
+__device__ __forceinline__ void topk_token(const RouteArgs& a) {
   extern __shared__ double tsm[];
   const int E = a.E, k = a.k;
   const size_t e8 = ((size_t)E + 7) / 8 * 8;
@@ -699,6 +699,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
       a.topk_idx[(size_t)t * k + lane] = order[lane];
       a.gates[(size_t)t * k + lane] = g / den;
     }
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
+  topk_token(a);
+  if (a.fuse_bucket) {  // one token: bucket its k pairs right here (no further launch)
+    __shared__ int sel_smem[kMaxK];
+    __syncthreads();
+    bucket_one_token(a.bucket, sel_smem);
   }
 }
 
