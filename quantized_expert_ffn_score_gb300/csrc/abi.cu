@@ -64,6 +64,7 @@ struct moe_ctx {
   int device;
   int num_sms;
   int gemm_min;  // experts with at least this many tokens take the tensor-core GEMM path (0: never)
+  int mxfp4_kernel;  // moe_mxfp4_kernel: block-scaled MMA path, or the GEMV/GEMM pair
   int* err;  // device: [0] status, [1] detail, [2..3] spare
   moe::Profiler* prof;
 };
@@ -84,6 +85,9 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 // Sequential carving of a workspace into 256-byte aligned regions.
+// Largest SM count the block-scaled path's per-CTA workspace is sized for.
+constexpr int kMaxSms = 160;
+
 struct Carver {
   char* base;
   size_t off = 0;
@@ -214,6 +218,7 @@ struct FfnWs {
   float* xscale;     // the per-slot scales of the activations and of h,
   float* hscale;
   uint8_t* row_ref;  // and each hot expert row's largest scale byte
+  void* bs;          // block-scaled path workspace (MXFP4, d and ff multiples of 512)
 };
 FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   FfnWs f;
@@ -225,6 +230,9 @@ FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   f.xs = nullptr;
   f.xscale = f.hscale = nullptr;
   f.row_ref = nullptr;
+  f.bs = nullptr;
+  if (q == MOE_QUANT_MXFP4 && moe::mxfp4_bs_supported(d, ff, E, MOE_BF16))
+    f.bs = c.take<uint8_t>(moe::mxfp4_bs_ws_bytes(T, k, d, ff, kMaxSms));
   if (q == MOE_QUANT_MXFP4 && moe::mxfp4_gemm_supported(d, ff, MOE_BF16)) {
     f.hot = c.take<int32_t>((size_t)E + 1);
     f.hot_blk = c.take<int32_t>((size_t)E + 1);
@@ -234,6 +242,30 @@ FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
     f.row_ref = c.take<uint8_t>((size_t)E * (2 * (size_t)ff + d));
   }
   return f;
+}
+
+// Whether this call's MXFP4 experts run on the block-scaled MMA path.
+bool use_bs(const moe_ctx* ctx, const FfnWs& w, int d, int ff, int E, moe_dtype x_dtype) {
+  return ctx->mxfp4_kernel == MOE_MXFP4_BLOCK_SCALED && w.bs != nullptr && moe::mxfp4_bs_supported(d, ff, E, x_dtype);
+}
+
+moe::BsLaunch bs_launch(const moe::FfnArgs& f, const FfnWs& w) {
+  moe::BsLaunch b;
+  b.records = f.records;
+  b.d = f.d;
+  b.ff = f.ff;
+  b.E = f.E;
+  b.k = f.k;
+  b.T = f.T;
+  b.act = f.act;
+  b.x = f.x;
+  b.offsets = f.offsets;
+  b.pair_ids = f.pair_ids;
+  b.active = f.active;
+  b.y_pairs = f.y_pairs;
+  b.ws = w.bs;
+  b.err = f.err;
+  return b;
 }
 
 // The GEMM-path split for one call: experts with at least ctx->gemm_min tokens
@@ -347,8 +379,9 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   int32_t* counts = counts_out ? counts_out : w.counts;
   moe::RouteArgs ra = route_args(x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, T, L->d, L->E, L->k,
                                  w.route, const_cast<int32_t*>(topk), const_cast<float*>(gates), ctx->err);
-  const moe::HotSplit split =
-      L->quant == MOE_QUANT_MXFP4 ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype) : moe::HotSplit{0, nullptr, nullptr};
+  const bool bs = L->quant == MOE_QUANT_MXFP4 && use_bs(ctx, w.ffn, L->d, L->ff, L->E, x_dtype);
+  const moe::HotSplit split = L->quant == MOE_QUANT_MXFP4 && !bs ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype)
+                                                                 : moe::HotSplit{0, nullptr, nullptr};
   moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
   if (T == 1) {  // one token: the top-k kernel buckets its pairs itself
     ra.fuse_bucket = 1;
@@ -363,7 +396,10 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, L->k, L->d, L->ff, L->E, L->act, w.offsets, w.pairs, w.y_pairs,
                              w.ffn);
   fa.max_x = w.route.max_x;  // computed by the router kernel
-  if (L->quant == MOE_QUANT_MXFP4) {
+  if (L->quant == MOE_QUANT_MXFP4 && bs) {
+    fa.records = L->mxfp4.records;
+    st = cuda_status(moe::launch_mxfp4_bs(bs_launch(fa, w.ffn), ctx->num_sms, true, s));
+  } else if (L->quant == MOE_QUANT_MXFP4) {
     fa.records = L->mxfp4.records;
     if (split.hot != nullptr) {
       st = cuda_status(moe::launch_mxfp4_gemm(gemm_args(fa, w.ffn), ctx->num_sms, true, s));
@@ -413,6 +449,7 @@ moe_status moe_ctx_create(moe_ctx** ctx, int device) {
   } else {
     c->device = device;
     c->gemm_min = kDefaultGemmMinTokens;
+    c->mxfp4_kernel = MOE_MXFP4_BLOCK_SCALED;
     if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         cudaMalloc(&c->err, 4 * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, 4 * sizeof(int)) != cudaSuccess) {
       if (c->err) cudaFree(c->err);
@@ -446,6 +483,14 @@ moe_status moe_ctx_set_gemm_min_tokens(moe_ctx* ctx, int min_tokens) {
 }
 
 int moe_ctx_gemm_min_tokens(const moe_ctx* ctx) { return ctx ? ctx->gemm_min : -1; }
+
+moe_status moe_ctx_set_mxfp4_kernel(moe_ctx* ctx, int kernel) {
+  if (ctx == nullptr || (kernel != MOE_MXFP4_BLOCK_SCALED && kernel != MOE_MXFP4_GEMV_GEMM)) return MOE_ERR_INVALID_ARG;
+  ctx->mxfp4_kernel = kernel;
+  return MOE_OK;
+}
+
+int moe_ctx_mxfp4_kernel(const moe_ctx* ctx) { return ctx ? ctx->mxfp4_kernel : -1; }
 
 moe_status moe_ctx_profile(moe_ctx* ctx, int capacity) {
   if (ctx == nullptr || capacity < 0) return MOE_ERR_INVALID_ARG;
@@ -666,6 +711,12 @@ moe_status moe_expert_ffn_mxfp4(moe_ctx* ctx, const void* x, moe_dtype x_dtype, 
                                     MOE_QUANT_MXFP4, offsets, pair_ids, y_pairs, ws, ws_bytes, &a, &w);
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
+  if (use_bs(ctx, w, experts->d, experts->ff, experts->E, x_dtype)) {
+    st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active),
+                                                     moe::HotSplit{0, nullptr, nullptr}, false, stream));
+    if (st != MOE_OK) return st;
+    return cuda_status(moe::launch_mxfp4_bs(bs_launch(a, w), ctx->num_sms, true, stream));
+  }
   const moe::HotSplit split = gemm_split(ctx, w, T, experts->d, experts->ff, x_dtype);
   st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), split, false,
                                                    stream));

@@ -199,6 +199,24 @@ struct FfnArgs {
 cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, const HotSplit& split, bool pdl,
                                        cudaStream_t s);
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
+// The FFN on the block-scaled tensor-core MMA (mxfp4_bs.cu): every expert
+// with tokens (active[] lists them all), bf16 activations, d and ff multiples
+// of 512.  ws: mxfp4_bs_ws_bytes(T, k, d, ff, num_sms) bytes, 256-byte aligned.
+struct BsLaunch {
+  const uint8_t* const* records;
+  int d, ff, E, k, T;
+  int act;
+  const void* x;
+  const int32_t* offsets;
+  const int32_t* pair_ids;
+  const int32_t* active;
+  float* y_pairs;
+  void* ws;
+  int* err;
+};
+bool mxfp4_bs_supported(int d, int ff, int E, int x_dtype);
+size_t mxfp4_bs_ws_bytes(int T, int k, int d, int ff, int max_sms);
+cudaError_t launch_mxfp4_bs(const BsLaunch& L, int num_sms, bool pdl, cudaStream_t s);
 // The same FFN with the inner products on mma.sync (mxfp4_mma_gemv.cu); bf16 activations.
 bool mxfp4_mma_gemv_supported(int d, int ff, int x_dtype);
 cudaError_t launch_mxfp4_ffn_mma(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);

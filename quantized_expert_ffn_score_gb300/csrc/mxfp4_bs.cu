@@ -1,0 +1,769 @@
+// mxfp4_bs.cu -- routed-expert FFN on MXFP4 weights with the block-scaled
+// tensor-core MMA (tcgen05.mma kind::mxf8f6f4): the E2M1 codes and their E8M0
+// block scales (OCP Microscaling Formats v1.0: one scale per 32 elements along
+// the contraction axis) go to the tensor core as stored, so no core decodes a
+// weight (LazyLoRA README, "The engine": a fused MXFP4 decode-and-dot that
+// consumes the packed weights, expert sums in fp32).
+//
+// Operands of one MMA (M = 128 weight rows, K = 32, N = activation columns):
+//   A  128 rows of one weight matrix: the record's code bytes, moved by TMA
+//      with the 16 x U4 (16-byte aligned) tensor-map type, which places every
+//      8 code bytes in a 16-byte slot of shared memory (the operand layout of
+//      4-bit types in this MMA kind); scale factors = the record's E8M0 bytes.
+//   B  activation terms in E4M3 with their own E8M0 block scales: an
+//      activation a is written as a sum of E4M3 terms, t_1 = RN(a / 2^s1),
+//      t_2 = RN((a - t_1 2^s1) / 2^s2), ..., each with a per-32-block scale
+//      that maps the block's largest remaining magnitude into [128, 256).
+//      Two terms reproduce a bf16 x exactly (8 significant bits; E4M3 holds 4),
+//      three terms carry about 12 significant bits of the fp32 h.  Term i of
+//      token n is row (i * nt + n) of B, so one MMA computes every term and the
+//      epilogue adds the columns of a token.
+//   D  fp32 in tensor memory.
+// Products and their sum are formed by the tensor core in fp32.
+//
+// Work units: (active expert, 128-row tile, n-tile of up to nt tokens,
+// K part).  gate/up (MODE 0) keeps the gate and up rows of the same 128 ff
+// indices in two accumulators, so the epilogue applies the activation; down
+// (MODE 1) writes y_pairs.  The persistent grid takes contiguous unit ranges.
+// With few units (decode) each tile's K is split in parts of 512 so that
+// every SM streams weights; consecutive parts of one tile in one CTA
+// accumulate in tensor memory, and a tile split between two CTAs is finished
+// by the one that arrives last (fp32 partial sums added in memory, then the
+// activation), which depends on no timing: two partial sums, and fp32
+// addition of two values is commutative.
+//
+// Warp roles (320 threads): 0 TMA producer (and the per-expert tensor maps),
+// 1 MMA issuer and TMEM owner, 2-5 scale-factor writers (one per TMEM lane
+// quarter), 6-9 epilogue (one per lane quarter).  Every wait is bounded.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "bucket_body.cuh"
+#include "moe_internal.cuh"
+#include "tc_ops.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;           // weight rows per tile (MMA M)
+constexpr int kBK = 128;           // K per pipeline stage
+constexpr int kGroupK = 512;       // K per scale-factor group (4 stages)
+constexpr int kMaxNT = 32;         // tokens per n-tile
+constexpr int kMaxStages = 12;
+constexpr int kMaxSfSlots = 4;
+constexpr int kThreads = 320;
+constexpr int kSplitMaxPairs = 128;  // K is split only for at most this many pairs
+constexpr int kMaxExperts = 4096;
+constexpr int kABytes = kBM * kBK;   // one A box in shared memory: 128 rows x 128 codes in 8-bit slots
+constexpr int kTxA = kBM * kBK / 2;  // bytes TMA moves for it
+constexpr int kBarBytes = 512;
+constexpr int kSmemBudget = 227 * 1024;
+
+template <int MODE>
+struct Bs {
+  static constexpr int kMats = MODE == 0 ? 2 : 1;   // weight matrices per tile
+  static constexpr int kTerms = MODE == 0 ? 2 : 3;  // activation terms
+  static constexpr int kSfACols = kMats * 16;       // per slot: 4 stages x 4 column groups per matrix
+  static constexpr int kSlotCols = kSfACols + 16;
+};
+
+// Pipeline and tensor-memory geometry of one launch (host computed).
+struct BsGeom {
+  int n_mma;        // MMA N (activation rows: terms x nt, rounded to 16)
+  int stages;       // shared-memory pipeline stages
+  int stage_bytes;  // kMats A boxes + the B rows (1 KB multiple)
+  int dcols;        // TMEM columns of one accumulator buffer (kMats x n_mma)
+  int sf_base;      // first scale-factor column (two accumulator buffers before it)
+  int sf_slots;
+};
+
+struct BsArgs {
+  const uint8_t* const* records;
+  int d, ff, E, k, T, P;
+  int act;
+  int nt;             // tokens per n-tile (multiple of 8, at most kMaxNT)
+  const int32_t* offsets;
+  const int32_t* pair_ids;
+  const int32_t* active;  // active[0] = count, then every expert with tokens
+  int* counters;          // [4 * units] split-tile arrival counts (zeroed by the prep kernel)
+  float* gsum;            // [P][ff] split accumulators of the gate and up sums (P <= kSplitMaxPairs)
+  float* usum;
+  uint8_t* xq;   // [2][P][d]   E4M3 terms of x, slot order
+  uint8_t* xsf;  // [2][P][d/32]
+  uint8_t* hq;   // [3][P][ff]  E4M3 terms of h, slot order
+  uint8_t* hsf;  // [3][P][ff/32]
+  float* y_pairs;
+  CUtensorMap* gmaps;  // [grid][2 matrices][2 buffers] per-CTA tensor maps of the current expert
+  int* err;
+  BsGeom g[2];  // per MODE
+  int max_units;  // per CTA (bound of the unit table in shared memory)
+};
+
+__device__ __forceinline__ bool rec_ok32(const uint8_t* rec) {
+  return rec != nullptr && ((reinterpret_cast<uintptr_t>(rec) & 31u) == 0);
+}
+
+__device__ __forceinline__ uint4 ldg128(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Round-to-nearest-even E4M3 byte of v (|v| < 448) and its exact value.
+__device__ __forceinline__ uint32_t to_e4m3(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(v));
+  return r & 0xFFu;
+}
+__device__ __forceinline__ float from_e4m3(uint32_t b) {
+  uint32_t h2;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(b | (b << 8)));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Writes the E4M3 terms of one 32-element block held one value per lane:
+// q[i * plane + lane] and the scale bytes sf[i * splane] (lane 0).
+template <int TERMS>
+__device__ __forceinline__ void emit_terms(float v, uint8_t* q, size_t plane, uint8_t* sf, size_t splane, int lane) {
+  float r = v;
+#pragma unroll
+  for (int i = 0; i < TERMS; ++i) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(r)));
+    const int e = (int)((mx >> 23) & 0xFFu);
+    // scale 2^(sb - 127) maps the block maximum into [128, 256)
+    const int sb = mx == 0u ? 127 : max(1, min(254, e - 7));
+    const uint32_t c = to_e4m3(r * pow2f(127 - sb));
+    r -= from_e4m3(c) * pow2f(sb - 127);
+    q[i * plane] = (uint8_t)c;
+    if (lane == 0) sf[i * splane] = (uint8_t)sb;
+  }
+}
+
+// x terms per slot (bucket order) and the zeroing of the split accumulators.
+__global__ void __launch_bounds__(256) bs_prep_x_kernel(const BsArgs a, const void* x) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long w0 = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nb = a.d / 32;
+  const long long tasks = (long long)a.P * nb;
+  const size_t plane = (size_t)a.P * a.d, splane = (size_t)a.P * nb;
+  for (long long t = w0; t < tasks; t += warps) {
+    const int slot = (int)(t / nb), b = (int)(t % nb);
+    const int tok = a.pair_ids[slot] / a.k;
+    const float v = bf16_bits_to_f32(static_cast<const uint16_t*>(x)[(size_t)tok * a.d + 32 * b + lane]);
+    emit_terms<2>(v, a.xq + (size_t)slot * a.d + 32 * b + lane, plane, a.xsf + (size_t)slot * nb + b, splane, lane);
+  }
+  if (a.P <= kSplitMaxPairs) {  // the split path accumulates into these
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x, nth = (long long)gridDim.x * blockDim.x;
+    const long long ng = (long long)a.P * a.ff, ny = (long long)a.P * a.d;
+    for (long long i = tid; i < ng; i += nth) {
+      a.gsum[i] = 0.f;
+      a.usum[i] = 0.f;
+    }
+    for (long long i = tid; i < ny; i += nth) a.y_pairs[i] = 0.f;
+    for (long long i = tid; i < 4LL * 8 * 160 * 2; i += nth) a.counters[i] = 0;
+  }
+}
+
+struct Unit {
+  int e, tile, kpart, s0, ntok;
+};
+// One entry of a CTA's unit table in shared memory (decoded once, in parallel,
+// so that no role waits on the dependent global loads of the decoding).
+struct UnitRec {
+  const uint8_t* rec;
+  int e, tile, kpart, s0, ntok, ok;
+};
+
+struct Plan {
+  int units, kparts, gpk;  // total units, K parts per tile, scale groups per part
+  const int* off;          // [n_active + 1] unit offsets (shared memory)
+};
+
+__device__ __forceinline__ Unit decode_unit(const BsArgs& a, const Plan& pl, int u) {
+  const int na = a.active[0];
+  int lo = 0, hi = na - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pl.off[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  Unit t;
+  t.e = a.active[1 + lo];
+  const int s_beg = a.offsets[t.e], ne = a.offsets[t.e + 1] - s_beg;
+  const int ntiles = (ne + a.nt - 1) / a.nt;
+  int local = u - pl.off[lo];
+  t.kpart = local % pl.kparts;
+  local /= pl.kparts;
+  const int ntile = local % ntiles;
+  t.tile = local / ntiles;
+  t.s0 = s_beg + ntile * a.nt;
+  t.ntok = min(a.nt, ne - ntile * a.nt);
+  return t;
+}
+
+// Position in a CTA's sequence of scale groups (units in order, each unit's
+// groups in order), skipping units whose expert record is unusable.
+struct Cursor {
+  int u, gi;  // u indexes the CTA's unit table
+  UnitRec t;
+  bool valid;
+  __device__ void seek(const UnitRec* tab, int nu) {
+    valid = false;
+    for (; u < nu; ++u) {
+      t = tab[u];
+      if (t.ok) {
+        valid = true;
+        return;
+      }
+    }
+  }
+  __device__ void advance(const UnitRec* tab, int nu, int gpk) {
+    if (++gi < gpk) return;
+    gi = 0;
+    ++u;
+    seek(tab, nu);
+  }
+};
+
+// The scale bytes one lane moves into TMEM for one group: its weight row's
+// 16 bytes per matrix (the group's 16 blocks = 4 stages x 4 K steps) and the
+// 16 bytes of activation rows 32 j + lane, j < 4.
+template <int MODE>
+struct SfRegs {
+  uint4 a[Bs<MODE>::kMats];
+  uint4 b[4];
+};
+
+template <int MODE>
+__device__ __forceinline__ void sf_load(SfRegs<MODE>& r, const BsArgs& a, const UnitRec& t, int grp, int q, int lane,
+                                        int nt) {
+  using C = Bs<MODE>;
+  const int K = MODE == 0 ? a.d : a.ff, rows = MODE == 0 ? a.ff : a.d, nbk = K / 32;
+  const size_t mat = (size_t)a.ff * a.d / 2 + (size_t)a.ff * a.d / 32;
+  const uint8_t* rec = t.rec;
+#pragma unroll
+  for (int m = 0; m < C::kMats; ++m) {
+    // the matrix's scale bytes [rows][K/32] follow its codes
+    const uint8_t* sc = rec + (MODE == 0 ? m * mat : 2 * mat) + (size_t)rows * (K / 2);
+    r.a[m] = ldg128(sc + (size_t)(t.tile * kBM + 32 * q + lane) * nbk + 16 * grp);
+  }
+  const uint8_t* bsf = MODE == 0 ? a.xsf : a.hsf;
+  const size_t bplane = (size_t)a.P * nbk;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int n = 32 * j + lane;
+    r.b[j] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    if (n < C::kTerms * nt) {
+      const int p = n / nt, sl = t.s0 + n % nt;
+      if (sl < a.P) r.b[j] = ldg128(bsf + p * bplane + (size_t)sl * nbk + 16 * grp);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    mxfp4_bs_kernel(const __grid_constant__ CUtensorMap tmpl, const __grid_constant__ CUtensorMap bm0,
+                    const __grid_constant__ CUtensorMap bm1, const __grid_constant__ CUtensorMap bm2, const BsArgs a) {
+  using C = Bs<MODE>;
+  const BsGeom G = a.g[MODE];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint8_t* smaps = smem + (size_t)G.stages * G.stage_bytes;  // [kMats] 128-byte tensor maps
+  uint64_t* full = reinterpret_cast<uint64_t*>(smaps + C::kMats * 128);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* sf_full = empty + kMaxStages;
+  uint64_t* sf_empty = sf_full + kMaxSfSlots;
+  uint64_t* acc_full = sf_empty + kMaxSfSlots;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done = acc_empty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  int* scan_scratch = reinterpret_cast<int*>(tslot + 2);  // [kThreads / 32]
+  int* unit_off = reinterpret_cast<int*>(smaps + C::kMats * 128 + kBarBytes);  // [n_active]
+  UnitRec* table = reinterpret_cast<UnitRec*>(
+      (reinterpret_cast<uintptr_t>(unit_off + a.E + 1) + 15) & ~uintptr_t(15));  // [max_units]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 1) {
+    tc::tmem_alloc(tslot, 512);
+    tc::tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int j = 0; j < G.sf_slots; ++j) {
+      mbar_init(&sf_full[j], 4);
+      mbar_init(&sf_empty[j], 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&acc_full[j], 1);
+      mbar_init(&acc_empty[j], 4);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {  // one copy of the weight tensor-map template per matrix, patched per expert
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&tmpl);
+    for (int m = 0; m < C::kMats; ++m) reinterpret_cast<uint32_t*>(smaps + m * 128)[lane] = src[lane];
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // ---- the unit plan (identical in every CTA)
+  const int K = MODE == 0 ? a.d : a.ff;
+  const int rows = MODE == 0 ? a.ff : a.d;
+  const int ntiles_rows = rows / kBM, ngroups = K / kGroupK;
+  const int na = a.active[0];
+  int total0 = 0;
+  Plan pl;
+  {
+    const int per = (na + kThreads - 1) / kThreads;
+    const int i0 = min(na, (int)threadIdx.x * per), i1 = min(na, i0 + per);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) {
+      const int e = a.active[1 + i], ne = a.offsets[e + 1] - a.offsets[e];
+      local += ntiles_rows * ((ne + a.nt - 1) / a.nt);
+    }
+    int base = bucket_detail::block_exclusive_scan(local, scan_scratch, &total0);
+    // few units (decode): split every tile's K into parts of one scale group
+    const bool split = total0 < 8 * (int)gridDim.x && a.P <= kSplitMaxPairs && ngroups > 1;
+    pl.kparts = split ? ngroups : 1;
+    pl.gpk = ngroups / pl.kparts;
+    pl.units = total0 * pl.kparts;
+    pl.off = unit_off;
+    for (int i = i0; i < i1; ++i) {
+      unit_off[i] = base * pl.kparts;
+      const int e = a.active[1 + i], ne = a.offsets[e + 1] - a.offsets[e];
+      base += ntiles_rows * ((ne + a.nt - 1) / a.nt);
+    }
+  }
+  __syncthreads();
+  const int ub = (int)((long long)pl.units * blockIdx.x / gridDim.x);
+  int nu = (int)((long long)pl.units * (blockIdx.x + 1) / gridDim.x) - ub;
+  if (nu > a.max_units) {  // cannot happen with the host's bound; leave the rest undone, reported
+    if (threadIdx.x == 0) dev_error(a.err, MOE_ERR_UNSUPPORTED, nu);
+    nu = a.max_units;
+  }
+  for (int i = threadIdx.x; i < nu; i += kThreads) {
+    const Unit t = decode_unit(a, pl, ub + i);
+    UnitRec r;
+    r.rec = a.records[t.e];
+    r.e = t.e;
+    r.tile = t.tile;
+    r.kpart = t.kpart;
+    r.s0 = t.s0;
+    r.ntok = t.ntok;
+    r.ok = rec_ok32(r.rec) ? 1 : 0;
+    table[i] = r;
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const size_t mat = (size_t)a.ff * a.d / 2 + (size_t)a.ff * a.d / 32;
+  const int nt = a.nt;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int it = 0, cur_e = -1, mbuf = 0;
+    bool ok = true;
+    for (int u = 0; u < nu && ok; ++u) {
+      const UnitRec t = table[u];
+      const uint8_t* rec = t.rec;
+      if (!t.ok) {
+        if (lane == 0) dev_error(a.err, rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG, t.e);
+        continue;
+      }
+      CUtensorMap* gm = a.gmaps + (size_t)blockIdx.x * 4;
+      if (t.e != cur_e) {  // this expert's weight tensor maps, in the buffer not used by copies in flight
+        cur_e = t.e;
+        mbuf ^= 1;
+        for (int m = 0; m < C::kMats; ++m) {
+          const uint8_t* base = rec + (MODE == 0 ? m * mat : 2 * mat);
+          if (lane == 0) tc::tensormap_set_address(smaps + m * 128, base);
+          __syncwarp();
+          tc::tensormap_publish(gm + m * 2 + mbuf, smaps + m * 128);
+          if (lane == 0) tc::tensormap_acquire(gm + m * 2 + mbuf);
+          __syncwarp();
+        }
+      }
+      if (lane == 0) {
+        const int c_end = (t.kpart + 1) * pl.gpk * 4;
+        for (int c = t.kpart * pl.gpk * 4; c < c_end; ++c, ++it) {
+          const int stage = it % G.stages, n = it / G.stages;
+          if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(C::kMats * kTxA + C::kTerms * nt * kBK));
+          uint8_t* st = stages + (size_t)stage * G.stage_bytes;
+          for (int m = 0; m < C::kMats; ++m)
+            tc::tma_load_2d(st + m * kABytes, gm + m * 2 + mbuf, c * kBK, t.tile * kBM, &full[stage]);
+          uint8_t* sb = st + C::kMats * kABytes;
+          tc::tma_load_2d(sb, &bm0, c * kBK, t.s0, &full[stage]);
+          tc::tma_load_2d(sb + nt * kBK, &bm1, c * kBK, t.s0, &full[stage]);
+          if (MODE == 1) tc::tma_load_2d(sb + 2 * nt * kBK, &bm2, c * kBK, t.s0, &full[stage]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0)  // never leave with copies in flight
+      for (int j = (it > G.stages ? it - G.stages : 0); j < it; ++j)
+        mbar_wait(&full[j % G.stages], (j / G.stages) & 1, a.err);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_e2m1_e4m3_bs(kBM, G.n_mma);
+      int it = 0, sfi = 0, seg = 0, buf = 0;
+      bool ok = true, fresh = true;
+      for (int u = 0; u < nu && ok; ++u) {
+        const UnitRec t = table[u];
+        if (!t.ok) continue;
+        const bool seg_start = u == 0 || t.kpart == 0;
+        const bool seg_end = u + 1 == nu || t.kpart == pl.kparts - 1;
+        if (seg_start) {
+          buf = seg & 1;
+          if (seg >= 2 && !mbar_wait(&acc_empty[buf], ((seg >> 1) - 1) & 1, a.err)) break;
+          tc::fence_after();
+          fresh = true;
+        }
+        const uint32_t d0 = tmem + (uint32_t)(buf * G.dcols);
+        for (int g = 0; g < pl.gpk && ok; ++g, ++sfi) {
+          const int slot = sfi % G.sf_slots;
+          if (!mbar_wait(&sf_full[slot], (sfi / G.sf_slots) & 1, a.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          const uint32_t sfa = tmem + (uint32_t)(G.sf_base + slot * C::kSlotCols);
+          for (int c = 0; c < 4; ++c, ++it) {
+            const int stage = it % G.stages;
+            if (!mbar_wait(&full[stage], (it / G.stages) & 1, a.err)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after();
+            const uint8_t* st = stages + (size_t)stage * G.stage_bytes;
+            const uint64_t bdesc = tc::desc_kmajor_sw128(tc::saddr(st + C::kMats * kABytes));
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t id = idesc | tc::idesc_sf_ids((uint32_t)ks, (uint32_t)ks);
+#pragma unroll
+              for (int m = 0; m < C::kMats; ++m) {
+                const uint64_t adesc = tc::desc_kmajor_sw128(tc::saddr(st + m * kABytes));
+                tc::mma_bs(d0 + m * G.n_mma, adesc + 2 * ks, bdesc + 2 * ks, id, sfa + m * 16 + 4 * c,
+                           sfa + C::kSfACols + 4 * c, fresh ? 0u : 1u);
+              }
+              fresh = false;
+            }
+            tc::mma_commit(&empty[stage]);
+          }
+          if (ok) tc::mma_commit(&sf_empty[slot]);
+        }
+        if (ok && seg_end) {
+          tc::mma_commit(&acc_full[buf]);
+          ++seg;
+        }
+      }
+      tc::mma_commit(done);  // every MMA issued above has completed before teardown
+      mbar_wait(done, 0, a.err);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ scale factors into TMEM
+    // Weight rows: lane quarter q reads row 32 q + r of every 128-row tile from
+    // lane 32 q + r, column (4 c + q) of the matrix's slot area for stage c of
+    // the group.  Activation rows 32 j + r: every quarter reads column (4 c + j)
+    // of its own lanes, so each quarter writes all of them.
+    const int q = warp & 3;
+    const uint32_t lb = (uint32_t)(32 * q) << 16;
+    Cursor cur;
+    cur.u = 0;
+    cur.gi = 0;
+    cur.seek(table, nu);
+    SfRegs<MODE> r0, r1;
+    if (cur.valid) sf_load<MODE>(r0, a, cur.t, cur.t.kpart * pl.gpk + cur.gi, q, lane, nt);
+    int sfi = 0;
+    while (cur.valid) {
+      Cursor nx = cur;
+      nx.advance(table, nu, pl.gpk);
+      if (nx.valid) sf_load<MODE>(r1, a, nx.t, nx.t.kpart * pl.gpk + nx.gi, q, lane, nt);  // in flight below
+      const int slot = sfi % G.sf_slots;
+      if (sfi >= G.sf_slots && !mbar_wait(&sf_empty[slot], ((sfi / G.sf_slots) - 1) & 1, a.err)) break;
+      tc::fence_after();
+      const uint32_t col = tmem + lb + (uint32_t)(G.sf_base + slot * C::kSlotCols);
+#pragma unroll
+      for (int m = 0; m < C::kMats; ++m) {
+        const uint32_t w[4] = {r0.a[m].x, r0.a[m].y, r0.a[m].z, r0.a[m].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_st1(col + m * 16 + 4 * c + q, w[c]);
+      }
+      {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[j] = r0.b[j].x;
+          v[4 + j] = r0.b[j].y;
+          v[8 + j] = r0.b[j].z;
+          v[12 + j] = r0.b[j].w;
+        }
+        tc::tmem_st16(col + C::kSfACols, v);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_full[slot]);
+      ++sfi;
+      cur = nx;
+      r0 = r1;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lb = (uint32_t)(32 * q) << 16;
+    int seg = 0, kp0 = 0;
+    for (int u = 0; u < nu; ++u) {
+      const UnitRec t = table[u];
+      if (!t.ok) continue;
+      if (u == 0 || t.kpart == 0) kp0 = t.kpart;
+      if (!(u + 1 == nu || t.kpart == pl.kparts - 1)) continue;
+      const int buf = seg & 1;
+      if (!mbar_wait(&acc_full[buf], (seg >> 1) & 1, a.err)) break;
+      tc::fence_after();
+      ++seg;
+      const bool whole = kp0 == 0 && t.kpart == pl.kparts - 1;
+      const int row = t.tile * kBM + 32 * q + lane;
+      const uint32_t dcol = tmem + lb + (uint32_t)(buf * G.dcols);
+      float s0[kMaxNT], s1[kMaxNT];  // MODE 0: gate and up sums; MODE 1: y in s0
+#pragma unroll
+      for (int n0 = 0; n0 < kMaxNT; n0 += 8) {
+        if (n0 < t.ntok) {
+          uint32_t v0[8], v1[8];
+#pragma unroll
+          for (int m = 0; m < C::kMats; ++m) {
+            tc::tmem_ld8_sync(dcol + m * G.n_mma + n0, v0);
+            tc::tmem_ld8_sync(dcol + m * G.n_mma + nt + n0, v1);
+            float* dst = m == 0 ? s0 : s1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[n0 + i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
+            if (MODE == 1) {
+              tc::tmem_ld8_sync(dcol + 2 * nt + n0, v0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[n0 + i] += __uint_as_float(v0[i]);
+            }
+          }
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+
+      if (MODE == 1) {
+#pragma unroll
+        for (int n = 0; n < kMaxNT; ++n) {
+          if (n < t.ntok) {
+            float* dst = a.y_pairs + (size_t)a.pair_ids[t.s0 + n] * a.d + row;
+            if (whole) *dst = s0[n];
+            else atomicAdd(dst, s0[n]);
+          }
+        }
+      } else {
+        const size_t hplane = (size_t)a.P * a.ff, hsplane = (size_t)a.P * (a.ff / 32);
+        bool finish = whole;
+        if (!whole) {  // add this part's sums; the last of the tile's parts to arrive finishes it
+#pragma unroll
+          for (int n = 0; n < kMaxNT; ++n) {
+            if (n < t.ntok) {
+              atomicAdd(a.gsum + (size_t)(t.s0 + n) * a.ff + row, s0[n]);
+              atomicAdd(a.usum + (size_t)(t.s0 + n) * a.ff + row, s1[n]);
+            }
+          }
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            const int id = (ub + u - t.kpart) / pl.kparts;
+            const int parts = t.kpart - kp0 + 1;
+            last = atomicAdd(a.counters + 4 * id + q, parts) + parts == pl.kparts;
+          }
+          finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+          if (finish) {
+            __threadfence();
+#pragma unroll
+            for (int n = 0; n < kMaxNT; ++n) {
+              if (n < t.ntok) {
+                s0[n] = __ldcg(a.gsum + (size_t)(t.s0 + n) * a.ff + row);
+                s1[n] = __ldcg(a.usum + (size_t)(t.s0 + n) * a.ff + row);
+              }
+            }
+          }
+        }
+        if (finish) {
+#pragma unroll
+          for (int n = 0; n < kMaxNT; ++n) {
+            if (n < t.ntok) {
+              const int slot = t.s0 + n;
+              const float h = act_fast(s0[n], s1[n], a.act);
+              emit_terms<3>(h, a.hq + (size_t)slot * a.ff + row, hplane, a.hsf + (size_t)slot * (a.ff / 32) + row / 32,
+                            hsplane, lane);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+}
+
+// Stage and tensor-memory geometry for nt tokens per n-tile and E experts.
+template <int MODE>
+bool make_geom(BsGeom* g, int nt, int E, int max_units) {
+  using C = Bs<MODE>;
+  g->n_mma = (C::kTerms * nt + 15) & ~15;
+  const int b_bytes = (g->n_mma * kBK + 1023) & ~1023;
+  g->stage_bytes = C::kMats * kABytes + b_bytes;
+  const int avail = kSmemBudget - 1024 - C::kMats * 128 - kBarBytes - (E + 1) * (int)sizeof(int) - 16 -
+                    max_units * (int)sizeof(UnitRec);
+  g->stages = avail / g->stage_bytes < kMaxStages ? avail / g->stage_bytes : kMaxStages;
+  g->dcols = C::kMats * g->n_mma;
+  g->sf_base = 2 * g->dcols;
+  const int slots = (512 - g->sf_base) / C::kSlotCols;
+  g->sf_slots = slots < kMaxSfSlots ? slots : kMaxSfSlots;
+  return g->stages >= 2 && g->sf_slots >= 2;
+}
+template <int MODE>
+size_t smem_bytes(const BsGeom& g, int E, int max_units) {
+  return 1024 + (size_t)g.stages * g.stage_bytes + Bs<MODE>::kMats * 128 + kBarBytes + ((size_t)E + 1) * sizeof(int) +
+         16 + (size_t)max_units * sizeof(UnitRec);
+}
+
+// Bound on the units one CTA gets: every active expert has at most
+// ceil(ne / nt) <= ne / nt + 1 n-tiles, and K is split only for few pairs.
+int max_units_per_cta(int rows, int K, int P, int E, int nt, int grid) {
+  const long long ntiles = (long long)(P + nt - 1) / nt + (P < E ? P : E);
+  const long long u0 = (long long)(rows / kBM) * ntiles;
+  const long long kp = P <= kSplitMaxPairs ? K / kGroupK : 1;
+  return (int)((u0 * kp + grid - 1) / grid) + 1;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Weight matrix [rows][K] of E2M1 codes (K / 2 bytes a row), boxes of 128
+// codes x 128 rows; the address is replaced per expert on the device.
+bool make_weight_map(CUtensorMap* m, const void* any_base, int K, int rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+  cuuint32_t box[2] = {kBK, kBM};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(any_base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// One plane of activation terms [P][K] E4M3, boxes of 128 x nt rows.
+bool make_term_map(CUtensorMap* m, const void* base, int K, int P, int nt) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {kBK, (cuuint32_t)nt};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool mxfp4_bs_supported(int d, int ff, int E, int x_dtype) {
+  return x_dtype == MOE_BF16 && d % kGroupK == 0 && ff % kGroupK == 0 && E <= kMaxExperts;
+}
+
+size_t mxfp4_bs_ws_bytes(int T, int k, int d, int ff, int max_sms) {
+  const size_t P = (size_t)T * k, Ps = P <= (size_t)kSplitMaxPairs ? P : 1;
+  return 2 * P * (d + d / 32) + 3 * P * (ff + ff / 32) + 2 * Ps * ff * sizeof(float) +
+         (size_t)4 * 8 * 160 * 2 * sizeof(int) + (size_t)max_sms * 4 * sizeof(CUtensorMap) + 8 * 256;
+}
+
+cudaError_t launch_mxfp4_bs(const BsLaunch& L, int num_sms, bool pdl, cudaStream_t s) {
+  if (L.T == 0) return cudaSuccess;
+  BsArgs a;
+  a.records = L.records;
+  a.d = L.d;
+  a.ff = L.ff;
+  a.E = L.E;
+  a.k = L.k;
+  a.T = L.T;
+  a.P = L.T * L.k;
+  a.act = L.act;
+  a.nt = L.T >= kMaxNT ? kMaxNT : ((L.T + 7) & ~7);
+  a.offsets = L.offsets;
+  a.pair_ids = L.pair_ids;
+  a.active = L.active;
+  // carve the workspace
+  uint8_t* p = static_cast<uint8_t*>(L.ws);
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p;
+    p += (bytes + 255) & ~size_t(255);
+    return r;
+  };
+  const size_t P = (size_t)a.P, Ps = P <= (size_t)kSplitMaxPairs ? P : 1;
+  a.gmaps = reinterpret_cast<CUtensorMap*>(take((size_t)num_sms * 4 * sizeof(CUtensorMap)));
+  a.xq = take(2 * P * a.d);
+  a.xsf = take(2 * P * (a.d / 32));
+  a.hq = take(3 * P * a.ff);
+  a.hsf = take(3 * P * (a.ff / 32));
+  a.gsum = reinterpret_cast<float*>(take(Ps * a.ff * sizeof(float)));
+  a.usum = reinterpret_cast<float*>(take(Ps * a.ff * sizeof(float)));
+  a.counters = reinterpret_cast<int*>(take((size_t)4 * 8 * 160 * 2 * sizeof(int)));
+  a.y_pairs = L.y_pairs;
+  a.err = L.err;
+  if (num_sms > 160) return cudaErrorInvalidValue;  // the split counters are sized for 8 units per SM
+  CUtensorMap w0, w1, x0, x1, h0, h1, h2;
+  if (!make_weight_map(&w0, a.xq, a.d, a.ff) || !make_weight_map(&w1, a.xq, a.ff, a.d) ||
+      !make_term_map(&x0, a.xq, a.d, a.P, a.nt) || !make_term_map(&x1, a.xq + P * a.d, a.d, a.P, a.nt) ||
+      !make_term_map(&h0, a.hq, a.ff, a.P, a.nt) || !make_term_map(&h1, a.hq + P * a.ff, a.ff, a.P, a.nt) ||
+      !make_term_map(&h2, a.hq + 2 * P * a.ff, a.ff, a.P, a.nt))
+    return cudaErrorInvalidValue;
+  const int mu0 = max_units_per_cta(a.ff, a.d, a.P, a.E, a.nt, num_sms);
+  const int mu1 = max_units_per_cta(a.d, a.ff, a.P, a.E, a.nt, num_sms);
+  a.max_units = mu0 > mu1 ? mu0 : mu1;
+  if (!make_geom<0>(&a.g[0], a.nt, a.E, a.max_units) || !make_geom<1>(&a.g[1], a.nt, a.E, a.max_units))
+    return cudaErrorInvalidValue;
+  cudaError_t err = launch("bs_prep_x", bs_prep_x_kernel, dim3(4 * num_sms), dim3(256), 0, s, pdl, a, L.x);
+  if (err != cudaSuccess) return err;
+  const size_t smem0 = smem_bytes<0>(a.g[0], a.E, a.max_units), smem1 = smem_bytes<1>(a.g[1], a.E, a.max_units);
+  ensure_smem(mxfp4_bs_kernel<0>, smem0);
+  err = launch("mxfp4_bs_gate_up", mxfp4_bs_kernel<0>, dim3(num_sms), dim3(kThreads), smem0, s, true, w0, x0, x1, x1,
+               a);
+  if (err != cudaSuccess) return err;
+  ensure_smem(mxfp4_bs_kernel<1>, smem1);
+  return launch("mxfp4_bs_down", mxfp4_bs_kernel<1>, dim3(num_sms), dim3(kThreads), smem1, s, true, w1, h0, h1, h2,
+                a);
+}
+
+}  // namespace moe

@@ -148,6 +148,64 @@ __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
                : "memory");
 }
 
+// ------------------------------------------------------------------ block-scaled MMA
+// Instruction descriptor, kind::mxf8f6f4 with E8M0 block scales (one per 32
+// along K): A E2M1 (bits 7-9 = 5), B E4M3 (bits 10-12 = 0), both K-major,
+// N >> 3 in bits 17-22, scale type E8M0 (bit 23), M >> 4 in bits 24-28.  The
+// scale-factor byte selectors (bits 29-30 for A, 4-5 for B) are added per
+// K step by the caller.
+__host__ __device__ constexpr uint32_t idesc_e2m1_e4m3_bs(int M, int N) {
+  return (5u << 7) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) { return (a_id << 29) | (b_id << 4); }
+// D[tmem] (+)= (A * sfA) (B * sfB)^T over K = 32: A and B in shared memory (the
+// A operand E2M1 codes as the 16 x U4, 16-byte-aligned tensor-map type lays
+// them out: 8 code bytes then an 8-byte gap per 16 codes; 128-byte swizzle),
+// scale factors in TMEM.  Scale layout for an operand of R rows (R <= 128):
+// row 32 j + r is read from lane (32 q + r) of column (sf + j) for the lane
+// quarter q that computes it, byte = the selector in the descriptor, so each
+// column group is written to all four lane quarters.
+__device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v));
+}
+__device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile(
+      "{\n tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+      " tcgen05.wait::ld.sync.aligned;\n}"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+      : "r"(taddr));
+}
+
+// ------------------------------------------------------------------ tensor maps patched on the device
+// Sets the global address of the tensor map held in shared memory.
+__device__ __forceinline__ void tensormap_set_address(void* smem_map, const void* gaddr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(saddr(smem_map)),
+               "l"(reinterpret_cast<uint64_t>(gaddr))
+               : "memory");
+}
+// Copies a tensor map from shared to global memory with a release of the
+// tensor-map proxy (whole warp).
+__device__ __forceinline__ void tensormap_publish(void* gmap, const void* smem_map) {
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;" ::"l"(
+          reinterpret_cast<uint64_t>(gmap)),
+      "r"(saddr(smem_map))
+      : "memory");
+}
+// Acquire side before the tensor map in global memory is used by TMA.
+__device__ __forceinline__ void tensormap_acquire(const void* gmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(gmap))
+               : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 // 2-D tiled load of one box at element coordinates (c0 inner, c1 outer),
 // completing its bytes on `mbar`.  c0 * element size must be a multiple of 16.

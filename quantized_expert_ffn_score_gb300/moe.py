@@ -19,10 +19,12 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 MOE_F32, MOE_BF16 = 0, 1
 ACT = {"swiglu": 0, "situ": 1}
 QUANT = {"mxfp4": 0, "rvq3": 1}
+MXFP4_KERNEL = {"block_scaled": 0, "gemv_gemm": 1}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy", "moe_ctx_check", "moe_ctx_num_sms",
            "moe_ctx_set_gemm_min_tokens", "moe_ctx_gemm_min_tokens",
+           "moe_ctx_set_mxfp4_kernel", "moe_ctx_mxfp4_kernel",
            "moe_ctx_profile", "moe_ctx_profile_read", "moe_ctx_stats",
            "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
@@ -107,6 +109,8 @@ def lib():
         L.moe_ctx_num_sms.restype = i32
         L.moe_ctx_set_gemm_min_tokens.argtypes, L.moe_ctx_set_gemm_min_tokens.restype = [vp, i32], i32
         L.moe_ctx_gemm_min_tokens.argtypes, L.moe_ctx_gemm_min_tokens.restype = [vp], i32
+        L.moe_ctx_set_mxfp4_kernel.argtypes, L.moe_ctx_set_mxfp4_kernel.restype = [vp, i32], i32
+        L.moe_ctx_mxfp4_kernel.argtypes, L.moe_ctx_mxfp4_kernel.restype = [vp], i32
         _lib = L
     return _lib
 
@@ -172,6 +176,16 @@ class Context:
     @gemm_min_tokens.setter
     def gemm_min_tokens(self, n):
         _check(lib().moe_ctx_set_gemm_min_tokens(self.handle, int(n)), "moe_ctx_set_gemm_min_tokens")
+
+    @property
+    def mxfp4_kernel(self):
+        """'block_scaled' (tensor-core MMA on the stored codes and scales) or 'gemv_gemm'."""
+        v = lib().moe_ctx_mxfp4_kernel(self.handle)
+        return {k: n for n, k in MXFP4_KERNEL.items()}.get(v, v)
+
+    @mxfp4_kernel.setter
+    def mxfp4_kernel(self, name):
+        _check(lib().moe_ctx_set_mxfp4_kernel(self.handle, MXFP4_KERNEL[name]), "moe_ctx_set_mxfp4_kernel")
 
     def profile(self, capacity):
         """Turns per-launch event timing on (capacity launches between reads) or off (0)."""

@@ -7,7 +7,8 @@ with several 128-token blocks and ragged tails, many with a handful), alone
 (threshold 1: every expert, down to one token, on the tensor cores), with the
 last bucket of the slot range hot (its final token box reaches past the end of
 the activations), with SiTU, through the standalone expert call, and with a
-hot expert's record missing."""
+hot expert's record missing.  The context selects that kernel pair
+(moe_ctx_set_mxfp4_kernel); the block-scaled kernel has its own tests."""
 import numpy as np
 import pytest
 import torch
@@ -33,6 +34,7 @@ def lib():
 @pytest.fixture()
 def ctx(lib):
     c = lib.Context(0)
+    c.mxfp4_kernel = "gemv_gemm"  # these cases are about that kernel pair
     yield c
     c.close()
 
