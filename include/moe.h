@@ -189,22 +189,25 @@ MOE_API int moe_ctx_gemm_min_tokens(const moe_ctx* ctx);
 
 /* MXFP4 expert kernels (OCP MX v1.0 E2M1 codes with E8M0 scales per 32; the
  * pages' MXFP4 experts, LazyLoRA README "The engine").
- *   MOE_MXFP4_BLOCK_SCALED (default): every routed expert on the block-scaled
- *     tensor-core MMA: the record's codes and scale bytes are the A operand as
- *     stored; the activations enter as a sum of E4M3 terms with their own
- *     E8M0 scales (x: two terms, exactly the bf16 value; h: three terms, about
- *     12 significant bits); products and sums in fp32.  Used when the
- *     activations are bf16, d and ff are multiples of 512, E <= 4096, the
- *     device has at most 160 SMs and every routed record is 32-byte aligned
- *     (a misaligned record sets MOE_ERR_INVALID_ARG on the error word);
- *     otherwise the call falls back to the pair below.
+ *   MOE_MXFP4_BLOCK_SCALED: every routed expert on the block-scaled tensor-core
+ *     MMA: the record's codes and scale bytes are the A operand as stored; the
+ *     activations enter as a sum of E4M3 terms with their own E8M0 scales (x:
+ *     two terms, exactly the bf16 value; h: three terms, about 12 significant
+ *     bits); products and sums in fp32.  Used when the activations are bf16,
+ *     d and ff are multiples of 512, E <= 4096, the device has at most 160
+ *     SMs and every routed record is 32-byte aligned (a misaligned record sets
+ *     MOE_ERR_INVALID_ARG on the error word); otherwise the call falls back to
+ *     the pair below.
  *   MOE_MXFP4_GEMV_GEMM: the warp-level GEMV for experts with few tokens and
  *     the f16 grouped GEMM for experts with at least moe_ctx_gemm_min_tokens
  *     tokens (every product exact in f16/fp32).
- * Both compute the same layer within the fp32 tolerance.  Other values return
+ *   MOE_MXFP4_AUTO (default): the GEMV pair for calls of one token, the
+ *     block-scaled kernel for more (the faster of the two on a GB300 for
+ *     each case).
+ * All compute the same layer within the fp32 tolerance.  Other values return
  * MOE_ERR_INVALID_ARG.  moe_ctx_mxfp4_kernel returns the setting, or -1 for a
  * NULL context. */
-typedef enum { MOE_MXFP4_BLOCK_SCALED = 0, MOE_MXFP4_GEMV_GEMM = 1 } moe_mxfp4_kernel;
+typedef enum { MOE_MXFP4_BLOCK_SCALED = 0, MOE_MXFP4_GEMV_GEMM = 1, MOE_MXFP4_AUTO = 2 } moe_mxfp4_kernel;
 MOE_API moe_status moe_ctx_set_mxfp4_kernel(moe_ctx* ctx, int kernel);
 MOE_API int moe_ctx_mxfp4_kernel(const moe_ctx* ctx);
 

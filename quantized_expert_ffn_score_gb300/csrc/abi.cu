@@ -245,8 +245,9 @@ FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
 }
 
 // Whether this call's MXFP4 experts run on the block-scaled MMA path.
-bool use_bs(const moe_ctx* ctx, const FfnWs& w, int d, int ff, int E, moe_dtype x_dtype) {
-  return ctx->mxfp4_kernel == MOE_MXFP4_BLOCK_SCALED && w.bs != nullptr && moe::mxfp4_bs_supported(d, ff, E, x_dtype);
+bool use_bs(const moe_ctx* ctx, const FfnWs& w, int T, int d, int ff, int E, moe_dtype x_dtype) {
+  const bool want = ctx->mxfp4_kernel == MOE_MXFP4_BLOCK_SCALED || (ctx->mxfp4_kernel == MOE_MXFP4_AUTO && T >= 2);
+  return want && w.bs != nullptr && moe::mxfp4_bs_supported(d, ff, E, x_dtype);
 }
 
 moe::BsLaunch bs_launch(const moe::FfnArgs& f, const FfnWs& w) {
@@ -379,7 +380,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   int32_t* counts = counts_out ? counts_out : w.counts;
   moe::RouteArgs ra = route_args(x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, T, L->d, L->E, L->k,
                                  w.route, const_cast<int32_t*>(topk), const_cast<float*>(gates), ctx->err);
-  const bool bs = L->quant == MOE_QUANT_MXFP4 && use_bs(ctx, w.ffn, L->d, L->ff, L->E, x_dtype);
+  const bool bs = L->quant == MOE_QUANT_MXFP4 && use_bs(ctx, w.ffn, T, L->d, L->ff, L->E, x_dtype);
   const moe::HotSplit split = L->quant == MOE_QUANT_MXFP4 && !bs ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype)
                                                                  : moe::HotSplit{0, nullptr, nullptr};
   moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
@@ -449,7 +450,7 @@ moe_status moe_ctx_create(moe_ctx** ctx, int device) {
   } else {
     c->device = device;
     c->gemm_min = kDefaultGemmMinTokens;
-    c->mxfp4_kernel = MOE_MXFP4_BLOCK_SCALED;
+    c->mxfp4_kernel = MOE_MXFP4_AUTO;
     if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         cudaMalloc(&c->err, 4 * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, 4 * sizeof(int)) != cudaSuccess) {
       if (c->err) cudaFree(c->err);
@@ -485,7 +486,8 @@ moe_status moe_ctx_set_gemm_min_tokens(moe_ctx* ctx, int min_tokens) {
 int moe_ctx_gemm_min_tokens(const moe_ctx* ctx) { return ctx ? ctx->gemm_min : -1; }
 
 moe_status moe_ctx_set_mxfp4_kernel(moe_ctx* ctx, int kernel) {
-  if (ctx == nullptr || (kernel != MOE_MXFP4_BLOCK_SCALED && kernel != MOE_MXFP4_GEMV_GEMM)) return MOE_ERR_INVALID_ARG;
+  if (ctx == nullptr || (kernel != MOE_MXFP4_BLOCK_SCALED && kernel != MOE_MXFP4_GEMV_GEMM && kernel != MOE_MXFP4_AUTO))
+    return MOE_ERR_INVALID_ARG;
   ctx->mxfp4_kernel = kernel;
   return MOE_OK;
 }
@@ -711,7 +713,7 @@ moe_status moe_expert_ffn_mxfp4(moe_ctx* ctx, const void* x, moe_dtype x_dtype, 
                                     MOE_QUANT_MXFP4, offsets, pair_ids, y_pairs, ws, ws_bytes, &a, &w);
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
-  if (use_bs(ctx, w, experts->d, experts->ff, experts->E, x_dtype)) {
+  if (use_bs(ctx, w, T, experts->d, experts->ff, experts->E, x_dtype)) {
     st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active),
                                                      moe::HotSplit{0, nullptr, nullptr}, false, stream));
     if (st != MOE_OK) return st;

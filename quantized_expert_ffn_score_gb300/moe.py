@@ -19,7 +19,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 MOE_F32, MOE_BF16 = 0, 1
 ACT = {"swiglu": 0, "situ": 1}
 QUANT = {"mxfp4": 0, "rvq3": 1}
-MXFP4_KERNEL = {"block_scaled": 0, "gemv_gemm": 1}
+MXFP4_KERNEL = {"block_scaled": 0, "gemv_gemm": 1, "auto": 2}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy", "moe_ctx_check", "moe_ctx_num_sms",
@@ -179,7 +179,7 @@ class Context:
 
     @property
     def mxfp4_kernel(self):
-        """'block_scaled' (tensor-core MMA on the stored codes and scales) or 'gemv_gemm'."""
+        """'auto' (default), 'block_scaled' (tensor-core MMA on the stored codes and scales) or 'gemv_gemm'."""
         v = lib().moe_ctx_mxfp4_kernel(self.handle)
         return {k: n for n, k in MXFP4_KERNEL.items()}.get(v, v)
 

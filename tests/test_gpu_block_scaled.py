@@ -1,14 +1,15 @@
-"""The block-scaled tensor-core kernel of the MXFP4 expert FFN (the default
-for bf16 activations with d, ff multiples of 512) against the fp64 oracle,
-through the C ABI.
+"""The block-scaled tensor-core kernel of the MXFP4 expert FFN (chosen by
+default for bf16 activations with d, ff multiples of 512 and more than one
+token; selected explicitly here) against the fp64 oracle, through the C ABI.
 
 Cases: the smallest shapes (one scale group along K, a single 8-token
 n-tile, ragged buckets), K split across CTAs with the last-arriver epilogue
 (few pairs: every tile's K in parts of 512), several n-tiles of 32 tokens with
 ragged tails under a Zipf-skewed router, SiTU, the standalone expert call
 against the oracle's per-pair outputs, agreement with the GEMV/GEMM kernel
-pair, and a missing expert reported on the error word.  The K3 decode and
-prefill layers run on this kernel in test_gpu_parity.py."""
+pair, one-token decode at the K3 shape, and a missing expert reported on
+the error word.  The K3 prefill layers run on this kernel by default in
+test_gpu_parity.py."""
 import numpy as np
 import pytest
 import torch
@@ -39,14 +40,16 @@ def lib():
 @pytest.fixture()
 def ctx(lib):
     c = lib.Context(0)
-    assert c.mxfp4_kernel == "block_scaled"
+    assert c.mxfp4_kernel == "auto"
+    c.mxfp4_kernel = "block_scaled"
     yield c
     c.close()
 
 
 def test_setting_round_trips(lib, ctx):
-    ctx.mxfp4_kernel = "gemv_gemm"
-    assert ctx.mxfp4_kernel == "gemv_gemm"
+    for name in ("gemv_gemm", "auto"):
+        ctx.mxfp4_kernel = name
+        assert ctx.mxfp4_kernel == name
     ctx.mxfp4_kernel = "block_scaled"
     assert ctx.mxfp4_kernel == "block_scaled"
 
@@ -137,3 +140,7 @@ def test_missing_expert_is_reported(lib, ctx):
     with pytest.raises(lib.MoeError) as ei:
         ctx.check()
     assert ei.value.name == "MOE_ERR_MISSING_EXPERT"
+
+
+def test_k3_decode_one_token(lib, ctx):
+    gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_decode_e64"))
