@@ -143,24 +143,61 @@ __device__ __forceinline__ void emit_terms(float v, uint8_t* q, size_t plane, ui
   }
 }
 
-// x terms per slot (bucket order) and the zeroing of the split accumulators.
+// The TERMS E4M3 terms of one 32-element block held by one thread: codes to
+// q[i * plane + j] (16-byte stores), scale bytes to sf[i * splane].
+template <int TERMS>
+__device__ __forceinline__ void block_terms(float (&r)[32], uint8_t* q, size_t plane, uint8_t* sf, size_t splane) {
+#pragma unroll
+  for (int i = 0; i < TERMS; ++i) {
+    uint32_t mx = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = max(mx, __float_as_uint(fabsf(r[j])));
+    const int e = (int)((mx >> 23) & 0xFFu);
+    const int sb = mx == 0u ? 127 : max(1, min(254, e - 7));
+    const float inv = pow2f(127 - sb), scl = pow2f(sb - 127);
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t c = to_e4m3(r[j] * inv);
+      r[j] -= from_e4m3(c) * scl;
+      w[j >> 2] |= c << (8 * (j & 3));
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q + i * plane);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    sf[i * splane] = (uint8_t)sb;
+  }
+}
+
+// x terms per slot (bucket order), one 32-element block per thread, and the
+// zeroing of the split accumulators.
 __global__ void __launch_bounds__(256) bs_prep_x_kernel(const BsArgs a, const void* x) {
   pdl_wait();
   pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long w0 = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x, nth = (long long)gridDim.x * blockDim.x;
   const int nb = a.d / 32;
   const long long tasks = (long long)a.P * nb;
   const size_t plane = (size_t)a.P * a.d, splane = (size_t)a.P * nb;
-  for (long long t = w0; t < tasks; t += warps) {
+  for (long long t = tid; t < tasks; t += nth) {
     const int slot = (int)(t / nb), b = (int)(t % nb);
     const int tok = a.pair_ids[slot] / a.k;
-    const float v = bf16_bits_to_f32(static_cast<const uint16_t*>(x)[(size_t)tok * a.d + 32 * b + lane]);
-    emit_terms<2>(v, a.xq + (size_t)slot * a.d + 32 * b + lane, plane, a.xsf + (size_t)slot * nb + b, splane, lane);
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)tok * a.d + 32 * b);
+    float r[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = src[q];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        r[8 * q + 2 * h] = __uint_as_float(u[h] << 16);
+        r[8 * q + 2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+      }
+    }
+    block_terms<2>(r, a.xq + (size_t)slot * a.d + 32 * b, plane, a.xsf + (size_t)slot * nb + b, splane);
   }
   if (a.P <= kSplitMaxPairs) {  // the split path accumulates into these
-    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x, nth = (long long)gridDim.x * blockDim.x;
     const long long ng = (long long)a.P * a.ff, ny = (long long)a.P * a.d;
     for (long long i = tid; i < ng; i += nth) {
       a.gsum[i] = 0.f;

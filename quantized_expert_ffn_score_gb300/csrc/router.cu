@@ -92,12 +92,15 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
 }
 
-// One warp per expert row, up to kTokTile tokens per CTA (x staged in shared
-// memory as fp32).  Lane chunk c covers columns (32c + lane) * N .. + N, and
-// the lane keeps one accumulator per element position of its chunk, so the
-// depth of the summation tree is ceil(d/(32N)) + log2(N) + 5.  The weights do
-// not depend on the previous kernel, so a lane issues the loads of its first
-// kLoadBatch chunks before waiting for it.
+// kRowsPerWarp expert rows per warp, taken one after the other, up to
+// kTokTile tokens per CTA (x staged in shared memory as fp32 once for the
+// CTA's kLogitWarps * kRowsPerWarp rows).  Lane chunk c covers columns
+// (32c + lane) * N .. + N, and the lane keeps one accumulator per element
+// position of its chunk, so the depth of the summation tree is
+// ceil(d/(32N)) + log2(N) + 5.  The weights do not depend on the previous
+// kernel, so a lane issues the loads of its first row's first kLoadBatch
+// chunks before waiting for it.
+constexpr int kRowsPerWarp = 4;
 template <typename WT>
 __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteArgs a) {
   extern __shared__ float xs[];  // [kTokTile][d]
@@ -106,76 +109,88 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   const int t0 = blockIdx.y * kTokTile;
   const int nt = min(kTokTile, a.T - t0);
   const int d = a.d;
-  const int e = blockIdx.x * kLogitWarps + warp;
   const int nch = d / (32 * N);        // whole warp-wide chunk rows
   const int rem = d - nch * 32 * N;    // columns left over (a multiple of N)
+  const int e_first = (blockIdx.x * kLogitWarps + warp) * kRowsPerWarp;
   uint4 wv[kLoadBatch];
-  const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)(e < a.E ? e : 0) * d);
+  {
+    const uint4* wrow =
+        reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)(e_first < a.E ? e_first : 0) * d);
 #pragma unroll
-  for (int u = 0; u < kLoadBatch; ++u)
-    if (e < a.E && u < nch) wv[u] = __ldg(wrow + u * 32 + lane);
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (e_first < a.E && u < nch) wv[u] = __ldg(wrow + u * 32 + lane);
+  }
   pdl_wait();
   stage_x(a, t0, nt, xs);
   __syncthreads();
   if (blockIdx.x == 0 && warp < nt) token_stats(a, xs + warp * d, t0 + warp);
-  if (e >= a.E) return;
-  float acc[kTokTile][N];
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int e = e_first + r;
+    if (e >= a.E) break;
+    const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)e * d);
+    if (r > 0) {
 #pragma unroll
-  for (int t = 0; t < kTokTile; ++t)
+      for (int u = 0; u < kLoadBatch; ++u)
+        if (u < nch) wv[u] = __ldg(wrow + u * 32 + lane);
+    }
+    float acc[kTokTile][N];
 #pragma unroll
-    for (int m = 0; m < N; ++m) acc[t][m] = 0.f;
-  float sq = 0.f;
-  auto consume = [&](const uint4 raw, int c) {
-    float w[N];
-    Vec16<WT>::unpack(raw, w);
+    for (int t = 0; t < kTokTile; ++t)
 #pragma unroll
-    for (int m = 0; m < N; ++m) sq = fmaf(w[m], w[m], sq);
+      for (int m = 0; m < N; ++m) acc[t][m] = 0.f;
+    float sq = 0.f;
+    auto consume = [&](const uint4 raw, int c) {
+      float w[N];
+      Vec16<WT>::unpack(raw, w);
 #pragma unroll
-    for (int t = 0; t < kTokTile; ++t) {
-      if (t < nt) {
-        const float4* xv = reinterpret_cast<const float4*>(xs + t * d + c);  // d, c multiples of 4
+      for (int m = 0; m < N; ++m) sq = fmaf(w[m], w[m], sq);
 #pragma unroll
-        for (int q = 0; q < N / 4; ++q) {
-          const float4 x4 = xv[q];
-          acc[t][4 * q + 0] = fmaf(w[4 * q + 0], x4.x, acc[t][4 * q + 0]);
-          acc[t][4 * q + 1] = fmaf(w[4 * q + 1], x4.y, acc[t][4 * q + 1]);
-          acc[t][4 * q + 2] = fmaf(w[4 * q + 2], x4.z, acc[t][4 * q + 2]);
-          acc[t][4 * q + 3] = fmaf(w[4 * q + 3], x4.w, acc[t][4 * q + 3]);
+      for (int t = 0; t < kTokTile; ++t) {
+        if (t < nt) {
+          const float4* xv = reinterpret_cast<const float4*>(xs + t * d + c);  // d, c multiples of 4
+#pragma unroll
+          for (int q = 0; q < N / 4; ++q) {
+            const float4 x4 = xv[q];
+            acc[t][4 * q + 0] = fmaf(w[4 * q + 0], x4.x, acc[t][4 * q + 0]);
+            acc[t][4 * q + 1] = fmaf(w[4 * q + 1], x4.y, acc[t][4 * q + 1]);
+            acc[t][4 * q + 2] = fmaf(w[4 * q + 2], x4.z, acc[t][4 * q + 2]);
+            acc[t][4 * q + 3] = fmaf(w[4 * q + 3], x4.w, acc[t][4 * q + 3]);
+          }
         }
       }
+    };
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (u < nch) consume(wv[u], (u * 32 + lane) * N);
+    for (int cb = kLoadBatch; cb < nch; cb += kLoadBatch) {
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u)
+        if (cb + u < nch) wv[u] = __ldg(wrow + (cb + u) * 32 + lane);
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u)
+        if (cb + u < nch) consume(wv[u], ((cb + u) * 32 + lane) * N);
     }
-  };
+    if (lane * N < rem) consume(__ldg(wrow + nch * 32 + lane), (nch * 32 + lane) * N);
+    if (blockIdx.y == 0) {
 #pragma unroll
-  for (int u = 0; u < kLoadBatch; ++u)
-    if (u < nch) consume(wv[u], (u * 32 + lane) * N);
-  for (int cb = kLoadBatch; cb < nch; cb += kLoadBatch) {
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      if (lane == 0) a.nrm_w[e] = sqrtf(sq);
+    }
+    const float b = a.bias ? a.bias[e] : 0.f;
 #pragma unroll
-    for (int u = 0; u < kLoadBatch; ++u)
-      if (cb + u < nch) wv[u] = __ldg(wrow + (cb + u) * 32 + lane);
+    for (int t = 0; t < kTokTile; ++t) {
+      if (t >= nt) break;
 #pragma unroll
-    for (int u = 0; u < kLoadBatch; ++u)
-      if (cb + u < nch) consume(wv[u], ((cb + u) * 32 + lane) * N);
-  }
-  if (lane * N < rem) consume(__ldg(wrow + nch * 32 + lane), (nch * 32 + lane) * N);
-  if (blockIdx.y == 0) {
+      for (int w = N / 2; w > 0; w >>= 1)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) a.nrm_w[e] = sqrtf(sq);
+        for (int m = 0; m < w; ++m) acc[t][m] += acc[t][m + w];
+      float s = acc[t][0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) a.logits[(size_t)(t0 + t) * a.E + e] = s + b;
+    }
   }
   pdl_launch_dependents();
-  const float b = a.bias ? a.bias[e] : 0.f;
-#pragma unroll
-  for (int t = 0; t < kTokTile; ++t) {
-    if (t >= nt) break;
-#pragma unroll
-    for (int w = N / 2; w > 0; w >>= 1)
-#pragma unroll
-      for (int m = 0; m < w; ++m) acc[t][m] += acc[t][m + w];
-    float s = acc[t][0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) a.logits[(size_t)(t0 + t) * a.E + e] = s + b;
-  }
 }
 
 // Compensated variant (used for small T; TT tokens per CTA, 1 when T = 1 so
@@ -288,11 +303,6 @@ __device__ __forceinline__ bool better(double v1, int e1, double v2, int e2) {
   return v1 > v2 || (v1 == v2 && e1 < e2);
 }
 
-__device__ __forceinline__ double load_d(const void* p, int dtype, size_t i) {
-  if (dtype == MOE_BF16) return (double)bf16_bits_to_f32(static_cast<const uint16_t*>(p)[i]);
-  return (double)static_cast<const float*>(p)[i];
-}
-
 // Eight consecutive elements i0 .. i0+7 (i0 a multiple of 8) of a bf16 or fp32
 // row as doubles, with one or two 16-byte loads.
 __device__ __forceinline__ void load8_d(const void* p, int dtype, size_t i0, double (&v)[8]) {
@@ -312,76 +322,8 @@ __device__ __forceinline__ void load8_d(const void* p, int dtype, size_t i0, dou
   }
 }
 
-// The same eight elements as fp32 (exact for bf16 and fp32 inputs).
-__device__ __forceinline__ void load8_f(const void* p, int dtype, size_t i0, float (&v)[8]) {
-  if (dtype == MOE_BF16) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + i0));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[2 * j] = __uint_as_float(w[j] << 16);
-      v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-  } else {
-    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i0);
-    const float4 f0 = __ldg(q), f1 = __ldg(q + 1);
-    v[0] = f0.x, v[1] = f0.y, v[2] = f0.z, v[3] = f0.w;
-    v[4] = f1.x, v[5] = f1.y, v[6] = f1.z, v[7] = f1.w;
-  }
-}
-
 constexpr int kGroupsInFlight = 4;  // 8-element groups a lane loads before summing them
 
-// Compensated fp32 logit by one warp (the Dot2 scheme of Ogita, Rump and Oishi,
-// "Accurate sum and dot product", 2005): every rounding error of the products
-// and of the running sums is captured exactly and summed separately, lanes are
-// merged with TwoSum.  With n = d terms, the result val (returned in fp64 with
-// the bias added) satisfies |val - exact| <= u|val| + gamma_n^2 sum|w_i x_i|;
-// abs_sum receives that sum in fp32 (relative error <= gamma_n).
-__device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, double* abs_sum) {
-  const int lane = threadIdx.x & 31;
-  float s = 0.f, c = 0.f, sa = 0.f;
-  const size_t xr = (size_t)t * a.d, wr = (size_t)e * a.d;
-  const int ng = a.d / 8;
-  for (int g0 = lane; g0 < ng; g0 += 32 * kGroupsInFlight) {
-    float w[kGroupsInFlight][8], x[kGroupsInFlight][8];
-#pragma unroll
-    for (int u = 0; u < kGroupsInFlight; ++u) {
-      const int g = g0 + 32 * u;
-      if (g < ng) {
-        load8_f(a.w, a.w_dtype, wr + 8 * (size_t)g, w[u]);
-        load8_f(a.x, a.x_dtype, xr + 8 * (size_t)g, x[u]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kGroupsInFlight; ++u) {
-      if (g0 + 32 * u >= ng) break;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float wf = w[u][j], xf = x[u][j];
-        const float p = __fmul_rn(wf, xf);
-        const float ep = __fmaf_rn(wf, xf, -p);  // p + ep == wf * xf exactly
-        float t2, es;
-        two_sum(s, p, t2, es);
-        s = t2;
-        c = __fadd_rn(c, __fadd_rn(es, ep));
-        sa = __fadd_rn(sa, fabsf(p));
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
-    sa = __fadd_rn(sa, __shfl_xor_sync(0xffffffffu, sa, o));
-    float t2, es;
-    two_sum(s, s2, t2, es);
-    s = t2;
-    c = __fadd_rn(__fadd_rn(c, c2), es);
-  }
-  *val = (double)s + (double)c + (a.bias ? (double)a.bias[e] : 0.0);
-  *abs_sum = sa;
-}
 
 // The reference arithmetic itself: sequential fp64 sum in ascending i, then the
 // bias.  Every product is exact in fp64, so fma equals multiply-then-add.  The
@@ -408,6 +350,47 @@ __device__ double logit_fp64_sequential(const RouteArgs& a, int t, int e) {
   }
   if (a.bias) s += (double)a.bias[e];
   return s;
+}
+
+// Warp-parallel fp64 logit: bf16 x bf16 and fp32 x fp32 products are exact in
+// fp64; lane l sums the products of groups l, l+32, ... in order, then a
+// 5-level butterfly adds the lanes, and the bias comes last.  Against the
+// exact value the error is at most gamma64(d/32 + 6) * sum|p| + u |val|; the
+// reference's sequential sum is within gamma64(d) * sum|p| of it.
+__device__ void logit_fp64_warp(const RouteArgs& a, int t, int e, double* val, double* abs_sum) {
+  const int lane = threadIdx.x & 31;
+  double s = 0.0, sa = 0.0;
+  const size_t xr = (size_t)t * a.d, wr = (size_t)e * a.d;
+  const int ng = a.d / 8;
+  for (int g0 = lane; g0 < ng; g0 += 32 * kGroupsInFlight) {
+    double w[kGroupsInFlight][8], x[kGroupsInFlight][8];
+#pragma unroll
+    for (int u = 0; u < kGroupsInFlight; ++u) {
+      const int g = g0 + 32 * u;
+      if (g < ng) {
+        load8_d(a.w, a.w_dtype, wr + 8 * (size_t)g, w[u]);
+        load8_d(a.x, a.x_dtype, xr + 8 * (size_t)g, x[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGroupsInFlight; ++u) {
+      if (g0 + 32 * u >= ng) break;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const double pr = w[u][j] * x[u][j];
+        s += pr;
+        sa += fabs(pr);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+  }
+  if (a.bias) s += (double)a.bias[e];
+  *val = s;
+  *abs_sum = sa;
 }
 
 __device__ __forceinline__ double gamma64(int n) {
@@ -618,7 +601,7 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a) {
   }
   __syncthreads();
   const int n = n_cand;
-  // pass 1: candidates whose interval meets another one's get a compensated value
+  // pass 1: candidates whose interval meets another one's get a warp-parallel fp64 value
   for (int c = tid; c < n; c += blockDim.x) {
     unsigned char f = 0;
     for (int c2 = 0; c2 < n; ++c2)
@@ -626,17 +609,17 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a) {
     cflag[c] = f;
   }
   __syncthreads();
-  // bound of the compensated sum: gamma_n^2 * sum|p| (sum|p| itself within
-  // gamma_n), u |val|, and the fp64 reference's own error gamma64_d * sum|p|
-  const double u32 = 5.9604644775390625e-8;
-  const double gn = (a.d + 32) * u32 / (1.0 - (a.d + 32) * u32);
-  const double bound_scale = (gn * gn * (1.0 + gn) + gamma64(a.d + 1)) * 1.01;
+  // bound of the warp-parallel fp64 sum against the reference's sequential one:
+  // its own error gamma64(d/32 + 6) * sum|p| (sum|p| itself within
+  // gamma64(d/32 + 5), absorbed by the factor), the reference's gamma64(d + 1) * sum|p|,
+  // and the rounding of the bias additions
+  const double bound_scale = (gamma64(a.d / 32 + 6) + gamma64(a.d + 1)) * 1.01;
   for (int c = warp; c < n; c += kTopkThreads / 32) {
-    if (!cflag[c] || a.comp) continue;  // compensated logits: this level would add nothing
+    if (!cflag[c]) continue;
     double val, sa;
-    logit_dot2_warp(a, t, cand[c], &val, &sa);
+    logit_fp64_warp(a, t, cand[c], &val, &sa);
     if (lane == 0) {
-      const double bd = bound_scale * (double)sa + 1.2e-7 * fabs(val) + 1e-30;
+      const double bd = bound_scale * sa + 4.5e-16 * fabs(val) + 1e-300;
       clo[c] = val - bd;
       chi[c] = val + bd;
     }
@@ -741,12 +724,15 @@ cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s) {
       err = launch("router_logits", router_logits_comp_kernel<float, kTokTile>, grid, dim3(kLogitWarps * 32), smem, s,
                    false, a);
     }
-  } else if (a.w_dtype == MOE_BF16) {
-    ensure_smem(router_logits_kernel<uint16_t>, smem);
-    err = launch("router_logits", router_logits_kernel<uint16_t>, grid, dim3(kLogitWarps * 32), smem, s, false, a);
   } else {
-    ensure_smem(router_logits_kernel<float>, smem);
-    err = launch("router_logits", router_logits_kernel<float>, grid, dim3(kLogitWarps * 32), smem, s, false, a);
+    const dim3 gp((a.E + kLogitWarps * kRowsPerWarp - 1) / (kLogitWarps * kRowsPerWarp), (a.T + kTokTile - 1) / kTokTile);
+    if (a.w_dtype == MOE_BF16) {
+      ensure_smem(router_logits_kernel<uint16_t>, smem);
+      err = launch("router_logits", router_logits_kernel<uint16_t>, gp, dim3(kLogitWarps * 32), smem, s, false, a);
+    } else {
+      ensure_smem(router_logits_kernel<float>, smem);
+      err = launch("router_logits", router_logits_kernel<float>, gp, dim3(kLogitWarps * 32), smem, s, false, a);
+    }
   }
   if (err != cudaSuccess) return err;
   const size_t tsm = topk_smem_bytes(a.E);
