@@ -41,7 +41,7 @@ constexpr int kTok = 8;  // tokens per pass (MMA N)
 constexpr int kRows = 32;  // weight rows per tile (two 16-row M tiles)
 constexpr int kMaxStagesM = 4;
 constexpr int kSmemBudgetM = 224 * 1024;
-constexpr int kMaxConsumerWarps = 15;
+constexpr int kMaxConsumerWarps = 14;  // compute warps (plus one reducer and one producer warp)
 
 struct GeomM {
   int K;            // contraction length
@@ -202,12 +202,12 @@ __device__ __forceinline__ void note_tokens(const FfnArgs& a, int slot0, int nt,
 }
 
 // Consumers: `warps` warps (warp w owns blocks [BPW w, BPW w + BPW)), then one
-// producer warp.  As in the FMA kernel, consumers never meet at a CTA-wide
-// barrier: each pass's partial sums go to a double-buffered shared array whose
-// fill is counted by an mbarrier, and consumer warp 0 alone reduces it and
-// writes the pass's outputs.  Every wait is bounded.
+// producer warp.  Consumers never meet at a CTA-wide barrier: each pass's
+// partial sums go to a double-buffered shared array whose fill is counted by an
+// mbarrier, and a reducer warp (warp 0, which computes nothing else) adds them
+// and writes the pass's outputs.  Every wait is bounded.
 template <int MODE, int BPW>
-__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gemv_kernel(const FfnArgs a, const GeomM g) {
+__global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gemv_kernel(const FfnArgs a, const GeomM g) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)g.stages * g.stage_bytes);
   uint64_t* empty = full + kMaxStagesM;
@@ -217,6 +217,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
   float* tok_f = red + 2 * g.red_floats;                  // [8] per token of the pass: 2^s (MODE 0)
   int* tok_i = reinterpret_cast<int*>(tok_f + kTok);      // [8] per token: slot (MODE 0) or pair id (MODE 1)
 
+  // warp 0 reduces, warps 1 .. W compute (warp w owns blocks [BPW (w-1), BPW w)), warp W + 1 loads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = g.warps;
   if (threadIdx.x == 0) {
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
   const size_t mat = (size_t)a.ff * a.d / 2 + (size_t)a.ff * a.d / 32;
   const int K = g.K;
 
-  if (warp == W) {
+  if (warp == W + 1) {
     // ------------------------------------------------------------ producer (whole warp: one row copy per lane)
     int it = 0, cur_a = -1;
     const uint8_t* rec = nullptr;
@@ -296,9 +297,58 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
     return;
   }
 
-  // -------------------------------------------------------------- consumers
+  if (warp == 0) {
+    // -------------------------------------------------------------- reducer
+    int pc = 0, cur_a = -1, s0 = 0, ne = 0;
+    bool rec_good = false;
+    for (int tile = t_begin; tile < t_end; ++tile) {
+      const int ai = tile / g.tpe;
+      if (ai != cur_a) {
+        cur_a = ai;
+        const int e = a.active[1 + ai];
+        rec_good = rec_ok(a.records[e]);
+        s0 = a.offsets[e];
+        ne = a.offsets[e + 1] - s0;
+      }
+      if (!rec_good) continue;
+      const int rt = tile % g.tpe;
+      for (int c0 = 0; c0 < ne; c0 += kTok) {
+        const int nt = min(kTok, ne - c0);
+        const int bi = pc & 1, use = pc >> 1;
+        ++pc;
+        note_tokens<MODE>(a, s0 + c0, nt, lane, tok_f, tok_i);
+        if (!mbar_wait(&red_full[bi], use & 1, a.err)) return;
+        const float* rbase = red + bi * g.red_floats;
+        if (MODE == 0) {
+          for (int idx = lane; idx < 16 * nt; idx += 32) {
+            const int r = idx & 15, n = idx >> 4;
+            float gs = 0.f, us = 0.f;
+            for (int w = 0; w < W; ++w) {
+              gs += rbase[((size_t)w * kRows + r) * kTok + n];
+              us += rbase[((size_t)w * kRows + 16 + r) * kTok + n];
+            }
+            const float pw = tok_f[n];
+            a.h[(size_t)tok_i[n] * a.ff + (size_t)rt * 16 + r] = act_fast(gs * pw, us * pw, a.act);
+          }
+        } else {
+          for (int idx = lane; idx < kRows * nt; idx += 32) {
+            const int r = idx & 31, n = idx >> 5;
+            float ys = 0.f;
+            for (int w = 0; w < W; ++w) ys += rbase[((size_t)w * kRows + r) * kTok + n];
+            a.y_pairs[(size_t)tok_i[n] * a.d + (size_t)rt * kRows + r] = ys;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_empty[bi]);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute warps
+  const int cw = warp - 1;
   const int gq = lane >> 2, tq = lane & 3;
-  const int b0 = warp * BPW;
+  const int b0 = cw * BPW;
   Frags<MODE, BPW> fr;
   int it = 0, pc = 0, cur_a = -1, s0 = 0, ne = 0;
   bool rec_good = false;
@@ -310,13 +360,9 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
       rec_good = rec_ok(a.records[e]);
       s0 = a.offsets[e];
       ne = a.offsets[e + 1] - s0;
-      if (rec_good && ne <= kTok) {
-        fr.load(a, s0, ne, b0, g.nblk, lane);
-        if (warp == 0) note_tokens<MODE>(a, s0, ne, lane, tok_f, tok_i);
-      }
+      if (rec_good && ne <= kTok) fr.load(a, s0, ne, b0, g.nblk, lane);
     }
     if (!rec_good) continue;
-    const int rt = tile % g.tpe;
     const int stage = it % g.stages;
     if (!mbar_wait(&full[stage], (it / g.stages) & 1, a.err)) return;
     ++it;
@@ -324,10 +370,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
     const uint8_t* sc = st + (size_t)kRows * g.pitch;
     for (int c0 = 0; c0 < ne; c0 += kTok) {
       const int nt = min(kTok, ne - c0);
-      if (ne > kTok) {
-        fr.load(a, s0 + c0, nt, b0, g.nblk, lane);
-        if (warp == 0) note_tokens<MODE>(a, s0 + c0, nt, lane, tok_f, tok_i);
-      }
+      if (ne > kTok) fr.load(a, s0 + c0, nt, b0, g.nblk, lane);
       float acc[2][4];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -377,7 +420,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
       const int bi = pc & 1, use = pc >> 1;
       ++pc;
       if (use > 0 && !mbar_wait(&red_empty[bi], (use - 1) & 1, a.err)) return;
-      float* rb = red + bi * g.red_floats + (size_t)warp * kRows * kTok;
+      float* rb = red + bi * g.red_floats + (size_t)cw * kRows * kTok;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int ra = 16 * m + gq;
@@ -388,31 +431,6 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_full[bi]);
-      if (warp == 0) {  // the pass's outputs, once every consumer warp has published
-        if (!mbar_wait(&red_full[bi], use & 1, a.err)) return;
-        const float* rbase = red + bi * g.red_floats;
-        if (MODE == 0) {
-          for (int idx = lane; idx < 16 * nt; idx += 32) {
-            const int r = idx & 15, n = idx >> 4;
-            float gs = 0.f, us = 0.f;
-            for (int w = 0; w < W; ++w) {
-              gs += rbase[((size_t)w * kRows + r) * kTok + n];
-              us += rbase[((size_t)w * kRows + 16 + r) * kTok + n];
-            }
-            const float pw = tok_f[n];
-            a.h[(size_t)tok_i[n] * a.ff + (size_t)rt * 16 + r] = act_fast(gs * pw, us * pw, a.act);
-          }
-        } else {
-          for (int idx = lane; idx < kRows * nt; idx += 32) {
-            const int r = idx & 31, n = idx >> 5;
-            float ys = 0.f;
-            for (int w = 0; w < W; ++w) ys += rbase[((size_t)w * kRows + r) * kTok + n];
-            a.y_pairs[(size_t)tok_i[n] * a.d + (size_t)rt * kRows + r] = ys;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&red_empty[bi]);
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -422,14 +440,14 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) mxfp4_mma_gem
 template <int MODE, int BPW>
 cudaError_t launch_m(const FfnArgs& a, const GeomM& g, int num_sms, bool pdl, cudaStream_t s, const char* name) {
   ensure_smem(mxfp4_mma_gemv_kernel<MODE, BPW>, g.smem);
-  return launch(name, mxfp4_mma_gemv_kernel<MODE, BPW>, dim3(num_sms), dim3((g.warps + 1) * 32), g.smem, s, pdl, a,
+  return launch(name, mxfp4_mma_gemv_kernel<MODE, BPW>, dim3(num_sms), dim3((g.warps + 2) * 32), g.smem, s, pdl, a,
                 g);
 }
 
 }  // namespace
 
 // bf16 activations (the gate/up B fragments are their exact f16 rescale);
-// at most 15 consumer warps of 8 blocks (d, ff <= 3840), so that every thread
+// at most 14 compute warps of 8 blocks (d, ff <= 3584), so that every thread
 // of the 16-warp CTA keeps its fragments in 128 registers.
 bool mxfp4_mma_gemv_supported(int d, int ff, int x_dtype) {
   return x_dtype == MOE_BF16 && d <= kMaxConsumerWarps * 8 * 32 && ff <= kMaxConsumerWarps * 8 * 32;
