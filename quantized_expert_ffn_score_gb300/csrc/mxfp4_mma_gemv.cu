@@ -319,16 +319,21 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
         note_tokens<MODE>(a, s0 + c0, nt, lane, tok_f, tok_i);
         if (!mbar_wait(&red_full[bi], use & 1, a.err)) return;
         const float* rbase = red + bi * g.red_floats;
-        if (MODE == 0) {
-          for (int idx = lane; idx < 16 * nt; idx += 32) {
-            const int r = idx & 15, n = idx >> 4;
-            float gs = 0.f, us = 0.f;
-            for (int w = 0; w < W; ++w) {
-              gs += rbase[((size_t)w * kRows + r) * kTok + n];
-              us += rbase[((size_t)w * kRows + 16 + r) * kTok + n];
+        if (MODE == 0) {  // lane = (half, row): gate rows on lanes 0-15, up rows on lanes 16-31
+          for (int n = 0; n < nt; ++n) {
+            float sum0 = 0.f, sum1 = 0.f;
+            int w = 0;
+            for (; w + 1 < W; w += 2) {
+              sum0 += rbase[((size_t)w * kRows + lane) * kTok + n];
+              sum1 += rbase[((size_t)(w + 1) * kRows + lane) * kTok + n];
             }
-            const float pw = tok_f[n];
-            a.h[(size_t)tok_i[n] * a.ff + (size_t)rt * 16 + r] = act_fast(gs * pw, us * pw, a.act);
+            if (w < W) sum0 += rbase[((size_t)w * kRows + lane) * kTok + n];
+            const float sum = sum0 + sum1;
+            const float us = __shfl_down_sync(0xffffffffu, sum, 16);
+            if (lane < 16) {
+              const float pw = tok_f[n];
+              a.h[(size_t)tok_i[n] * a.ff + (size_t)rt * 16 + lane] = act_fast(sum * pw, us * pw, a.act);
+            }
           }
         } else {
           for (int idx = lane; idx < kRows * nt; idx += 32) {
@@ -376,6 +381,29 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
       for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+      // the warp's 8 block scales of its rows ra = 16 m + gq and rb = ra + 8: one 8-byte load each when
+      // the scale rows are 8-byte aligned (K / 32 a multiple of 8), else bytes (only blocks < nblk)
+      uint2 sra[2], srb[2];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint8_t* pa = sc + (size_t)(16 * m + gq) * (K / 32) + b0;
+        const uint8_t* pb = sc + (size_t)(16 * m + gq + 8) * (K / 32) + b0;
+        if (((K / 32) & 7) == 0) {
+          sra[m] = *reinterpret_cast<const uint2*>(pa);
+          srb[m] = *reinterpret_cast<const uint2*>(pb);
+        } else {
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < g.nblk) {
+              w[j >> 2] |= (uint32_t)pa[j] << (8 * (j & 3));
+              w[2 + (j >> 2)] |= (uint32_t)pb[j] << (8 * (j & 3));
+            }
+          }
+          sra[m] = make_uint2(w[0], w[1]);
+          srb[m] = make_uint2(w[2], w[3]);
+        }
+      }
 #pragma unroll
       for (int j = 0; j < BPW; ++j) {
         const int b = b0 + j;
@@ -398,8 +426,10 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
             mma16816(d, A1, fr.lo[MODE == 1 ? j : 0][2], fr.lo[MODE == 1 ? j : 0][3]);
           }
           float sa, sb;
-          e8m0x2_to_f32((uint32_t)sc[(size_t)ra * (K / 32) + b] | ((uint32_t)sc[(size_t)rb * (K / 32) + b] << 8), sa,
-                        sb);
+          {  // bytes j of rows ra and rb as one 16-bit pair
+            const uint32_t wa2 = j < 4 ? sra[m].x : sra[m].y, wb2 = j < 4 ? srb[m].x : srb[m].y;
+            e8m0x2_to_f32(__byte_perm(wa2, wb2, (uint32_t)(j & 3) | ((uint32_t)((j & 3) + 4) << 4)), sa, sb);
+          }
           acc[m][0] = fmaf(sa, d[0], acc[m][0]);
           acc[m][1] = fmaf(sa, d[1], acc[m][1]);
           acc[m][2] = fmaf(sb, d[2], acc[m][2]);
