@@ -63,6 +63,7 @@ WORKLOADS = {
     # profiler captures; one token still streams 16 experts (281 MB > L2)
     "k3_mxfp4_decode_e64": LayerRecipe("k3_mxfp4_decode_e64", T=1, seed=1, **dict(K3, E=64)),
     "k3_rvq3_decode_e64": LayerRecipe("k3_rvq3_decode_e64", T=1, seed=2, quant="rvq3", **dict(K3, E=64)),
+    "k3_rvq3_decode_b8_e64": LayerRecipe("k3_rvq3_decode_b8_e64", T=8, seed=2, quant="rvq3", **dict(K3, E=64)),
     # K3 layer with RVQ3 experts, decode batch 1 and batch 8
     "k3_rvq3_decode_b1": LayerRecipe("k3_rvq3_decode_b1", T=1, seed=2, quant="rvq3", **K3),
     "k3_rvq3_decode_b8": LayerRecipe("k3_rvq3_decode_b8", T=8, seed=2, quant="rvq3", **K3),
