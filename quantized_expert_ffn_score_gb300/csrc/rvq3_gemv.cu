@@ -164,11 +164,12 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq3_unit_kernel(const FfnArgs
 // The same lookups with the table shared by every expert of a token (gate/up:
 // the codebooks are per layer and the experts of a token see the same x) or
 // of a slot (down: h is per slot).  Work units, in this order:
-//   (group g, kind, slice, 128-row chunk)  g = token (MODE 0) or slot (MODE 1),
-// each unit streaming that slice of its rows for every slot of the group;
-// persistent CTAs take contiguous unit ranges and rebuild the table only when
-// (g, kind, slice) changes.  For 2 .. kLutMaxPairs pairs (decode batches).
-constexpr int kLutChunk = 128;
+//   (group g, kind, slice, slot of the group, 1536-row chunk)
+// with g = token (MODE 0, the token's k slots) or slot (MODE 1, one slot);
+// each unit streams one expert's rows of the slice (long contiguous runs per
+// vector position), persistent CTAs take contiguous unit ranges and rebuild
+// the table only when (g, kind, slice) changes.  For at most kLutMaxPairs pairs.
+constexpr int kLutChunk = 1536;
 constexpr int kLutMaxPairs = 512;
 constexpr size_t kLutSmem = kRvqSmem + 2 * kLutMaxPairs * sizeof(uint16_t);  // two CTAs per SM
 
@@ -192,14 +193,16 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq3_lut_kernel(const FfnArgs 
   }
   const int ngroups = MODE == 0 ? a.T : P;
   const int nchunks = (g.rows + kLutChunk - 1) / kLutChunk;
-  const long long total = (long long)ngroups * g.kinds * g.ns * nchunks;
-  const int ub = (int)(total * blockIdx.x / gridDim.x), ue = (int)(total * (blockIdx.x + 1) / gridDim.x);
   const int nslots = MODE == 0 ? a.k : 1;
+  const long long total = (long long)ngroups * g.kinds * g.ns * nslots * nchunks;
+  const int ub = (int)(total * blockIdx.x / gridDim.x), ue = (int)(total * (blockIdx.x + 1) / gridDim.x);
   int cur_key = -1, cur_kind = -1;
   for (int unit = ub; unit < ue; ++unit) {
     int u = unit;
     const int chunk = u % nchunks;
     u /= nchunks;
+    const int j = u % nslots;
+    u /= nslots;
     const int slice = u % g.ns;
     u /= g.ns;
     const int kind = u % g.kinds;
@@ -247,10 +250,10 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq3_lut_kernel(const FfnArgs 
     const float* l2 = lut + 2 * 256 * kSlicePos + lane;
     const int r_begin = chunk * kLutChunk, r_end = min(g.rows, r_begin + kLutChunk);
     const int ngrp = (r_end - r_begin + 31) / 32;
-    // tasks: (slot of the group, 32-row group); warp w takes tasks w, w + 8, ...
-    for (int task = warp; task < nslots * ngrp; task += kRvqWarps) {
-      const int j = task / ngrp, rg = r_begin + 32 * (task % ngrp);
-      const int slot = MODE == 0 ? slot_of_pair[grp * a.k + j] : grp;
+    // 32-row groups of the unit's expert rows; warp w takes groups w, w + 8, ...
+    const int slot = MODE == 0 ? slot_of_pair[grp * a.k + j] : grp;
+    for (int task = warp; task < ngrp; task += kRvqWarps) {
+      const int rg = r_begin + 32 * task;
       const int e = expert_of_slot[slot];
       const uint8_t* rec = a.records[e];
       if (rec == nullptr || (reinterpret_cast<uintptr_t>(rec) & 15u)) {
@@ -317,9 +320,10 @@ cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_
   const int P = a.T * a.k;
   const RGeom g0 = make_rgeom(0, a.d, a.ff), g1 = make_rgeom(1, a.d, a.ff);
   const dim3 grid(2 * num_sms);
-  // the shared tables pay off from two tokens on (measured at the K3 shape: batch 8 gate/up 695 -> 614 us;
-  // one token 96 -> 116 us, where the per-expert units stream longer contiguous row runs)
-  const bool lut_shared = a.T >= 2 && P <= kLutMaxPairs && a.E <= 65536 && g0.rows % 32 == 0 && g1.rows % 32 == 0;
+  const bool lut_shared = P <= kLutMaxPairs && a.E <= 65536 && g0.rows % 32 == 0 && g1.rows % 32 == 0;
+  // down tables are per slot: sharing saves nothing at one token, where the per-expert units are faster
+  // (K3 shape: 59 against 64 us); gate/up tables are shared by the token's experts (93 -> 90 us)
+  const bool lut_down = lut_shared && a.T >= 2;
   cudaError_t err;
   if (lut_shared) {
     ensure_smem(rvq3_lut_kernel<0>, kLutSmem);
@@ -332,7 +336,7 @@ cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_
   const size_t n0 = (size_t)P * g0.rows, n1 = (size_t)P * g1.rows;
   err = launch("rvq3_gate_up_sum", rvq3_finalize_kernel<0>, dim3((unsigned)((n0 + 255) / 256)), dim3(256), 0, s, true, a, g0, P);
   if (err != cudaSuccess) return err;
-  if (lut_shared) {
+  if (lut_down) {
     ensure_smem(rvq3_lut_kernel<1>, kLutSmem);
     err = launch("rvq3_down", rvq3_lut_kernel<1>, grid, dim3(kRvqThreads), kLutSmem, s, true, a, g1);
   } else {
