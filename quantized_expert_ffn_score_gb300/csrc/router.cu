@@ -193,6 +193,142 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   pdl_launch_dependents();
 }
 
+// Tiled form of the same sums for bf16 x and W with d a multiple of 256 (the
+// prefill router): 8 tokens staged per CTA as fp32 with the two halves of
+// every 8-element chunk stored apart (xs[(2t + h) * d/8 + c] holds elements
+// 8c + 4h .. 8c + 4h + 3 of token t), so that lane l's loads of chunk
+// c = 32u + l are conflict-free; each warp takes 4 expert rows, two at a time,
+// against 4 tokens at a time.  Every logit is summed exactly as in
+// router_logits_kernel (lane chunks, one accumulator per element position, the
+// same tree), so the error bound and the values are unchanged.
+constexpr int kTiledTok = 8;       // tokens staged per CTA
+constexpr int kTiledPass = 4;      // tokens per accumulator pass
+constexpr int kTiledRows = 4;      // expert rows per warp
+constexpr int kTiledBatch = 2;     // chunks of both rows loaded ahead
+constexpr int kTiledExperts = kLogitWarps * kTiledRows;
+
+__host__ __device__ inline size_t tiled_smem_bytes(int d) { return (size_t)kTiledTok * d * sizeof(float); }
+
+__global__ void __launch_bounds__(kLogitWarps * 32, 2) router_logits_tiled_kernel(RouteArgs a) {
+  extern __shared__ float4 xs4[];  // [kTiledTok][2][d/8]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, nc = d / 8, nch = d / 256;
+  const int t0 = blockIdx.y * kTiledTok;
+  const int nt = min(kTiledTok, a.T - t0);
+  pdl_wait();
+  {  // stage the tokens (zeros past T)
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)t0 * d);
+    for (int i = threadIdx.x; i < kTiledTok * nc; i += blockDim.x) {
+      const int t = i / nc, c = i % nc;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < nt) v = src[(size_t)t * nc + c];
+      xs4[(2 * t) * nc + c] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                          __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+      xs4[(2 * t + 1) * nc + c] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                              __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && warp < nt) {  // ||x_t|| and max|x_t|, in the order of token_stats
+    const float* xf = reinterpret_cast<const float*>(xs4);
+    float s = 0.f, m = 0.f;
+    for (int i = lane; i < d; i += 32) {
+      const int c = i >> 3, p = i & 7;
+      const float v = xf[((2 * warp + (p >> 2)) * nc + c) * 4 + (p & 3)];
+      s = fmaf(v, v, s);
+      m = fmaxf(m, fabsf(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, o);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+    if (lane == 0) {
+      a.nrm_x[t0 + warp] = sqrtf(s);
+      a.max_x[t0 + warp] = m;
+    }
+  }
+  const int e_first = blockIdx.x * kTiledExperts + warp * kTiledRows;
+  const uint16_t* wbase = static_cast<const uint16_t*>(a.w);
+  for (int rp = 0; rp < kTiledRows; rp += 2) {
+    const int e0 = e_first + rp, e1 = e0 + 1;
+    if (e0 >= a.E) break;
+    const bool has1 = e1 < a.E;
+    const uint4* w0 = reinterpret_cast<const uint4*>(wbase + (size_t)e0 * d);
+    const uint4* w1 = reinterpret_cast<const uint4*>(wbase + (size_t)(has1 ? e1 : e0) * d);
+    float sq0 = 0.f, sq1 = 0.f;
+    for (int tp = 0; tp < nt; tp += kTiledPass) {
+      float acc[kTiledPass][2][8];
+#pragma unroll
+      for (int t = 0; t < kTiledPass; ++t)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[t][0][m] = acc[t][1][m] = 0.f;
+      for (int cb = 0; cb < nch; cb += kTiledBatch) {
+        uint4 wa[kTiledBatch], wb[kTiledBatch];
+#pragma unroll
+        for (int u = 0; u < kTiledBatch; ++u)
+          if (cb + u < nch) {
+            wa[u] = __ldg(w0 + (cb + u) * 32 + lane);
+            wb[u] = __ldg(w1 + (cb + u) * 32 + lane);
+          }
+#pragma unroll
+        for (int u = 0; u < kTiledBatch; ++u) {
+          if (cb + u >= nch) break;
+          const int c = (cb + u) * 32 + lane;
+          float fa[8], fb[8];
+          Vec16<uint16_t>::unpack(wa[u], fa);
+          Vec16<uint16_t>::unpack(wb[u], fb);
+          if (tp == 0 && blockIdx.y == 0) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              sq0 = fmaf(fa[m], fa[m], sq0);
+              sq1 = fmaf(fb[m], fb[m], sq1);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < kTiledPass; ++t) {
+            const float4 x0 = xs4[(2 * (tp + t)) * nc + c], x1 = xs4[(2 * (tp + t) + 1) * nc + c];
+            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              acc[t][0][m] = fmaf(fa[m], xv[m], acc[t][0][m]);
+              acc[t][1][m] = fmaf(fb[m], xv[m], acc[t][1][m]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTiledPass; ++t) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int m = 0; m < w; ++m) acc[t][r][m] += acc[t][r][m + w];
+          float s = acc[t][r][0];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          const int e = r == 0 ? e0 : e1;
+          if (lane == 0 && tp + t < nt && (r == 0 || has1))
+            a.logits[(size_t)(t0 + tp + t) * a.E + e] = s + (a.bias ? a.bias[e] : 0.f);
+        }
+      }
+    }
+    if (blockIdx.y == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sq0 += __shfl_xor_sync(0xffffffffu, sq0, o);
+        sq1 += __shfl_xor_sync(0xffffffffu, sq1, o);
+      }
+      if (lane == 0) {
+        a.nrm_w[e0] = sqrtf(sq0);
+        if (has1) a.nrm_w[e1] = sqrtf(sq1);
+      }
+    }
+  }
+  pdl_launch_dependents();
+}
+
 // Compensated variant (used for small T; TT tokens per CTA, 1 when T = 1 so
 // that the unrolled code stays small): per lane and token a running sum s,
 // the exact rounding errors of the products and of the sums accumulated in c
@@ -724,6 +860,12 @@ cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s) {
       err = launch("router_logits", router_logits_comp_kernel<float, kTokTile>, grid, dim3(kLogitWarps * 32), smem, s,
                    false, a);
     }
+  } else if (a.T >= 2 * kTiledTok && a.w_dtype == MOE_BF16 && a.x_dtype == MOE_BF16 && a.d % 256 == 0 &&
+             tiled_smem_bytes(a.d) <= 112 * 1024) {
+    const dim3 gt((a.E + kTiledExperts - 1) / kTiledExperts, (a.T + kTiledTok - 1) / kTiledTok);
+    ensure_smem(router_logits_tiled_kernel, tiled_smem_bytes(a.d));
+    err = launch("router_logits", router_logits_tiled_kernel, gt, dim3(kLogitWarps * 32), tiled_smem_bytes(a.d), s,
+                 false, a);
   } else {
     const dim3 gp((a.E + kLogitWarps * kRowsPerWarp - 1) / (kLogitWarps * kRowsPerWarp), (a.T + kTokTile - 1) / kTokTile);
     if (a.w_dtype == MOE_BF16) {

@@ -46,6 +46,12 @@ def test_mid_mxfp4_bf16_x_fp32_router(lib, ctx):
     gu.full_check(lib, ctx, MID_MX.with_(w_dtype="f32", seed=14, T=5, k=1))
 
 
+def test_mid_mxfp4_odd_expert_count_tiled_router(lib, ctx):
+    # 37 experts (the last expert-row pair of a warp has one row) and 29 tokens
+    # (a ragged last tile of 8 and a ragged second pass of 4)
+    gu.full_check(lib, ctx, MID_MX.with_(E=37, k=5, T=29, seed=17))
+
+
 def test_mid_mxfp4_all_experts_selected(lib, ctx):
     gu.full_check(lib, ctx, MID_MX.with_(E=8, k=8, T=3, seed=15))
 
