@@ -10,6 +10,10 @@
 //      with the 16 x U4 (16-byte aligned) tensor-map type, which places every
 //      8 code bytes in a 16-byte slot of shared memory (the operand layout of
 //      4-bit types in this MMA kind); scale factors = the record's E8M0 bytes.
+//      One pipeline stage holds one or two K chunks of 128 for both matrices
+//      of a tile, brought by a single 4-D box (codes, rows, chunk, matrix):
+//      a CTA's copy engine completes about one stage per 0.4 us however few
+//      bytes it holds, so stages are made as large as shared memory allows.
 //   B  activation terms in E4M3 with their own E8M0 block scales: an
 //      activation a is written as a sum of E4M3 terms, t_1 = RN(a / 2^s1),
 //      t_2 = RN((a - t_1 2^s1) / 2^s2), ..., each with a per-32-block scale
@@ -17,7 +21,8 @@
 //      Two terms reproduce a bf16 x exactly (8 significant bits; E4M3 holds 4),
 //      three terms carry about 12 significant bits of the fp32 h.  Term i of
 //      token n is row (i * nt + n) of B, so one MMA computes every term and the
-//      epilogue adds the columns of a token.
+//      epilogue adds the columns of a token.  The terms and chunks of a stage
+//      also come as one 4-D box (K bytes, tokens, term, chunk).
 //   D  fp32 in tensor memory.
 // Products and their sum are formed by the tensor core in fp32.
 //
@@ -47,7 +52,8 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;           // weight rows per tile (MMA M)
-constexpr int kBK = 128;           // K per pipeline stage
+constexpr int kBK = 128;           // K per chunk (one A box plane, four MMAs)
+constexpr int kMaxChunks = 2;      // K chunks per pipeline stage
 constexpr int kGroupK = 512;       // K per scale-factor group (4 stages)
 constexpr int kMaxNT = 32;         // tokens per n-tile
 constexpr int kMaxStages = 12;
@@ -71,8 +77,10 @@ struct Bs {
 // Pipeline and tensor-memory geometry of one launch (host computed).
 struct BsGeom {
   int n_mma;        // MMA N (activation rows: terms x nt, rounded to 16)
+  int chunks;       // K chunks of kBK per stage (1, 2 or 4 stages per scale group)
+  int b_chunk;      // shared-memory bytes of one chunk's activation rows (terms x nt x kBK)
   int stages;       // shared-memory pipeline stages
-  int stage_bytes;  // kMats A boxes + the B rows (1 KB multiple)
+  int stage_bytes;  // kMats x chunks A planes + chunks x the B rows (1 KB multiple)
   int dcols;        // TMEM columns of one accumulator buffer (kMats x n_mma)
   int sf_base;      // first scale-factor column (two accumulator buffers before it)
   int sf_slots;
@@ -306,14 +314,13 @@ __device__ __forceinline__ void sf_load(SfRegs<MODE>& r, const BsArgs& a, const 
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    mxfp4_bs_kernel(const __grid_constant__ CUtensorMap tmpl, const __grid_constant__ CUtensorMap bm0,
-                    const __grid_constant__ CUtensorMap bm1, const __grid_constant__ CUtensorMap bm2, const BsArgs a) {
+    mxfp4_bs_kernel(const __grid_constant__ CUtensorMap tmpl, const __grid_constant__ CUtensorMap bmap, const BsArgs a) {
   using C = Bs<MODE>;
   const BsGeom G = a.g[MODE];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint8_t* smaps = smem + (size_t)G.stages * G.stage_bytes;  // [kMats] 128-byte tensor maps
+  uint8_t* smaps = smem + (size_t)G.stages * G.stage_bytes;  // the 128-byte weight tensor map being patched
   uint64_t* full = reinterpret_cast<uint64_t*>(smaps + C::kMats * 128);
   uint64_t* empty = full + kMaxStages;
   uint64_t* sf_full = empty + kMaxStages;
@@ -348,9 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(done, 1);
     fence_mbar_init();
   }
-  if (warp == 0) {  // one copy of the weight tensor-map template per matrix, patched per expert
+  if (warp == 0) {  // a copy of the weight tensor-map template, patched per expert
     const uint32_t* src = reinterpret_cast<const uint32_t*>(&tmpl);
-    for (int m = 0; m < C::kMats; ++m) reinterpret_cast<uint32_t*>(smaps + m * 128)[lane] = src[lane];
+    reinterpret_cast<uint32_t*>(smaps)[lane] = src[lane];
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -384,14 +391,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  const int ub = (int)((long long)pl.units * blockIdx.x / gridDim.x);
-  int nu = (int)((long long)pl.units * (blockIdx.x + 1) / gridDim.x) - ub;
+  // Whole-K units are dealt round robin: at any time the CTAs work on a window
+  // of consecutive units, so the n-tiles of one weight tile are streamed by
+  // several CTAs together and all but the first read it from L2.  Split units
+  // stay in contiguous ranges (the parts of a tile meet in one CTA).
+  const bool dealt = pl.kparts == 1;
+  const int ub = dealt ? (int)blockIdx.x : (int)((long long)pl.units * blockIdx.x / gridDim.x);
+  int nu = dealt ? (pl.units > (int)blockIdx.x ? (pl.units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0)
+                 : (int)((long long)pl.units * (blockIdx.x + 1) / gridDim.x) - ub;
   if (nu > a.max_units) {  // cannot happen with the host's bound; leave the rest undone, reported
     if (threadIdx.x == 0) dev_error(a.err, MOE_ERR_UNSUPPORTED, nu);
     nu = a.max_units;
   }
   for (int i = threadIdx.x; i < nu; i += kThreads) {
-    const Unit t = decode_unit(a, pl, ub + i);
+    const Unit t = decode_unit(a, pl, dealt ? ub + i * (int)gridDim.x : ub + i);
     UnitRec r;
     r.rec = a.records[t.e];
     r.e = t.e;
@@ -421,34 +434,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       CUtensorMap* gm = a.gmaps + (size_t)blockIdx.x * 4;
-      if (t.e != cur_e) {  // this expert's weight tensor maps, in the buffer not used by copies in flight
+      if (t.e != cur_e) {  // this expert's weight tensor map, in the buffer not used by copies in flight
         cur_e = t.e;
         mbuf ^= 1;
-        for (int m = 0; m < C::kMats; ++m) {
-          const uint8_t* base = rec + (MODE == 0 ? m * mat : 2 * mat);
-          if (lane == 0) tc::tensormap_set_address(smaps + m * 128, base);
-          __syncwarp();
-          tc::tensormap_publish(gm + m * 2 + mbuf, smaps + m * 128);
-          if (lane == 0) tc::tensormap_acquire(gm + m * 2 + mbuf);
-          __syncwarp();
-        }
+        if (lane == 0) tc::tensormap_set_address(smaps, rec + (MODE == 0 ? 0 : 2 * mat));
+        __syncwarp();
+        tc::tensormap_publish(gm + mbuf, smaps);
+        if (lane == 0) tc::tensormap_acquire(gm + mbuf);
+        __syncwarp();
       }
       if (lane == 0) {
-        const int c_end = (t.kpart + 1) * pl.gpk * 4;
-        for (int c = t.kpart * pl.gpk * 4; c < c_end; ++c, ++it) {
+        // stage cs covers K chunks cs * chunks .. + chunks - 1; a scale group is 4 chunks
+        const int spg = 4 / G.chunks;
+        const uint32_t tx = (uint32_t)(G.chunks * (C::kMats * kTxA + C::kTerms * nt * kBK));
+        const int c_end = (t.kpart + 1) * pl.gpk * spg;
+        for (int cs = t.kpart * pl.gpk * spg; cs < c_end; ++cs, ++it) {
           const int stage = it % G.stages, n = it / G.stages;
           if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(C::kMats * kTxA + C::kTerms * nt * kBK));
+          mbar_arrive_expect_tx(&full[stage], tx);
           uint8_t* st = stages + (size_t)stage * G.stage_bytes;
-          for (int m = 0; m < C::kMats; ++m)
-            tc::tma_load_2d(st + m * kABytes, gm + m * 2 + mbuf, c * kBK, t.tile * kBM, &full[stage]);
-          uint8_t* sb = st + C::kMats * kABytes;
-          tc::tma_load_2d(sb, &bm0, c * kBK, t.s0, &full[stage]);
-          tc::tma_load_2d(sb + nt * kBK, &bm1, c * kBK, t.s0, &full[stage]);
-          if (MODE == 1) tc::tma_load_2d(sb + 2 * nt * kBK, &bm2, c * kBK, t.s0, &full[stage]);
+          // A box (codes, rows, chunk, matrix) -> [matrix][chunk][128 rows][128 slots]
+          tc::tma_load_4d(st, gm + mbuf, 0, t.tile * kBM, cs * G.chunks, 0, &full[stage]);
+          // B box (K bytes, tokens, term, chunk) -> [chunk][term][nt rows][128 bytes]
+          tc::tma_load_4d(st + C::kMats * G.chunks * kABytes, &bmap, 0, t.s0, 0, cs * G.chunks, &full[stage]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -482,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after();
           const uint32_t sfa = tmem + (uint32_t)(G.sf_base + slot * C::kSlotCols);
-          for (int c = 0; c < 4; ++c, ++it) {
+          for (int c = 0; c < 4 && ok; ++it) {  // the group's 4 chunks, G.chunks per stage
             const int stage = it % G.stages;
             if (!mbar_wait(&full[stage], (it / G.stages) & 1, a.err)) {
               ok = false;
@@ -490,17 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_after();
             const uint8_t* st = stages + (size_t)stage * G.stage_bytes;
-            const uint64_t bdesc = tc::desc_kmajor_sw128(tc::saddr(st + C::kMats * kABytes));
+            for (int ch = 0; ch < G.chunks; ++ch, ++c) {
+              const uint64_t bdesc =
+                  tc::desc_kmajor_sw128(tc::saddr(st + C::kMats * G.chunks * kABytes + ch * G.b_chunk));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t id = idesc | tc::idesc_sf_ids((uint32_t)ks, (uint32_t)ks);
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t id = idesc | tc::idesc_sf_ids((uint32_t)ks, (uint32_t)ks);
 #pragma unroll
-              for (int m = 0; m < C::kMats; ++m) {
-                const uint64_t adesc = tc::desc_kmajor_sw128(tc::saddr(st + m * kABytes));
-                tc::mma_bs(d0 + m * G.n_mma, adesc + 2 * ks, bdesc + 2 * ks, id, sfa + m * 16 + 4 * c,
-                           sfa + C::kSfACols + 4 * c, fresh ? 0u : 1u);
+                for (int m = 0; m < C::kMats; ++m) {
+                  const uint64_t adesc = tc::desc_kmajor_sw128(tc::saddr(st + (m * G.chunks + ch) * kABytes));
+                  tc::mma_bs(d0 + m * G.n_mma, adesc + 2 * ks, bdesc + 2 * ks, id, sfa + m * 16 + 4 * c,
+                             sfa + C::kSfACols + 4 * c, fresh ? 0u : 1u);
+                }
+                fresh = false;
               }
-              fresh = false;
             }
             tc::mma_commit(&empty[stage]);
           }
@@ -664,13 +678,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
-// Stage and tensor-memory geometry for nt tokens per n-tile and E experts.
+// Stage and tensor-memory geometry for nt tokens per n-tile, E experts and
+// `chunks` K chunks per stage.  The B rows of the last chunk are followed by
+// room for the n_mma - terms x nt rows the MMA reads past them (ignored
+// accumulator columns).
 template <int MODE>
-bool make_geom(BsGeom* g, int nt, int E, int max_units) {
+bool make_geom(BsGeom* g, int nt, int E, int max_units, int chunks) {
   using C = Bs<MODE>;
   g->n_mma = (C::kTerms * nt + 15) & ~15;
-  const int b_bytes = (g->n_mma * kBK + 1023) & ~1023;
-  g->stage_bytes = C::kMats * kABytes + b_bytes;
+  g->chunks = chunks;
+  g->b_chunk = C::kTerms * nt * kBK;
+  const int b_bytes = (chunks * g->b_chunk + (g->n_mma - C::kTerms * nt) * kBK + 1023) & ~1023;
+  g->stage_bytes = C::kMats * chunks * kABytes + b_bytes;
   const int avail = kSmemBudget - 1024 - C::kMats * 128 - kBarBytes - (E + 1) * (int)sizeof(int) - 16 -
                     max_units * (int)sizeof(UnitRec);
   g->stages = avail / g->stage_bytes < kMaxStages ? avail / g->stage_bytes : kMaxStages;
@@ -678,7 +697,7 @@ bool make_geom(BsGeom* g, int nt, int E, int max_units) {
   g->sf_base = 2 * g->dcols;
   const int slots = (512 - g->sf_base) / C::kSlotCols;
   g->sf_slots = slots < kMaxSfSlots ? slots : kMaxSfSlots;
-  return g->stages >= 2 && g->sf_slots >= 2;
+  return g->stages >= 2 && g->sf_slots >= 2 && chunks >= 1 && chunks <= kMaxChunks && 4 % chunks == 0;
 }
 template <int MODE>
 size_t smem_bytes(const BsGeom& g, int E, int max_units) {
@@ -708,31 +727,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Weight matrix [rows][K] of E2M1 codes (K / 2 bytes a row), boxes of 128
-// codes x 128 rows; the address is replaced per expert on the device.
-bool make_weight_map(CUtensorMap* m, const void* any_base, int K, int rows) {
+// The weight matrices of a record as a 4-D tensor (codes within a K chunk,
+// row, K chunk, matrix): strides K / 2 bytes (row), 64 bytes (chunk of 128
+// codes) and `mat_bytes` (matrix); one box = `chunks` chunks of 128 rows of
+// `mats` matrices.  The address is replaced per expert on the device.
+bool make_weight_map(CUtensorMap* m, const void* any_base, int K, int rows, int mats, size_t mat_bytes, int chunks) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-  cuuint32_t box[2] = {kBK, kBM};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(any_base), dims, strides, box, es,
+  cuuint64_t dims[4] = {(cuuint64_t)kBK, (cuuint64_t)rows, (cuuint64_t)(K / kBK), (cuuint64_t)mats};
+  cuuint64_t strides[3] = {(cuuint64_t)K / 2, (cuuint64_t)kBK / 2, (cuuint64_t)mat_bytes};
+  cuuint32_t box[4] = {kBK, kBM, (cuuint32_t)chunks, (cuuint32_t)mats};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<void*>(any_base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// One plane of activation terms [P][K] E4M3, boxes of 128 x nt rows.
-bool make_term_map(CUtensorMap* m, const void* base, int K, int P, int nt) {
+// The E4M3 activation terms [terms][P][K] as a 4-D tensor (K byte within a
+// chunk, slot, term, K chunk); one box = nt slots x all terms x `chunks`
+// chunks, landing as [chunk][term][slot][128 bytes].
+bool make_term_map(CUtensorMap* m, const void* base, int K, int P, int nt, int terms, int chunks) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {kBK, (cuuint32_t)nt};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[4] = {(cuuint64_t)kBK, (cuuint64_t)P, (cuuint64_t)terms, (cuuint64_t)(K / kBK)};
+  cuuint64_t strides[3] = {(cuuint64_t)K, (cuuint64_t)P * K, (cuuint64_t)kBK};
+  cuuint32_t box[4] = {kBK, (cuuint32_t)nt, (cuuint32_t)terms, (cuuint32_t)chunks};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// K chunks per stage: two where two stages of that size fit, else one.
+constexpr int kChunksGateUp = 2;
+constexpr int kChunksDown = 2;
 
 }  // namespace
 
@@ -780,27 +807,29 @@ cudaError_t launch_mxfp4_bs(const BsLaunch& L, int num_sms, bool pdl, cudaStream
   a.y_pairs = L.y_pairs;
   a.err = L.err;
   if (num_sms > 160) return cudaErrorInvalidValue;  // the split counters are sized for 8 units per SM
-  CUtensorMap w0, w1, x0, x1, h0, h1, h2;
-  if (!make_weight_map(&w0, a.xq, a.d, a.ff) || !make_weight_map(&w1, a.xq, a.ff, a.d) ||
-      !make_term_map(&x0, a.xq, a.d, a.P, a.nt) || !make_term_map(&x1, a.xq + P * a.d, a.d, a.P, a.nt) ||
-      !make_term_map(&h0, a.hq, a.ff, a.P, a.nt) || !make_term_map(&h1, a.hq + P * a.ff, a.ff, a.P, a.nt) ||
-      !make_term_map(&h2, a.hq + 2 * P * a.ff, a.ff, a.P, a.nt))
-    return cudaErrorInvalidValue;
   const int mu0 = max_units_per_cta(a.ff, a.d, a.P, a.E, a.nt, num_sms);
   const int mu1 = max_units_per_cta(a.d, a.ff, a.P, a.E, a.nt, num_sms);
   a.max_units = mu0 > mu1 ? mu0 : mu1;
-  if (!make_geom<0>(&a.g[0], a.nt, a.E, a.max_units) || !make_geom<1>(&a.g[1], a.nt, a.E, a.max_units))
+  if (!make_geom<0>(&a.g[0], a.nt, a.E, a.max_units, kChunksGateUp) &&
+      !make_geom<0>(&a.g[0], a.nt, a.E, a.max_units, 1))
+    return cudaErrorInvalidValue;
+  if (!make_geom<1>(&a.g[1], a.nt, a.E, a.max_units, kChunksDown) && !make_geom<1>(&a.g[1], a.nt, a.E, a.max_units, 1))
+    return cudaErrorInvalidValue;
+  const size_t mat = (size_t)a.ff * a.d / 2 + (size_t)a.ff * a.d / 32;  // bytes of one matrix in a record
+  CUtensorMap w0, w1, xm, hm;
+  if (!make_weight_map(&w0, a.xq, a.d, a.ff, 2, mat, a.g[0].chunks) ||
+      !make_weight_map(&w1, a.xq, a.ff, a.d, 1, mat, a.g[1].chunks) ||
+      !make_term_map(&xm, a.xq, a.d, a.P, a.nt, 2, a.g[0].chunks) ||
+      !make_term_map(&hm, a.hq, a.ff, a.P, a.nt, 3, a.g[1].chunks))
     return cudaErrorInvalidValue;
   cudaError_t err = launch("bs_prep_x", bs_prep_x_kernel, dim3(4 * num_sms), dim3(256), 0, s, pdl, a, L.x);
   if (err != cudaSuccess) return err;
   const size_t smem0 = smem_bytes<0>(a.g[0], a.E, a.max_units), smem1 = smem_bytes<1>(a.g[1], a.E, a.max_units);
   ensure_smem(mxfp4_bs_kernel<0>, smem0);
-  err = launch("mxfp4_bs_gate_up", mxfp4_bs_kernel<0>, dim3(num_sms), dim3(kThreads), smem0, s, true, w0, x0, x1, x1,
-               a);
+  err = launch("mxfp4_bs_gate_up", mxfp4_bs_kernel<0>, dim3(num_sms), dim3(kThreads), smem0, s, true, w0, xm, a);
   if (err != cudaSuccess) return err;
   ensure_smem(mxfp4_bs_kernel<1>, smem1);
-  return launch("mxfp4_bs_down", mxfp4_bs_kernel<1>, dim3(num_sms), dim3(kThreads), smem1, s, true, w1, h0, h1, h2,
-                a);
+  return launch("mxfp4_bs_down", mxfp4_bs_kernel<1>, dim3(num_sms), dim3(kThreads), smem1, s, true, w1, hm, a);
 }
 
 }  // namespace moe
