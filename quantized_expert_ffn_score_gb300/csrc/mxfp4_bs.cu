@@ -312,6 +312,31 @@ __device__ __forceinline__ void sf_load(SfRegs<MODE>& r, const BsArgs& a, const 
   }
 }
 
+// The MMAs of one stage: CH chunks x 4 K steps x the tile's matrices.  sd is
+// the shared-memory descriptor of the stage's first byte; descriptors count
+// in 16-byte units, so operand offsets are added to it directly (every
+// operand address stays below 2^18, so the 14-bit address field never
+// carries).  sfc = scale-factor columns of the stage's first chunk.
+template <int MODE, int CH>
+__device__ __forceinline__ void issue_stage(uint64_t sd, uint32_t b_off16, uint32_t b_step16, uint32_t d0,
+                                            uint32_t n_mma, const uint32_t (&id)[4], uint32_t sfc, bool& fresh) {
+  using C = Bs<MODE>;
+#pragma unroll
+  for (int ch = 0; ch < CH; ++ch) {
+    const uint64_t bd = sd + b_off16 + (uint32_t)ch * b_step16;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int m = 0; m < C::kMats; ++m) {
+        const uint64_t ad = sd + (uint32_t)((m * CH + ch) * (kABytes >> 4) + 2 * ks);
+        tc::mma_bs(d0 + m * n_mma, ad, bd + 2 * ks, id[ks], sfc + m * 16 + 4 * ch, sfc + C::kSfACols + 4 * ch,
+                   fresh ? 0u : 1u);
+      }
+      fresh = false;
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     mxfp4_bs_kernel(const __grid_constant__ CUtensorMap tmpl, const __grid_constant__ CUtensorMap bmap, const BsArgs a) {
@@ -424,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    int it = 0, cur_e = -1, mbuf = 0;
+    int it = 0, cur_e = -1, mbuf = 0, pstage = 0;
+    uint32_t pph = 0;  // phase of the current round over the stage ring
     bool ok = true;
     for (int u = 0; u < nu && ok; ++u) {
       const UnitRec t = table[u];
@@ -449,10 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx = (uint32_t)(G.chunks * (C::kMats * kTxA + C::kTerms * nt * kBK));
         const int c_end = (t.kpart + 1) * pl.gpk * spg;
         for (int cs = t.kpart * pl.gpk * spg; cs < c_end; ++cs, ++it) {
-          const int stage = it % G.stages, n = it / G.stages;
-          if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) {
+          const int stage = pstage;
+          if (it >= G.stages && !mbar_wait(&empty[stage], pph ^ 1u, a.err)) {
             ok = false;
             break;
+          }
+          if (++pstage == G.stages) {
+            pstage = 0;
+            pph ^= 1u;
           }
           mbar_arrive_expect_tx(&full[stage], tx);
           uint8_t* st = stages + (size_t)stage * G.stage_bytes;
@@ -469,9 +499,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&full[j % G.stages], (j / G.stages) & 1, a.err);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // (one thread: ring positions and descriptors advance incrementally, so
+    // the issue loop carries no division and little address arithmetic)
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_e2m1_e4m3_bs(kBM, G.n_mma);
-      int it = 0, sfi = 0, seg = 0, buf = 0;
+      uint32_t id[4];
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) id[ks] = idesc | tc::idesc_sf_ids((uint32_t)ks, (uint32_t)ks);
+      const uint64_t sd0 = tc::desc_kmajor_sw128(tc::saddr(stages));
+      const uint32_t step16 = (uint32_t)G.stage_bytes >> 4;
+      const uint32_t b_off16 = (uint32_t)(C::kMats * G.chunks * kABytes) >> 4, b_step16 = (uint32_t)G.b_chunk >> 4;
+      int stage = 0, slot = 0, seg = 0, buf = 0;
+      uint32_t ph = 0, sph = 0;
       bool ok = true, fresh = true;
       for (int u = 0; u < nu && ok; ++u) {
         const UnitRec t = table[u];
@@ -485,40 +524,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           fresh = true;
         }
         const uint32_t d0 = tmem + (uint32_t)(buf * G.dcols);
-        for (int g = 0; g < pl.gpk && ok; ++g, ++sfi) {
-          const int slot = sfi % G.sf_slots;
-          if (!mbar_wait(&sf_full[slot], (sfi / G.sf_slots) & 1, a.err)) {
+        for (int g = 0; g < pl.gpk && ok; ++g) {
+          if (!mbar_wait(&sf_full[slot], sph, a.err)) {
             ok = false;
             break;
           }
           tc::fence_after();
           const uint32_t sfa = tmem + (uint32_t)(G.sf_base + slot * C::kSlotCols);
-          for (int c = 0; c < 4 && ok; ++it) {  // the group's 4 chunks, G.chunks per stage
-            const int stage = it % G.stages;
-            if (!mbar_wait(&full[stage], (it / G.stages) & 1, a.err)) {
+          for (int c = 0; c < 4; c += G.chunks) {  // the group's 4 chunks, G.chunks per stage
+            if (!mbar_wait(&full[stage], ph, a.err)) {
               ok = false;
               break;
             }
             tc::fence_after();
-            const uint8_t* st = stages + (size_t)stage * G.stage_bytes;
-            for (int ch = 0; ch < G.chunks; ++ch, ++c) {
-              const uint64_t bdesc =
-                  tc::desc_kmajor_sw128(tc::saddr(st + C::kMats * G.chunks * kABytes + ch * G.b_chunk));
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t id = idesc | tc::idesc_sf_ids((uint32_t)ks, (uint32_t)ks);
-#pragma unroll
-                for (int m = 0; m < C::kMats; ++m) {
-                  const uint64_t adesc = tc::desc_kmajor_sw128(tc::saddr(st + (m * G.chunks + ch) * kABytes));
-                  tc::mma_bs(d0 + m * G.n_mma, adesc + 2 * ks, bdesc + 2 * ks, id, sfa + m * 16 + 4 * c,
-                             sfa + C::kSfACols + 4 * c, fresh ? 0u : 1u);
-                }
-                fresh = false;
-              }
-            }
+            const uint64_t sd = sd0 + (uint32_t)stage * step16;
+            if (G.chunks == 2)
+              issue_stage<MODE, 2>(sd, b_off16, b_step16, d0, (uint32_t)G.n_mma, id, sfa + 4 * c, fresh);
+            else
+              issue_stage<MODE, 1>(sd, b_off16, b_step16, d0, (uint32_t)G.n_mma, id, sfa + 4 * c, fresh);
             tc::mma_commit(&empty[stage]);
+            if (++stage == G.stages) {
+              stage = 0;
+              ph ^= 1u;
+            }
           }
-          if (ok) tc::mma_commit(&sf_empty[slot]);
+          if (!ok) break;
+          tc::mma_commit(&sf_empty[slot]);
+          if (++slot == G.sf_slots) {
+            slot = 0;
+            sph ^= 1u;
+          }
         }
         if (ok && seg_end) {
           tc::mma_commit(&acc_full[buf]);
@@ -542,13 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     cur.seek(table, nu);
     SfRegs<MODE> r0, r1;
     if (cur.valid) sf_load<MODE>(r0, a, cur.t, cur.t.kpart * pl.gpk + cur.gi, q, lane, nt);
-    int sfi = 0;
+    int sfi = 0, slot = 0;
+    uint32_t sph = 0;  // phase of the current round over the scale-factor slots
     while (cur.valid) {
       Cursor nx = cur;
       nx.advance(table, nu, pl.gpk);
       if (nx.valid) sf_load<MODE>(r1, a, nx.t, nx.t.kpart * pl.gpk + nx.gi, q, lane, nt);  // in flight below
-      const int slot = sfi % G.sf_slots;
-      if (sfi >= G.sf_slots && !mbar_wait(&sf_empty[slot], ((sfi / G.sf_slots) - 1) & 1, a.err)) break;
+      if (sfi >= G.sf_slots && !mbar_wait(&sf_empty[slot], sph ^ 1u, a.err)) break;
       tc::fence_after();
       const uint32_t col = tmem + lb + (uint32_t)(G.sf_base + slot * C::kSlotCols);
 #pragma unroll
@@ -573,6 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sf_full[slot]);
       ++sfi;
+      if (++slot == G.sf_slots) {
+        slot = 0;
+        sph ^= 1u;
+      }
       cur = nx;
       r0 = r1;
     }
