@@ -566,162 +566,19 @@ __device__ float block_max(float v, float* scratch) {
   return m;
 }
 
-// One CTA per token (the body of the top-k kernel): a radix select finds the (k+1)-th largest fp32 logit,
-// the k+1 experts at or above it are ordered by counting, and the bounds then
-// certify the selection or send the CTA down the recheck path.
-__device__ __forceinline__ void topk_token(const RouteArgs& a) {
-  extern __shared__ double tsm[];
-  const int E = a.E, k = a.k;
-  const size_t e8 = ((size_t)E + 7) / 8 * 8;
-  double* clo = tsm;  // recheck path: candidate bounds
-  double* chi = clo + e8;
-  float* sv = reinterpret_cast<float*>(chi + e8);  // fp32 logits
-  float* sb = sv + e8;                             // their error bounds
-  int* cand = reinterpret_cast<int*>(sb + e8);     // recheck path: candidate experts
-  unsigned char* insel = reinterpret_cast<unsigned char*>(cand + e8);
-  unsigned char* cflag = insel + e8;
-  __shared__ int sel[kMaxK + 1];
-  __shared__ int candA[kMaxK + 1];
-  __shared__ int hist[256];
-  __shared__ int s_digit, s_need, s_na, s_nb;
-  __shared__ int n_cand, certified;
-  __shared__ float scratch[kTopkWarps];
+// Recheck path of one token's top-k (the fp32 bounds did not certify the
+// selection): every expert that could be in the top k (selected, or upper
+// bound at least m, the lowest selected lower bound) gets an interval; those
+// meeting another one's are recomputed in fp64 (warp-parallel, with its own
+// bound) and, if still undecided, by the reference's sequential fp64 sum.
+__device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float* sv, const float* sb,
+                                          const unsigned char* insel, float m, double* clo, double* chi, int* cand,
+                                          unsigned char* cflag) {
+  __shared__ int n_cand;
   __shared__ int order[kMaxK];
   __shared__ double oval[kMaxK];
-
-  const int t = blockIdx.x;
+  const int E = a.E, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();
-  const float nx = a.comp ? 0.f : a.nrm_x[t];
-  // load: thread tid holds experts e = tid + 256 i as order-preserving keys
-  uint32_t key[kSlicePerLane];
-#pragma unroll
-  for (int i = 0; i < kSlicePerLane; ++i) {
-    const int e = tid + kTopkThreads * i;
-    key[i] = 0u;
-    if (e < E) {
-      const float v = a.logits[(size_t)t * E + e];
-      sv[e] = v;
-      sb[e] = a.comp ? a.gamma * a.absdot[(size_t)t * E + e] + 2.4e-7f * fabsf(v) + 1e-30f
-                     : a.gamma * a.nrm_w[e] * nx + 1.2e-7f * fabsf(v) + 1e-30f;
-      insel[e] = 0;
-      key[i] = ord_bits(v);
-    }
-  }
-  pdl_launch_dependents();
-  const int nsel = min(k + 1, E);
-  // radix select of the nsel-th largest key, 8 bits per pass from the top
-  uint32_t prefix = 0u, mask = 0u;
-  int need = nsel;  // how many keys >= the threshold still to account for at this digit
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kSlicePerLane; ++i)
-      if (tid + kTopkThreads * i < E && (key[i] & mask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
-    __syncthreads();
-    if (warp == 0) {  // lane l scans bins 255-8l .. 248-8l, top down
-      int c[8], lsum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - 8 * lane - j];
-        lsum += c[j];
-      }
-      int incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - lsum;
-      if (excl < need && need <= incl) {
-        int run = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run + c[j] >= need) {
-            s_digit = 255 - 8 * lane - j;
-            s_need = need - run;
-            break;
-          }
-          run += c[j];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)s_digit << shift;
-    mask |= 255u << shift;
-    need = s_need;
-  }
-  // the selection: every key above the threshold, then the `need` lowest-index
-  // experts whose key equals it
-  if (tid == 0) {
-    s_na = 0;
-    s_nb = 0;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kSlicePerLane; ++i) {
-    const int e = tid + kTopkThreads * i;
-    if (e < E) {
-      if (key[i] > prefix) candA[atomicAdd(&s_na, 1)] = e;
-      else if (key[i] == prefix) cand[atomicAdd(&s_nb, 1)] = e;
-    }
-  }
-  __syncthreads();
-  const int na = s_na, nb = s_nb;
-  for (int c = tid; c < nb; c += blockDim.x) {
-    int r = 0;
-    for (int c2 = 0; c2 < nb; ++c2) r += cand[c2] < cand[c];
-    if (r < need) candA[na + r] = cand[c];
-  }
-  __syncthreads();
-  if (tid < nsel) {  // order by (logit descending, index ascending): rank by counting
-    const int e = candA[tid];
-    const float v = sv[e];
-    int r = 0;
-    for (int c2 = 0; c2 < nsel; ++c2) {
-      const int e2 = candA[c2];
-      r += before(sv[e2], e2, v, e);
-    }
-    sel[r] = e;
-  }
-  __syncthreads();
-  if (tid < k) insel[sel[tid]] = 1;
-  __syncthreads();
-  // certification: every outsider's upper bound below the lowest selected lower
-  // bound, and strict separation of consecutive selected experts
-  float hi_out = -INFINITY;
-  for (int e = tid; e < E; e += blockDim.x)
-    if (!insel[e]) hi_out = fmaxf(hi_out, sv[e] + sb[e]);
-  hi_out = block_max(hi_out, scratch);
-  float lo_neg = -INFINITY;  // max of -lo_j: the lowest selected lower bound, negated
-  bool bad = false;
-  if (tid < k) {
-    const int e = sel[tid];
-    const float lo = sv[e] - sb[e];
-    lo_neg = -lo;
-    if (tid + 1 < k) bad = !(lo > sv[sel[tid + 1]] + sb[sel[tid + 1]]);
-  }
-  const float m = -block_max(lo_neg, scratch);
-  const int nbad = __syncthreads_or(bad ? 1 : 0);
-  if (tid == 0) certified = (!nbad && hi_out < m) ? 1 : 0;
-  __syncthreads();
-  if (certified) {
-    if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum
-      const float v0 = sv[sel[0]];
-      const float g = lane < k ? expf(sv[sel[lane]] - v0) : 0.f;
-      float den = g;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      if (lane < k) {
-        a.topk_idx[(size_t)t * k + lane] = sel[lane];
-        a.gates[(size_t)t * k + lane] = g / den;
-      }
-    }
-    return;
-  }
-
-  // ---- recheck path: every expert that could be in the top k ----------------
   if (tid == 0) {
     atomicAdd(a.err + 2, 1);
     n_cand = 0;
@@ -819,6 +676,167 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a) {
       a.gates[(size_t)t * k + lane] = g / den;
     }
   }
+}
+
+// One CTA per token (the body of the top-k kernel): a radix select finds the (k+1)-th largest fp32 logit,
+// the k+1 experts at or above it are ordered by counting, and the bounds then
+// certify the selection or send the CTA down the recheck path.
+__device__ __forceinline__ void topk_token(const RouteArgs& a) {
+  extern __shared__ double tsm[];
+  const int E = a.E, k = a.k;
+  const size_t e8 = ((size_t)E + 7) / 8 * 8;
+  double* clo = tsm;  // recheck path: candidate bounds
+  double* chi = clo + e8;
+  float* sv = reinterpret_cast<float*>(chi + e8);  // fp32 logits
+  float* sb = sv + e8;                             // their error bounds
+  int* cand = reinterpret_cast<int*>(sb + e8);     // recheck path: candidate experts
+  unsigned char* insel = reinterpret_cast<unsigned char*>(cand + e8);
+  unsigned char* cflag = insel + e8;
+  __shared__ int sel[kMaxK + 1];
+  __shared__ int candA[kMaxK + 1];
+  __shared__ int hist[256];
+  __shared__ int s_digit, s_need, s_full, s_na, s_nb;
+  __shared__ int certified;
+  __shared__ float scratch[kTopkWarps];
+
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  const float nx = a.comp ? 0.f : a.nrm_x[t];
+  // load: thread tid holds experts e = tid + 256 i as order-preserving keys
+  uint32_t key[kSlicePerLane];
+#pragma unroll
+  for (int i = 0; i < kSlicePerLane; ++i) {
+    const int e = tid + kTopkThreads * i;
+    key[i] = 0u;
+    if (e < E) {
+      const float v = a.logits[(size_t)t * E + e];
+      sv[e] = v;
+      sb[e] = a.comp ? a.gamma * a.absdot[(size_t)t * E + e] + 2.4e-7f * fabsf(v) + 1e-30f
+                     : a.gamma * a.nrm_w[e] * nx + 1.2e-7f * fabsf(v) + 1e-30f;
+      insel[e] = 0;
+      key[i] = ord_bits(v);
+    }
+  }
+  pdl_launch_dependents();
+  const int nsel = min(k + 1, E);
+  // radix select of the nsel-th largest key, 8 bits per pass from the top
+  uint32_t prefix = 0u, mask = 0u;
+  int need = nsel;  // how many keys >= the threshold still to account for at this digit
+  // A pass whose chosen digit bucket holds exactly the keys still needed ends
+  // the search: the selection is then every key whose masked value is at or
+  // above the prefix (usually after two of the four passes).
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kSlicePerLane; ++i)
+      if (tid + kTopkThreads * i < E && (key[i] & mask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+    __syncthreads();
+    if (warp == 0) {  // lane l scans bins 255-8l .. 248-8l, top down
+      int c[8], lsum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        lsum += c[j];
+      }
+      int incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - lsum;
+      if (excl < need && need <= incl) {
+        int run = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= need) {
+            s_digit = 255 - 8 * lane - j;
+            s_need = need - run;
+            s_full = (need - run) == c[j];
+            break;
+          }
+          run += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)s_digit << shift;
+    mask |= 255u << shift;
+    need = s_need;
+    if (s_full) break;
+  }
+  // the selection: every key above the threshold, then the `need` lowest-index
+  // experts whose key equals it
+  if (tid == 0) {
+    s_na = 0;
+    s_nb = 0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kSlicePerLane; ++i) {
+    const int e = tid + kTopkThreads * i;
+    if (e < E) {
+      if ((key[i] & mask) > prefix) candA[atomicAdd(&s_na, 1)] = e;
+      else if ((key[i] & mask) == prefix) cand[atomicAdd(&s_nb, 1)] = e;
+    }
+  }
+  __syncthreads();
+  const int na = s_na, nb = s_nb;
+  for (int c = tid; c < nb; c += blockDim.x) {
+    int r = 0;
+    for (int c2 = 0; c2 < nb; ++c2) r += cand[c2] < cand[c];
+    if (r < need) candA[na + r] = cand[c];
+  }
+  __syncthreads();
+  if (tid < nsel) {  // order by (logit descending, index ascending): rank by counting
+    const int e = candA[tid];
+    const float v = sv[e];
+    int r = 0;
+    for (int c2 = 0; c2 < nsel; ++c2) {
+      const int e2 = candA[c2];
+      r += before(sv[e2], e2, v, e);
+    }
+    sel[r] = e;
+  }
+  __syncthreads();
+  if (tid < k) insel[sel[tid]] = 1;
+  __syncthreads();
+  // certification: every outsider's upper bound below the lowest selected lower
+  // bound, and strict separation of consecutive selected experts
+  float hi_out = -INFINITY;
+  for (int e = tid; e < E; e += blockDim.x)
+    if (!insel[e]) hi_out = fmaxf(hi_out, sv[e] + sb[e]);
+  hi_out = block_max(hi_out, scratch);
+  float lo_neg = -INFINITY;  // max of -lo_j: the lowest selected lower bound, negated
+  bool bad = false;
+  if (tid < k) {
+    const int e = sel[tid];
+    const float lo = sv[e] - sb[e];
+    lo_neg = -lo;
+    if (tid + 1 < k) bad = !(lo > sv[sel[tid + 1]] + sb[sel[tid + 1]]);
+  }
+  const float m = -block_max(lo_neg, scratch);
+  const int nbad = __syncthreads_or(bad ? 1 : 0);
+  if (tid == 0) certified = (!nbad && hi_out < m) ? 1 : 0;
+  __syncthreads();
+  if (certified) {
+    if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum
+      const float v0 = sv[sel[0]];
+      const float g = lane < k ? expf(sv[sel[lane]] - v0) : 0.f;
+      float den = g;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (lane < k) {
+        a.topk_idx[(size_t)t * k + lane] = sel[lane];
+        a.gates[(size_t)t * k + lane] = g / den;
+      }
+    }
+    return;
+  }
+
+  topk_recheck(a, t, sv, sb, insel, m, clo, chi, cand, cflag);
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {

@@ -115,6 +115,28 @@ def test_route_topk_and_bucket_standalone_match_oracle(lib, ctx):
         np.testing.assert_array_equal(pairs.cpu().numpy(), p_ref)
 
 
+@pytest.mark.parametrize("E,k,T", [(1536, 8, 5), (100, 32, 7), (1024, 31, 3)])
+def test_route_topk_radix_and_warp_select_paths(lib, ctx, E, k, T):
+    # E > 1024 or k + 1 > 32 take the radix select; E <= 1024 with k + 1 <= 32
+    # the warp select (the last case sits at both limits)
+    moe = lib
+    d = 256
+    rng = np.random.default_rng(E + k)
+    Wb = torch.from_numpy((rng.standard_normal((E, d)) / 16).astype(np.float32)).to(torch.bfloat16)
+    x = torch.from_numpy(rng.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16)
+    topk = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.route_topk_ws_bytes(T, d, E, k))
+    moe.moe_route_topk(ctx, x.cuda(), Wb.cuda(), None, k, topk, gates, ws)
+    ctx.check()
+    xh = x.view(torch.int16).numpy().view(np.uint16)
+    Wh = Wb.view(torch.int16).numpy().view(np.uint16)
+    logits, idx, g = oracle.router(xh, Wh, None, k)
+    # logits are O(1) here, so the fp32 logit and gate roundings move a gate by
+    # a few 1e-7 relative; 2e-5 leaves ample room
+    gu.check_routing(topk.cpu().numpy(), gates.cpu().numpy(), idx, g, np.full(T, 2e-5))
+
+
 def test_router_certifies_exact_ties_and_near_ties(lib, ctx):
     # duplicated router rows give exactly equal logits (ties must go to the lower
     # index); rows differing in one low bit give near-ties the fp32 bound cannot
