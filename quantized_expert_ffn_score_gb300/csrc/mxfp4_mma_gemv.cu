@@ -381,14 +381,15 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
       for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
-      // the warp's 8 block scales of its rows ra = 16 m + gq and rb = ra + 8: one 8-byte load each when
-      // the scale rows are 8-byte aligned (K / 32 a multiple of 8), else bytes (only blocks < nblk)
+      // the warp's block scales of its rows ra = 16 m + gq and rb = ra + 8: one 8-byte load each when
+      // the warp's first scale byte is 8-byte aligned (8 blocks per warp and K / 32 a multiple of 8),
+      // else bytes (only blocks < nblk)
       uint2 sra[2], srb[2];
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const uint8_t* pa = sc + (size_t)(16 * m + gq) * (K / 32) + b0;
         const uint8_t* pb = sc + (size_t)(16 * m + gq + 8) * (K / 32) + b0;
-        if (((K / 32) & 7) == 0) {
+        if (BPW == 8 && ((K / 32) & 7) == 0) {
           sra[m] = *reinterpret_cast<const uint2*>(pa);
           srb[m] = *reinterpret_cast<const uint2*>(pb);
         } else {
