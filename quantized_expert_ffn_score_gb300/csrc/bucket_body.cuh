@@ -168,11 +168,11 @@ __device__ __forceinline__ void bucket_block(const BucketArgs& a, int nw, int* b
 // number of selected ids below it, pair j lands at the rank of sel[j], and
 // every selected expert has one token (GEMM path only when gemm_min <= 1).
 // Every thread of the block calls it.
-__device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_smem) {
+__device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_smem, bool preloaded = false) {
   const int E = a.E, k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < k) {
-    int e = a.topk_idx[threadIdx.x];
+    int e = preloaded ? sel_smem[threadIdx.x] : a.topk_idx[threadIdx.x];
     if (e < 0 || e >= E) {
       dev_error(a.err, MOE_ERR_BAD_EXPERT_INDEX, e);
       e = E;  // sorts last, never counted

@@ -573,7 +573,7 @@ __device__ float block_max(float v, float* scratch) {
 // bound) and, if still undecided, by the reference's sequential fp64 sum.
 __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float* sv, const float* sb,
                                           const unsigned char* insel, float m, double* clo, double* chi, int* cand,
-                                          unsigned char* cflag) {
+                                          unsigned char* cflag, int* out_sel) {
   __shared__ int n_cand;
   __shared__ int order[kMaxK];
   __shared__ double oval[kMaxK];
@@ -674,6 +674,7 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
     if (lane < k) {
       a.topk_idx[(size_t)t * k + lane] = order[lane];
       a.gates[(size_t)t * k + lane] = g / den;
+      out_sel[lane] = order[lane];
     }
   }
 }
@@ -681,7 +682,8 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
 // One CTA per token (the body of the top-k kernel): a radix select finds the (k+1)-th largest fp32 logit,
 // the k+1 experts at or above it are ordered by counting, and the bounds then
 // certify the selection or send the CTA down the recheck path.
-__device__ __forceinline__ void topk_token(const RouteArgs& a) {
+// The selection also lands in out_sel[0 .. k-1] (shared memory of the CTA).
+__device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   extern __shared__ double tsm[];
   const int E = a.E, k = a.k;
   const size_t e8 = ((size_t)E + 7) / 8 * 8;
@@ -831,20 +833,21 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a) {
       if (lane < k) {
         a.topk_idx[(size_t)t * k + lane] = sel[lane];
         a.gates[(size_t)t * k + lane] = g / den;
+        out_sel[lane] = sel[lane];
       }
     }
     return;
   }
 
-  topk_recheck(a, t, sv, sb, insel, m, clo, chi, cand, cflag);
+  topk_recheck(a, t, sv, sb, insel, m, clo, chi, cand, cflag, out_sel);
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
-  topk_token(a);
+  __shared__ int sel_smem[kMaxK];
+  topk_token(a, sel_smem);
   if (a.fuse_bucket) {  // one token: bucket its k pairs right here (no further launch)
-    __shared__ int sel_smem[kMaxK];
     __syncthreads();
-    bucket_one_token(a.bucket, sel_smem);
+    bucket_one_token(a.bucket, sel_smem, true);
   }
 }
 
