@@ -312,6 +312,15 @@ __device__ __forceinline__ void sf_load(SfRegs<MODE>& r, const BsArgs& a, const 
   }
 }
 
+// One token's activation and its three E4M3 terms, kept out of line: ten
+// warps in four roles share the SM's instruction caches, and an epilogue
+// unrolled over every token of an n-tile evicted the issuing thread's loop
+// (measured: gate/up 974 -> 930 us on the 512-token Zipf layer).
+__device__ __noinline__ void finish_token(float g, float u, int act, uint8_t* q, size_t plane, uint8_t* sf,
+                                          size_t splane, int lane) {
+  emit_terms<3>(act_fast(g, u, act), q, plane, sf, splane, lane);
+}
+
 // The MMAs of one stage: CH chunks x 4 K steps x the tile's matrices.  sd is
 // the shared-memory descriptor of the stage's first byte; descriptors count
 // in 16-byte units, so operand offsets are added to it directly (every
@@ -403,8 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       local += ntiles_rows * ((ne + a.nt - 1) / a.nt);
     }
     int base = bucket_detail::block_exclusive_scan(local, scan_scratch, &total0);
-    // few units (decode): split every tile's K into parts of one scale group
-    const bool split = total0 < 8 * (int)gridDim.x && a.P <= kSplitMaxPairs && ngroups > 1;
+    // at most half as many tiles as CTAs: every tile's K is split in two halves
+    // (parts of one scale group) for two CTAs; whole tiles are kept otherwise
+    // (one token's 384 gate/up tiles run 53 us whole against 56 us split in
+    // parts spread over all CTAs: the imbalance of 2 or 3 tiles per CTA costs
+    // less than the split tiles' partial-sum round trips)
+    const bool split = 2 * total0 <= (int)gridDim.x && a.P <= kSplitMaxPairs && ngroups > 1;
     pl.kparts = split ? ngroups : 1;
     pl.gpk = ngroups / pl.kparts;
     pl.units = total0 * pl.kparts;
@@ -418,12 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // Whole-K units are dealt round robin: at any time the CTAs work on a window
   // of consecutive units, so the n-tiles of one weight tile are streamed by
-  // several CTAs together and all but the first read it from L2.  Split units
-  // stay in contiguous ranges (the parts of a tile meet in one CTA).
+  // several CTAs together and all but the first read it from L2.  A split tile
+  // goes to CTAs 2 t and 2 t + 1, the first half of its parts to the first:
+  // exactly two partial sums meet in memory, and fp32 addition of two values
+  // (to a zeroed word) does not depend on their order.
   const bool dealt = pl.kparts == 1;
-  const int ub = dealt ? (int)blockIdx.x : (int)((long long)pl.units * blockIdx.x / gridDim.x);
-  int nu = dealt ? (pl.units > (int)blockIdx.x ? (pl.units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0)
-                 : (int)((long long)pl.units * (blockIdx.x + 1) / gridDim.x) - ub;
+  int ub, nu;
+  if (dealt) {
+    ub = (int)blockIdx.x;
+    nu = pl.units > (int)blockIdx.x ? (pl.units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  } else {
+    const int tile = (int)blockIdx.x >> 1, half = (int)blockIdx.x & 1, h = pl.kparts / 2;
+    ub = tile * pl.kparts + (half ? h : 0);
+    nu = tile < total0 ? (half ? pl.kparts - h : h) : 0;
+  }
   if (nu > a.max_units) {  // cannot happen with the host's bound; leave the rest undone, reported
     if (threadIdx.x == 0) dev_error(a.err, MOE_ERR_UNSUPPORTED, nu);
     nu = a.max_units;
@@ -701,9 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int n = 0; n < kMaxNT; ++n) {
             if (n < t.ntok) {
               const int slot = t.s0 + n;
-              const float h = act_fast(s0[n], s1[n], a.act);
-              emit_terms<3>(h, a.hq + (size_t)slot * a.ff + row, hplane, a.hsf + (size_t)slot * (a.ff / 32) + row / 32,
-                            hsplane, lane);
+              finish_token(s0[n], s1[n], a.act, a.hq + (size_t)slot * a.ff + row, hplane,
+                           a.hsf + (size_t)slot * (a.ff / 32) + row / 32, hsplane, lane);
             }
           }
         }
@@ -745,12 +765,14 @@ size_t smem_bytes(const BsGeom& g, int E, int max_units) {
 }
 
 // Bound on the units one CTA gets: every active expert has at most
-// ceil(ne / nt) <= ne / nt + 1 n-tiles, and K is split only for few pairs.
+// ceil(ne / nt) <= ne / nt + 1 n-tiles dealt round robin, and a split tile
+// gives a CTA at most the larger half of its K parts.
 int max_units_per_cta(int rows, int K, int P, int E, int nt, int grid) {
   const long long ntiles = (long long)(P + nt - 1) / nt + (P < E ? P : E);
   const long long u0 = (long long)(rows / kBM) * ntiles;
-  const long long kp = P <= kSplitMaxPairs ? K / kGroupK : 1;
-  return (int)((u0 * kp + grid - 1) / grid) + 1;
+  const int whole = (int)((u0 + grid - 1) / grid) + 1;
+  const int half = P <= kSplitMaxPairs ? (K / kGroupK + 1) / 2 : 0;
+  return whole > half ? whole : half;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -21,8 +21,9 @@ pytestmark = pytest.mark.gpu
 
 # one scale group along K (d = ff = 512), 5 tokens: every n-tile padded from <= 8 tokens
 SMALL = si.LayerRecipe("bs_small", d=512, ff=512, E=8, k=2, T=5, seed=51, scale_lo=118, scale_hi=121)
-# 32 pairs over 16 experts: few units, so K is split (2 parts) and tiles are finished by the last arriver
-SPLIT = si.LayerRecipe("bs_split", d=1024, ff=1024, E=16, k=4, T=8, seed=52, scale_lo=118, scale_hi=121)
+# 8 pairs over at most 8 experts: at most 64 tiles (half the CTAs or fewer), so every tile's K is
+# split in two halves for two CTAs and finished by the one that arrives last
+SPLIT = si.LayerRecipe("bs_split", d=1024, ff=1024, E=16, k=2, T=4, seed=52, scale_lo=118, scale_hi=121)
 # 37 tokens x 6 of 40 experts: 32-token n-tiles with ragged tails, d != ff
 MID = si.LayerRecipe("bs_mid", d=1024, ff=512, E=40, k=6, T=37, seed=53, scale_lo=118, scale_hi=121)
 # Zipf(1) bias: buckets from 1 token to a few hundred (many n-tiles per expert)
@@ -62,6 +63,17 @@ def test_small_single_group_padded_ntile(lib, ctx):
 def test_split_k_last_arriver(lib, ctx):
     _, counts = gu.full_check(lib, ctx, SPLIT)
     assert counts.sum() == SPLIT.T * SPLIT.k <= 128
+    assert 2 * 8 * int((counts > 0).sum()) <= ctx.num_sms  # (d / 128) tiles per expert, two CTAs per tile
+
+
+def test_split_k_is_deterministic(lib, ctx):
+    # two partial sums per split tile, added to a zeroed word: the same bits on every run
+    from quantized_expert_ffn_score_gb300 import synthetic
+    layer = synthetic.device_layer(SPLIT)
+    x = synthetic.device_x(SPLIT)
+    outs = [gu.run_layer(lib, ctx, layer, x)[0] for _ in range(3)]
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
 
 
 def test_mid_ragged_ntiles(lib, ctx):
