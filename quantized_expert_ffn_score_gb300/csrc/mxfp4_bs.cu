@@ -26,7 +26,8 @@
 //   D  fp32 in tensor memory.
 // Products and their sum are formed by the tensor core in fp32.
 //
-// Work units: (active expert, 128-row tile, n-tile of up to nt tokens,
+// Work units: (active expert, 128-row tile, n-tile of up to nt tokens (48 for
+// gate/up, 40 for down),
 // K part).  gate/up (MODE 0) keeps the gate and up rows of the same 128 ff
 // indices in two accumulators, so the epilogue applies the activation; down
 // (MODE 1) writes y_pairs.  The persistent grid takes contiguous unit ranges.
@@ -55,7 +56,7 @@ constexpr int kBM = 128;           // weight rows per tile (MMA M)
 constexpr int kBK = 128;           // K per chunk (one A box plane, four MMAs)
 constexpr int kMaxChunks = 2;      // K chunks per pipeline stage
 constexpr int kGroupK = 512;       // K per scale-factor group (4 stages)
-constexpr int kMaxNT = 32;         // tokens per n-tile
+
 constexpr int kMaxStages = 12;
 constexpr int kMaxSfSlots = 4;
 constexpr int kThreads = 320;
@@ -70,6 +71,13 @@ template <int MODE>
 struct Bs {
   static constexpr int kMats = MODE == 0 ? 2 : 1;   // weight matrices per tile
   static constexpr int kTerms = MODE == 0 ? 2 : 3;  // activation terms
+  // Tokens per n-tile at most (more tokens per MMA: an MMA's issue time is
+  // nearly flat in N up to 128).  terms x tokens rows of B must fit the 128
+  // rows whose scale factors one tensor-memory column group holds (down:
+  // 3 x 40 = 120), and gate/up's two double-buffered accumulators (2 x 2 x 96
+  // columns) leave room for two scale-factor slots.  Measured on the 512-token
+  // layers: Zipf gate/up 930 -> 894 us, uniform 2049 -> 2069 us.
+  static constexpr int kNt = MODE == 0 ? 48 : 40;
   static constexpr int kSfACols = kMats * 16;       // per slot: 4 stages x 4 column groups per matrix
   static constexpr int kSlotCols = kSfACols + 16;
 };
@@ -90,7 +98,7 @@ struct BsArgs {
   const uint8_t* const* records;
   int d, ff, E, k, T, P;
   int act;
-  int nt;             // tokens per n-tile (multiple of 8, at most kMaxNT)
+  int nt[2];          // tokens per n-tile of each kernel (multiple of 8, at most Bs<MODE>::kNt)
   const int32_t* offsets;
   const int32_t* pair_ids;
   const int32_t* active;  // active[0] = count, then every expert with tokens
@@ -231,7 +239,7 @@ struct Plan {
   const int* off;          // [n_active + 1] unit offsets (shared memory)
 };
 
-__device__ __forceinline__ Unit decode_unit(const BsArgs& a, const Plan& pl, int u) {
+__device__ __forceinline__ Unit decode_unit(const BsArgs& a, const Plan& pl, int u, int nt) {
   const int na = a.active[0];
   int lo = 0, hi = na - 1;
   while (lo < hi) {
@@ -242,14 +250,14 @@ __device__ __forceinline__ Unit decode_unit(const BsArgs& a, const Plan& pl, int
   Unit t;
   t.e = a.active[1 + lo];
   const int s_beg = a.offsets[t.e], ne = a.offsets[t.e + 1] - s_beg;
-  const int ntiles = (ne + a.nt - 1) / a.nt;
+  const int ntiles = (ne + nt - 1) / nt;
   int local = u - pl.off[lo];
   t.kpart = local % pl.kparts;
   local /= pl.kparts;
   const int ntile = local % ntiles;
   t.tile = local / ntiles;
-  t.s0 = s_beg + ntile * a.nt;
-  t.ntok = min(a.nt, ne - ntile * a.nt);
+  t.s0 = s_beg + ntile * nt;
+  t.ntok = min(nt, ne - ntile * nt);
   return t;
 }
 
@@ -409,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int i = i0; i < i1; ++i) {
       const int e = a.active[1 + i], ne = a.offsets[e + 1] - a.offsets[e];
-      local += ntiles_rows * ((ne + a.nt - 1) / a.nt);
+      local += ntiles_rows * ((ne + a.nt[MODE] - 1) / a.nt[MODE]);
     }
     int base = bucket_detail::block_exclusive_scan(local, scan_scratch, &total0);
     // at most half as many tiles as CTAs: every tile's K is split in two halves
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = i0; i < i1; ++i) {
       unit_off[i] = base * pl.kparts;
       const int e = a.active[1 + i], ne = a.offsets[e + 1] - a.offsets[e];
-      base += ntiles_rows * ((ne + a.nt - 1) / a.nt);
+      base += ntiles_rows * ((ne + a.nt[MODE] - 1) / a.nt[MODE]);
     }
   }
   __syncthreads();
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     nu = a.max_units;
   }
   for (int i = threadIdx.x; i < nu; i += kThreads) {
-    const Unit t = decode_unit(a, pl, dealt ? ub + i * (int)gridDim.x : ub + i);
+    const Unit t = decode_unit(a, pl, dealt ? ub + i * (int)gridDim.x : ub + i, a.nt[MODE]);
     UnitRec r;
     r.rec = a.records[t.e];
     r.e = t.e;
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = *tslot;
   const size_t mat = (size_t)a.ff * a.d / 2 + (size_t)a.ff * a.d / 32;
-  const int nt = a.nt;
+  const int nt = a.nt[MODE];
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -653,9 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = kp0 == 0 && t.kpart == pl.kparts - 1;
       const int row = t.tile * kBM + 32 * q + lane;
       const uint32_t dcol = tmem + lb + (uint32_t)(buf * G.dcols);
-      float s0[kMaxNT], s1[kMaxNT];  // MODE 0: gate and up sums; MODE 1: y in s0
+      float s0[C::kNt], s1[MODE == 0 ? C::kNt : 1];  // MODE 0: gate and up sums; MODE 1: y in s0
 #pragma unroll
-      for (int n0 = 0; n0 < kMaxNT; n0 += 8) {
+      for (int n0 = 0; n0 < C::kNt; n0 += 8) {
         if (n0 < t.ntok) {
           uint32_t v0[8], v1[8];
 #pragma unroll
@@ -679,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (MODE == 1) {
 #pragma unroll
-        for (int n = 0; n < kMaxNT; ++n) {
+        for (int n = 0; n < C::kNt; ++n) {
           if (n < t.ntok) {
             float* dst = a.y_pairs + (size_t)a.pair_ids[t.s0 + n] * a.d + row;
             if (whole) *dst = s0[n];
@@ -691,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool finish = whole;
         if (!whole) {  // add this part's sums; the last of the tile's parts to arrive finishes it
 #pragma unroll
-          for (int n = 0; n < kMaxNT; ++n) {
+          for (int n = 0; n < C::kNt; ++n) {
             if (n < t.ntok) {
               atomicAdd(a.gsum + (size_t)(t.s0 + n) * a.ff + row, s0[n]);
               atomicAdd(a.usum + (size_t)(t.s0 + n) * a.ff + row, s1[n]);
@@ -709,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (finish) {
             __threadfence();
 #pragma unroll
-            for (int n = 0; n < kMaxNT; ++n) {
+            for (int n = 0; n < C::kNt; ++n) {
               if (n < t.ntok) {
                 s0[n] = __ldcg(a.gsum + (size_t)(t.s0 + n) * a.ff + row);
                 s1[n] = __ldcg(a.usum + (size_t)(t.s0 + n) * a.ff + row);
@@ -719,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (finish) {
 #pragma unroll
-          for (int n = 0; n < kMaxNT; ++n) {
+          for (int n = 0; n < C::kNt; ++n) {
             if (n < t.ntok) {
               const int slot = t.s0 + n;
               finish_token(s0[n], s1[n], a.act, a.hq + (size_t)slot * a.ff + row, hplane,
@@ -845,7 +853,8 @@ cudaError_t launch_mxfp4_bs(const BsLaunch& L, int num_sms, bool pdl, cudaStream
   a.T = L.T;
   a.P = L.T * L.k;
   a.act = L.act;
-  a.nt = L.T >= kMaxNT ? kMaxNT : ((L.T + 7) & ~7);
+  a.nt[0] = L.T >= Bs<0>::kNt ? Bs<0>::kNt : ((L.T + 7) & ~7);
+  a.nt[1] = L.T >= Bs<1>::kNt ? Bs<1>::kNt : ((L.T + 7) & ~7);
   a.offsets = L.offsets;
   a.pair_ids = L.pair_ids;
   a.active = L.active;
@@ -868,20 +877,21 @@ cudaError_t launch_mxfp4_bs(const BsLaunch& L, int num_sms, bool pdl, cudaStream
   a.y_pairs = L.y_pairs;
   a.err = L.err;
   if (num_sms > 160) return cudaErrorInvalidValue;  // the split counters are sized for 8 units per SM
-  const int mu0 = max_units_per_cta(a.ff, a.d, a.P, a.E, a.nt, num_sms);
-  const int mu1 = max_units_per_cta(a.d, a.ff, a.P, a.E, a.nt, num_sms);
+  const int mu0 = max_units_per_cta(a.ff, a.d, a.P, a.E, a.nt[0], num_sms);
+  const int mu1 = max_units_per_cta(a.d, a.ff, a.P, a.E, a.nt[1], num_sms);
   a.max_units = mu0 > mu1 ? mu0 : mu1;
-  if (!make_geom<0>(&a.g[0], a.nt, a.E, a.max_units, kChunksGateUp) &&
-      !make_geom<0>(&a.g[0], a.nt, a.E, a.max_units, 1))
+  if (!make_geom<0>(&a.g[0], a.nt[0], a.E, a.max_units, kChunksGateUp) &&
+      !make_geom<0>(&a.g[0], a.nt[0], a.E, a.max_units, 1))
     return cudaErrorInvalidValue;
-  if (!make_geom<1>(&a.g[1], a.nt, a.E, a.max_units, kChunksDown) && !make_geom<1>(&a.g[1], a.nt, a.E, a.max_units, 1))
+  if (!make_geom<1>(&a.g[1], a.nt[1], a.E, a.max_units, kChunksDown) &&
+      !make_geom<1>(&a.g[1], a.nt[1], a.E, a.max_units, 1))
     return cudaErrorInvalidValue;
   const size_t mat = (size_t)a.ff * a.d / 2 + (size_t)a.ff * a.d / 32;  // bytes of one matrix in a record
   CUtensorMap w0, w1, xm, hm;
   if (!make_weight_map(&w0, a.xq, a.d, a.ff, 2, mat, a.g[0].chunks) ||
       !make_weight_map(&w1, a.xq, a.ff, a.d, 1, mat, a.g[1].chunks) ||
-      !make_term_map(&xm, a.xq, a.d, a.P, a.nt, 2, a.g[0].chunks) ||
-      !make_term_map(&hm, a.hq, a.ff, a.P, a.nt, 3, a.g[1].chunks))
+      !make_term_map(&xm, a.xq, a.d, a.P, a.nt[0], 2, a.g[0].chunks) ||
+      !make_term_map(&hm, a.hq, a.ff, a.P, a.nt[1], 3, a.g[1].chunks))
     return cudaErrorInvalidValue;
   cudaError_t err = launch("bs_prep_x", bs_prep_x_kernel, dim3(4 * num_sms), dim3(256), 0, s, pdl, a, L.x);
   if (err != cudaSuccess) return err;
