@@ -664,20 +664,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s0[C::kNt], s1[MODE == 0 ? C::kNt : 1];  // MODE 0: gate and up sums; MODE 1: y in s0
 #pragma unroll
       for (int n0 = 0; n0 < C::kNt; n0 += 8) {
-        if (n0 < t.ntok) {
-          uint32_t v0[8], v1[8];
+        if (n0 < t.ntok) {  // this chunk's term columns of every matrix, with one wait
+          uint32_t v0[8], v1[8], v2[8], v3[8];
+          tc::tmem_ld8(dcol + n0, v0);
+          tc::tmem_ld8(dcol + nt + n0, v1);
+          if (MODE == 0) {
+            tc::tmem_ld8(dcol + G.n_mma + n0, v2);
+            tc::tmem_ld8(dcol + G.n_mma + nt + n0, v3);
+            tc::tmem_wait_ld_bind(v0, v1, v2, v3);
 #pragma unroll
-          for (int m = 0; m < C::kMats; ++m) {
-            tc::tmem_ld8_sync(dcol + m * G.n_mma + n0, v0);
-            tc::tmem_ld8_sync(dcol + m * G.n_mma + nt + n0, v1);
-            float* dst = m == 0 ? s0 : s1;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[n0 + i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
-            if (MODE == 1) {
-              tc::tmem_ld8_sync(dcol + 2 * nt + n0, v0);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) dst[n0 + i] += __uint_as_float(v0[i]);
+            for (int i = 0; i < 8; ++i) {
+              s0[n0 + i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
+              s1[n0 + i] = __uint_as_float(v2[i]) + __uint_as_float(v3[i]);
             }
+          } else {
+            tc::tmem_ld8(dcol + 2 * nt + n0, v2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v3[i] = 0u;
+            tc::tmem_wait_ld_bind(v0, v1, v2, v3);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              s0[n0 + i] = (__uint_as_float(v0[i]) + __uint_as_float(v1[i])) + __uint_as_float(v2[i]);
           }
         }
       }
