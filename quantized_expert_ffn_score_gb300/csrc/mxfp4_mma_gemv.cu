@@ -30,6 +30,7 @@
 // The producer warp copies each tile row by row (bulk async copies, one per
 // lane) into shared memory rows padded by 16 bytes, so that the fragment
 // loads (32-bit words of 8 rows at the same column) hit distinct banks.
+#include <type_traits>
 #include <utility>
 
 #include "moe_internal.cuh"
@@ -405,38 +406,47 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
           srb[m] = make_uint2(w[2], w[3]);
         }
       }
-#pragma unroll
-      for (int j = 0; j < BPW; ++j) {
-        const int b = b0 + j;
-        if (b >= g.nblk) continue;  // (fully unrolled: the fragments stay in registers)
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int ra = 16 * m + gq, rb = ra + 8;
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(st + (size_t)ra * g.pitch + 16 * b + 4 * tq);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(st + (size_t)rb * g.pitch + 16 * b + 4 * tq);
-          uint32_t pa[4], pb[4];
-          e2m1x8_to_f16x2(wa, pa);
-          e2m1x8_to_f16x2(wb, pb);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t A0[4] = {pa[0], pb[0], pa[1], pb[1]};
-          const uint32_t A1[4] = {pa[2], pb[2], pa[3], pb[3]};
-          mma16816(d, A0, fr.hi[j][0], fr.hi[j][1]);
-          mma16816(d, A1, fr.hi[j][2], fr.hi[j][3]);
-          if (MODE == 1) {
-            mma16816(d, A0, fr.lo[MODE == 1 ? j : 0][0], fr.lo[MODE == 1 ? j : 0][1]);
-            mma16816(d, A1, fr.lo[MODE == 1 ? j : 0][2], fr.lo[MODE == 1 ? j : 0][3]);
+      // the block loop, compiled twice: a pass of one token (decode) skips the
+      // products of the MMA's second token column, which are zero
+      auto blocks = [&](auto one_tag) {
+        constexpr bool ONE = decltype(one_tag)::value;
+  #pragma unroll
+        for (int j = 0; j < BPW; ++j) {
+          const int b = b0 + j;
+          if (b >= g.nblk) continue;  // (fully unrolled: the fragments stay in registers)
+  #pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const int ra = 16 * m + gq, rb = ra + 8;
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(st + (size_t)ra * g.pitch + 16 * b + 4 * tq);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(st + (size_t)rb * g.pitch + 16 * b + 4 * tq);
+            uint32_t pa[4], pb[4];
+            e2m1x8_to_f16x2(wa, pa);
+            e2m1x8_to_f16x2(wb, pb);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t A0[4] = {pa[0], pb[0], pa[1], pb[1]};
+            const uint32_t A1[4] = {pa[2], pb[2], pa[3], pb[3]};
+            mma16816(d, A0, fr.hi[j][0], fr.hi[j][1]);
+            mma16816(d, A1, fr.hi[j][2], fr.hi[j][3]);
+            if (MODE == 1) {
+              mma16816(d, A0, fr.lo[MODE == 1 ? j : 0][0], fr.lo[MODE == 1 ? j : 0][1]);
+              mma16816(d, A1, fr.lo[MODE == 1 ? j : 0][2], fr.lo[MODE == 1 ? j : 0][3]);
+            }
+            float sa, sb;
+            {  // bytes j of rows ra and rb as one 16-bit pair
+              const uint32_t wa2 = j < 4 ? sra[m].x : sra[m].y, wb2 = j < 4 ? srb[m].x : srb[m].y;
+              e8m0x2_to_f32(__byte_perm(wa2, wb2, (uint32_t)(j & 3) | ((uint32_t)((j & 3) + 4) << 4)), sa, sb);
+            }
+            acc[m][0] = fmaf(sa, d[0], acc[m][0]);
+            acc[m][2] = fmaf(sb, d[2], acc[m][2]);
+            if (!ONE) {  // token columns 2 tq + 1 (all zero when the pass holds one token)
+              acc[m][1] = fmaf(sa, d[1], acc[m][1]);
+              acc[m][3] = fmaf(sb, d[3], acc[m][3]);
+            }
           }
-          float sa, sb;
-          {  // bytes j of rows ra and rb as one 16-bit pair
-            const uint32_t wa2 = j < 4 ? sra[m].x : sra[m].y, wb2 = j < 4 ? srb[m].x : srb[m].y;
-            e8m0x2_to_f32(__byte_perm(wa2, wb2, (uint32_t)(j & 3) | ((uint32_t)((j & 3) + 4) << 4)), sa, sb);
-          }
-          acc[m][0] = fmaf(sa, d[0], acc[m][0]);
-          acc[m][1] = fmaf(sa, d[1], acc[m][1]);
-          acc[m][2] = fmaf(sb, d[2], acc[m][2]);
-          acc[m][3] = fmaf(sb, d[3], acc[m][3]);
         }
-      }
+      };
+      if (nt == 1) blocks(std::true_type{});
+      else blocks(std::false_type{});
       if (MODE == 1) {  // undo this warp's rescale for tokens 2t, 2t+1
         const float u0 = __shfl_sync(0xffffffffu, fr.unscale, (2 * tq) * 4);
         const float u1 = __shfl_sync(0xffffffffu, fr.unscale, (2 * tq + 1) * 4);
