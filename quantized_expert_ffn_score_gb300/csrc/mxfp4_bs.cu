@@ -26,17 +26,16 @@
 //   D  fp32 in tensor memory.
 // Products and their sum are formed by the tensor core in fp32.
 //
-// Work units: (active expert, 128-row tile, n-tile of up to nt tokens (48 for
-// gate/up, 40 for down),
-// K part).  gate/up (MODE 0) keeps the gate and up rows of the same 128 ff
-// indices in two accumulators, so the epilogue applies the activation; down
-// (MODE 1) writes y_pairs.  The persistent grid takes contiguous unit ranges.
-// With few units (decode) each tile's K is split in parts of 512 so that
-// every SM streams weights; consecutive parts of one tile in one CTA
-// accumulate in tensor memory, and a tile split between two CTAs is finished
-// by the one that arrives last (fp32 partial sums added in memory, then the
-// activation), which depends on no timing: two partial sums, and fp32
-// addition of two values is commutative.
+// Work units: (active expert, 128-row tile, n-tile of up to nt tokens -- 48
+// for gate/up, 40 for down -- K part).  gate/up (MODE 0) keeps the gate and
+// up rows of the same 128 ff indices in two accumulators, so the epilogue
+// applies the activation; down (MODE 1) writes y_pairs.  Whole-K units are
+// dealt round robin over the persistent CTAs.  When there are at most half as
+// many tiles as CTAs, each tile's K is split in two halves (parts of 512) for
+// two CTAs; consecutive parts in one CTA accumulate in tensor memory, and the
+// CTA that arrives last finishes the tile (fp32 partial sums added in memory,
+// then the activation), which depends on no timing: two partial sums, and
+// fp32 addition of two values is commutative.
 //
 // Warp roles (320 threads): 0 TMA producer (and the per-expert tensor maps),
 // 1 MMA issuer and TMEM owner, 2-5 scale-factor writers (one per TMEM lane
