@@ -337,16 +337,18 @@ template <int MODE, int CH>
 __device__ __forceinline__ void issue_stage(uint64_t sd, uint32_t b_off16, uint32_t b_step16, uint32_t d0,
                                             uint32_t n_mma, const uint32_t (&id)[4], uint32_t sfc, bool& fresh) {
   using C = Bs<MODE>;
+  // the descriptors' address field is in the low half and never carries (see above)
+  const uint32_t lo = (uint32_t)sd, hi = (uint32_t)(sd >> 32);
 #pragma unroll
   for (int ch = 0; ch < CH; ++ch) {
-    const uint64_t bd = sd + b_off16 + (uint32_t)ch * b_step16;
+    const uint32_t blo = lo + b_off16 + (uint32_t)ch * b_step16;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
       for (int m = 0; m < C::kMats; ++m) {
-        const uint64_t ad = sd + (uint32_t)((m * CH + ch) * (kABytes >> 4) + 2 * ks);
-        tc::mma_bs(d0 + m * n_mma, ad, bd + 2 * ks, id[ks], sfc + m * 16 + 4 * ch, sfc + C::kSfACols + 4 * ch,
-                   fresh ? 0u : 1u);
+        const uint32_t alo = lo + (uint32_t)((m * CH + ch) * (kABytes >> 4) + 2 * ks);
+        tc::mma_bs_lohi(d0 + m * n_mma, alo, blo + 2 * ks, hi, id[ks], sfc + m * 16 + 4 * ch,
+                        sfc + C::kSfACols + 4 * ch, fresh ? 0u : 1u);
       }
       fresh = false;
     }
