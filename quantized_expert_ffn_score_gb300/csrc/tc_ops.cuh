@@ -165,17 +165,8 @@ __host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id
 // row 32 j + r is read from lane (32 q + r) of column (sf + j) for the lane
 // quarter q that computes it, byte = the selector in the descriptor, so each
 // column group is written to all four lane quarters.
-__device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
-}
-// The same MMA with each shared-memory descriptor given as its two 32-bit
-// halves (the issuing thread offsets only the low half, which holds the
-// operand address).
+// The shared-memory descriptors are given as their two 32-bit halves (the
+// issuing thread offsets only the low half, which holds the operand address).
 __device__ __forceinline__ void mma_bs_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t desc_hi,
                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                             uint32_t accumulate) {
@@ -213,13 +204,6 @@ __device__ __forceinline__ void tmem_wait_ld_bind(uint32_t (&a)[8], uint32_t (&b
                  "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3]), "+r"(d[4]), "+r"(d[5]), "+r"(d[6]), "+r"(d[7])
                :
                : "memory");
-}
-__device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&v)[8]) {
-  asm volatile(
-      "{\n tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
-      " tcgen05.wait::ld.sync.aligned;\n}"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-      : "r"(taddr));
 }
 
 // ------------------------------------------------------------------ tensor maps patched on the device
