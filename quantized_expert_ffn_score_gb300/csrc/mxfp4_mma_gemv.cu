@@ -410,11 +410,11 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
       // products of the MMA's second token column, which are zero
       auto blocks = [&](auto one_tag) {
         constexpr bool ONE = decltype(one_tag)::value;
-  #pragma unroll
+#pragma unroll
         for (int j = 0; j < BPW; ++j) {
           const int b = b0 + j;
           if (b >= g.nblk) continue;  // (fully unrolled: the fragments stay in registers)
-  #pragma unroll
+#pragma unroll
           for (int m = 0; m < 2; ++m) {
             const int ra = 16 * m + gq, rb = ra + 8;
             const uint32_t wa = *reinterpret_cast<const uint32_t*>(st + (size_t)ra * g.pitch + 16 * b + 4 * tq);
