@@ -36,6 +36,7 @@ def lib():
         L.or_mxfp4_record_bytes.argtypes, L.or_mxfp4_record_bytes.restype = [i32, i32], ctypes.c_size_t
         L.or_rvq3_record_bytes.argtypes, L.or_rvq3_record_bytes.restype = [i32, i32], ctypes.c_size_t
         L.or_router.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]
+        L.or_router_mode.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         L.or_topk_gates.argtypes = [vp, i32, i32, i32, vp, vp]
         L.or_bucket.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.or_expert_mxfp4.argtypes = [vp, vp, i32, i32, i32, vp]
@@ -43,6 +44,8 @@ def lib():
         L.or_combine.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.or_layer_forward.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                        vp, i32, vp, vp, vp, vp]
+        L.or_layer_forward_ex.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp,
+                                          vp, vp, vp, i32, vp, vp, vp, vp]
         L.or_partial_delta.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
                                        vp]
         for f in ("or_router", "or_topk_gates", "or_bucket", "or_expert_mxfp4", "or_expert_rvq3", "or_combine",
@@ -117,7 +120,13 @@ def rvq3_record_bytes(d, ff):
     return int(lib().or_rvq3_record_bytes(d, ff))
 
 
-def router(x, W, bias, k):
+BIAS_MODE = {"logit": 0, "select": 1}
+
+
+def router(x, W, bias, k, bias_mode="logit"):
+    """Returns (selection keys l + bias [T][E], topk_idx [T][k], gates [T][k]).
+    bias_mode "logit": the bias enters selection and gates; "select": the
+    selection only (gates from the logits without it)."""
     x = np.ascontiguousarray(x)
     W = np.ascontiguousarray(W)
     T, d = x.shape
@@ -126,8 +135,8 @@ def router(x, W, bias, k):
     idx = np.empty((T, k), dtype=np.int32)
     gates = np.empty((T, k), dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
-    _check(lib().or_router(_p(x), _dt(x), _p(W), _dt(W), _p(b), T, d, E, k, _p(logits), _p(idx), _p(gates)),
-           "router")
+    _check(lib().or_router_mode(_p(x), _dt(x), _p(W), _dt(W), _p(b), BIAS_MODE[bias_mode], T, d, E, k, _p(logits),
+                                _p(idx), _p(gates)), "router")
     return logits, idx, gates
 
 
@@ -191,11 +200,12 @@ def _records_array(records, E):
 
 
 def layer_forward(x, W, bias, d, ff, E, k, records, quant="mxfp4", act_kind="swiglu", codebooks=None,
-                  token_mask=None, nthreads=1):
+                  token_mask=None, nthreads=1, n_shared=0, bias_mode="logit"):
     """Returns (topk_idx [T][k], gates [T][k], y_delta [T][d], out [T][d]) in fp64.
-    records: list/dict expert -> uint8 record (None = absent).  codebooks:
-    (cb_gate, cb_up, cb_down) fp16 [3][256][8] arrays for RVQ3.  Rows of tokens
-    outside token_mask come back as NaN."""
+    records: list/dict expert -> uint8 record (None = absent), E + n_shared
+    entries: records[E + s] is shared expert s (every token, weight 1).
+    codebooks: (cb_gate, cb_up, cb_down) fp16 [3][256][8] arrays for RVQ3.
+    Rows of tokens outside token_mask come back as NaN."""
     x = np.ascontiguousarray(x)
     W = np.ascontiguousarray(W)
     T = x.shape[0]
@@ -203,13 +213,14 @@ def layer_forward(x, W, bias, d, ff, E, k, records, quant="mxfp4", act_kind="swi
     gates = np.empty((T, k), dtype=np.float64)
     y = np.full((T, d), np.nan)
     out = np.full((T, d), np.nan)
-    arr, keep = _records_array(records, E)
+    arr, keep = _records_array(records, E + n_shared)
     cbs = [None, None, None] if codebooks is None else [np.ascontiguousarray(c, dtype=np.uint16) for c in codebooks]
     mask = None if token_mask is None else np.ascontiguousarray(token_mask, dtype=np.uint8)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
-    rc = lib().or_layer_forward(_p(x), _dt(x), _p(W), _dt(W), _p(b), T, d, ff, E, k, ACT[act_kind], QUANT[quant],
-                                ctypes.cast(arr, ctypes.c_void_p), _p(cbs[0]), _p(cbs[1]), _p(cbs[2]), _p(mask),
-                                int(nthreads), _p(idx), _p(gates), _p(y), _p(out))
+    rc = lib().or_layer_forward_ex(_p(x), _dt(x), _p(W), _dt(W), _p(b), BIAS_MODE[bias_mode], T, d, ff, E, k,
+                                   int(n_shared), ACT[act_kind], QUANT[quant], ctypes.cast(arr, ctypes.c_void_p),
+                                   _p(cbs[0]), _p(cbs[1]), _p(cbs[2]), _p(mask), int(nthreads), _p(idx), _p(gates),
+                                   _p(y), _p(out))
     del keep
     _check(rc, "layer_forward")
     return idx, gates, y, out

@@ -90,12 +90,17 @@ size_t or_rvq3_record_bytes(int d, int ff) { return 9 * (size_t)ff * d / 8; }
 /* Router                                                                    */
 /* ------------------------------------------------------------------------ */
 
-int or_topk_gates(const double* logits, int T, int E, int k, int32_t* topk_idx, double* gates) {
+/* Top-k on the selection keys, gates from gate_logits (the same array unless
+ * the bias takes part in the selection only). */
+static int topk_select_gates(const double* keys, const double* gate_logits, int T, int E, int k, int32_t* topk_idx,
+                             double* gates) {
   if (T < 0 || E <= 0 || k <= 0 || k > E) return -1;
   unsigned char* taken = (unsigned char*)malloc((size_t)E);
   if (!taken) return -1;
   for (int t = 0; t < T; ++t) {
-    const double* l = logits + (size_t)t * E;
+    const double* l = keys + (size_t)t * E;
+    const double* gl = gate_logits + (size_t)t * E;
+    int32_t* sel = topk_idx + (size_t)t * k;
     memset(taken, 0, (size_t)E);
     /* k rounds of arg-max; a strictly greater value wins, so among equal values
      * the lowest expert index (scanned first) is kept. */
@@ -106,36 +111,54 @@ int or_topk_gates(const double* logits, int T, int E, int k, int32_t* topk_idx, 
         if (best < 0 || l[e] > l[best]) best = e;
       }
       taken[best] = 1;
-      topk_idx[(size_t)t * k + j] = best;
+      sel[j] = best;
     }
     /* Softmax over all E experts restricted to the selected ones and
-     * renormalised equals the softmax over the selected logits alone. */
-    double lmax = l[topk_idx[(size_t)t * k]];
+     * renormalised equals the softmax over the selected logits alone; the
+     * largest selected gate logit is subtracted before exp. */
+    double lmax = gl[sel[0]];
+    for (int j = 1; j < k; ++j)
+      if (gl[sel[j]] > lmax) lmax = gl[sel[j]];
     double den = 0.0;
-    for (int j = 0; j < k; ++j) den += exp(l[topk_idx[(size_t)t * k + j]] - lmax);
-    for (int j = 0; j < k; ++j) gates[(size_t)t * k + j] = exp(l[topk_idx[(size_t)t * k + j]] - lmax) / den;
+    for (int j = 0; j < k; ++j) den += exp(gl[sel[j]] - lmax);
+    for (int j = 0; j < k; ++j) gates[(size_t)t * k + j] = exp(gl[sel[j]] - lmax) / den;
   }
   free(taken);
   return 0;
 }
 
-int or_router(const void* x, int x_dtype, const void* w, int w_dtype, const float* bias, int T, int d, int E,
-              int k, double* logits, int32_t* topk_idx, double* gates) {
-  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return -1;
-  double* l = logits ? logits : (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * E);
-  if (!l) return -1;
+int or_topk_gates(const double* logits, int T, int E, int k, int32_t* topk_idx, double* gates) {
+  return topk_select_gates(logits, logits, T, E, k, topk_idx, gates);
+}
+
+int or_router_mode(const void* x, int x_dtype, const void* w, int w_dtype, const float* bias, int bias_mode, int T,
+                   int d, int E, int k, double* logits, int32_t* topk_idx, double* gates) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || (bias_mode != 0 && bias_mode != 1)) return -1;
+  const size_t n = (size_t)(T > 0 ? T : 1) * E;
+  double* l = logits ? logits : (double*)malloc(sizeof(double) * n);
+  double* plain = bias_mode == 1 ? (double*)malloc(sizeof(double) * n) : NULL;
+  int rc = -1;
+  if (!l || (bias_mode == 1 && !plain)) goto done;
   for (int t = 0; t < T; ++t) {
     for (int e = 0; e < E; ++e) {
       double s = 0.0;
       for (int i = 0; i < d; ++i)
         s += load_val(w, w_dtype, (size_t)e * d + i) * load_val(x, x_dtype, (size_t)t * d + i);
+      if (plain) plain[(size_t)t * E + e] = s;
       if (bias) s += (double)bias[e];
       l[(size_t)t * E + e] = s;
     }
   }
-  int rc = or_topk_gates(l, T, E, k, topk_idx, gates);
+  rc = topk_select_gates(l, plain ? plain : l, T, E, k, topk_idx, gates);
+done:
   if (!logits) free(l);
+  free(plain);
   return rc;
+}
+
+int or_router(const void* x, int x_dtype, const void* w, int w_dtype, const float* bias, int T, int d, int E,
+              int k, double* logits, int32_t* topk_idx, double* gates) {
+  return or_router_mode(x, x_dtype, w, w_dtype, bias, 0, T, d, E, k, logits, topk_idx, gates);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -302,25 +325,36 @@ static int pair_outputs(const void* x, int x_dtype, const int32_t* topk_idx, con
   return rc;
 }
 
-int or_layer_forward(const void* x, int x_dtype, const void* router_w, int w_dtype, const float* bias, int T,
-                     int d, int ff, int E, int k, int act, int quant, const uint8_t* const* records,
-                     const uint16_t* cb_gate, const uint16_t* cb_up, const uint16_t* cb_down,
-                     const uint8_t* token_mask, int nthreads, int32_t* topk_idx, double* gates, double* y_delta,
-                     double* out) {
-  if (T < 0 || d <= 0 || ff <= 0 || E <= 0 || k <= 0 || k > E || (d % 32) || (ff % 32)) return -1;
-  size_t P = (size_t)T * k;
+int or_layer_forward_ex(const void* x, int x_dtype, const void* router_w, int w_dtype, const float* bias,
+                        int bias_mode, int T, int d, int ff, int E, int k, int n_shared, int act, int quant,
+                        const uint8_t* const* records, const uint16_t* cb_gate, const uint16_t* cb_up,
+                        const uint16_t* cb_down, const uint8_t* token_mask, int nthreads, int32_t* topk_idx,
+                        double* gates, double* y_delta, double* out) {
+  if (T < 0 || d <= 0 || ff <= 0 || E <= 0 || k <= 0 || k > E || n_shared < 0 || (d % 32) || (ff % 32)) return -1;
+  /* Every token's pairs: the k routed experts with their gates, then the
+   * n_shared shared experts (records E .. E + n_shared - 1) with weight 1. */
+  const int ks = k + n_shared;
+  size_t P = (size_t)T * k, Ps = (size_t)T * ks;
   int32_t* idx = topk_idx ? topk_idx : (int32_t*)malloc(sizeof(int32_t) * (P ? P : 1));
   double* g = gates ? gates : (double*)malloc(sizeof(double) * (P ? P : 1));
-  double* yp = (double*)malloc(sizeof(double) * (P ? P : 1) * d);
+  int32_t* idx_s = (int32_t*)malloc(sizeof(int32_t) * (Ps ? Ps : 1));
+  double* g_s = (double*)malloc(sizeof(double) * (Ps ? Ps : 1));
+  double* yp = (double*)malloc(sizeof(double) * (Ps ? Ps : 1) * d);
   double* delta = (double*)malloc(sizeof(double) * (size_t)(T ? T : 1) * d);
   int rc = -1;
-  if (!idx || !g || !yp || !delta) goto done;
-  rc = or_router(x, x_dtype, router_w, w_dtype, bias, T, d, E, k, NULL, idx, g);
+  if (!idx || !g || !idx_s || !g_s || !yp || !delta) goto done;
+  rc = or_router_mode(x, x_dtype, router_w, w_dtype, bias, bias_mode, T, d, E, k, NULL, idx, g);
   if (rc) goto done;
-  rc = pair_outputs(x, x_dtype, idx, g, T, d, ff, k, act, quant, records, cb_gate, cb_up, cb_down, token_mask, 0,
-                    E, nthreads, yp);
+  for (int t = 0; t < T; ++t) {
+    for (int j = 0; j < ks; ++j) {
+      idx_s[(size_t)t * ks + j] = j < k ? idx[(size_t)t * k + j] : E + (j - k);
+      g_s[(size_t)t * ks + j] = j < k ? g[(size_t)t * k + j] : 1.0;
+    }
+  }
+  rc = pair_outputs(x, x_dtype, idx_s, g_s, T, d, ff, ks, act, quant, records, cb_gate, cb_up, cb_down, token_mask,
+                    0, E + n_shared, nthreads, yp);
   if (rc) goto done;
-  or_combine(NULL, yp, g, T, k, d, delta);
+  or_combine(NULL, yp, g_s, T, ks, d, delta);
   for (int t = 0; t < T; ++t) {
     if (token_mask && !token_mask[t]) continue;
     for (int i = 0; i < d; ++i) {
@@ -332,9 +366,20 @@ int or_layer_forward(const void* x, int x_dtype, const void* router_w, int w_dty
 done:
   if (!topk_idx) free(idx);
   if (!gates) free(g);
+  free(idx_s);
+  free(g_s);
   free(yp);
   free(delta);
   return rc;
+}
+
+int or_layer_forward(const void* x, int x_dtype, const void* router_w, int w_dtype, const float* bias, int T,
+                     int d, int ff, int E, int k, int act, int quant, const uint8_t* const* records,
+                     const uint16_t* cb_gate, const uint16_t* cb_up, const uint16_t* cb_down,
+                     const uint8_t* token_mask, int nthreads, int32_t* topk_idx, double* gates, double* y_delta,
+                     double* out) {
+  return or_layer_forward_ex(x, x_dtype, router_w, w_dtype, bias, 0, T, d, ff, E, k, 0, act, quant, records, cb_gate,
+                             cb_up, cb_down, token_mask, nthreads, topk_idx, gates, y_delta, out);
 }
 
 int or_partial_delta(const void* x, int x_dtype, const int32_t* topk_idx, const double* gates, int T, int d,

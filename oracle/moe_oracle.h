@@ -13,6 +13,8 @@
  * Sources (page title, section):
  *   LazyLoRA README, "The engine": top-16 routing over 896 routed experts,
  *     MXFP4 experts, fp32 (here: fp64) expert accumulation;
+ *   LazyLoRA README, "The engine": 2 shared experts in each MoE layer beside
+ *     the routed ones;
  *   LazyLoRA README, "File map": the router (top-16 gating with a
  *     score-correction bias) and SiTU 4*tanh(g/4)*sigmoid(g) x 25*tanh(u/25);
  *   WASTE README, "3 bits per expert weight": RVQ with 3 stages of 256-entry
@@ -60,6 +62,14 @@ size_t or_rvq3_record_bytes(int d, int ff);
  * logits (nullable) [T][E]; topk_idx [T][k]; gates [T][k]. */
 int or_router(const void* x, int x_dtype, const void* w, int w_dtype, const float* bias, int T, int d, int E,
               int k, double* logits, int32_t* topk_idx, double* gates);
+/* The same with a choice of where the bias enters: bias_mode 0 adds it to the
+ * logits used for both the selection and the gates (or_router); bias_mode 1
+ * (the score-correction reading: the bias steers which experts are chosen, not
+ * how much they weigh) selects on l + bias but takes the gates from l alone,
+ * g_j = exp(l_j - max_sel l) / sum_sel exp(l - max_sel l).  logits (nullable)
+ * receives the selection keys l + bias. */
+int or_router_mode(const void* x, int x_dtype, const void* w, int w_dtype, const float* bias, int bias_mode, int T,
+                   int d, int E, int k, double* logits, int32_t* topk_idx, double* gates);
 /* The top-k/gate step alone, on given fp64 logits [T][E]. */
 int or_topk_gates(const double* logits, int T, int E, int k, int32_t* topk_idx, double* gates);
 
@@ -96,6 +106,17 @@ int or_layer_forward(const void* x, int x_dtype, const void* router_w, int w_dty
                      const uint16_t* cb_gate, const uint16_t* cb_up, const uint16_t* cb_down,
                      const uint8_t* token_mask, int nthreads, int32_t* topk_idx, double* gates, double* y_delta,
                      double* out);
+
+/* or_layer_forward with the bias mode of or_router_mode and n_shared shared
+ * experts: records has E + n_shared entries, and records[E + s] is shared
+ * expert s, which every token passes through with weight 1:
+ *   out[t] = x[t] + sum_{j < k} g[t][j] y_{e_j}(x[t]) + sum_{s < n_shared} y_{E+s}(x[t]).
+ * topk_idx and gates stay [T][k] (the routed part). */
+int or_layer_forward_ex(const void* x, int x_dtype, const void* router_w, int w_dtype, const float* bias,
+                        int bias_mode, int T, int d, int ff, int E, int k, int n_shared, int act, int quant,
+                        const uint8_t* const* records, const uint16_t* cb_gate, const uint16_t* cb_up,
+                        const uint16_t* cb_down, const uint8_t* token_mask, int nthreads, int32_t* topk_idx,
+                        double* gates, double* y_delta, double* out);
 
 /* Expert-parallel partial: like or_layer_forward's delta but summing only the
  * pairs whose expert lies in [e_begin, e_end), given the routing. */

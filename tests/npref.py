@@ -105,19 +105,26 @@ def gates_full_softmax(logits, idx):
     return sel / sel.sum(axis=1, keepdims=True)
 
 
-def layer(x, W, bias, k, expert_mats, act="swiglu"):
+def layer(x, W, bias, k, expert_mats, act="swiglu", bias_mode="logit", n_shared=0):
+    """bias_mode "select": the bias only chooses the experts, the gates come from
+    the logits without it.  Experts E .. E + n_shared - 1 are shared: every
+    token adds their outputs unweighted."""
     xf = to_f64(x)
-    logits = xf @ to_f64(W).T
+    plain = xf @ to_f64(W).T
+    logits = plain
     if bias is not None:
-        logits = logits + np.asarray(bias, dtype=np.float64)[None, :]
+        logits = plain + np.asarray(bias, dtype=np.float64)[None, :]
     idx = topk_sorted(logits, k)
-    g = gates_full_softmax(logits, idx)
+    g = gates_full_softmax(plain if bias_mode == "select" else logits, idx)
     T, d = xf.shape
+    E = W.shape[0]
     delta = np.zeros((T, d))
     for t in range(T):
         for j in range(k):
             if g[t, j] != 0.0:
                 delta[t] += g[t, j] * expert(xf[t], expert_mats(int(idx[t, j])), act)
+        for s in range(n_shared):
+            delta[t] += expert(xf[t], expert_mats(E + s), act)
     return logits, idx, g, delta
 
 

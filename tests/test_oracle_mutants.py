@@ -34,6 +34,11 @@ MUTANTS = [
     ("RVQ codes read row-major", "codes[((size_t)s * nv + v) * rows + r]", "codes[((size_t)s * rows + r) * nv + v]"),
     ("SiTU cap", "25.0 * tanh(u / 25.0)", "25.0 * tanh(u / 20.0)"),
     ("f16 exponent bias", "ldexp(1024.0 + m, e - 25)", "ldexp(1024.0 + m, e - 24)"),
+    ("selection-only gates take the biased logits", "topk_select_gates(l, plain ? plain : l,",
+     "topk_select_gates(l, l,"),
+    ("shared experts dropped", "0, E + n_shared, nthreads, yp);", "0, E, nthreads, yp);"),
+    ("shared expert reads a routed record", ": E + (j - k);", ": (j - k);"),
+    ("shared expert weighted like a routed one", ": 1.0;", ": g[(size_t)t * k];"),
 ]
 
 

@@ -159,6 +159,62 @@ def test_gates_sum_to_one_and_equal_renormalised_full_softmax():
     assert np.all(np.diff(g, axis=1) <= 0)  # ordered with the logits
 
 
+def test_select_bias_mode_without_bias_or_with_uniform_bias_is_the_plain_router():
+    x, W = _tiny_xw(T=16, E=30)
+    l0, i0, g0 = oracle.router(x, W, None, 5)
+    l1, i1, g1 = oracle.router(x, W, None, 5, bias_mode="select")
+    np.testing.assert_array_equal(i1, i0)
+    np.testing.assert_array_equal(g1, g0)
+    # a bias equal for every expert moves no selection; the selection-only
+    # gates ignore it, the additive ones cancel it in the softmax
+    c = np.full(30, 2.5, dtype=np.float32)
+    l2, i2, g2 = oracle.router(x, W, c, 5, bias_mode="select")
+    np.testing.assert_array_equal(i2, i0)
+    np.testing.assert_array_equal(g2, g0)
+    np.testing.assert_array_equal(l2, l0 + 2.5)
+
+
+def test_select_bias_forces_the_selection_and_gates_follow_the_unbiased_logits():
+    # the bias lifts a fixed set of k experts 1000 (plus distinct offsets that
+    # fix their order) above the rest: they are the selection whatever the
+    # logits, and their gates are the softmax of the logits WITHOUT the bias,
+    # i.e. g_a / g_b = exp(l_a - l_b) with l from a plain matmul
+    T, d, E, k = 10, 64, 24, 4
+    x, W = _tiny_xw(T=T, d=d, E=E)
+    chosen = [17, 3, 22, 8]
+    bias = np.zeros(E, dtype=np.float32)
+    for r, e in enumerate(chosen):
+        bias[e] = 1000.0 - 10.0 * r
+    keys, idx, g = oracle.router(x, W, bias, k, bias_mode="select")
+    assert np.all(idx == np.array(chosen)[None, :])
+    plain = npref.to_f64(x) @ npref.to_f64(W).T
+    for t in range(T):
+        lsel = plain[t, chosen]
+        for a in range(k):
+            for b in range(k):
+                assert g[t, a] / g[t, b] == pytest.approx(math.exp(lsel[a] - lsel[b]), rel=1e-12)
+    assert np.all(np.abs(g.sum(axis=1) - 1.0) <= 1e-15 * k)
+    # the offsets among the chosen experts change nothing in the selection-only
+    # gates (they would, in the additive mode)
+    bias2 = bias.copy()
+    bias2[chosen] += np.array([0.0, 3.0, 1.0, 2.0], dtype=np.float32)
+    _, idx2, g2 = oracle.router(x, W, bias2, k, bias_mode="select")
+    _, _, g_add = oracle.router(x, W, bias2, k)
+    np.testing.assert_array_equal(idx2, idx)
+    np.testing.assert_array_equal(g2, g)
+    assert np.max(np.abs(g_add - g)) > 0.1
+
+
+def test_select_bias_gates_match_renormalised_full_softmax_of_plain_logits():
+    x, W = _tiny_xw(T=32, E=40)
+    bias = si.zipf_bias(40)
+    keys, idx, g = oracle.router(x, W, bias, 6, bias_mode="select")
+    plain = npref.to_f64(x) @ npref.to_f64(W).T
+    np.testing.assert_array_equal(idx, npref.topk_sorted(plain + bias.astype(np.float64)[None], 6))
+    ref = npref.gates_full_softmax(plain, idx)
+    assert np.all(np.abs(g - ref) <= 1e-13 * ref)
+
+
 # ----------------------------------------------------------------------------- bucketing
 
 def test_bucket_matches_brute_force_scan():
@@ -289,6 +345,42 @@ def test_layer_rvq3_matches_numpy_chain():
                                                lambda e: npref.rvq3_record_mats(recs[e], [cbs] * 3, r.d, r.ff))
     np.testing.assert_array_equal(idx, idx_ref)
     assert np.max(np.abs(y - delta_ref)) <= 1e-12 * np.max(np.abs(delta_ref))
+
+
+def test_layer_select_bias_and_shared_experts_match_numpy_chain():
+    E, S = 12, 2
+    r, x, W, recs = _tiny_layer(E=E + S, seed=6)
+    bias = si.zipf_bias(E)
+    W = W[:E]
+    mats = lambda e: npref.mxfp4_record_mats(recs[e], r.d, r.ff)
+    for mode in ("logit", "select"):
+        idx, g, y, out = oracle.layer_forward(x, W, bias, r.d, r.ff, E, r.k, recs, n_shared=S, bias_mode=mode)
+        _, idx_ref, g_ref, delta_ref = npref.layer(x, W, bias, r.k, mats, bias_mode=mode, n_shared=S)
+        np.testing.assert_array_equal(idx, idx_ref)
+        assert np.all(np.abs(g - g_ref) <= 1e-13 * g_ref)
+        assert np.max(np.abs(y - delta_ref)) <= 1e-12 * np.max(np.abs(delta_ref))
+
+
+def test_shared_experts_add_their_unweighted_outputs():
+    E, S = 12, 2
+    r, x, W, recs = _tiny_layer(E=E + S, seed=8)
+    W = W[:E]
+    idx0, g0, y0, _ = oracle.layer_forward(x, W, None, r.d, r.ff, E, r.k, recs[:E])
+    idx, g, y, out = oracle.layer_forward(x, W, None, r.d, r.ff, E, r.k, recs, n_shared=S)
+    np.testing.assert_array_equal(idx, idx0)
+    np.testing.assert_array_equal(g, g0)
+    for t in range(r.T):
+        xt = x[t].astype(np.float64)
+        shared = sum(oracle.expert_mxfp4(xt, recs[E + s], r.d, r.ff) for s in range(S))
+        np.testing.assert_allclose(y[t] - y0[t], shared, rtol=0, atol=1e-12 * np.max(np.abs(y[t])))
+    # a shared expert whose codes are all zero adds exactly nothing
+    zero = recs[E].copy()
+    zero[:] = 0
+    _, _, y1, _ = oracle.layer_forward(x, W, None, r.d, r.ff, E, r.k, recs[:E] + [zero], n_shared=1)
+    np.testing.assert_array_equal(y1, y0)
+    # a missing shared record is an error, as for a routed one
+    with pytest.raises(RuntimeError):
+        oracle.layer_forward(x, W, None, r.d, r.ff, E, r.k, recs[:E] + [None], n_shared=1)
 
 
 def test_one_hot_gate_reproduces_single_expert():
