@@ -158,11 +158,13 @@ def oracle_sample(r, target_s, max_tokens=64, token_offset=1000):
     done, spent = 0, 0.0
     while done < max_tokens and spent < target_s:
         x = si.layer_x(r, T=1, token_offset=token_offset + done)
-        _, idx, _ = oracle.router(x, W, b, r.k)
-        recs = [si.layer_record(r, e) if e in set(idx.reshape(-1).tolist()) else None for e in range(r.E)]
+        _, idx, _ = oracle.router(x, W, b, r.k, bias_mode=r.bias_mode)
+        used = set(idx.reshape(-1).tolist()) | set(range(r.E, r.E + r.n_shared))
+        recs = [si.layer_record(r, e) if e in used else None for e in range(r.E + r.n_shared)]
         t0 = time.perf_counter()
         oracle.layer_forward(x, W, b, r.d, r.ff, r.E, r.k, recs, quant=r.quant, act_kind=r.act,
-                             codebooks=None if cb is None else (cb, cb, cb), nthreads=threads)
+                             codebooks=None if cb is None else (cb, cb, cb), nthreads=threads,
+                             n_shared=r.n_shared, bias_mode=r.bias_mode)
         spent += time.perf_counter() - t0
         done += 1
         del recs
@@ -245,7 +247,7 @@ def run_ours(args):
     layer = synthetic.device_layer(r, device=dev)
     x_pool = synthetic.device_x(r, T=X_POOL * T, device=dev).view(X_POOL, T, r.d)
     out = torch.empty((T, r.d), dtype=torch.float32, device=dev)
-    counts = torch.empty(r.E, dtype=torch.int32, device=dev)
+    counts = torch.empty(r.E + r.n_shared, dtype=torch.int32, device=dev)
     ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T), device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -358,7 +360,7 @@ def run_ours(args):
         # nominal fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s dense).  The binding one
         # (larger fraction) is reported.
         n, ms = prof["mxfp4_bs_gate_up"]
-        P = T * r.k
+        P = T * (r.k + r.n_shared)
         bs_bytes = mean_distinct * (2 * rec_bytes / 3) + 2 * P * (r.d + r.d // 32)
         bs_flops = 2.0 * 2 * r.ff * r.d * P
         sec = ms / n / 1e3
@@ -384,7 +386,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator; random-init weights)",
             "config": {"workload": args.workload, "d": r.d, "ff": r.ff, "E": r.E, "k": r.k, "tokens_per_step": T,
-                       "quant": r.quant, "experts_resident_gb": round(r.E * rec_bytes / 1e9, 2),
+                       "quant": r.quant, "experts_resident_gb": round((r.E + r.n_shared) * rec_bytes / 1e9, 2),
+                       "shared_experts": r.n_shared, "bias": r.bias, "bias_mode": r.bias_mode,
                        "l2": "flushed between steps outside the timed events (512 MiB write, then 512 MiB read of another buffer)",
                        "x_pool": X_POOL, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "mxfp4_kernel": ctx.mxfp4_kernel if r.quant == "mxfp4" else None},

@@ -84,6 +84,12 @@ typedef enum {
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SITU = 1 } moe_act;
 typedef enum { MOE_QUANT_MXFP4 = 0, MOE_QUANT_RVQ3 = 1 } moe_quant;
+/* Where the router's score-correction bias enters (LazyLoRA README, "File
+ * map": top-16 gating with a score-correction bias).  LOGIT: added to the
+ * logits, so it moves both the selection and the gates.  SELECT: added to the
+ * selection keys only; the gates are the renormalised softmax of the logits
+ * without it. */
+typedef enum { MOE_BIAS_LOGIT = 0, MOE_BIAS_SELECT = 1 } moe_bias_mode;
 
 typedef struct moe_ctx moe_ctx;
 
@@ -122,8 +128,13 @@ typedef struct {
   int d, ff, E;
 } moe_rvq3_experts;
 
-/* One MoE layer: router (W [E][d] row-major, optional additive fp32 logit bias
- * [E]) and its expert bank. */
+/* One MoE layer: router (W [E][d] row-major, optional fp32 score-correction
+ * bias [E] entering as bias_mode says) and its expert bank.  The bank holds
+ * E + n_shared records: records[0 .. E) are the routed experts and records[E + s]
+ * is shared expert s, which every token passes through with weight 1
+ * (LazyLoRA README, "The engine": 896 routed and 2 shared experts in each MoE
+ * layer).  The bank's E field is E + n_shared; k + n_shared <= 32.  The shared
+ * experts use the bank's quantisation (and, for RVQ3, its codebooks). */
 typedef struct {
   int d, ff, E, k;
   moe_act act;
@@ -133,6 +144,8 @@ typedef struct {
   const float* router_bias; /* nullable */
   moe_mxfp4_experts mxfp4;  /* used when quant == MOE_QUANT_MXFP4 */
   moe_rvq3_experts rvq3;    /* used when quant == MOE_QUANT_RVQ3  */
+  int n_shared;             /* shared experts after the routed ones (0: none) */
+  moe_bias_mode bias_mode;  /* MOE_BIAS_LOGIT unless the bias steers the selection only */
 } moe_layer;
 
 /* ---- context ------------------------------------------------------------- */
@@ -244,6 +257,21 @@ MOE_API moe_status moe_route_topk(moe_ctx* ctx, const void* x, moe_dtype x_dtype
                           size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * moe_route_topk with a choice of bias mode (same arguments and workspace
+ * otherwise).  MOE_BIAS_LOGIT is moe_route_topk.  MOE_BIAS_SELECT ranks the
+ * experts by the key l[t][e] + bias[e] (ties to the lower index, certified as
+ * above against keys summed in fp64 in ascending i and then biased) and sets
+ *   gates[t][j] = exp(l_j - m) / sum_j' exp(l_j' - m),  m = max over the
+ *   selected j of l_j,
+ * with l the logits WITHOUT the bias.  An invalid bias_mode returns
+ * MOE_ERR_INVALID_ARG.
+ */
+MOE_API moe_status moe_route_topk_ex(moe_ctx* ctx, const void* x, moe_dtype x_dtype, const void* router_w,
+                                     moe_dtype w_dtype, const float* bias, moe_bias_mode bias_mode, int T, int d, int E,
+                                     int k, int32_t* topk_idx, float* gates, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
+
+/*
  * Bucketing: a stable counting sort of the pairs p = t*k + j by expert
  * topk_idx[p].  Writes counts [E] (pairs per expert), offsets [E+1] (exclusive
  * prefix sum, offsets[E] = T*k) and pair_ids [T*k] (pair ids grouped by expert
@@ -305,9 +333,12 @@ MOE_API moe_status moe_combine(moe_ctx* ctx, const void* x_resid, moe_dtype x_dt
 
 /*
  * The whole layer: route, bucket, expert FFN, combine (with x as residual).
- * x [T][d] (x_dtype), out [T][d] (out_dtype; may not alias x).  The optional
- * outputs topk_idx_out [T][k], gates_out [T][k], counts_out [E] receive the
- * routing when non-NULL.
+ * x [T][d] (x_dtype), out [T][d] (out_dtype; may not alias x).
+ *   out[t] = x[t] + sum_{j < k} g[t][j] y_{e_j}(x[t]) + sum_{s < n_shared} y_{E+s}(x[t])
+ * The optional outputs receive the pairs the layer evaluated when non-NULL:
+ * topk_idx_out [T][k + n_shared] and gates_out [T][k + n_shared] (the routed
+ * selection, then the shared experts E .. E + n_shared - 1 with gate 1) and
+ * counts_out [E + n_shared] (tokens per expert).
  */
 MOE_API moe_status moe_layer_forward(moe_ctx* ctx, const moe_layer* L, const void* x, moe_dtype x_dtype, int T, void* out,
                              moe_dtype out_dtype, int32_t* topk_idx_out, float* gates_out, int32_t* counts_out,

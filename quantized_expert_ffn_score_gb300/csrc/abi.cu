@@ -182,18 +182,21 @@ RouteWs carve_route(Carver& c, int T, int E) {
 }
 
 moe::RouteArgs route_args(const void* x, moe_dtype x_dtype, const void* w, moe_dtype w_dtype, const float* bias,
-                          int T, int d, int E, int k, const RouteWs& ws, int32_t* topk, float* gates, int* err) {
+                          int bias_mode, int T, int d, int E, int k, int n_shared, const RouteWs& ws, int32_t* topk,
+                          float* gates, int* err) {
   moe::RouteArgs ra;
   std::memset(&ra, 0, sizeof ra);
   ra.x = x;
   ra.x_dtype = x_dtype;
   ra.w = w;
   ra.w_dtype = w_dtype;
-  ra.bias = bias;
+  ra.bias = bias_mode == MOE_BIAS_SELECT ? nullptr : bias;
+  ra.sel_bias = bias_mode == MOE_BIAS_SELECT ? bias : nullptr;
   ra.T = T;
   ra.d = d;
   ra.E = E;
   ra.k = k;
+  ra.n_shared = n_shared;
   ra.logits = ws.logits;
   ra.nrm_w = ws.nrm_w;
   ra.nrm_x = ws.nrm_x;
@@ -313,16 +316,22 @@ struct LayerWs {
   FfnWs ffn;
   float* y_pairs;
 };
+// A layer's pairs: every token's k routed experts followed by its n_shared
+// shared ones (expert ids E .. E + n_shared - 1, gate 1).
+int layer_pairs_per_token(const moe_layer* L) { return L->k + L->n_shared; }
+int layer_experts(const moe_layer* L) { return L->E + L->n_shared; }
+
 LayerWs carve_layer(Carver& c, const moe_layer* L, int T) {
   LayerWs w;
-  const size_t P = (size_t)T * L->k;
+  const int ks = layer_pairs_per_token(L), Es = layer_experts(L);
+  const size_t P = (size_t)T * ks;
   w.route = carve_route(c, T, L->E);
   w.topk = c.take<int32_t>(P ? P : 1);
   w.gates = c.take<float>(P ? P : 1);
-  w.counts = c.take<int32_t>(L->E);
-  w.offsets = c.take<int32_t>((size_t)L->E + 1);
+  w.counts = c.take<int32_t>(Es);
+  w.offsets = c.take<int32_t>((size_t)Es + 1);
   w.pairs = c.take<int32_t>(P ? P : 1);
-  w.ffn = carve_ffn(c, T, L->k, L->d, L->ff, L->E, L->quant);
+  w.ffn = carve_ffn(c, T, ks, L->d, L->ff, Es, L->quant);
   w.y_pairs = c.take<float>(P * L->d);
   return w;
 }
@@ -334,12 +343,16 @@ moe_status check_layer(const moe_layer* L) {
   if (!dims_ok(L->d, L->ff)) return MOE_ERR_UNSUPPORTED;
   if (L->router_w == nullptr || !dtype_ok(L->router_w_dtype)) return MOE_ERR_INVALID_ARG;
   if (L->act != MOE_ACT_SWIGLU && L->act != MOE_ACT_SITU) return MOE_ERR_INVALID_ARG;
+  if (L->bias_mode != MOE_BIAS_LOGIT && L->bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
+  if (L->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (layer_pairs_per_token(L) > moe::kMaxK || layer_experts(L) > moe::kMaxE) return MOE_ERR_UNSUPPORTED;
+  const int Es = layer_experts(L);
   if (L->quant == MOE_QUANT_MXFP4) {
     const moe_mxfp4_experts& m = L->mxfp4;
-    if (m.records == nullptr || m.d != L->d || m.ff != L->ff || m.E != L->E) return MOE_ERR_INVALID_ARG;
+    if (m.records == nullptr || m.d != L->d || m.ff != L->ff || m.E != Es) return MOE_ERR_INVALID_ARG;
   } else if (L->quant == MOE_QUANT_RVQ3) {
     const moe_rvq3_experts& r = L->rvq3;
-    if (r.records == nullptr || r.d != L->d || r.ff != L->ff || r.E != L->E) return MOE_ERR_INVALID_ARG;
+    if (r.records == nullptr || r.d != L->d || r.ff != L->ff || r.E != Es) return MOE_ERR_INVALID_ARG;
     for (int m = 0; m < 3; ++m)
       if (r.codebooks[m] == nullptr || (reinterpret_cast<uintptr_t>(r.codebooks[m]) & 15u)) return MOE_ERR_INVALID_ARG;
   } else {
@@ -375,15 +388,17 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
                               moe_dtype out_dtype, int32_t* topk_out, float* gates_out, int32_t* counts_out,
                               const LayerWs& w, cudaStream_t s) {
   if (T == 0) return MOE_OK;
+  const int ks = layer_pairs_per_token(L), Es = layer_experts(L);
   const int32_t* topk = topk_out ? topk_out : w.topk;
   const float* gates = gates_out ? gates_out : w.gates;
   int32_t* counts = counts_out ? counts_out : w.counts;
-  moe::RouteArgs ra = route_args(x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, T, L->d, L->E, L->k,
-                                 w.route, const_cast<int32_t*>(topk), const_cast<float*>(gates), ctx->err);
-  const bool bs = L->quant == MOE_QUANT_MXFP4 && use_bs(ctx, w.ffn, T, L->d, L->ff, L->E, x_dtype);
+  moe::RouteArgs ra = route_args(x, x_dtype, L->router_w, L->router_w_dtype, L->router_bias, L->bias_mode, T, L->d,
+                                 L->E, L->k, L->n_shared, w.route, const_cast<int32_t*>(topk),
+                                 const_cast<float*>(gates), ctx->err);
+  const bool bs = L->quant == MOE_QUANT_MXFP4 && use_bs(ctx, w.ffn, T, L->d, L->ff, Es, x_dtype);
   const moe::HotSplit split = L->quant == MOE_QUANT_MXFP4 && !bs ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype)
                                                                  : moe::HotSplit{0, nullptr, nullptr};
-  moe::BucketArgs ba{topk, T, L->k, L->E, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
+  moe::BucketArgs ba{topk, T, ks, Es, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
   if (T == 1) {  // one token: the top-k kernel buckets its pairs itself
     ra.fuse_bucket = 1;
     ra.bucket = ba;
@@ -394,8 +409,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
     st = cuda_status(moe::launch_bucket(ba, true, s));
     if (st != MOE_OK) return st;
   }
-  moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, L->k, L->d, L->ff, L->E, L->act, w.offsets, w.pairs, w.y_pairs,
-                             w.ffn);
+  moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, ks, L->d, L->ff, Es, L->act, w.offsets, w.pairs, w.y_pairs, w.ffn);
   fa.max_x = w.route.max_x;  // computed by the router kernel
   if (L->quant == MOE_QUANT_MXFP4 && bs) {
     fa.records = L->mxfp4.records;
@@ -413,7 +427,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
     st = cuda_status(moe::launch_rvq3_ffn(fa, ctx->num_sms, true, s));
   }
   if (st != MOE_OK) return st;
-  moe::CombineArgs ca{x, x_dtype, w.y_pairs, gates, T, L->k, L->d, out, out_dtype};
+  moe::CombineArgs ca{x, x_dtype, w.y_pairs, gates, T, ks, L->d, out, out_dtype};
   return cuda_status(moe::launch_combine(ca, true, s));
 }
 
@@ -603,7 +617,7 @@ size_t moe_expert_ffn_ws_bytes(int T, int k, int d, int ff, int E, moe_quant qua
 }
 
 size_t moe_layer_forward_ws_bytes(const moe_layer* L, int T) {
-  if (check_layer(L) != MOE_OK || check_route_shape(T, L->d, L->E, L->k) != MOE_OK) return 0;
+  if (check_layer(L) != MOE_OK || check_route_shape(T, L->d, layer_experts(L), layer_pairs_per_token(L)) != MOE_OK) return 0;
   Carver c(nullptr);
   carve_layer(c, L, T);
   return c.off;
@@ -623,18 +637,27 @@ size_t moe_stack_forward_ws_bytes(const moe_layer* layers, int n_layers, int T) 
 moe_status moe_route_topk(moe_ctx* ctx, const void* x, moe_dtype x_dtype, const void* router_w, moe_dtype w_dtype,
                           const float* bias, int T, int d, int E, int k, int32_t* topk_idx, float* gates, void* ws,
                           size_t ws_bytes, cudaStream_t stream) {
+  return moe_route_topk_ex(ctx, x, x_dtype, router_w, w_dtype, bias, MOE_BIAS_LOGIT, T, d, E, k, topk_idx, gates, ws,
+                           ws_bytes, stream);
+}
+
+moe_status moe_route_topk_ex(moe_ctx* ctx, const void* x, moe_dtype x_dtype, const void* router_w, moe_dtype w_dtype,
+                             const float* bias, moe_bias_mode bias_mode, int T, int d, int E, int k, int32_t* topk_idx,
+                             float* gates, void* ws, size_t ws_bytes, cudaStream_t stream) {
   moe_status st = ctx_ok(ctx);
   if (st != MOE_OK) return st;
   ProfScope prof_scope(ctx);
   if ((st = check_route_shape(T, d, E, k)) != MOE_OK) return st;
   if (!dtype_ok(x_dtype) || !dtype_ok(w_dtype)) return MOE_ERR_INVALID_ARG;
+  if (bias_mode != MOE_BIAS_LOGIT && bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !router_w || !topk_idx || !gates) return MOE_ERR_INVALID_ARG;
   if (!al16(x) || !al16(router_w)) return MOE_ERR_INVALID_ARG;
   if ((st = ws_check(ws, ws_bytes, moe_route_topk_ws_bytes(T, d, E, k))) != MOE_OK) return st;
   Carver c(ws);
   RouteWs w = carve_route(c, T, E);
-  moe::RouteArgs ra = route_args(x, x_dtype, router_w, w_dtype, bias, T, d, E, k, w, topk_idx, gates, ctx->err);
+  moe::RouteArgs ra = route_args(x, x_dtype, router_w, w_dtype, bias, bias_mode, T, d, E, k, 0, w, topk_idx, gates,
+                                 ctx->err);
   return cuda_status(moe::launch_route_topk(ra, ctx->num_sms, stream));
 }
 
@@ -775,7 +798,7 @@ moe_status moe_layer_forward(moe_ctx* ctx, const moe_layer* L, const void* x, mo
   if (st != MOE_OK) return st;
   ProfScope prof_scope(ctx);
   if ((st = check_layer(L)) != MOE_OK) return st;
-  if ((st = check_route_shape(T, L->d, L->E, L->k)) != MOE_OK) return st;
+  if ((st = check_route_shape(T, L->d, layer_experts(L), layer_pairs_per_token(L))) != MOE_OK) return st;
   if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !out || x == out) return MOE_ERR_INVALID_ARG;
@@ -794,7 +817,7 @@ moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers
   if (layers == nullptr || n_layers <= 0) return MOE_ERR_INVALID_ARG;
   for (int l = 0; l < n_layers; ++l) {
     if ((st = check_layer(&layers[l])) != MOE_OK) return st;
-    if ((st = check_route_shape(T, layers[l].d, layers[l].E, layers[l].k)) != MOE_OK) return st;
+    if ((st = check_route_shape(T, layers[l].d, layer_experts(&layers[l]), layer_pairs_per_token(&layers[l]))) != MOE_OK) return st;
     if (layers[l].d != layers[0].d) return MOE_ERR_INVALID_ARG;
   }
   if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype)) return MOE_ERR_INVALID_ARG;

@@ -163,8 +163,10 @@ struct RouteArgs {
   int x_dtype;
   const void* w;
   int w_dtype;
-  const float* bias;
+  const float* bias;      // added to the logits by the router kernels (selection and gates), or null
+  const float* sel_bias;  // added by the top-k to the selection keys only (gates without it), or null
   int T, d, E, k;
+  int n_shared;   // shared experts E .. E + n_shared - 1 appended to every token's row (gate 1)
   float* logits;  // [T][E]   workspace
   float* nrm_w;   // [E]      workspace: ||W_e||_2
   float* nrm_x;   // [T]      workspace: ||x_t||_2
@@ -172,8 +174,8 @@ struct RouteArgs {
   float* absdot;  // [T][E]   workspace: sum_i |W[e][i] x[t][i]| (compensated logits only)
   int comp;       // logits by compensated (Dot2) sums; bounds from absdot
   float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
-  int32_t* topk_idx;
-  float* gates;
+  int32_t* topk_idx;  // [T][k + n_shared]
+  float* gates;       // [T][k + n_shared]
   int* err;
   int fuse_bucket;    // one token: the top-k kernel also buckets the pairs (with `bucket`)
   BucketArgs bucket;

@@ -10,6 +10,13 @@
 // recomputed in fp64 (parallel, with its own bound) and, if still undecided,
 // by one thread with a sequential fp64 sum in ascending i, which reproduces
 // l_ref exactly (bf16 x bf16 and fp32 x fp32 products are exact in fp64).
+//
+// The score-correction bias either joins the logits (selection and gates), or
+// steers the selection only: the top-k then ranks fl(l32 + bias) (one more
+// rounding in the bound) and takes the gates from l32 itself.  A layer's
+// shared experts (LazyLoRA README, "The engine": 2 per MoE layer) close every
+// token's row of the routing with gate 1, so that the bucketing, the expert
+// FFN and the combine treat them as ordinary pairs.
 #include <utility>
 
 #include "bucket_body.cuh"
@@ -484,7 +491,8 @@ __device__ double logit_fp64_sequential(const RouteArgs& a, int t, int e) {
       for (int j = 0; j < 8; ++j) s = fma(w[u][j], x[u][j], s);
     }
   }
-  if (a.bias) s += (double)a.bias[e];
+  const float* kb = a.bias ? a.bias : a.sel_bias;  // the selection key's bias (at most one is set)
+  if (kb) s += (double)kb[e];
   return s;
 }
 
@@ -524,7 +532,8 @@ __device__ void logit_fp64_warp(const RouteArgs& a, int t, int e, double* val, d
     s += __shfl_xor_sync(0xffffffffu, s, o);
     sa += __shfl_xor_sync(0xffffffffu, sa, o);
   }
-  if (a.bias) s += (double)a.bias[e];
+  const float* kb = a.bias ? a.bias : a.sel_bias;
+  if (kb) s += (double)kb[e];
   *val = s;
   *abs_sum = sa;
 }
@@ -667,13 +676,23 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
       }
       __syncwarp();
     }
-    const float g = lane < k ? expf((float)(oval[lane] - oval[0])) : 0.f;
+    // gate logits: the keys, or (selection-only bias) the router's fp32 logits
+    // without the bias, as on the certified path (a key that was not
+    // recomputed is an fp32 sum rounded once more by the bias addition); the
+    // largest of them is subtracted before exp
+    double lj = -INFINITY;
+    if (lane < k) lj = a.sel_bias ? (double)a.logits[(size_t)t * E + order[lane]] : oval[lane];
+    double lm = lj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lm = fmax(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+    const float g = lane < k ? expf((float)(lj - lm)) : 0.f;
     float den = g;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     if (lane < k) {
-      a.topk_idx[(size_t)t * k + lane] = order[lane];
-      a.gates[(size_t)t * k + lane] = g / den;
+      const size_t r = (size_t)t * (k + a.n_shared) + lane;
+      a.topk_idx[r] = order[lane];
+      a.gates[r] = g / den;
       out_sel[lane] = order[lane];
     }
   }
@@ -682,7 +701,8 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
 // One CTA per token (the body of the top-k kernel): a radix select finds the (k+1)-th largest fp32 logit,
 // the k+1 experts at or above it are ordered by counting, and the bounds then
 // certify the selection or send the CTA down the recheck path.
-// The selection also lands in out_sel[0 .. k-1] (shared memory of the CTA).
+// The selection also lands in out_sel[0 .. k-1] (shared memory of the CTA),
+// the shared experts in out_sel[k .. k + n_shared - 1].
 __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   extern __shared__ double tsm[];
   const int E = a.E, k = a.k;
@@ -712,13 +732,25 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
     const int e = tid + kTopkThreads * i;
     key[i] = 0u;
     if (e < E) {
+      // v: the router's logit (with the additive bias b, if any); the key adds
+      // the selection-only bias.  The compensated sum is rounded before b is
+      // added, and that rounding is relative to |v - b|, hence |v| + |b|.
       const float v = a.logits[(size_t)t * E + e];
-      sv[e] = v;
-      sb[e] = a.comp ? a.gamma * a.absdot[(size_t)t * E + e] + 2.4e-7f * fabsf(v) + 1e-30f
-                     : a.gamma * a.nrm_w[e] * nx + 1.2e-7f * fabsf(v) + 1e-30f;
+      const float b = a.bias ? a.bias[e] : 0.f;
+      const float kv = a.sel_bias ? v + a.sel_bias[e] : v;
+      sv[e] = kv;
+      sb[e] = (a.comp ? a.gamma * a.absdot[(size_t)t * E + e] + 2.4e-7f * (fabsf(v) + fabsf(b))
+                      : a.gamma * a.nrm_w[e] * nx + 1.2e-7f * fabsf(v)) +
+              (a.sel_bias ? 1.2e-7f * fabsf(kv) : 0.f) + 1e-30f;
       insel[e] = 0;
-      key[i] = ord_bits(v);
+      key[i] = ord_bits(kv);
     }
+  }
+  if (tid < a.n_shared) {  // the shared experts close every token's row with gate 1
+    const int j = k + tid;
+    a.topk_idx[(size_t)t * (k + a.n_shared) + j] = E + tid;
+    a.gates[(size_t)t * (k + a.n_shared) + j] = 1.f;
+    out_sel[j] = E + tid;
   }
   pdl_launch_dependents();
   const int nsel = min(k + 1, E);
@@ -825,14 +857,21 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   __syncthreads();
   if (certified) {
     if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum
-      const float v0 = sv[sel[0]];
-      const float g = lane < k ? expf(sv[sel[lane]] - v0) : 0.f;
+      // gate logits: the keys, or (selection-only bias) the router's logits
+      // without the bias; the largest of them is subtracted before exp
+      float lj = -INFINITY;
+      if (lane < k) lj = a.sel_bias ? a.logits[(size_t)t * E + sel[lane]] : sv[sel[lane]];
+      float lm = lj;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+      const float g = lane < k ? expf(lj - lm) : 0.f;
       float den = g;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
       if (lane < k) {
-        a.topk_idx[(size_t)t * k + lane] = sel[lane];
-        a.gates[(size_t)t * k + lane] = g / den;
+        const size_t r = (size_t)t * (k + a.n_shared) + lane;
+        a.topk_idx[r] = sel[lane];
+        a.gates[r] = g / den;
         out_sel[lane] = sel[lane];
       }
     }

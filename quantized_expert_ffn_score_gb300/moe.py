@@ -19,6 +19,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 MOE_F32, MOE_BF16 = 0, 1
 ACT = {"swiglu": 0, "situ": 1}
 QUANT = {"mxfp4": 0, "rvq3": 1}
+BIAS_MODE = {"logit": 0, "select": 1}
 MXFP4_KERNEL = {"block_scaled": 0, "gemv_gemm": 1, "auto": 2}
 
 # every symbol include/moe.h declares
@@ -28,6 +29,7 @@ EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy",
            "moe_ctx_profile", "moe_ctx_profile_read", "moe_ctx_stats",
            "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
+           "moe_route_topk_ex",
            "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
            "moe_stack_forward", "moe_expert_ffn_mxfp4_static", "moe_expert_ffn_mxfp4_static_max_bytes"]
 
@@ -53,7 +55,7 @@ class LayerStruct(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("ff", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
                 ("act", ctypes.c_int), ("quant", ctypes.c_int), ("router_w", ctypes.c_void_p),
                 ("router_w_dtype", ctypes.c_int), ("router_bias", ctypes.c_void_p), ("mxfp4", MxExperts),
-                ("rvq3", RvqExperts)]
+                ("rvq3", RvqExperts), ("n_shared", ctypes.c_int), ("bias_mode", ctypes.c_int)]
 
 
 _lib = None
@@ -90,6 +92,7 @@ def lib():
         L.moe_stack_forward_ws_bytes.argtypes = [ctypes.POINTER(LayerStruct), i32, i32]
         L.moe_stack_forward_ws_bytes.restype = sz
         L.moe_route_topk.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+        L.moe_route_topk_ex.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         L.moe_bucket_tokens.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
         L.moe_expert_ffn_mxfp4.argtypes = [vp, vp, i32, i32, i32, ctypes.POINTER(MxExperts), i32, vp, vp, vp, vp, sz,
                                            vp]
@@ -103,7 +106,8 @@ def lib():
         L.moe_layer_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), vp, i32, i32, vp, i32, vp, vp, vp, vp, sz,
                                         vp]
         L.moe_stack_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), i32, vp, i32, i32, vp, i32, vp, sz, vp]
-        for f in ("moe_ctx_create", "moe_ctx_check", "moe_route_topk", "moe_bucket_tokens", "moe_expert_ffn_mxfp4",
+        for f in ("moe_ctx_create", "moe_ctx_check", "moe_route_topk", "moe_route_topk_ex", "moe_bucket_tokens",
+                  "moe_expert_ffn_mxfp4",
                   "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward", "moe_stack_forward"):
             getattr(L, f).restype = i32
         L.moe_ctx_num_sms.restype = i32
@@ -253,11 +257,13 @@ def workspace(nbytes, device=None):
 # ----------------------------------------------------------------------------- experts / layer
 
 class Layer:
-    """A moe_layer: keeps the tensors it points at alive."""
+    """A moe_layer: keeps the tensors it points at alive.  records: device
+    array of E + n_shared record pointers (the shared experts last)."""
 
     def __init__(self, d, ff, E, k, router_w, records, quant="mxfp4", act="swiglu", router_bias=None,
-                 codebooks=None, keep=()):
+                 codebooks=None, keep=(), n_shared=0, bias_mode="logit"):
         self.d, self.ff, self.E, self.k = d, ff, E, k
+        self.n_shared, self.bias_mode = n_shared, bias_mode
         self.quant, self.act = quant, act
         self.router_w, self.router_bias, self.records, self.codebooks = router_w, router_bias, records, codebooks
         self._keep = list(keep)
@@ -267,17 +273,19 @@ class Layer:
         s.router_w = _ptr(router_w)
         s.router_w_dtype = _dt(router_w)
         s.router_bias = _ptr(router_bias)
-        s.mxfp4 = MxExperts(_ptr(records), d, ff, E)
+        s.mxfp4 = MxExperts(_ptr(records), d, ff, E + n_shared)
         cbs = (ctypes.c_void_p * 3)(*([_ptr(c) for c in codebooks] if codebooks is not None else [None] * 3))
-        s.rvq3 = RvqExperts(_ptr(records), cbs, d, ff, E)
+        s.rvq3 = RvqExperts(_ptr(records), cbs, d, ff, E + n_shared)
+        s.n_shared = n_shared
+        s.bias_mode = BIAS_MODE[bias_mode]
         self.struct = s
 
     def mx_experts(self):
-        return MxExperts(_ptr(self.records), self.d, self.ff, self.E)
+        return MxExperts(_ptr(self.records), self.d, self.ff, self.E + self.n_shared)
 
     def rvq_experts(self):
         cbs = (ctypes.c_void_p * 3)(*[_ptr(c) for c in self.codebooks])
-        return RvqExperts(_ptr(self.records), cbs, self.d, self.ff, self.E)
+        return RvqExperts(_ptr(self.records), cbs, self.d, self.ff, self.E + self.n_shared)
 
 
 # ----------------------------------------------------------------------------- the steps
@@ -288,6 +296,14 @@ def moe_route_topk(ctx, x, router_w, bias, k, topk_idx, gates, ws, stream=None):
     _check(lib().moe_route_topk(ctx.handle, _ptr(x), _dt(x), _ptr(router_w), _dt(router_w), _ptr(bias), T, d, E, k,
                                 _ptr(topk_idx), _ptr(gates), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_route_topk")
+
+
+def moe_route_topk_ex(ctx, x, router_w, bias, bias_mode, k, topk_idx, gates, ws, stream=None):
+    T, d = x.shape
+    E = router_w.shape[0]
+    _check(lib().moe_route_topk_ex(ctx.handle, _ptr(x), _dt(x), _ptr(router_w), _dt(router_w), _ptr(bias),
+                                   BIAS_MODE[bias_mode], T, d, E, k, _ptr(topk_idx), _ptr(gates), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "moe_route_topk_ex")
 
 
 def moe_bucket_tokens(ctx, topk_idx, E, counts, offsets, pair_ids, ws, stream=None):

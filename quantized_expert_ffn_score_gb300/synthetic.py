@@ -21,8 +21,9 @@ def record_stride(r):
 
 
 def device_layer(r, device="cuda", missing=()):
-    """Builds layer recipe `r` on the device; experts listed in `missing` get a
-    NULL record pointer."""
+    """Builds layer recipe `r` on the device (E routed records, then the
+    n_shared shared ones); experts listed in `missing` get a NULL record
+    pointer."""
     stream = torch.cuda.current_stream().cuda_stream
     W = torch.empty((r.E, r.d), dtype=_DT[r.w_dtype], device=device)
     si.dev_layer_router_w(r, W.data_ptr(), cuda_stream=stream)
@@ -31,9 +32,10 @@ def device_layer(r, device="cuda", missing=()):
     if b is not None:
         bias = torch.from_numpy(b).to(device)
     stride = record_stride(r)
-    bank = torch.empty(stride * r.E, dtype=torch.uint8, device=device)
-    si.dev_record_bank(r, bank.data_ptr(), stride, cuda_stream=stream)
-    ptrs = np.array([bank.data_ptr() + e * stride for e in range(r.E)], dtype=np.int64)
+    n_rec = r.E + r.n_shared
+    bank = torch.empty(stride * n_rec, dtype=torch.uint8, device=device)
+    si.dev_record_bank(r, bank.data_ptr(), stride, n_exp=n_rec, cuda_stream=stream)
+    ptrs = np.array([bank.data_ptr() + e * stride for e in range(n_rec)], dtype=np.int64)
     for e in missing:
         ptrs[e] = 0
     records = torch.from_numpy(ptrs).to(device)
@@ -44,7 +46,7 @@ def device_layer(r, device="cuda", missing=()):
         si.dev_layer_codebooks(r, cb.data_ptr(), cuda_stream=stream)
         cbs = (cb, cb, cb)
     layer = moe.Layer(r.d, r.ff, r.E, r.k, W, records, quant=r.quant, act=r.act, router_bias=bias, codebooks=cbs,
-                      keep=keep)
+                      keep=keep, n_shared=r.n_shared, bias_mode=r.bias_mode)
     layer.bank = bank
     layer.stride = stride
     layer.recipe = r

@@ -42,6 +42,8 @@ class LayerRecipe:
     bias: str = "none"  # "none" | "zipf"
     zipf_s: float = 1.0
     act: str = "swiglu"  # "swiglu" | "situ"
+    n_shared: int = 0  # shared experts: records E .. E + n_shared - 1, every token, weight 1
+    bias_mode: str = "logit"  # "logit": the bias enters selection and gates | "select": selection only
 
     @property
     def w_sigma(self):
@@ -67,6 +69,13 @@ WORKLOADS = {
     # K3 layer with RVQ3 experts, decode batch 1 and batch 8
     "k3_rvq3_decode_b1": LayerRecipe("k3_rvq3_decode_b1", T=1, seed=2, quant="rvq3", **K3),
     "k3_rvq3_decode_b8": LayerRecipe("k3_rvq3_decode_b8", T=8, seed=2, quant="rvq3", **K3),
+    # the K3 MoE block with its 2 shared experts beside the 896 routed ones and
+    # the score-correction bias (here the Zipf prior) steering the selection
+    # only; decode batch 1 (18 records per token), and a small parity case
+    "k3_mxfp4_decode_shared2": LayerRecipe("k3_mxfp4_decode_shared2", T=1, seed=4, bias="zipf", bias_mode="select",
+                                           n_shared=2, **K3),
+    "k3_mxfp4_prefill_shared2_e64": LayerRecipe("k3_mxfp4_prefill_shared2_e64", T=40, seed=4, bias="zipf",
+                                                bias_mode="select", n_shared=2, **dict(K3, E=64)),
     # K3 prefill, 512 tokens: Zipf-skewed routing and the uniform control
     "k3_mxfp4_prefill_zipf": LayerRecipe("k3_mxfp4_prefill_zipf", T=512, seed=3, bias="zipf", **K3),
     "k3_mxfp4_prefill_uniform": LayerRecipe("k3_mxfp4_prefill_uniform", T=512, seed=3, **K3),

@@ -41,7 +41,7 @@ def oracle_layer(r, x_host, tokens=None, nthreads=NTHREADS, records=None):
     all) get expert outputs, and only their experts' records are generated."""
     W = si.layer_router_w(r)
     b = si.layer_bias(r)
-    logits, idx, g = oracle.router(x_host, W, b, r.k)
+    logits, idx, g = oracle.router(x_host, W, b, r.k, bias_mode=r.bias_mode)
     T = x_host.shape[0]
     mask = None
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
@@ -49,14 +49,15 @@ def oracle_layer(r, x_host, tokens=None, nthreads=NTHREADS, records=None):
         mask = np.zeros(T, dtype=np.uint8)
         mask[sel] = 1
     if records is None:
-        needed = set(int(e) for e in idx[sel].reshape(-1))
-        records = [si.layer_record(r, e) if e in needed else None for e in range(r.E)]
+        needed = set(int(e) for e in idx[sel].reshape(-1)) | set(range(r.E, r.E + r.n_shared))
+        records = [si.layer_record(r, e) if e in needed else None for e in range(r.E + r.n_shared)]
     cbs = None
     if r.quant == "rvq3":
         cb = si.layer_codebooks(r)
         cbs = (cb, cb, cb)
     idx2, g2, y, out = oracle.layer_forward(x_host, W, b, r.d, r.ff, r.E, r.k, records, quant=r.quant, act_kind=r.act,
-                                            codebooks=cbs, token_mask=mask, nthreads=nthreads)
+                                            codebooks=cbs, token_mask=mask, nthreads=nthreads, n_shared=r.n_shared,
+                                            bias_mode=r.bias_mode)
     assert np.array_equal(idx2, idx)
     return logits, idx, g, y, out
 
@@ -64,7 +65,8 @@ def oracle_layer(r, x_host, tokens=None, nthreads=NTHREADS, records=None):
 def gate_tolerance(r, x_host, logits_ref):
     """Bound on |g_gpu - g_ref| / g_ref from the fp32 logit error bound used by
     the router (gamma * ||W_e|| * ||x_t|| + 2^-23 |l|), applied to the logit
-    differences inside the softmax, plus fp32 rounding of the gates."""
+    differences inside the softmax, plus fp32 rounding of the gates.  With a
+    bias, |l| is bounded by |key| + |bias| (logits_ref are the selection keys)."""
     W = x_host_f64(si.layer_router_w(r))
     xs = x_host_f64(x_host)
     nw = np.sqrt((W ** 2).sum(axis=1))
@@ -73,7 +75,9 @@ def gate_tolerance(r, x_host, logits_ref):
     h = -(-r.d // (32 * N)) + (3 if N == 8 else 2) + 5 + (0 if (r.x_dtype == "bf16" and r.w_dtype == "bf16") else 1)
     u = 2.0 ** -24
     gamma = h * u / (1 - h * u) * 1.002 + 1e-12
-    beta = gamma * nx[:, None] * nw[None, :] + 1.2e-7 * np.abs(logits_ref)
+    b = si.layer_bias(r)
+    babs = 0.0 if b is None else np.abs(b.astype(np.float64))[None, :]
+    beta = gamma * nx[:, None] * nw[None, :] + 1.2e-7 * (np.abs(logits_ref) + babs)
     return 2 * beta.max(axis=1) * 2 + 1e-6  # per token, relative
 
 
@@ -88,10 +92,11 @@ def run_layer(moe, ctx, layer, x, out_dtype=None):
     out_dtype = torch.float32 if out_dtype is None else out_dtype
     T = x.shape[0]
     r = layer.recipe
+    ks = r.k + r.n_shared  # the routed slots, then the shared experts
     out = torch.empty((T, r.d), dtype=out_dtype, device="cuda")
-    topk = torch.full((T, r.k), -1, dtype=torch.int32, device="cuda")
-    gates = torch.empty((T, r.k), dtype=torch.float32, device="cuda")
-    counts = torch.empty(r.E, dtype=torch.int32, device="cuda")
+    topk = torch.full((T, ks), -1, dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, ks), dtype=torch.float32, device="cuda")
+    counts = torch.empty(r.E + r.n_shared, dtype=torch.int32, device="cuda")
     ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T))
     moe.moe_layer_forward(ctx, layer, x, out, ws, topk_idx_out=topk, gates_out=gates, counts_out=counts)
     ctx.check()
@@ -105,8 +110,12 @@ def full_check(moe, ctx, r, tokens=None):
     out, topk, gates, counts = run_layer(moe, ctx, layer, x)
     xh = si.layer_x(r)
     logits, idx, g, y, o = oracle_layer(r, xh, tokens=tokens)
-    check_routing(topk, gates, idx, g, gate_tolerance(r, xh, logits))
-    np.testing.assert_array_equal(counts, np.bincount(idx.reshape(-1), minlength=r.E))
+    check_routing(topk[:, :r.k], gates[:, :r.k], idx, g, gate_tolerance(r, xh, logits))
+    # shared experts close every row with gate 1
+    np.testing.assert_array_equal(topk[:, r.k:], np.broadcast_to(np.arange(r.E, r.E + r.n_shared), (r.T, r.n_shared)))
+    assert np.all(gates[:, r.k:] == 1.0)
+    np.testing.assert_array_equal(counts, np.bincount(topk.reshape(-1), minlength=r.E + r.n_shared))
+    np.testing.assert_array_equal(counts[:r.E], np.bincount(idx.reshape(-1), minlength=r.E))
     sel = np.arange(r.T) if tokens is None else np.asarray(tokens)
     delta = out[sel].astype(np.float64) - x_host_f64(xh)[sel]
     rel = assert_rms_close(delta, y[sel], what=r.name)

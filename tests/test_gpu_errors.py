@@ -71,6 +71,48 @@ def test_missing_routed_expert_is_reported(moe, ctx):
     ctx.check()
 
 
+def test_missing_shared_expert_is_reported(moe, ctx):
+    from quantized_expert_ffn_score_gb300 import synthetic
+    r = si.get_workload("tiny").with_(n_shared=2)
+    x = synthetic.device_x(r)
+    out = torch.empty((r.T, r.d), device="cuda")
+    broken = synthetic.device_layer(r, missing=[r.E + 1])
+    ws = moe.workspace(moe.layer_forward_ws_bytes(broken, r.T))
+    moe.moe_layer_forward(ctx, broken, x, out, ws)
+    with pytest.raises(moe.MoeError) as ei:
+        ctx.check()
+    assert ei.value.name == "MOE_ERR_MISSING_EXPERT" and ei.value.detail == r.E + 1
+    ctx.check()
+
+
+def test_layer_shared_expert_and_bias_mode_validation(moe, ctx):
+    from quantized_expert_ffn_score_gb300 import synthetic
+    r = si.get_workload("tiny").with_(n_shared=2)
+    layer = synthetic.device_layer(r)
+    x = synthetic.device_x(r)
+    out = torch.empty((r.T, r.d), device="cuda")
+    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, r.T))
+    s = layer.struct
+    s.bias_mode = 7
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_forward(ctx, layer, x, out, ws)
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"
+    s.bias_mode = 1
+    s.mxfp4.E = r.E  # the bank must hold the routed and the shared records
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_forward(ctx, layer, x, out, ws)
+    assert ei.value.name == "MOE_ERR_INVALID_ARG"
+    s.mxfp4.E = r.E + r.n_shared
+    s.n_shared = 32 - r.k + 1  # k + n_shared above 32
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_forward(ctx, layer, x, out, ws)
+    assert ei.value.name == "MOE_ERR_UNSUPPORTED"
+    s.n_shared = r.n_shared
+    s.bias_mode = 0
+    moe.moe_layer_forward(ctx, layer, x, out, ws)
+    ctx.check()
+
+
 def test_bad_expert_index_in_routing_is_reported(moe, ctx):
     T, k, E = 4, 2, 8
     topk = torch.tensor([[0, 1], [2, 3], [4, E + 3], [6, 7]], dtype=torch.int32, device="cuda")

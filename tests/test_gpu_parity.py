@@ -64,6 +64,43 @@ def test_mid_rvq3_situ(lib, ctx):
     gu.full_check(lib, ctx, MID_RVQ.with_(act="situ", seed=16, T=3))
 
 
+# Two shared experts after the routed ones and the score-correction bias
+# steering the selection only (the K3 MoE block's routing).
+SHARED_MX = MID_MX.with_(n_shared=2, bias="zipf", bias_mode="select", seed=21)
+
+
+@pytest.mark.parametrize("T", [1, 5, 37])
+def test_mid_mxfp4_shared_experts_select_bias(lib, ctx, T):
+    # one token: the top-k kernel buckets the 6 + 2 pairs itself and the GEMV
+    # runs them; 5 tokens: compensated router, block-scaled experts; 37 tokens:
+    # tiled router, shared experts with 37 tokens each
+    gu.full_check(lib, ctx, SHARED_MX.with_(T=T))
+
+
+def test_mid_mxfp4_shared_expert_additive_bias_fp32(lib, ctx):
+    # fp32 x and router: the FMA GEMV and the fp32 router kernels
+    gu.full_check(lib, ctx, MID_MX.with_(n_shared=1, bias="zipf", x_dtype="f32", w_dtype="f32", T=3, seed=22))
+
+
+def test_mid_mxfp4_select_bias_without_shared_experts(lib, ctx):
+    gu.full_check(lib, ctx, MID_MX.with_(bias="zipf", bias_mode="select", T=23, seed=24))
+
+
+def test_mid_rvq3_shared_experts(lib, ctx):
+    gu.full_check(lib, ctx, MID_RVQ.with_(n_shared=2, bias="zipf", bias_mode="select", seed=23))
+
+
+@pytest.mark.slow
+def test_k3_mxfp4_decode_shared2(lib, ctx):
+    gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_decode_shared2"))
+
+
+@pytest.mark.slow
+def test_k3_mxfp4_prefill_shared2_e64_sampled(lib, ctx):
+    # 40 tokens: routing and counts of all tokens, outputs of a sample
+    gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_prefill_shared2_e64"), tokens=[0, 7, 19, 39])
+
+
 @pytest.mark.slow
 def test_k3_mxfp4_decode_b1(lib, ctx):
     gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_decode"))
@@ -134,6 +171,59 @@ def test_route_topk_radix_and_warp_select_paths(lib, ctx, E, k, T):
     logits, idx, g = oracle.router(xh, Wh, None, k)
     # logits are O(1) here, so the fp32 logit and gate roundings move a gate by
     # a few 1e-7 relative; 2e-5 leaves ample room
+    gu.check_routing(topk.cpu().numpy(), gates.cpu().numpy(), idx, g, np.full(T, 2e-5))
+
+
+@pytest.mark.parametrize("T", [8, 512])
+def test_route_topk_ex_select_bias_matches_oracle(lib, ctx, T):
+    # the K3 router with the Zipf bias for the selection only: 8 tokens
+    # (compensated sums) and 512 (tiled); the selection equals the additive
+    # mode's (the keys are the same), the gates come from the unbiased logits
+    moe = lib
+    from quantized_expert_ffn_score_gb300 import synthetic
+    r = si.get_workload("k3_mxfp4_prefill_zipf").with_(T=T, bias_mode="select")
+    W = torch.empty((r.E, r.d), dtype=torch.bfloat16, device="cuda")
+    si.dev_layer_router_w(r, W.data_ptr())
+    b = si.layer_bias(r)
+    bias = torch.from_numpy(b).cuda()
+    x = synthetic.device_x(r)
+    topk = torch.empty((T, r.k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, r.k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.route_topk_ws_bytes(T, r.d, r.E, r.k))
+    moe.moe_route_topk_ex(ctx, x, W, bias, "select", r.k, topk, gates, ws)
+    topk_add = torch.empty_like(topk)
+    gates_add = torch.empty_like(gates)
+    moe.moe_route_topk(ctx, x, W, bias, r.k, topk_add, gates_add, ws)
+    ctx.check()
+    xh = si.layer_x(r)
+    logits, idx, g = oracle.router(xh, si.layer_router_w(r), b, r.k, bias_mode="select")
+    gu.check_routing(topk.cpu().numpy(), gates.cpu().numpy(), idx, g, gu.gate_tolerance(r, xh, logits))
+    np.testing.assert_array_equal(topk_add.cpu().numpy(), idx)
+    assert not np.allclose(gates_add.cpu().numpy(), gates.cpu().numpy(), rtol=1e-3)
+
+
+@pytest.mark.parametrize("T", [3, 20])
+def test_route_topk_ex_forced_selection_gates_ignore_the_bias(lib, ctx, T):
+    # a bias of about 1000 on k chosen experts makes them the selection; their
+    # gates are the softmax of the logits without the bias, which the bias's
+    # own fp32 rounding (about 6e-5 at 1000) must not reach
+    moe = lib
+    E, d, k = 256, 512, 8
+    rng = np.random.default_rng(T)
+    Wb = torch.from_numpy((rng.standard_normal((E, d)) / 16).astype(np.float32)).to(torch.bfloat16)
+    x = torch.from_numpy(rng.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16)
+    chosen = rng.choice(E, size=k, replace=False)
+    b = np.zeros(E, dtype=np.float32)
+    b[chosen] = 1000.0 - 10.0 * np.arange(k, dtype=np.float32)
+    topk = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.route_topk_ws_bytes(T, d, E, k))
+    moe.moe_route_topk_ex(ctx, x.cuda(), Wb.cuda(), torch.from_numpy(b).cuda(), "select", k, topk, gates, ws)
+    ctx.check()
+    xh = x.view(torch.int16).numpy().view(np.uint16)
+    Wh = Wb.view(torch.int16).numpy().view(np.uint16)
+    logits, idx, g = oracle.router(xh, Wh, b, k, bias_mode="select")
+    assert np.all(idx == chosen[None, :])
     gu.check_routing(topk.cpu().numpy(), gates.cpu().numpy(), idx, g, np.full(T, 2e-5))
 
 
