@@ -36,6 +36,7 @@ def lib():
         L.or_mxfp4_record_bytes.argtypes, L.or_mxfp4_record_bytes.restype = [i32, i32], ctypes.c_size_t
         L.or_rvq3_record_bytes.argtypes, L.or_rvq3_record_bytes.restype = [i32, i32], ctypes.c_size_t
         L.or_router.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]
+        L.or_crc32.argtypes, L.or_crc32.restype = [vp, ctypes.c_size_t], ctypes.c_uint32
         L.or_router_mode.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         L.or_topk_gates.argtypes = [vp, i32, i32, i32, vp, vp]
         L.or_bucket.argtypes = [vp, i32, i32, i32, vp, vp, vp]
@@ -118,6 +119,13 @@ def mxfp4_record_bytes(d, ff):
 
 def rvq3_record_bytes(d, ff):
     return int(lib().or_rvq3_record_bytes(d, ff))
+
+
+def crc32(data):
+    """CRC-32 (IEEE, as zlib) of a byte string or uint8 array."""
+    a = np.frombuffer(bytes(data), dtype=np.uint8) if isinstance(data, (bytes, bytearray)) else \
+        np.ascontiguousarray(data, dtype=np.uint8).reshape(-1)
+    return int(lib().or_crc32(_p(a) if a.size else None, a.size))
 
 
 BIAS_MODE = {"logit": 0, "select": 1}

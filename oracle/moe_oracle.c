@@ -87,6 +87,28 @@ size_t or_mxfp4_record_bytes(int d, int ff) {
 size_t or_rvq3_record_bytes(int d, int ff) { return 9 * (size_t)ff * d / 8; }
 
 /* ------------------------------------------------------------------------ */
+/* Record checksum                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* CRC-32 of the IEEE 802.3 / zlib kind: the bytes enter least significant bit
+ * first into a 32-bit register that starts as all ones; each bit shifts the
+ * register right and, when the bit shifted out differs from the input bit,
+ * xors in the reflected generator 0xEDB88320; the result is the register
+ * complemented.  One bit at a time, exactly as defined. */
+uint32_t or_crc32(const uint8_t* p, size_t n) {
+  uint32_t reg = 0xFFFFFFFFu;
+  for (size_t i = 0; i < n; ++i) {
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t in = (p[i] >> b) & 1u;
+      const uint32_t out = reg & 1u;
+      reg >>= 1;
+      if (in != out) reg ^= 0xEDB88320u;
+    }
+  }
+  return reg ^ 0xFFFFFFFFu;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Router                                                                    */
 /* ------------------------------------------------------------------------ */
 

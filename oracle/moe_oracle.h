@@ -56,6 +56,13 @@ void or_rvq3_row(const uint8_t* codes, const uint16_t* cb, int rows, int K, int 
 size_t or_mxfp4_record_bytes(int d, int ff);
 size_t or_rvq3_record_bytes(int d, int ff);
 
+/* ---- record checksum ------------------------------------------------------
+ * CRC-32 (IEEE 802.3 generator, reflected, initial value and final xor all
+ * ones: the zlib/PNG/Ethernet checksum) of n bytes.  WASTE README, "How it
+ * works": every expert record carries a CRC32 of its payload, checked when
+ * asked to verify. */
+uint32_t or_crc32(const uint8_t* p, size_t n);
+
 /* ---- router --------------------------------------------------------------
  * l[t][e] = sum_i W[e][i] x[t][i] (ascending i) + bias[e];
  * top-k by (l descending, e ascending); g_j = exp(l_j - l_max) / sum_sel exp(.)

@@ -39,6 +39,10 @@ MUTANTS = [
     ("shared experts dropped", "0, E + n_shared, nthreads, yp);", "0, E, nthreads, yp);"),
     ("shared expert reads a routed record", ": E + (j - k);", ": (j - k);"),
     ("shared expert weighted like a routed one", ": 1.0;", ": g[(size_t)t * k];"),
+    ("CRC generator not reflected", "reg ^= 0xEDB88320u;", "reg ^= 0x04C11DB7u;"),
+    ("CRC register starts at zero", "uint32_t reg = 0xFFFFFFFFu;", "uint32_t reg = 0u;"),
+    ("CRC result not complemented", "return reg ^ 0xFFFFFFFFu;", "return reg;"),
+    ("CRC bits most significant first", "(p[i] >> b) & 1u", "(p[i] >> (7 - b)) & 1u"),
 ]
 
 

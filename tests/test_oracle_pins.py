@@ -104,6 +104,34 @@ def test_record_sizes_match_page_figures():
     assert si.mxfp4_record_size(d, ff) == b and si.rvq3_record_size(d, ff) == rv
 
 
+# ----------------------------------------------------------------------------- record checksum
+
+def test_crc32_published_check_value_and_empty_input():
+    # the catalogue check value of CRC-32/ISO-HDLC (the zlib/PNG CRC) over "123456789"
+    assert oracle.crc32(b"123456789") == 0xCBF43926
+    assert oracle.crc32(b"") == 0
+    assert oracle.crc32(b"\x00") == 0xD202EF8D
+
+
+def test_crc32_matches_zlib_on_random_buffers():
+    import zlib
+    rng = np.random.default_rng(7)
+    for n in (1, 3, 16, 63, 64, 65, 1000, 4096, 52224):
+        buf = rng.integers(0, 256, n, dtype=np.uint8)
+        assert oracle.crc32(buf) == zlib.crc32(buf.tobytes()), n
+
+
+def test_crc32_of_a_record_changes_with_any_single_bit():
+    r = si.LayerRecipe("c", d=64, ff=64, E=2, k=1, T=1, x_dtype="f32", w_dtype="f32", seed=3)
+    rec = si.layer_record(r, 1)
+    c0 = oracle.crc32(rec)
+    rng = np.random.default_rng(1)
+    for pos in rng.integers(0, rec.size, 8):
+        bad = rec.copy()
+        bad[pos] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        assert oracle.crc32(bad) != c0
+
+
 # ----------------------------------------------------------------------------- router
 
 def _tiny_xw(T=12, d=64, E=24, seed=5, dt="bf16"):
