@@ -78,7 +78,8 @@ typedef enum {
   MOE_ERR_CUDA = 4,             /* a CUDA runtime call failed               */
   MOE_ERR_BAD_EXPERT_INDEX = 5, /* routing named an expert outside [0, E)   */
   MOE_ERR_MISSING_EXPERT = 6,   /* a routed expert's record pointer is NULL */
-  MOE_ERR_TIMEOUT = 7           /* a bounded device-side wait gave up       */
+  MOE_ERR_TIMEOUT = 7,          /* a bounded device-side wait gave up       */
+  MOE_ERR_BAD_RECORD = 8        /* a record failed its check (moe_records_check) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -351,6 +352,27 @@ MOE_API moe_status moe_layer_forward(moe_ctx* ctx, const moe_layer* L, const voi
  */
 MOE_API moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers, const void* x, moe_dtype x_dtype,
                              int T, void* out, moe_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Record check (WASTE README, "How it works": every expert record carries a
+ * CRC32 of its payload, verified on request, so that a truncated or spliced
+ * bank names the bad record instead of answering from wrong bytes).
+ * records: device array [n] of device pointers to records of record_bytes
+ * bytes each (a multiple of 16; every record 16-byte aligned).  Computes the
+ * CRC-32 of each record (IEEE 802.3 generator, reflected, initial value and
+ * final xor all ones: the value zlib's crc32 gives) into crc_out [n] (device,
+ * nullable) and, when expected [n] (device) is given, compares.  A NULL record
+ * sets MOE_ERR_MISSING_EXPERT, a misaligned one or a mismatch
+ * MOE_ERR_BAD_RECORD on the context's error word (detail: the record's
+ * index; with several bad records, one of them); moe_ctx_check reports it.
+ * crc_out of a NULL or misaligned record is 0.  Reads every byte once (an
+ * HBM-bound pass, meant for load time: a 15.7 GB bank of 896 K3 experts).
+ * ws: moe_records_check_ws_bytes(n, record_bytes) bytes.  n = 0 is a no-op.
+ */
+MOE_API size_t moe_records_check_ws_bytes(int n, size_t record_bytes);
+MOE_API moe_status moe_records_check(moe_ctx* ctx, const uint8_t* const* records, int n, size_t record_bytes,
+                                     const uint32_t* expected, uint32_t* crc_out, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
 
 #ifdef __cplusplus
 }

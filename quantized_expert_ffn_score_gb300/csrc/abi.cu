@@ -445,6 +445,7 @@ const char* moe_status_str(moe_status s) {
     case MOE_ERR_BAD_EXPERT_INDEX: return "routing named an expert outside [0, E)";
     case MOE_ERR_MISSING_EXPERT: return "a routed expert's record is missing";
     case MOE_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case MOE_ERR_BAD_RECORD: return "a record failed its check (checksum mismatch or misaligned)";
   }
   return "unknown status";
 }
@@ -659,6 +660,25 @@ moe_status moe_route_topk_ex(moe_ctx* ctx, const void* x, moe_dtype x_dtype, con
   moe::RouteArgs ra = route_args(x, x_dtype, router_w, w_dtype, bias, bias_mode, T, d, E, k, 0, w, topk_idx, gates,
                                  ctx->err);
   return cuda_status(moe::launch_route_topk(ra, ctx->num_sms, stream));
+}
+
+size_t moe_records_check_ws_bytes(int n, size_t record_bytes) {
+  if (n < 0 || record_bytes == 0 || record_bytes % 16) return 0;
+  return align_up((size_t)(n > 0 ? n : 1) * moe::records_crc_segments(record_bytes) * sizeof(uint32_t));
+}
+
+moe_status moe_records_check(moe_ctx* ctx, const uint8_t* const* records, int n, size_t record_bytes,
+                             const uint32_t* expected, uint32_t* crc_out, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  ProfScope prof_scope(ctx);
+  if (n < 0 || record_bytes == 0 || record_bytes % 16) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (records == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(ws, ws_bytes, moe_records_check_ws_bytes(n, record_bytes))) != MOE_OK) return st;
+  return cuda_status(moe::launch_records_check(records, n, record_bytes, expected, crc_out,
+                                               static_cast<uint32_t*>(ws), ctx->err, ctx->num_sms, stream));
 }
 
 moe_status moe_bucket_tokens(moe_ctx* ctx, const int32_t* topk_idx, int T, int k, int E, int32_t* counts,

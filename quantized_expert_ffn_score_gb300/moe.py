@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
-          4: "MOE_ERR_CUDA", 5: "MOE_ERR_BAD_EXPERT_INDEX", 6: "MOE_ERR_MISSING_EXPERT", 7: "MOE_ERR_TIMEOUT"}
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_BAD_EXPERT_INDEX", 6: "MOE_ERR_MISSING_EXPERT", 7: "MOE_ERR_TIMEOUT",
+          8: "MOE_ERR_BAD_RECORD"}
 MOE_F32, MOE_BF16 = 0, 1
 ACT = {"swiglu": 0, "situ": 1}
 QUANT = {"mxfp4": 0, "rvq3": 1}
@@ -31,7 +32,8 @@ EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
            "moe_route_topk_ex",
            "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
-           "moe_stack_forward", "moe_expert_ffn_mxfp4_static", "moe_expert_ffn_mxfp4_static_max_bytes"]
+           "moe_stack_forward", "moe_expert_ffn_mxfp4_static", "moe_expert_ffn_mxfp4_static_max_bytes",
+           "moe_records_check_ws_bytes", "moe_records_check"]
 
 
 class MoeError(RuntimeError):
@@ -103,6 +105,8 @@ def lib():
                                                   vp]
         L.moe_expert_ffn_mxfp4_static.restype = i32
         L.moe_expert_ffn_mxfp4_static_max_bytes.restype = sz
+        L.moe_records_check_ws_bytes.argtypes, L.moe_records_check_ws_bytes.restype = [i32, sz], sz
+        L.moe_records_check.argtypes, L.moe_records_check.restype = [vp, vp, i32, sz, vp, vp, vp, sz, vp], i32
         L.moe_layer_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), vp, i32, i32, vp, i32, vp, vp, vp, vp, sz,
                                         vp]
         L.moe_stack_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), i32, vp, i32, i32, vp, i32, vp, sz, vp]
@@ -353,6 +357,18 @@ def moe_layer_forward(ctx, layer, x, out, ws, topk_idx_out=None, gates_out=None,
     _check(lib().moe_layer_forward(ctx.handle, ctypes.byref(layer.struct), _ptr(x), _dt(x), T, _ptr(out), _dt(out),
                                    _ptr(topk_idx_out), _ptr(gates_out), _ptr(counts_out), _ptr(ws), ws.numel(),
                                    _stream(stream)), "moe_layer_forward")
+
+
+def records_check_ws_bytes(n, record_bytes):
+    return int(lib().moe_records_check_ws_bytes(n, record_bytes))
+
+
+def moe_records_check(ctx, records, n, record_bytes, ws, expected=None, crc_out=None, stream=None):
+    """CRC-32 of n device records (records: device int64 tensor of pointers)
+    into crc_out (device int32/uint32 [n]); compared with expected when given
+    (a mismatch surfaces at ctx.check())."""
+    _check(lib().moe_records_check(ctx.handle, _ptr(records), n, record_bytes, _ptr(expected), _ptr(crc_out),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_records_check")
 
 
 def moe_stack_forward(ctx, layers, x, out, ws, stream=None):

@@ -56,6 +56,10 @@ def test_host_only_queries(built):
     assert moe.expert_ffn_ws_bytes(8, 16, 3584, 3072, 896, "rvq3") > moe.expert_ffn_ws_bytes(8, 16, 3584, 3072, 896)
     assert moe.expert_ffn_ws_bytes(1, 16, 3584, 8192, 896) == 0  # ff above the limit
     assert "sm_103a" in moe.version()
+    # record check: one word per 128 KiB segment of every record
+    assert moe.records_check_ws_bytes(896, 17_547_264) >= 896 * 134 * 4
+    assert moe.records_check_ws_bytes(4, 1000) == 0  # not a multiple of 16
+    assert moe.records_check_ws_bytes(4, 0) == 0
 
 
 def test_null_context_is_rejected_without_touching_a_gpu(built):
@@ -66,3 +70,5 @@ def test_null_context_is_rejected_without_touching_a_gpu(built):
     rc = L.moe_layer_forward(None, None, None, 0, 1, None, 0, None, None, None, None, 0, None)
     assert rc == 1
     assert L.moe_status_str(6) == b"a routed expert's record is missing"
+    assert L.moe_records_check(None, None, 1, 64, None, None, None, 0, None) == 1
+    assert L.moe_route_topk_ex(None, None, 0, None, 0, None, 0, 1, 32, 4, 2, None, None, None, 0, None) == 1
