@@ -367,7 +367,9 @@ MOE_API moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int 
  * index; with several bad records, one of them); moe_ctx_check reports it.
  * crc_out of a NULL or misaligned record is 0.  Reads every byte once (an
  * HBM-bound pass, meant for load time: a 15.7 GB bank of 896 K3 experts).
- * ws: moe_records_check_ws_bytes(n, record_bytes) bytes.  n = 0 is a no-op.
+ * ws: moe_records_check_ws_bytes(n, record_bytes) bytes (one word per 4 KiB
+ * of every record).  n = 0 is a no-op; n times the record's 4 KiB units at or
+ * above 2^31 returns MOE_ERR_UNSUPPORTED.
  */
 MOE_API size_t moe_records_check_ws_bytes(int n, size_t record_bytes);
 MOE_API moe_status moe_records_check(moe_ctx* ctx, const uint8_t* const* records, int n, size_t record_bytes,

@@ -676,6 +676,7 @@ moe_status moe_records_check(moe_ctx* ctx, const uint8_t* const* records, int n,
   if (n < 0 || record_bytes == 0 || record_bytes % 16) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
   if (records == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((long long)n * moe::records_crc_segments(record_bytes) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   if ((st = ws_check(ws, ws_bytes, moe_records_check_ws_bytes(n, record_bytes))) != MOE_OK) return st;
   return cuda_status(moe::launch_records_check(records, n, record_bytes, expected, crc_out,
                                                static_cast<uint32_t*>(ws), ctx->err, ctx->num_sms, stream));

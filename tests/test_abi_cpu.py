@@ -56,8 +56,8 @@ def test_host_only_queries(built):
     assert moe.expert_ffn_ws_bytes(8, 16, 3584, 3072, 896, "rvq3") > moe.expert_ffn_ws_bytes(8, 16, 3584, 3072, 896)
     assert moe.expert_ffn_ws_bytes(1, 16, 3584, 8192, 896) == 0  # ff above the limit
     assert "sm_103a" in moe.version()
-    # record check: one word per 128 KiB segment of every record
-    assert moe.records_check_ws_bytes(896, 17_547_264) >= 896 * 134 * 4
+    # record check: one word per 4 KiB unit of every record
+    assert moe.records_check_ws_bytes(896, 17_547_264) >= 896 * 4284 * 4
     assert moe.records_check_ws_bytes(4, 1000) == 0  # not a multiple of 16
     assert moe.records_check_ws_bytes(4, 0) == 0
 
