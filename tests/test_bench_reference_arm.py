@@ -5,12 +5,16 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_reference_arm_prints_one_contract_line():
+@pytest.mark.parametrize("workload", [None, "k3_mxfp4_decode_shared2"])
+def test_reference_arm_prints_one_contract_line(workload):
+    extra = [] if workload is None else ["--workload", workload]
     proc = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
-                           "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+                           "--warmup", "3"] + extra, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-2000:]
     lines = [ln for ln in proc.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -21,7 +25,7 @@ def test_reference_arm_prints_one_contract_line():
         assert key in d, key
     assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["higher_is_better"] is True
-    assert d["config"]["workload"] == "k3_mxfp4_decode"
+    assert d["config"]["workload"] == (workload or "k3_mxfp4_decode")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
