@@ -62,6 +62,30 @@ def test_host_only_queries(built):
     assert moe.records_check_ws_bytes(4, 0) == 0
 
 
+def test_layer_workspace_covers_shared_experts_and_validates_them(built):
+    # host-only: the layer struct's pointers are never dereferenced by the size query
+    from quantized_expert_ffn_score_gb300 import moe
+    L = moe.lib()
+
+    def ws(n_shared=0, bias_mode=0, bank_E=None, k=16, T=4):
+        s = moe.LayerStruct()
+        s.d, s.ff, s.E, s.k = 3584, 3072, 896, k
+        s.act, s.quant = 0, 0
+        s.router_w, s.router_w_dtype = 0x1000, 1
+        s.mxfp4 = moe.MxExperts(0x2000, 3584, 3072, 896 + n_shared if bank_E is None else bank_E)
+        s.n_shared, s.bias_mode = n_shared, bias_mode
+        return L.moe_layer_forward_ws_bytes(ctypes.byref(s), T)
+
+    base, shared = ws(), ws(n_shared=2)
+    # two more pairs per token: their h (ff floats) and y (d floats), plus the larger expert tables
+    assert shared - base >= 4 * 2 * (3072 + 3584) * 4
+    assert ws(n_shared=2, bias_mode=1) == shared
+    assert ws(bias_mode=2) == 0                  # unknown bias mode
+    assert ws(n_shared=2, bank_E=896) == 0       # the bank must hold the shared records too
+    assert ws(n_shared=17) == 0                  # k + n_shared above 32
+    assert ws(n_shared=-1) == 0
+
+
 def test_null_context_is_rejected_without_touching_a_gpu(built):
     from quantized_expert_ffn_score_gb300 import moe
     L = moe.lib()
