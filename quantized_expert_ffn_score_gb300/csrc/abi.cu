@@ -664,7 +664,7 @@ moe_status moe_route_topk_ex(moe_ctx* ctx, const void* x, moe_dtype x_dtype, con
 
 size_t moe_records_check_ws_bytes(int n, size_t record_bytes) {
   if (n < 0 || record_bytes == 0 || record_bytes % 16) return 0;
-  return align_up((size_t)(n > 0 ? n : 1) * moe::records_crc_segments(record_bytes) * sizeof(uint32_t));
+  return align_up((size_t)(n > 0 ? n : 1) * moe::records_crc_units(record_bytes) * sizeof(uint32_t));
 }
 
 moe_status moe_records_check(moe_ctx* ctx, const uint8_t* const* records, int n, size_t record_bytes,
@@ -676,7 +676,7 @@ moe_status moe_records_check(moe_ctx* ctx, const uint8_t* const* records, int n,
   if (n < 0 || record_bytes == 0 || record_bytes % 16) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
   if (records == nullptr) return MOE_ERR_INVALID_ARG;
-  if ((long long)n * moe::records_crc_segments(record_bytes) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((long long)n * moe::records_crc_units(record_bytes) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   if ((st = ws_check(ws, ws_bytes, moe_records_check_ws_bytes(n, record_bytes))) != MOE_OK) return st;
   return cuda_status(moe::launch_records_check(records, n, record_bytes, expected, crc_out,
                                                static_cast<uint32_t*>(ws), ctx->err, ctx->num_sms, stream));

@@ -260,11 +260,11 @@ struct CombineArgs {
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 
 // CRC-32 of n records of record_bytes (a multiple of 16) each; checks them
-// against expected[] when given (records_check.cu).  seg_ws holds
-// n * records_crc_segments(record_bytes) words.
-int records_crc_segments(size_t record_bytes);
+// against expected[] when given (records_check.cu).  unit_ws holds one word
+// per 4 KiB unit of every record: n * records_crc_units(record_bytes) words.
+int records_crc_units(size_t record_bytes);
 cudaError_t launch_records_check(const uint8_t* const* records, int n, size_t record_bytes, const uint32_t* expected,
-                                 uint32_t* crc_out, uint32_t* seg_ws, int* err, int num_sms, cudaStream_t s);
+                                 uint32_t* crc_out, uint32_t* unit_ws, int* err, int num_sms, cudaStream_t s);
 
 // ABI-layer helpers (abi.cu) shared with other translation units' entry points.
 moe_status check_expert_ffn_call(const moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k, int d, int ff,

@@ -177,17 +177,17 @@ __global__ void crc_finish_kernel(const CrcArgs a) {
 
 }  // namespace
 
-int records_crc_segments(size_t record_bytes) { return (int)((record_bytes + kCrcUnit - 1) / kCrcUnit); }
+int records_crc_units(size_t record_bytes) { return (int)((record_bytes + kCrcUnit - 1) / kCrcUnit); }
 
 cudaError_t launch_records_check(const uint8_t* const* records, int n, size_t record_bytes, const uint32_t* expected,
-                                 uint32_t* crc_out, uint32_t* seg_ws, int* err, int num_sms, cudaStream_t s) {
+                                 uint32_t* crc_out, uint32_t* unit_ws, int* err, int num_sms, cudaStream_t s) {
   CrcArgs a;
   a.records = records;
   a.n = n;
   a.bytes = (long long)record_bytes;
-  a.units = records_crc_segments(record_bytes);
+  a.units = records_crc_units(record_bytes);
   a.pad = (long long)a.units * kCrcUnit - a.bytes;
-  a.unit_crc = seg_ws;
+  a.unit_crc = unit_ws;
   a.expected = expected;
   a.crc_out = crc_out;
   a.err = err;
