@@ -33,6 +33,7 @@ def lib():
         L.or_act.argtypes, L.or_act.restype = [dbl, dbl, i32], dbl
         L.or_mxfp4_row.argtypes = [vp, vp, i32, i32, vp]
         L.or_rvq3_row.argtypes = [vp, vp, i32, i32, i32, vp]
+        L.or_rvq3_row_rowmajor.argtypes = [vp, vp, i32, i32, i32, vp]
         L.or_mxfp4_record_bytes.argtypes, L.or_mxfp4_record_bytes.restype = [i32, i32], ctypes.c_size_t
         L.or_rvq3_record_bytes.argtypes, L.or_rvq3_record_bytes.restype = [i32, i32], ctypes.c_size_t
         L.or_router.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp]
@@ -42,6 +43,7 @@ def lib():
         L.or_bucket.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.or_expert_mxfp4.argtypes = [vp, vp, i32, i32, i32, vp]
         L.or_expert_rvq3.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
+        L.or_expert_rvq3_rowmajor.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
         L.or_combine.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.or_layer_forward.argtypes = [vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                        vp, i32, vp, vp, vp, vp]
@@ -49,7 +51,8 @@ def lib():
                                           vp, vp, vp, i32, vp, vp, vp, vp]
         L.or_partial_delta.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
                                        vp]
-        for f in ("or_router", "or_topk_gates", "or_bucket", "or_expert_mxfp4", "or_expert_rvq3", "or_combine",
+        for f in ("or_router", "or_topk_gates", "or_bucket", "or_expert_mxfp4", "or_expert_rvq3",
+                  "or_expert_rvq3_rowmajor", "or_combine",
                   "or_layer_forward", "or_partial_delta"):
             getattr(L, f).restype = i32
         _lib = L
@@ -111,6 +114,16 @@ def rvq3_row(codes, cb, rows, K, r):
 
 def rvq3_matrix(codes, cb, rows, K):
     return np.stack([rvq3_row(codes, cb, rows, K, r) for r in range(rows)])
+
+
+def rvq3_row_rowmajor(codes, cb, rows, K, r):
+    w = np.empty(K, dtype=np.float64)
+    lib().or_rvq3_row_rowmajor(_p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(cb)), rows, K, r, _p(w))
+    return w
+
+
+def rvq3_matrix_rowmajor(codes, cb, rows, K):
+    return np.stack([rvq3_row_rowmajor(codes, cb, rows, K, r) for r in range(rows)])
 
 
 def mxfp4_record_bytes(d, ff):
@@ -179,6 +192,15 @@ def expert_rvq3(x, rec, cb_gate, cb_up, cb_down, d, ff, act_kind="swiglu"):
     y = np.empty(d, dtype=np.float64)
     _check(lib().or_expert_rvq3(_p(x), _p(np.ascontiguousarray(rec)), _p(cb_gate), _p(cb_up), _p(cb_down), d, ff,
                                 ACT[act_kind], _p(y)), "expert_rvq3")
+    return y
+
+
+def expert_rvq3_rowmajor(x, rec, cb_gate, cb_up, cb_down, d, ff, act_kind="swiglu"):
+    """expert_rvq3 on a record whose code planes are stored row by row."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(d, dtype=np.float64)
+    _check(lib().or_expert_rvq3_rowmajor(_p(x), _p(np.ascontiguousarray(rec)), _p(cb_gate), _p(cb_up), _p(cb_down),
+                                         d, ff, ACT[act_kind], _p(y)), "expert_rvq3_rowmajor")
     return y
 
 

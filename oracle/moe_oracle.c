@@ -80,6 +80,23 @@ void or_rvq3_row(const uint8_t* codes, const uint16_t* cb, int rows, int K, int 
   }
 }
 
+/* The same weights when each stage's codes are stored row by row: plane
+ * [3][rows][K/8], stage s's code for weights r, 8v..8v+7 at
+ * codes[(s * rows + r) * nv + v]. */
+void or_rvq3_row_rowmajor(const uint8_t* codes, const uint16_t* cb, int rows, int K, int r, double* w) {
+  int nv = K / 8;
+  for (int v = 0; v < nv; ++v) {
+    for (int i = 0; i < 8; ++i) {
+      double acc = 0.0;
+      for (int s = 0; s < 3; ++s) {
+        int c = codes[((size_t)s * rows + r) * nv + v];
+        acc += or_f16(cb[((size_t)s * 256 + c) * 8 + i]);
+      }
+      w[8 * v + i] = acc;
+    }
+  }
+}
+
 size_t or_mxfp4_record_bytes(int d, int ff) {
   return 3 * ((size_t)ff * d / 2 + (size_t)ff * d / 32);
 }
@@ -257,13 +274,16 @@ int or_expert_mxfp4(const double* x, const uint8_t* rec, int d, int ff, int act,
   return 0;
 }
 
-int or_expert_rvq3(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
-                   const uint16_t* cb_down, int d, int ff, int act, double* y) {
+/* The RVQ3 expert on a record whose planes are stored position-major
+ * (row_major == 0) or row by row (row_major == 1). */
+static int expert_rvq3_layout(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
+                              const uint16_t* cb_down, int d, int ff, int act, int row_major, double* y) {
   if (!rec) return -2;
   size_t mb = 3 * (size_t)ff * d / 8;
   const uint8_t* g_codes = rec;
   const uint8_t* u_codes = rec + mb;
   const uint8_t* d_codes = rec + 2 * mb;
+  void (*row)(const uint8_t*, const uint16_t*, int, int, int, double*) = row_major ? or_rvq3_row_rowmajor : or_rvq3_row;
   int n = d > ff ? d : ff;
   double* w = (double*)malloc(sizeof(double) * (size_t)n);
   double* h = (double*)malloc(sizeof(double) * (size_t)ff);
@@ -273,19 +293,29 @@ int or_expert_rvq3(const double* x, const uint8_t* rec, const uint16_t* cb_gate,
     return -1;
   }
   for (int r = 0; r < ff; ++r) {
-    or_rvq3_row(g_codes, cb_gate, ff, d, r, w);
+    row(g_codes, cb_gate, ff, d, r, w);
     double g = dot(w, x, d);
-    or_rvq3_row(u_codes, cb_up, ff, d, r, w);
+    row(u_codes, cb_up, ff, d, r, w);
     double u = dot(w, x, d);
     h[r] = or_act(g, u, act);
   }
   for (int r = 0; r < d; ++r) {
-    or_rvq3_row(d_codes, cb_down, d, ff, r, w);
+    row(d_codes, cb_down, d, ff, r, w);
     y[r] = dot(w, h, ff);
   }
   free(w);
   free(h);
   return 0;
+}
+
+int or_expert_rvq3(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
+                   const uint16_t* cb_down, int d, int ff, int act, double* y) {
+  return expert_rvq3_layout(x, rec, cb_gate, cb_up, cb_down, d, ff, act, 0, y);
+}
+
+int or_expert_rvq3_rowmajor(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
+                            const uint16_t* cb_down, int d, int ff, int act, double* y) {
+  return expert_rvq3_layout(x, rec, cb_gate, cb_up, cb_down, d, ff, act, 1, y);
 }
 
 /* ------------------------------------------------------------------------ */

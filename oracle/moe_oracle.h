@@ -51,6 +51,10 @@ void or_mxfp4_row(const uint8_t* codes, const uint8_t* scales, int K, int r, dou
  * code[s][v][r]), codebooks cb fp16 [3][256][8];
  * w[r][8v+i] = sum over stages s of cb[s][code[s][v][r]][i]. */
 void or_rvq3_row(const uint8_t* codes, const uint16_t* cb, int rows, int K, int r, double* w);
+/* The same weights from codes stored row by row, [3][rows][K/8] (the
+ * row-major record layout, converted on the GPU side by moe_rvq3_repack):
+ * stage s's code for weights r, 8v..8v+7 is codes[(s * rows + r) * (K/8) + v]. */
+void or_rvq3_row_rowmajor(const uint8_t* codes, const uint16_t* cb, int rows, int K, int r, double* w);
 
 /* Byte offsets of the three matrices inside one expert record. */
 size_t or_mxfp4_record_bytes(int d, int ff);
@@ -91,6 +95,10 @@ int or_bucket(const int32_t* topk_idx, int T, int k, int E, int32_t* counts, int
 int or_expert_mxfp4(const double* x, const uint8_t* rec, int d, int ff, int act, double* y);
 int or_expert_rvq3(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
                    const uint16_t* cb_down, int d, int ff, int act, double* y);
+/* The same expert on a record whose nine code planes are stored row by row:
+ * gate [3][ff][d/8] | up [3][ff][d/8] | down [3][d][ff/8]. */
+int or_expert_rvq3_rowmajor(const double* x, const uint8_t* rec, const uint16_t* cb_gate, const uint16_t* cb_up,
+                            const uint16_t* cb_down, int d, int ff, int act, double* y);
 double or_act(double g, double u, int act);
 
 /* ---- combine ------------------------------------------------------------

@@ -32,6 +32,10 @@ MUTANTS = [
     ("RVQ stage dropped", "for (int s = 0; s < 3; ++s) {\n        int c", "for (int s = 0; s < 2; ++s) {\n        int c"),
     ("RVQ codebook stride", "cb[((size_t)s * 256 + c) * 8 + i]", "cb[((size_t)s * 256 + c) + i]"),
     ("RVQ codes read row-major", "codes[((size_t)s * nv + v) * rows + r]", "codes[((size_t)s * rows + r) * nv + v]"),
+    ("RVQ row-major reader indexed position-major", "codes[((size_t)s * rows + r) * nv + v]",
+     "codes[((size_t)s * nv + v) * rows + r]"),
+    ("RVQ row-major expert reads position-major rows", "row_major ? or_rvq3_row_rowmajor : or_rvq3_row",
+     "or_rvq3_row"),
     ("SiTU cap", "25.0 * tanh(u / 25.0)", "25.0 * tanh(u / 20.0)"),
     ("f16 exponent bias", "ldexp(1024.0 + m, e - 25)", "ldexp(1024.0 + m, e - 24)"),
     ("selection-only gates take the biased logits", "topk_select_gates(l, plain ? plain : l,",

@@ -86,6 +86,41 @@ def test_rvq3_is_sum_of_three_codewords():
                 assert got0[r, 8 * v + i] == npref.f16_to_f64(np.array([cb[0, c0[r, v], i]]))[0]
 
 
+def test_rvq3_row_major_reader_is_the_same_definition():
+    # codes stored row by row, [3][rows][K/8]: every weight is the sum of the
+    # three stages' codeword components, written out here index by index
+    rng = np.random.default_rng(5)
+    rows, K = 5, 48
+    nv = K // 8
+    codes = rng.integers(0, 256, size=3 * rows * nv, dtype=np.uint8)
+    cb = si.normal(12, 16, 0.02, 3 * 256 * 8, "f16").reshape(3, 256, 8)
+    cbf = npref.f16_to_f64(cb.reshape(-1)).reshape(3, 256, 8)
+    got = oracle.rvq3_matrix_rowmajor(codes, cb, rows, K)
+    for r in range(rows):
+        for v in range(nv):
+            for i in range(8):
+                want = 0.0
+                for s in range(3):
+                    want += cbf[s, codes[(s * rows + r) * nv + v], i]
+                assert got[r, 8 * v + i] == want
+    # the same weights as the position-major reader on the transposed planes
+    pm = codes.reshape(3, rows, nv).transpose(0, 2, 1).copy()
+    np.testing.assert_array_equal(got, oracle.rvq3_matrix(pm, cb, rows, K))
+    # a whole expert: row-major record = position-major record with every plane transposed
+    d, ff = 64, 96
+    rec = si.rvq3_record(7, 1, d, ff)
+    cbs = np.stack([si.normal(7, 16 + s, 0.02 / (s + 1), 256 * 8, "f16") for s in range(3)]).reshape(3, 256, 8)
+    x = npref.to_f64(si.normal(7, 1, 1.0, d, "bf16"))
+    parts, o = [], 0
+    for rws, kk in ((ff, d), (ff, d), (d, ff)):
+        n = 3 * rws * (kk // 8)
+        parts.append(rec[o:o + n].reshape(3, rws, kk // 8).transpose(0, 2, 1).reshape(-1))
+        o += n
+    y_rm = oracle.expert_rvq3_rowmajor(x, rec, cbs, cbs, cbs, d, ff)
+    y_pm = oracle.expert_rvq3(x, np.concatenate(parts), cbs, cbs, cbs, d, ff)
+    np.testing.assert_array_equal(y_rm, y_pm)
+
+
 def test_record_sizes_match_page_figures():
     with open(os.path.join(GOLDEN, "page_figures.json")) as f:
         pf = json.load(f)
