@@ -1,28 +1,34 @@
 #!/usr/bin/env python
 """MoE-layer forward benchmark on one (or N independent) GB300.
 
-Workload (default): the Kimi-K3-shaped MoE layer at decode batch 1 -- d = 3584,
-ff = 3072, 896 MXFP4 experts resident in HBM (15.7 GB), top-16 renormalised
-gates, bf16 activations; every step routes one new token (64 distinct seeded
-tokens cycled), so each step streams 16 fresh experts (287 MB) from HBM.  L2 is
-flushed between timed steps, outside the timed events: a 512 MiB write, then a
-512 MiB read of a second buffer, which writes the dirty lines back so that no
-step pays for the flush's own write-back.
+Headline workload (default): the Kimi-K3-shaped MoE layer at decode batch 1 --
+d = 3584, ff = 3072, 896 MXFP4 experts resident in HBM (15.7 GB), top-16
+renormalised gates, bf16 activations; every step routes one new token (64
+distinct seeded tokens cycled), so each step streams 16 fresh experts (287 MB)
+from HBM.  L2 is flushed between timed steps, outside the timed events: a 512
+MiB write, then a 512 MiB read of a second buffer, which writes the dirty lines
+back so that no step pays for the flush's own write-back.
 
   value        tokens/s from CUDA events around each moe_layer_forward call,
                inputs resident in HBM
   e2e          tokens/s through the same C-ABI call with the token copied in
                from pinned host memory and the layer output copied back, per step
-  roofline     the dominant kernel (mxfp4_gate_up): algorithmic bytes per launch
-               / its mean launch time (per-launch events from the library's
-               profiler in a second pass over the same steps) vs the measured
-               HBM copy bandwidth
+  roofline     the dominant expert kernel: algorithmic bytes (or flops) per
+               launch / its mean launch time (per-launch events from the
+               library's profiler in a second pass over the same steps) vs the
+               measured HBM copy bandwidth (or tensor peak)
   cpu_baseline the fp64 C oracle on a bounded sample of the same workload, on
                this machine's host cores
+  configs      the same measurement (value, ms_per_step, roofline, kernels,
+               cpu_baseline) for the other workloads: RVQ3 decode at batch 1
+               and 8, 512-token prefill with Zipf-skewed and uniform routing,
+               and the six-layer stack at 64 tokens per step (tokens/s through
+               all six layers)
 
 `--impl reference` times the oracle itself as the reference arm.  Under torchrun
-(N > 1) the ranks run independent replicas (the layer does not shard across
-GPUs here), value = all ranks' tokens / the slowest rank's time.
+(N > 1) the ranks run independent replicas of the headline workload (the layer
+does not shard across GPUs here), value = all ranks' tokens / the slowest
+rank's time.
 """
 import argparse
 import json
@@ -38,6 +44,9 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s on 1 GB300; achieved HBM GB/s (decode) / TC util vs peak"
 DEFAULT_WORKLOAD = "k3_mxfp4_decode"
+STACK_WORKLOAD = "k3_mxfp4_stack"
+CONFIG_WORKLOADS = ("k3_rvq3_decode_b1", "k3_rvq3_decode_b8", "k3_mxfp4_prefill_zipf", "k3_mxfp4_prefill_uniform",
+                    STACK_WORKLOAD)
 X_POOL = 64
 FLUSH_BYTES = 512 << 20
 
@@ -49,12 +58,15 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--configs", default="all",
+                    help="other workloads measured after the headline: 'all', 'none' or a comma-separated list")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps per other workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gemm-min", type=int, default=None,
-                    help="experts with at least this many tokens take the tensor-core GEMM path (library default)")
-    ap.add_argument("--mxfp4-kernel", choices=["block_scaled", "gemv_gemm"], default=None,
-                    help="MXFP4 expert kernels (library default: block_scaled)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work for the oracle sample")
+    ap.add_argument("--mxfp4-kernel", choices=["block_scaled", "gemv", "auto"], default=None,
+                    help="MXFP4 expert kernels (library default: auto)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work for the headline oracle sample")
+    ap.add_argument("--config-cpu-seconds", type=float, default=6.0,
+                    help="target CPU work for each other workload's oracle sample")
     ap.add_argument("--only", choices=["route_topk", "records_check"], default=None,
                     help="time one step of the layer alone (a small case for profiler captures)")
     return ap.parse_args()
@@ -81,7 +93,10 @@ def ncu_traffic(kernel, workload):
         return None
     h = hashlib.sha256()
     for src in rec["sources"]:
-        with open(os.path.join(ROOT, "quantized_expert_ffn_score_gb300", "csrc", src), "rb") as f:
+        p = os.path.join(ROOT, "quantized_expert_ffn_score_gb300", "csrc", src)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as f:
             h.update(f.read())
     return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["source_sha256"] else None
 
@@ -105,7 +120,6 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
-        self.out = None
 
     def start(self):
         try:
@@ -142,33 +156,58 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- workloads
+
+def stack_recipes():
+    from seeded_inputs.workloads import STACK_LAYERS, stack_layer
+    return [stack_layer(l) for l in range(STACK_LAYERS)]
+
+
+def workload_recipes(name):
+    """The layer recipes one step runs: one layer, or the six-layer stack."""
+    import seeded_inputs as si
+    if name == STACK_WORKLOAD:
+        return stack_recipes()
+    return [si.get_workload(name)]
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
-def oracle_sample(r, target_s, max_tokens=64, token_offset=1000):
-    """Times the fp64 oracle on whole tokens of recipe r until ~target_s of wall
-    time; returns (tokens, seconds, threads).  Record generation is excluded."""
+def _bf16_bits(a32):
     import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
 
+
+def oracle_sample(recipes, target_s, max_tokens=64, token_offset=1000):
+    """Times the fp64 oracle on whole tokens of the workload (one token through
+    every layer of `recipes`, each layer's fp64 output rounded to bf16 for the
+    next) until ~target_s of wall time; returns (tokens, seconds, threads).
+    Record generation is excluded from the time."""
     import oracle
     import seeded_inputs as si
     threads = host_cores()
-    W = si.layer_router_w(r)
-    b = si.layer_bias(r)
-    cb = si.layer_codebooks(r) if r.quant == "rvq3" else None
+    W = [si.layer_router_w(r) for r in recipes]
+    b = [si.layer_bias(r) for r in recipes]
+    cb = [si.layer_codebooks(r) if r.quant == "rvq3" else None for r in recipes]
     done, spent = 0, 0.0
     while done < max_tokens and spent < target_s:
-        x = si.layer_x(r, T=1, token_offset=token_offset + done)
-        _, idx, _ = oracle.router(x, W, b, r.k, bias_mode=r.bias_mode)
-        used = set(idx.reshape(-1).tolist()) | set(range(r.E, r.E + r.n_shared))
-        recs = [si.layer_record(r, e) if e in used else None for e in range(r.E + r.n_shared)]
-        t0 = time.perf_counter()
-        oracle.layer_forward(x, W, b, r.d, r.ff, r.E, r.k, recs, quant=r.quant, act_kind=r.act,
-                             codebooks=None if cb is None else (cb, cb, cb), nthreads=threads,
-                             n_shared=r.n_shared, bias_mode=r.bias_mode)
-        spent += time.perf_counter() - t0
+        x = si.layer_x(recipes[0], T=1, token_offset=token_offset + done)
+        for l, r in enumerate(recipes):
+            _, idx, _ = oracle.router(x, W[l], b[l], r.k, bias_mode=r.bias_mode)
+            used = set(idx.reshape(-1).tolist()) | set(range(r.E, r.E + r.n_shared))
+            recs = si.layer_records(r, used, nthreads=threads)
+            t0 = time.perf_counter()
+            _, _, _, out = oracle.layer_forward(x, W[l], b[l], r.d, r.ff, r.E, r.k, recs, quant=r.quant,
+                                                act_kind=r.act,
+                                                codebooks=None if cb[l] is None else (cb[l], cb[l], cb[l]),
+                                                nthreads=threads, n_shared=r.n_shared, bias_mode=r.bias_mode)
+            spent += time.perf_counter() - t0
+            del recs
+            if l + 1 < len(recipes):
+                x = _bf16_bits(out.astype("float32")).reshape(1, -1)
         done += 1
-        del recs
-    np.asarray(0)
     return done, spent, threads
 
 
@@ -197,26 +236,26 @@ def dist_barrier(world):
         dist.barrier()
 
 
-# ----------------------------------------------------------------------------- arms
+# ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    import seeded_inputs as si
-    r = si.get_workload(args.workload)
+    recipes = workload_recipes(args.workload)
+    T = recipes[0].T
     per_step = max(1.0, 60.0 / max(1, args.steps))  # whole run within a few minutes
-    oracle_sample(r, target_s=0.0, max_tokens=min(args.warmup, 1))
+    oracle_sample(recipes, target_s=0.0, max_tokens=min(args.warmup, 1))
     tokens, secs, threads = 0, 0.0, host_cores()
     for i in range(args.steps):
-        t, s, threads = oracle_sample(r, target_s=per_step, max_tokens=1, token_offset=2000 + i)
+        t, s, threads = oracle_sample(recipes, target_s=per_step, max_tokens=1, token_offset=2000 + i)
         tokens += t
         secs += s
-    value = tokens * r.T / secs
+    value = tokens / secs
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": args.workload, "tokens_per_step": r.T},
+            "data": "synthetic (seeded)", "config": {"workload": args.workload, "tokens_per_step": T},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": f"{tokens} tokens of {args.workload}, one token per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -224,150 +263,90 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+# ----------------------------------------------------------------------------- our arm
+
+class Target:
+    """One workload on the device: its layers, a pool of seeded inputs, the
+    output and workspace, and one step (a layer call or a stack call)."""
+
+    def __init__(self, name, ctx, dev):
+        import torch
+
+        from quantized_expert_ffn_score_gb300 import moe, synthetic
+        self.name = name
+        self.moe = moe
+        self.ctx = ctx
+        self.recipes = workload_recipes(name)
+        r0 = self.recipes[0]
+        self.r0, self.T, self.stack = r0, r0.T, len(self.recipes) > 1
+        self.layers = [synthetic.device_layer(r, device=dev) for r in self.recipes]
+        self.x_pool = synthetic.device_x(r0, T=X_POOL * self.T, device=dev).view(X_POOL, self.T, r0.d)
+        self.out = torch.empty((self.T, r0.d), dtype=torch.float32, device=dev)
+        ne = [r.E + r.n_shared for r in self.recipes]
+        self.counts = torch.empty(sum(ne), dtype=torch.int32, device=dev)
+        self.ne = ne
+        if self.stack:
+            self.ws = moe.workspace(moe.stack_forward_ws_bytes(self.layers, self.T), device=dev)
+        else:
+            self.ws = moe.workspace(moe.layer_forward_ws_bytes(self.layers[0], self.T), device=dev)
+
+    def step(self, i, counts=False, x=None):
+        x = self.x_pool[i % X_POOL] if x is None else x
+        if self.stack:
+            self.moe.moe_stack_forward_ex(self.ctx, self.layers, x, self.out, self.ws,
+                                          counts_trace=self.counts if counts else None)
+        else:
+            self.moe.moe_layer_forward(self.ctx, self.layers[0], x, self.out, self.ws,
+                                       counts_out=self.counts if counts else None)
+
+    def layer_counts(self):
+        """Tokens per expert of the last counted step, one array per layer."""
+        c = self.counts.cpu().numpy()
+        out, o = [], 0
+        for n in self.ne:
+            out.append(c[o:o + n].copy())
+            o += n
+        return out
+
+
+def expert_rooflines(t, prof, step_counts, peaks):
+    """Rooflines of the expert kernels that ran: algorithmic bytes (and for the
+    block-scaled kernel also flops) per launch over the mean launch time.
+
+    Bytes per launch, per layer call: each distinct expert's gate and up
+    matrices (codes and scales, 2/3 of a record) once, plus the activations in
+    (x as bf16, or for the block-scaled kernel its two E4M3 terms and their
+    scales) and h out (fp32) per pair.  Flops: 2 x 2 x ff x d per pair."""
     import numpy as np
-    import torch
-
     import seeded_inputs as si
-    from quantized_expert_ffn_score_gb300 import moe, synthetic
-
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    r = si.get_workload(args.workload)
-    T = r.T
-    ctx = moe.Context(local)
-    if args.gemm_min is not None:
-        ctx.gemm_min_tokens = args.gemm_min
-    if args.mxfp4_kernel is not None:
-        ctx.mxfp4_kernel = args.mxfp4_kernel
-    layer = synthetic.device_layer(r, device=dev)
-    x_pool = synthetic.device_x(r, T=X_POOL * T, device=dev).view(X_POOL, T, r.d)
-    out = torch.empty((T, r.d), dtype=torch.float32, device=dev)
-    counts = torch.empty(r.E + r.n_shared, dtype=torch.int32, device=dev)
-    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, T), device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    def flush_l2(i):
-        flush.fill_(i & 0xFF)
-        flush_rd.max()  # reads 512 MiB: the L2 ends up holding clean lines of this buffer
-
-    stream = torch.cuda.current_stream()
-
-    def step(i, counts_out=None):
-        moe.moe_layer_forward(ctx, layer, x_pool[i % X_POOL], out, ws, counts_out=counts_out)
-
-    for i in range(args.warmup):
-        flush_l2(i)
-        step(i)
-    ctx.check()
-
-    # ---- timed region: device events around each layer call -----------------
-    K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    stops = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    clocks = ClockSampler(torch.cuda.current_device())
-    dist_barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    wall0 = time.perf_counter()
-    for i in range(K):
-        flush_l2(i)
-        starts[i].record(stream)
-        step(i)
-        stops[i].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    dist_barrier(world)
-    ctx.check()
-    fp64_tokens, seq_logits = ctx.stats()
-    dev_ms = sum(s.elapsed_time(e) for s, e in zip(starts, stops))
-    dev_ms_max = dist_max(dev_ms, world, dev)
-
-    # ---- per-kernel pass (same steps, library profiler) ------------------------
-    ctx.profile(16 * K + 64)
-    step_counts = []
-    for i in range(K):
-        flush_l2(i)
-        step(i, counts_out=counts)
-        step_counts.append(counts.cpu().numpy().copy())
-    prof = ctx.profile_read()
-    ctx.profile(0)
-    launches_per_step = sum(n for n, _ in prof.values()) / K
-
-    # ---- end to end through the ABI with host buffers --------------------------
-    x_host = torch.empty((X_POOL, T, r.d), dtype=x_pool.dtype, pin_memory=True)
-    x_host.copy_(x_pool.cpu())
-    out_host = torch.empty((T, r.d), dtype=torch.float32, pin_memory=True)
-    x_dev = torch.empty((T, r.d), dtype=x_pool.dtype, device=dev)
-    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        flush_l2(i)
-        e_starts[i].record(stream)
-        x_dev.copy_(x_host[i % X_POOL], non_blocking=True)
-        moe.moe_layer_forward(ctx, layer, x_dev, out, ws)
-        out_host.copy_(out, non_blocking=True)
-        e_stops[i].record(stream)
-    torch.cuda.synchronize()
-    ctx.check()
-    e2e_ms = dist_max(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_stops)), world, dev)
-
-    tokens_total = world * K * T
-    value = tokens_total / (dev_ms_max / 1e3)
-    peaks = measured_peaks()
-    rec_bytes = si.mxfp4_record_size(r.d, r.ff) if r.quant == "mxfp4" else si.rvq3_record_size(r.d, r.ff)
-    # The expert kernels' algorithmic work per launch.  Experts with at least
-    # gemm_min tokens run on the tensor-core GEMM path when it ran at all; the
-    # others stream through the GEMV path.
-    gemm_ran = "mxfp4_gemm_gate_up" in prof
-    gmin = ctx.gemm_min_tokens if gemm_ran else 1 << 30
-    cnts = np.stack(step_counts)
-    mean_distinct = float(np.mean((cnts > 0).sum(axis=1)))
-    cold_distinct = float(np.mean(((cnts > 0) & (cnts < gmin)).sum(axis=1)))
-    hot_pairs = float(np.mean(np.where(cnts >= gmin, cnts, 0).sum(axis=1)))
-    cold_pairs = float(np.mean(np.where(cnts < gmin, cnts, 0).sum(axis=1)))
-    gemv = "mxfp4_gate_up" if r.quant == "mxfp4" else "rvq3_gate_up"
-    gemv_bytes = cold_distinct * (2 * rec_bytes / 3) + cold_pairs * (r.d * 2 + r.ff * 4)
-    gemm_flops = 2.0 * 2 * r.ff * r.d * hot_pairs
+    r = t.r0
+    rec_bytes = si.record_size(r)
+    # per (step, layer): distinct experts and pairs
+    distinct = np.array([[float((c > 0).sum()) for c in sc] for sc in step_counts])
+    pairs = np.array([[float(c.sum()) for c in sc] for sc in step_counts])
+    mean_distinct, mean_pairs = float(distinct.mean()), float(pairs.mean())
     rooflines = {}
-    if gemv in prof:
-        n, ms = prof[gemv]
-        ach = gemv_bytes / (ms / n / 1e3) / 1e9
-        rooflines[gemv] = {"bound": "hbm", "kernel": gemv, "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": ach / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                           "bytes_per_launch": gemv_bytes, "mean_launch_us": 1e3 * ms / n,
-                           "traffic": ncu_traffic(gemv, args.workload)}
-    if gemm_ran:
-        n, ms = prof["mxfp4_gemm_gate_up"]
-        ach = gemm_flops / (ms / n / 1e3) / 1e12
-        rooflines["mxfp4_gemm_gate_up"] = {
-            "bound": "tensor", "kernel": "mxfp4_gemm_gate_up", "achieved": ach, "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "peak_source": peaks["source"] + " (f16 = bf16 rate)",
-            "flops_per_launch": gemm_flops, "mean_launch_us": 1e3 * ms / n,
-            "traffic": ncu_traffic("mxfp4_gemm_gate_up", args.workload)}
+    for kern in ("mxfp4_gate_up", "rvq3_gate_up"):
+        if kern in prof:
+            n, ms = prof[kern]
+            nbytes = mean_distinct * (2 * rec_bytes / 3) + mean_pairs * (r.d * 2 + r.ff * 4)
+            ach = nbytes / (ms / n / 1e3) / 1e9
+            rooflines[kern] = {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                               "bytes_per_launch": nbytes, "mean_launch_us": 1e3 * ms / n,
+                               "traffic": ncu_traffic(kern, t.name)}
     if "mxfp4_bs_gate_up" in prof:
-        # Block-scaled kernel (every expert): the gate and up codes and scales of
-        # each distinct expert once, plus the two E4M3 planes of x and their
-        # scales; against HBM.  Its useful flops (2 x 2 x ff x d per pair)
-        # against the E2M1 x E4M3 MMA's peak, the measured bf16 rate x 2 (the
-        # nominal fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s dense).  The binding one
-        # (larger fraction) is reported.
+        # the binding bound (larger fraction) is reported; the E2M1 x E4M3
+        # MMA's peak is the measured bf16 rate x 2 (the nominal fp8 / bf16
+        # ratio, 4.5 / 2.25 PFLOP/s dense)
         n, ms = prof["mxfp4_bs_gate_up"]
-        P = T * (r.k + r.n_shared)
-        bs_bytes = mean_distinct * (2 * rec_bytes / 3) + 2 * P * (r.d + r.d // 32)
-        bs_flops = 2.0 * 2 * r.ff * r.d * P
+        bs_bytes = mean_distinct * (2 * rec_bytes / 3) + 2 * mean_pairs * (r.d + r.d // 32)
+        bs_flops = 2.0 * 2 * r.ff * r.d * mean_pairs
         sec = ms / n / 1e3
         hb = {"bound": "hbm", "kernel": "mxfp4_bs_gate_up", "achieved": bs_bytes / sec / 1e9, "peak": peaks["hbm_gbs"],
               "unit": "GB/s", "frac": bs_bytes / sec / 1e9 / peaks["hbm_gbs"], "peak_source": peaks["source"],
               "bytes_per_launch": bs_bytes, "mean_launch_us": 1e3 * sec,
-              "traffic": ncu_traffic("mxfp4_bs_gate_up", args.workload)}
+              "traffic": ncu_traffic("mxfp4_bs_gate_up", t.name)}
         fp8_peak = 2 * peaks["bf16_tflops"]
         tc_ = {"bound": "tensor", "kernel": "mxfp4_bs_gate_up", "achieved": bs_flops / sec / 1e12, "peak": fp8_peak,
                "unit": "TFLOP/s", "frac": bs_flops / sec / 1e12 / fp8_peak,
@@ -375,36 +354,172 @@ def run_ours(args):
                "mean_launch_us": 1e3 * sec, "traffic": hb["traffic"]}
         rooflines["mxfp4_bs_gate_up"] = hb if hb["frac"] >= tc_["frac"] else tc_
         rooflines["mxfp4_bs_gate_up_other_bound"] = tc_ if hb["frac"] >= tc_["frac"] else hb
-    # the dominant kernel: the expert kernel with the longest launches
     roofline = max((v for k_, v in rooflines.items() if not k_.endswith("_other_bound")),
                    key=lambda v: v["mean_launch_us"]) if rooflines else None
-    step_bytes = mean_distinct * rec_bytes + r.E * r.d * 2 + T * r.d * 2
-    kernels = {k: {"launches": n, "mean_us": 1e3 * ms / n} for k, (n, ms) in prof.items()}
+    return roofline, rooflines, mean_distinct, mean_pairs
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak",
+
+def measure(t, K, warmup, flush_l2, world, dev, with_clocks=True):
+    """Times K steps of target t with CUDA events (L2 flushed between steps,
+    outside the events), then a second pass with the library's per-launch
+    profiler for the per-kernel times and the routed experts."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        flush_l2(i)
+        t.step(i)
+    t.ctx.check()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device()) if with_clocks else None
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush_l2(i)
+        starts[i].record(stream)
+        t.step(i)
+        stops[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if clocks else None
+    dist_barrier(world)
+    t.ctx.check()
+    fp64_tokens, seq_logits = t.ctx.stats()
+    dev_ms = dist_max(sum(s.elapsed_time(e) for s, e in zip(starts, stops)), world, dev)
+    # per-kernel pass (same steps, library profiler).  The event pairs around
+    # each launch keep launches from overlapping their neighbours, so these
+    # per-kernel means are upper bounds of the kernels' times inside the timed
+    # steps (they add up to more than a step).
+    t.ctx.profile(64 * len(t.recipes) * K + 64)
+    step_counts = []
+    for i in range(K):
+        flush_l2(i)
+        t.step(i, counts=True)
+        step_counts.append(t.layer_counts())
+    prof = t.ctx.profile_read(max_entries=64)
+    t.ctx.profile(0)
+    return {"dev_ms": dev_ms, "wall_s": wall, "clocks": clk, "prof": prof, "step_counts": step_counts,
+            "fp64_tokens": fp64_tokens, "seq_logits": seq_logits}
+
+
+def workload_line(t, m, K, peaks, cpu_seconds, rank, world, with_cpu):
+    """The measured figures of one workload as a dict of the bench line's keys."""
+    import seeded_inputs as si
+    tokens_total = world * K * t.T
+    value = tokens_total / (m["dev_ms"] / 1e3)
+    roofline, rooflines, mean_distinct, mean_pairs = expert_rooflines(t, m["prof"], m["step_counts"], peaks)
+    rec_bytes = si.record_size(t.r0)
+    n_layers = len(t.recipes)
+    # whole-step bytes: every layer's distinct experts, router weights and activations
+    step_bytes = n_layers * (mean_distinct * rec_bytes + t.r0.E * t.r0.d * 2 + t.T * t.r0.d * 2)
+    launches_per_step = sum(n for n, _ in m["prof"].values()) / K
+    d = {"value": value, "unit": "tokens/s", "ms_per_step": m["dev_ms"] / K, "steps": K,
+         "config": {"workload": t.name, "d": t.r0.d, "ff": t.r0.ff, "E": t.r0.E, "k": t.r0.k, "tokens_per_step": t.T,
+                    "layers_per_step": n_layers, "quant": t.r0.quant,
+                    "experts_resident_gb": round(n_layers * (t.r0.E + t.r0.n_shared) * rec_bytes / 1e9, 2),
+                    "shared_experts": t.r0.n_shared, "bias": t.r0.bias, "bias_mode": t.r0.bias_mode,
+                    "mxfp4_kernel": t.ctx.mxfp4_kernel if t.r0.quant == "mxfp4" else None},
+         "layer_hbm_gbs": step_bytes / (m["dev_ms"] / K / 1e3) / 1e9,
+         "layer_hbm_frac": step_bytes / (m["dev_ms"] / K / 1e3) / 1e9 / peaks["hbm_gbs"],
+         "roofline": roofline, "rooflines": rooflines,
+         "kernels": {k: {"launches": n, "mean_us": 1e3 * ms / n} for k, (n, ms) in m["prof"].items()},
+         "experts": {"distinct_per_layer_call": mean_distinct, "pairs_per_layer_call": mean_pairs},
+         "gpu_launches": int(round(launches_per_step * K)), "clocks": m["clocks"], "wall_s": m["wall_s"],
+         "router_fp64_recheck": {"tokens": m["fp64_tokens"], "sequential_logits": m["seq_logits"],
+                                 "of_tokens": K * t.T * n_layers}}
+    if rank == 0 and world == 1 and with_cpu:
+        tokens, secs, threads = oracle_sample(t.recipes, target_s=cpu_seconds)
+        d["cpu_baseline"] = {"value": tokens / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{tokens} tokens of {t.name} (one token per call through "
+                                       f"{n_layers} layer(s), pairs on {threads} OpenMP threads), {secs:.1f} s"}
+    return d
+
+
+def run_ours(args):
+    import torch
+
+    from quantized_expert_ffn_score_gb300 import moe
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    ctx = moe.Context(local)
+    if args.mxfp4_kernel is not None:
+        ctx.mxfp4_kernel = args.mxfp4_kernel
+    peaks = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush_rd.max()  # reads 512 MiB: the L2 ends up holding clean lines of this buffer
+
+    # ---- the headline workload ---------------------------------------------------
+    t = Target(args.workload, ctx, dev)
+    K = args.steps
+    m = measure(t, K, args.warmup, flush_l2, world, dev)
+    head = workload_line(t, m, K, peaks, args.cpu_seconds, rank, world, not args.no_cpu_baseline)
+
+    # ---- end to end through the ABI with host buffers (headline workload) -------------
+    stream = torch.cuda.current_stream()
+    x_host = torch.empty(tuple(t.x_pool.shape), dtype=t.x_pool.dtype, pin_memory=True)
+    x_host.copy_(t.x_pool.cpu())
+    out_host = torch.empty(tuple(t.out.shape), dtype=torch.float32, pin_memory=True)
+    x_dev = torch.empty(tuple(t.x_pool.shape[1:]), dtype=t.x_pool.dtype, device=dev)
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush_l2(i)
+        e_starts[i].record(stream)
+        x_dev.copy_(x_host[i % X_POOL], non_blocking=True)
+        t.step(i, x=x_dev)
+        out_host.copy_(t.out, non_blocking=True)
+        e_stops[i].record(stream)
+    torch.cuda.synchronize()
+    ctx.check()
+    e2e_ms = dist_max(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_stops)), world, dev)
+    tokens_total = world * K * t.T
+    e2e = {"value": tokens_total / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": t.T * t.r0.d * t.x_pool.element_size(), "d2h_bytes_per_step": t.T * t.r0.d * 4}
+    del t
+    torch.cuda.empty_cache()
+
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator; random-init weights)",
-            "config": {"workload": args.workload, "d": r.d, "ff": r.ff, "E": r.E, "k": r.k, "tokens_per_step": T,
-                       "quant": r.quant, "experts_resident_gb": round((r.E + r.n_shared) * rec_bytes / 1e9, 2),
-                       "shared_experts": r.n_shared, "bias": r.bias, "bias_mode": r.bias_mode,
-                       "l2": "flushed between steps outside the timed events (512 MiB write, then 512 MiB read of another buffer)",
-                       "x_pool": X_POOL, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "mxfp4_kernel": ctx.mxfp4_kernel if r.quant == "mxfp4" else None},
-            "layer_hbm_gbs": step_bytes / (dev_ms_max / K / 1e3) / 1e9,
-            "roofline": roofline, "rooflines": rooflines, "kernels": kernels,
-            "experts": {"distinct_per_step": mean_distinct, "gemm_path_pairs": hot_pairs, "gemv_path_experts": cold_distinct,
-                        "gemm_min_tokens": ctx.gemm_min_tokens},
-            "e2e": {"value": tokens_total / (e2e_ms / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * r.d * x_pool.element_size(), "d2h_bytes_per_step": T * r.d * 4},
-            "gpu_launches": int(round(launches_per_step * K)), "clocks": clk, "wall_s": wall,
-            "router_fp64_recheck": {"tokens": fp64_tokens, "sequential_logits": seq_logits, "of_tokens": K * T}}
+            "config": dict(head["config"], l2="flushed between steps outside the timed events (512 MiB write, "
+                                              "then 512 MiB read of another buffer)",
+                           x_pool=X_POOL, parallelism=f"replicas x{world}" if world > 1 else "single GPU")}
+    for key in ("layer_hbm_gbs", "layer_hbm_frac", "roofline", "rooflines", "kernels", "experts", "gpu_launches",
+                "clocks", "wall_s", "router_fp64_recheck", "cpu_baseline"):
+        if key in head:
+            line[key] = head[key]
+    line["e2e"] = e2e
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tokens, secs, threads = oracle_sample(r, target_s=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tokens * T / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{tokens} tokens of {args.workload} (one token per call, pairs on "
-                                          f"{threads} OpenMP threads), {secs:.1f} s"}
+    # ---- the other workloads (single GPU only) ---------------------------------------
+    names = [] if world > 1 or args.configs == "none" else (
+        [w for w in CONFIG_WORKLOADS if w != args.workload] if args.configs == "all" else
+        [w for w in args.configs.split(",") if w])
+    configs = {}
+    for name in names:
+        tc = Target(name, ctx, dev)
+        mc = measure(tc, args.config_steps, max(3, min(args.warmup, 5)), flush_l2, world, dev)
+        configs[name] = workload_line(tc, mc, args.config_steps, peaks, args.config_cpu_seconds, rank, world,
+                                      not args.no_cpu_baseline)
+        del tc
+        torch.cuda.empty_cache()
+    if configs:
+        line["configs"] = configs
+        line["gpu_launches"] = line["gpu_launches"] + sum(c["gpu_launches"] for c in configs.values())
+
     if rank == 0:
         print(json.dumps(line), flush=True)
     ctx.close()

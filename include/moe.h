@@ -183,26 +183,32 @@ MOE_API moe_status moe_ctx_profile(moe_ctx* ctx, int n);
 MOE_API int moe_ctx_profile_read(moe_ctx* ctx, cudaStream_t stream, int max_entries, char* names, int* launches,
                                  double* total_ms);
 
+/* Limit of the kernels' pipeline waits (a stage of weights arriving, a
+ * partial sum being consumed), in nanoseconds; 0 restores the default of 2 s.
+ * Values below 1000 are raised to 1000.  A wait that runs out records
+ * MOE_ERR_TIMEOUT on the error word, the kernel skips its remaining work and
+ * returns, and moe_ctx_check reports it; the context stays usable.  Waits
+ * for a CTA's own copies and tensor-core operations in flight before it
+ * leaves keep the 2 s limit whatever this setting.  Synchronous (it writes
+ * the setting to the device); it applies to launches made after it returns.
+ * Failure detection in the spirit of the pages' fail-loud checks (WASTE
+ * README, "How it works"; LazyLoRA README, "How you know this is real"). */
+MOE_API moe_status moe_ctx_set_wait_limit_ns(moe_ctx* ctx, unsigned long long ns);
+
+/* Diagnostic: launches one wait on a barrier that nothing completes, through
+ * the same bounded-wait helper as every pipeline wait, so that it runs out
+ * after the context's wait limit and records MOE_ERR_TIMEOUT (detail -1).
+ * Lets a caller check that timed-out waits return and are reported, without
+ * any fault or hang.  Asynchronous on `stream`. */
+MOE_API moe_status moe_ctx_wait_selftest(moe_ctx* ctx, cudaStream_t stream);
+
 /* Library version string and the SM count the context sizes its grids for. */
 MOE_API const char* moe_version(void);
 MOE_API int moe_ctx_num_sms(const moe_ctx* ctx);
 
-/* Expert FFN path selection (MXFP4 only; LazyLoRA README, "Batching is the
- * lever"): in one call, an expert routed at least `min_tokens` tokens runs as a
- * grouped GEMM on the tensor cores (its weights decoded once per 128 tokens),
- * the others as the streaming GEMV.  The GEMM path needs bf16 activations and
- * d, ff multiples of 256; otherwise every expert takes the GEMV path.
- * min_tokens = 0 turns the GEMM path off; the default is 2.  Negative values
- * return MOE_ERR_INVALID_ARG.  The setting belongs to the context; calls
- * already enqueued keep the value they were enqueued with.  Both paths compute
- * the same sums in fp32 (products exact; the GEMM path feeds h to the down
- * projection as a bf16 hi + lo pair), so results agree to rounding.
- * moe_ctx_gemm_min_tokens returns the setting, or -1 for a NULL context. */
-MOE_API moe_status moe_ctx_set_gemm_min_tokens(moe_ctx* ctx, int min_tokens);
-MOE_API int moe_ctx_gemm_min_tokens(const moe_ctx* ctx);
-
 /* MXFP4 expert kernels (OCP MX v1.0 E2M1 codes with E8M0 scales per 32; the
- * pages' MXFP4 experts, LazyLoRA README "The engine").
+ * pages' MXFP4 experts, LazyLoRA README "The engine"; batching, not caching,
+ * is the lever, "Cost, measured").
  *   MOE_MXFP4_BLOCK_SCALED: every routed expert on the block-scaled tensor-core
  *     MMA: the record's codes and scale bytes are the A operand as stored; the
  *     activations enter as a sum of E4M3 terms with their own E8M0 scales (x:
@@ -211,17 +217,18 @@ MOE_API int moe_ctx_gemm_min_tokens(const moe_ctx* ctx);
  *     d and ff are multiples of 512, E <= 4096, the device has at most 160
  *     SMs and every routed record is 32-byte aligned (a misaligned record sets
  *     MOE_ERR_INVALID_ARG on the error word); otherwise the call falls back to
- *     the pair below.
- *   MOE_MXFP4_GEMV_GEMM: the warp-level GEMV for experts with few tokens and
- *     the f16 grouped GEMM for experts with at least moe_ctx_gemm_min_tokens
- *     tokens (every product exact in f16/fp32).
+ *     the GEMV pair below.
+ *   MOE_MXFP4_GEMV: every routed expert on the streaming GEMV pair (gate/up,
+ *     then down): the weights are decoded in registers and multiplied on the
+ *     warp-level MMA (bf16 activations) or by fused multiply-adds (fp32
+ *     activations), every product exact and summed in fp32.
  *   MOE_MXFP4_AUTO (default): the GEMV pair for calls of one token, the
  *     block-scaled kernel for more (the faster of the two on a GB300 for
  *     each case).
  * All compute the same layer within the fp32 tolerance.  Other values return
  * MOE_ERR_INVALID_ARG.  moe_ctx_mxfp4_kernel returns the setting, or -1 for a
  * NULL context. */
-typedef enum { MOE_MXFP4_BLOCK_SCALED = 0, MOE_MXFP4_GEMV_GEMM = 1, MOE_MXFP4_AUTO = 2 } moe_mxfp4_kernel;
+typedef enum { MOE_MXFP4_BLOCK_SCALED = 0, MOE_MXFP4_GEMV = 1, MOE_MXFP4_AUTO = 2 } moe_mxfp4_kernel;
 MOE_API moe_status moe_ctx_set_mxfp4_kernel(moe_ctx* ctx, int kernel);
 MOE_API int moe_ctx_mxfp4_kernel(const moe_ctx* ctx);
 
@@ -303,20 +310,23 @@ MOE_API moe_status moe_expert_ffn_rvq3(moe_ctx* ctx, const void* x, moe_dtype x_
 /*
  * moe_expert_ffn_mxfp4 without a workspace, for callers that cannot allocate
  * device memory (an embedding framework or server that owns the allocator,
- * or code that must not allocate after start-up).  Same arguments, same
- * kernels and the same results as moe_expert_ffn_mxfp4, except that the
- * scratch those kernels keep between launches (the active-expert list, a
- * per-token scale and the hidden activations h, T*k*ff floats) lives in a
- * static device array inside the library, moe_expert_ffn_mxfp4_static_max_bytes()
- * bytes (4 MiB) that every GPU using the library reserves until the process
- * exits.  Calls whose scratch would not fit (about T*k*ff > 1,040,000; at
- * ff = 3072 up to T*k = 340 pairs) return MOE_ERR_UNSUPPORTED.  This call
- * allocates nothing: the first call on a device looks up the array's device
- * address (once per device), so make that first call before any stream
- * capture.  Every call, on every stream of a device, shares the one array and
- * it keeps the last call's contents: calls that overlap on the GPU race and
- * give undefined results; serialise them.  The source pages have no
- * counterpart to this entry point.
+ * or code that must not allocate after start-up).  Same arguments as
+ * moe_expert_ffn_mxfp4 minus the workspace.  Whatever the context's
+ * moe_ctx_set_mxfp4_kernel setting, this call always runs the streaming GEMV
+ * pair (MOE_MXFP4_GEMV), for any number of tokens; its outputs agree with
+ * moe_expert_ffn_mxfp4's within the fp32 tolerance, and are bit-identical to
+ * it when that call also runs the GEMV pair.  The scratch the GEMV pair keeps
+ * between launches (the active-expert list, a per-token scale and the hidden
+ * activations h, T*k*ff floats) lives in a static device array inside the
+ * library, moe_expert_ffn_mxfp4_static_max_bytes() bytes (4 MiB) that every
+ * GPU using the library reserves until the process exits.  Calls whose
+ * scratch would not fit (about T*k*ff > 1,040,000; at ff = 3072 up to
+ * T*k = 340 pairs) return MOE_ERR_UNSUPPORTED.  This call allocates nothing:
+ * the first call on a device looks up the array's device address (once per
+ * device), so make that first call before any stream capture.  Every call, on
+ * every stream of a device, shares the one array and it keeps the last call's
+ * contents: calls that overlap on the GPU race and give undefined results;
+ * serialise them.  The source pages have no counterpart to this entry point.
  */
 MOE_API moe_status moe_expert_ffn_mxfp4_static(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k,
                                                const moe_mxfp4_experts* experts, moe_act act, const int32_t* offsets,
@@ -352,6 +362,40 @@ MOE_API moe_status moe_layer_forward(moe_ctx* ctx, const moe_layer* L, const voi
  */
 MOE_API moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers, const void* x, moe_dtype x_dtype,
                              int T, void* out, moe_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Layer stack with its routing trace (LazyLoRA README, "How you know this is
+ * real": the routing a run took is recorded so it can be checked; WASTE
+ * README, "How it works").  As moe_stack_forward, and when non-NULL:
+ *   topk_trace, gates_trace: layer l's pairs [T][k_l + n_shared_l] (routed
+ *     selection, then the shared experts with gate 1), as moe_layer_forward's
+ *     topk_idx_out / gates_out, concatenated over the layers in order (layer l
+ *     starts at T * sum over l' < l of (k_l' + n_shared_l'));
+ *   counts_trace: layer l's tokens per expert [E_l + n_shared_l], concatenated
+ *     likewise.
+ * Device buffers owned by the caller; every layer's part is written.
+ */
+MOE_API moe_status moe_stack_forward_ex(moe_ctx* ctx, const moe_layer* layers, int n_layers, const void* x,
+                                        moe_dtype x_dtype, int T, void* out, moe_dtype out_dtype, int32_t* topk_trace,
+                                        float* gates_trace, int32_t* counts_trace, void* ws, size_t ws_bytes,
+                                        cudaStream_t stream);
+
+/*
+ * RVQ3 records from the row-major code layout to the position-major one that
+ * moe_rvq3_experts reads (WASTE README, "3 bits per expert weight": three
+ * 8-bit codes per 8 consecutive weights of a row).  Row-major record, each
+ * plane [rows][K/8] with a row's codes contiguous:
+ *   gate.codes [3][ff][d/8] | up.codes [3][ff][d/8] | down.codes [3][d][ff/8]
+ * Each of the 9 planes is transposed to [K/8][rows]; the size,
+ * moe_rvq3_record_bytes(d, ff), is unchanged.  src, dst: device arrays [n] of
+ * device pointers to records (a record may not be converted in place: src[i]
+ * == dst[i] sets MOE_ERR_INVALID_ARG on the error word with detail i, a NULL
+ * pointer MOE_ERR_MISSING_EXPERT; that record is skipped).  Meant for load
+ * time, outside any timed region; reads and writes every byte once.  n = 0 is
+ * a no-op.
+ */
+MOE_API moe_status moe_rvq3_repack(moe_ctx* ctx, const uint8_t* const* src, uint8_t* const* dst, int n, int d, int ff,
+                                   cudaStream_t stream);
 
 /*
  * Record check (WASTE README, "How it works": every expert record carries a

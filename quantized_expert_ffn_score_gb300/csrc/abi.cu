@@ -63,20 +63,15 @@ void profiler_end(Profiler* p, cudaStream_t s) {
 struct moe_ctx {
   int device;
   int num_sms;
-  int gemm_min;  // experts with at least this many tokens take the tensor-core GEMM path (0: never)
-  int mxfp4_kernel;  // moe_mxfp4_kernel: block-scaled MMA path, or the GEMV/GEMM pair
-  int* err;  // device: [0] status, [1] detail, [2..3] spare
+  int mxfp4_kernel;  // moe_mxfp4_kernel: block-scaled MMA path, the GEMV pair, or chosen by token count
+  int* err;  // device: [0] status, [1] detail, [2..3] router recheck counters, [4..5] wait limit (ns, u64)
   moe::Profiler* prof;
 };
 
-namespace {
-// Makes the context's profiler current for the launches of one entry point.
-struct ProfScope {
-  moe::Profiler* prev;
-  explicit ProfScope(const moe_ctx* c) : prev(moe::tl_profiler) { moe::tl_profiler = c ? c->prof : nullptr; }
-  ~ProfScope() { moe::tl_profiler = prev; }
-};
-}  // namespace
+namespace moe {
+Profiler* ctx_profiler(const moe_ctx* ctx) { return ctx->prof; }
+}  // namespace moe
+using moe::ProfScope;
 
 namespace {
 
@@ -152,10 +147,6 @@ float router_gamma(int d, moe_dtype x_dtype, moe_dtype w_dtype) {
 // top-k certify almost every token without the fp64 recheck.
 constexpr int kCompensatedMaxT = 16;
 
-// Experts with at least this many tokens in a call take the tensor-core GEMM
-// path by default (moe_ctx_set_gemm_min_tokens changes it).
-constexpr int kDefaultGemmMinTokens = 2;
-
 // Bound coefficient of the compensated logits: |l32 - l_ref| <= K * sum|w x| +
 // 4u |l32| with K = (gamma_n^2 (1 + gamma_n) + gamma64_{d+1}) * 1.01, n = d + 32.
 float router_gamma_comp(int d) {
@@ -215,12 +206,6 @@ struct FfnWs {
   float* max_x;
   float* h;
   float* partial;
-  int32_t* hot;      // GEMM path (MXFP4, d and ff multiples of 256): expert list,
-  int32_t* hot_blk;  // its token-block prefix,
-  uint16_t* xs;      // the activations in slot order (f16, rescaled per token)
-  float* xscale;     // the per-slot scales of the activations and of h,
-  float* hscale;
-  uint8_t* row_ref;  // and each hot expert row's largest scale byte
   void* bs;          // block-scaled path workspace (MXFP4, d and ff multiples of 512)
 };
 FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
@@ -229,21 +214,9 @@ FfnWs carve_ffn(Carver& c, int T, int k, int d, int ff, int E, moe_quant q) {
   f.max_x = c.take<float>(T > 0 ? T : 1);
   f.h = c.take<float>((size_t)T * k * ff);
   f.partial = q == MOE_QUANT_RVQ3 ? c.take<float>(moe::rvq3_partial_floats(T, k, d, ff)) : nullptr;
-  f.hot = f.hot_blk = nullptr;
-  f.xs = nullptr;
-  f.xscale = f.hscale = nullptr;
-  f.row_ref = nullptr;
   f.bs = nullptr;
   if (q == MOE_QUANT_MXFP4 && moe::mxfp4_bs_supported(d, ff, E, MOE_BF16))
     f.bs = c.take<uint8_t>(moe::mxfp4_bs_ws_bytes(T, k, d, ff, kMaxSms));
-  if (q == MOE_QUANT_MXFP4 && moe::mxfp4_gemm_supported(d, ff, MOE_BF16)) {
-    f.hot = c.take<int32_t>((size_t)E + 1);
-    f.hot_blk = c.take<int32_t>((size_t)E + 1);
-    f.xs = c.take<uint16_t>((size_t)T * k * d > 0 ? (size_t)T * k * d : 1);
-    f.xscale = c.take<float>((size_t)T * k > 0 ? (size_t)T * k : 1);
-    f.hscale = c.take<float>((size_t)T * k > 0 ? (size_t)T * k : 1);
-    f.row_ref = c.take<uint8_t>((size_t)E * (2 * (size_t)ff + d));
-  }
   return f;
 }
 
@@ -270,40 +243,6 @@ moe::BsLaunch bs_launch(const moe::FfnArgs& f, const FfnWs& w) {
   b.ws = w.bs;
   b.err = f.err;
   return b;
-}
-
-// The GEMM-path split for one call: experts with at least ctx->gemm_min tokens
-// (an expert has at most T), when the shapes and the activation type allow it.
-moe::HotSplit gemm_split(const moe_ctx* ctx, const FfnWs& w, int T, int d, int ff, moe_dtype x_dtype) {
-  moe::HotSplit sp{0, nullptr, nullptr};
-  if (w.hot != nullptr && ctx->gemm_min > 0 && T >= ctx->gemm_min && moe::mxfp4_gemm_supported(d, ff, x_dtype))
-    sp = moe::HotSplit{ctx->gemm_min, w.hot, w.hot_blk};
-  return sp;
-}
-
-moe::GemmArgs gemm_args(const moe::FfnArgs& f, const FfnWs& w) {
-  moe::GemmArgs g;
-  std::memset(&g, 0, sizeof g);
-  g.records = f.records;
-  g.d = f.d;
-  g.ff = f.ff;
-  g.k = f.k;
-  g.T = f.T;
-  g.act = f.act;
-  g.x = f.x;
-  g.max_x = f.max_x;
-  g.offsets = f.offsets;
-  g.pair_ids = f.pair_ids;
-  g.hot = w.hot;
-  g.hot_blk = w.hot_blk;
-  g.xs = w.xs;
-  g.xscale = w.xscale;
-  g.hscale = w.hscale;
-  g.row_ref = w.row_ref;
-  g.h = f.h;
-  g.y_pairs = f.y_pairs;
-  g.err = f.err;
-  return g;
 }
 
 struct LayerWs {
@@ -396,9 +335,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
                                  L->E, L->k, L->n_shared, w.route, const_cast<int32_t*>(topk),
                                  const_cast<float*>(gates), ctx->err);
   const bool bs = L->quant == MOE_QUANT_MXFP4 && use_bs(ctx, w.ffn, T, L->d, L->ff, Es, x_dtype);
-  const moe::HotSplit split = L->quant == MOE_QUANT_MXFP4 && !bs ? gemm_split(ctx, w.ffn, T, L->d, L->ff, x_dtype)
-                                                                 : moe::HotSplit{0, nullptr, nullptr};
-  moe::BucketArgs ba{topk, T, ks, Es, counts, w.offsets, w.pairs, w.ffn.active, split, ctx->err};
+  moe::BucketArgs ba{topk, T, ks, Es, counts, w.offsets, w.pairs, w.ffn.active, ctx->err};
   if (T == 1) {  // one token: the top-k kernel buckets its pairs itself
     ra.fuse_bucket = 1;
     ra.bucket = ba;
@@ -416,10 +353,6 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
     st = cuda_status(moe::launch_mxfp4_bs(bs_launch(fa, w.ffn), ctx->num_sms, true, s));
   } else if (L->quant == MOE_QUANT_MXFP4) {
     fa.records = L->mxfp4.records;
-    if (split.hot != nullptr) {
-      st = cuda_status(moe::launch_mxfp4_gemm(gemm_args(fa, w.ffn), ctx->num_sms, true, s));
-      if (st != MOE_OK) return st;
-    }
     st = cuda_status(moe::launch_mxfp4_ffn(fa, ctx->num_sms, true, s));
   } else {
     fa.records = L->rvq3.records;
@@ -464,10 +397,9 @@ moe_status moe_ctx_create(moe_ctx** ctx, int device) {
     st = MOE_ERR_CUDA;
   } else {
     c->device = device;
-    c->gemm_min = kDefaultGemmMinTokens;
     c->mxfp4_kernel = MOE_MXFP4_AUTO;
     if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaMalloc(&c->err, 4 * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, 4 * sizeof(int)) != cudaSuccess) {
+        cudaMalloc(&c->err, 8 * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, 8 * sizeof(int)) != cudaSuccess) {
       if (c->err) cudaFree(c->err);
       std::free(c);
       c = nullptr;
@@ -492,16 +424,35 @@ void moe_ctx_destroy(moe_ctx* ctx) {
 
 int moe_ctx_num_sms(const moe_ctx* ctx) { return ctx ? ctx->num_sms : 0; }
 
-moe_status moe_ctx_set_gemm_min_tokens(moe_ctx* ctx, int min_tokens) {
-  if (ctx == nullptr || min_tokens < 0) return MOE_ERR_INVALID_ARG;
-  ctx->gemm_min = min_tokens;
-  return MOE_OK;
+moe_status moe_ctx_set_wait_limit_ns(moe_ctx* ctx, unsigned long long ns) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  if (ns != 0 && ns < 1000ull) ns = 1000ull;
+  const uint64_t v = ns;
+  return cudaMemcpy(ctx->err + 4, &v, sizeof v, cudaMemcpyHostToDevice) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int moe_ctx_gemm_min_tokens(const moe_ctx* ctx) { return ctx ? ctx->gemm_min : -1; }
+moe_status moe_ctx_wait_selftest(moe_ctx* ctx, cudaStream_t stream) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  ProfScope prof_scope(ctx);
+  return cuda_status(moe::launch_wait_selftest(ctx->err, stream));
+}
+
+moe_status moe_rvq3_repack(moe_ctx* ctx, const uint8_t* const* src, uint8_t* const* dst, int n, int d, int ff,
+                           cudaStream_t stream) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  ProfScope prof_scope(ctx);
+  if (n < 0) return MOE_ERR_INVALID_ARG;
+  if (!dims_ok(d, ff)) return d > 0 && ff > 0 && d % 32 == 0 && ff % 32 == 0 ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (src == nullptr || dst == nullptr) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_rvq3_repack(src, dst, n, d, ff, ctx->err, ctx->num_sms, stream));
+}
 
 moe_status moe_ctx_set_mxfp4_kernel(moe_ctx* ctx, int kernel) {
-  if (ctx == nullptr || (kernel != MOE_MXFP4_BLOCK_SCALED && kernel != MOE_MXFP4_GEMV_GEMM && kernel != MOE_MXFP4_AUTO))
+  if (ctx == nullptr || (kernel != MOE_MXFP4_BLOCK_SCALED && kernel != MOE_MXFP4_GEMV && kernel != MOE_MXFP4_AUTO))
     return MOE_ERR_INVALID_ARG;
   ctx->mxfp4_kernel = kernel;
   return MOE_OK;
@@ -696,8 +647,7 @@ moe_status moe_bucket_tokens(moe_ctx* ctx, const int32_t* topk_idx, int T, int k
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  moe::BucketArgs ba{topk_idx, T, k, E, counts, offsets, pair_ids, static_cast<int32_t*>(ws),
-                     moe::HotSplit{0, nullptr, nullptr}, ctx->err};
+  moe::BucketArgs ba{topk_idx, T, k, E, counts, offsets, pair_ids, static_cast<int32_t*>(ws), ctx->err};
   return cuda_status(moe::launch_bucket(ba, false, stream));
 }
 
@@ -757,22 +707,13 @@ moe_status moe_expert_ffn_mxfp4(moe_ctx* ctx, const void* x, moe_dtype x_dtype, 
                                     MOE_QUANT_MXFP4, offsets, pair_ids, y_pairs, ws, ws_bytes, &a, &w);
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
-  if (use_bs(ctx, w, T, experts->d, experts->ff, experts->E, x_dtype)) {
-    st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active),
-                                                     moe::HotSplit{0, nullptr, nullptr}, false, stream));
-    if (st != MOE_OK) return st;
-    return cuda_status(moe::launch_mxfp4_bs(bs_launch(a, w), ctx->num_sms, true, stream));
-  }
-  const moe::HotSplit split = gemm_split(ctx, w, T, experts->d, experts->ff, x_dtype);
-  st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), split, false,
-                                                   stream));
+  st = cuda_status(
+      moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), false, stream));
   if (st != MOE_OK) return st;
+  if (use_bs(ctx, w, T, experts->d, experts->ff, experts->E, x_dtype))
+    return cuda_status(moe::launch_mxfp4_bs(bs_launch(a, w), ctx->num_sms, true, stream));
   st = cuda_status(moe::launch_token_absmax(x, x_dtype, T, experts->d, const_cast<float*>(a.max_x), true, stream));
   if (st != MOE_OK) return st;
-  if (split.hot != nullptr) {
-    st = cuda_status(moe::launch_mxfp4_gemm(gemm_args(a, w), ctx->num_sms, true, stream));
-    if (st != MOE_OK) return st;
-  }
   return cuda_status(moe::launch_mxfp4_ffn(a, ctx->num_sms, true, stream));
 }
 
@@ -792,8 +733,8 @@ moe_status moe_expert_ffn_rvq3(moe_ctx* ctx, const void* x, moe_dtype x_dtype, i
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
   for (int m = 0; m < 3; ++m) a.cb[m] = experts->codebooks[m];
-  st = cuda_status(moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active),
-                                                   moe::HotSplit{0, nullptr, nullptr}, false, stream));
+  st = cuda_status(
+      moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), false, stream));
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_rvq3_ffn(a, ctx->num_sms, true, stream));
 }
@@ -832,6 +773,13 @@ moe_status moe_layer_forward(moe_ctx* ctx, const moe_layer* L, const void* x, mo
 
 moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers, const void* x, moe_dtype x_dtype,
                              int T, void* out, moe_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return moe_stack_forward_ex(ctx, layers, n_layers, x, x_dtype, T, out, out_dtype, nullptr, nullptr, nullptr, ws,
+                              ws_bytes, stream);
+}
+
+moe_status moe_stack_forward_ex(moe_ctx* ctx, const moe_layer* layers, int n_layers, const void* x, moe_dtype x_dtype,
+                                int T, void* out, moe_dtype out_dtype, int32_t* topk_trace, float* gates_trace,
+                                int32_t* counts_trace, void* ws, size_t ws_bytes, cudaStream_t stream) {
   moe_status st = ctx_ok(ctx);
   if (st != MOE_OK) return st;
   ProfScope prof_scope(ctx);
@@ -856,6 +804,7 @@ moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers
   char* base = static_cast<char*>(ws);
   uint16_t* buf[2] = {reinterpret_cast<uint16_t*>(base + layer_ws),
                       reinterpret_cast<uint16_t*>(base + layer_ws + align_up((size_t)T * layers[0].d * 2))};
+  size_t pair_off = 0, exp_off = 0;  // where layer l's trace starts
   for (int l = 0; l < n_layers; ++l) {
     const void* in = l == 0 ? x : buf[(l - 1) & 1];
     const moe_dtype in_dt = l == 0 ? x_dtype : MOE_BF16;
@@ -863,9 +812,12 @@ moe_status moe_stack_forward(moe_ctx* ctx, const moe_layer* layers, int n_layers
     void* o = last ? out : buf[l & 1];
     Carver c(ws);
     LayerWs w = carve_layer(c, &layers[l], T);
-    st = layer_forward_impl(ctx, &layers[l], in, in_dt, T, o, last ? out_dtype : MOE_BF16, nullptr, nullptr, nullptr,
-                            w, stream);
+    st = layer_forward_impl(ctx, &layers[l], in, in_dt, T, o, last ? out_dtype : MOE_BF16,
+                            topk_trace ? topk_trace + pair_off : nullptr, gates_trace ? gates_trace + pair_off : nullptr,
+                            counts_trace ? counts_trace + exp_off : nullptr, w, stream);
     if (st != MOE_OK) return st;
+    pair_off += (size_t)T * layer_pairs_per_token(&layers[l]);
+    exp_off += (size_t)layer_experts(&layers[l]);
   }
   return MOE_OK;
 }

@@ -18,19 +18,18 @@ __global__ void bucket_kernel(BucketArgs a, int nw) {
   bucket_block(a, nw, bsm);
 }
 
-// Expert lists from offsets alone (used when the expert FFN is called on its
-// own): active[0] = count, active[1..] = GEMV-path experts with a non-empty
-// bucket; the GEMM-path experts go to split.hot.
-__global__ void active_kernel(const int32_t* offsets, int E, int32_t* active, HotSplit split) {
+// Expert list from offsets alone (used when the expert FFN is called on its
+// own): active[0] = count, active[1..] = the experts with a non-empty bucket.
+__global__ void active_kernel(const int32_t* offsets, int E, int32_t* active) {
   __shared__ int scratch[32];
   pdl_wait();
-  bucket_detail::SplitCarry sc;
+  int n_active = 0;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
     const int cnt = e < E ? offsets[e + 1] - offsets[e] : 0;
-    bucket_detail::split_step(e, cnt, active, split, scratch, sc);
+    bucket_detail::active_step(e, cnt, active, scratch, n_active);
   }
-  if (threadIdx.x == 0) bucket_detail::split_finish(active, split, sc);
+  if (threadIdx.x == 0) active[0] = n_active;
 }
 
 }  // namespace
@@ -49,9 +48,8 @@ cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s) {
   return launch("bucket", bucket_kernel, dim3(1), dim3(nthreads), smem, s, pdl, a, nw);
 }
 
-cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, const HotSplit& split, bool pdl,
-                                       cudaStream_t s) {
-  return launch("active_list", active_kernel, dim3(1), dim3(256), 0, s, pdl, offsets, E, active, split);
+cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s) {
+  return launch("active_list", active_kernel, dim3(1), dim3(256), 0, s, pdl, offsets, E, active);
 }
 
 }  // namespace moe

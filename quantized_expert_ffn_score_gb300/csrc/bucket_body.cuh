@@ -50,40 +50,15 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   return base + x - v;
 }
 
-// Running totals of the expert lists across chunks of the expert range.
-struct SplitCarry {
-  int cold = 0, hot = 0, blk = 0;
-};
-
 // One chunk of experts (one per thread, cnt = bucket size, 0 past E): appends
-// the GEMV-path experts to active[] and the GEMM-path experts to hot[] with
-// their token-block prefix.  Every thread of the block calls it.
-__device__ __forceinline__ void split_step(int e, int cnt, int32_t* active, const HotSplit& sp, int* scratch, SplitCarry& c) {
-  const bool is_hot = sp.hot != nullptr && sp.gemm_min > 0 && cnt >= sp.gemm_min;
-  const int f_cold = (cnt > 0 && !is_hot) ? 1 : 0;
-  int t_cold, t_hot, t_blk;
-  const int pos_cold = block_exclusive_scan(f_cold, scratch, &t_cold) + c.cold;
-  if (f_cold) active[1 + pos_cold] = e;
-  if (sp.hot != nullptr) {
-    const int nblk = is_hot ? (cnt + 127) / 128 : 0;
-    const int pos_hot = block_exclusive_scan(is_hot ? 1 : 0, scratch, &t_hot) + c.hot;
-    const int pos_blk = block_exclusive_scan(nblk, scratch, &t_blk) + c.blk;
-    if (is_hot) {
-      sp.hot[1 + pos_hot] = e;
-      sp.hot_blk[pos_hot] = pos_blk;
-    }
-    c.hot += t_hot;
-    c.blk += t_blk;
-  }
-  c.cold += t_cold;
-}
-
-__device__ __forceinline__ void split_finish(int32_t* active, const HotSplit& sp, const SplitCarry& c) {
-  active[0] = c.cold;
-  if (sp.hot != nullptr) {
-    sp.hot[0] = c.hot;
-    sp.hot_blk[c.hot] = c.blk;
-  }
+// the experts with a non-empty bucket to active[] in ascending order; `carry`
+// holds the running count across chunks.  Every thread of the block calls it.
+__device__ __forceinline__ void active_step(int e, int cnt, int32_t* active, int* scratch, int& carry) {
+  const int f = cnt > 0 ? 1 : 0;
+  int total;
+  const int pos = block_exclusive_scan(f, scratch, &total) + carry;
+  if (f) active[1 + pos] = e;
+  carry += total;
 }
 
 }  // namespace bucket_detail
@@ -116,9 +91,8 @@ __device__ __forceinline__ void bucket_block(const BucketArgs& a, int nw, int* b
   }
   __syncthreads();
   // 2. per expert: counts and per-warp bases; block scans over experts give
-  //    the offsets and the expert lists (GEMV-path and GEMM-path experts)
-  int carry = 0;
-  bucket_detail::SplitCarry sc;
+  //    the offsets and the list of experts with tokens
+  int carry = 0, n_active = 0;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
     int cnt = 0;
@@ -131,7 +105,7 @@ __device__ __forceinline__ void bucket_block(const BucketArgs& a, int nw, int* b
     }
     int total;
     const int off = bucket_detail::block_exclusive_scan(cnt, scan_scratch, &total) + carry;
-    bucket_detail::split_step(e, e < E ? cnt : 0, a.active, a.split, scan_scratch, sc);
+    bucket_detail::active_step(e, e < E ? cnt : 0, a.active, scan_scratch, n_active);
     if (e < E) {
       a.counts[e] = cnt;
       a.offsets[e] = off;
@@ -141,7 +115,7 @@ __device__ __forceinline__ void bucket_block(const BucketArgs& a, int nw, int* b
   }
   if (threadIdx.x == 0) {
     a.offsets[E] = carry;
-    bucket_detail::split_finish(a.active, a.split, sc);
+    a.active[0] = n_active;
   }
   __syncthreads();
   // 3. stable scatter, walking each warp's range in ascending p
@@ -166,8 +140,7 @@ __device__ __forceinline__ void bucket_block(const BucketArgs& a, int nw, int* b
 // The same result for a single token (T = 1, k <= 32 distinct experts): no
 // histogram or scan.  With the k selected ids sel[j], an expert's offset is the
 // number of selected ids below it, pair j lands at the rank of sel[j], and
-// every selected expert has one token (GEMM path only when gemm_min <= 1).
-// Every thread of the block calls it.
+// every selected expert has one token.  Every thread of the block calls it.
 __device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_smem, bool preloaded = false) {
   const int E = a.E, k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -180,7 +153,6 @@ __device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_s
     sel_smem[threadIdx.x] = e;
   }
   __syncthreads();
-  const bool hot = a.split.hot != nullptr && a.split.gemm_min > 0 && a.split.gemm_min <= 1;
   if (warp == 0) {
     const int e = lane < k ? sel_smem[lane] : 0x7fffffff;
     int rank = 0, nvalid = 0;
@@ -191,20 +163,9 @@ __device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_s
     }
     if (lane < k && e < E) {
       a.pair_ids[rank] = lane;
-      if (hot) {
-        a.split.hot[1 + rank] = e;
-        a.split.hot_blk[rank] = rank;
-      } else {
-        a.active[1 + rank] = e;
-      }
+      a.active[1 + rank] = e;
     }
-    if (lane == 0) {
-      a.active[0] = hot ? 0 : nvalid;
-      if (a.split.hot != nullptr) {
-        a.split.hot[0] = hot ? nvalid : 0;
-        a.split.hot_blk[hot ? nvalid : 0] = hot ? nvalid : 0;
-      }
-    }
+    if (lane == 0) a.active[0] = nvalid;
   }
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     int below = 0, is_sel = 0;

@@ -63,6 +63,7 @@ moe_status moe_expert_ffn_mxfp4_static(moe_ctx* ctx, const void* x, moe_dtype x_
       moe::check_expert_ffn_call(ctx, x, x_dtype, T, k, d, ff, E, act, offsets, pair_ids, y_pairs);
   if (st != MOE_OK || T == 0) return st;
   if (scratch_bytes(T, k, ff, E) > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
+  moe::ProfScope prof_scope(ctx);  // the launches below show in the context's per-launch profile
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return MOE_ERR_CUDA;
   void* base = nullptr;
@@ -95,9 +96,7 @@ moe_status moe_expert_ffn_mxfp4_static(moe_ctx* ctx, const void* x, moe_dtype x_
   a.h = h;
   a.y_pairs = y_pairs;
   a.err = moe::ctx_error_word(ctx);
-  if (moe::launch_active_from_offsets(offsets, E, active, moe::HotSplit{0, nullptr, nullptr}, false, stream) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (moe::launch_active_from_offsets(offsets, E, active, false, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_token_absmax(x, x_dtype, T, d, max_x, true, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (moe::launch_mxfp4_ffn(a, moe_ctx_num_sms(ctx), true, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;

@@ -66,18 +66,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false (and records MOE_ERR_TIMEOUT) if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// err[4..5] of the context's error word hold the limit of pipeline waits in
+// ns, set by moe_ctx_set_wait_limit_ns (0: kWaitLimitNs).
+__device__ __forceinline__ uint64_t wait_limit_ns(const int* err) {
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(err + 4);
+  return v != 0 ? v : kWaitLimitNs;
+}
+
+// Spins on the phase with the given parity for at most limit_ns.  Returns
+// false (and records MOE_ERR_TIMEOUT) if it gave up.
+static __device__ __noinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err, uint64_t limit_ns) {
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       dev_error(err, MOE_ERR_TIMEOUT, -1);
       return false;
     }
   }
+}
+
+// A pipeline wait: bounded by the context's wait limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_for(bar, parity, err, wait_limit_ns(err));
+}
+
+// A drain wait (copies or MMAs of this CTA still in flight before it leaves):
+// always the fixed kWaitLimitNs, so that a short pipeline limit never lets a
+// CTA exit while its copies can still write its shared memory.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
 
 // 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
@@ -135,17 +155,6 @@ __device__ __forceinline__ float load_act(const void* p, int dtype, size_t i) {
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  All pointers are device pointers.
 
-
-
-// Split of the experts with tokens: those with at least `gemm_min` tokens go
-// to the tensor-core GEMM path (hot list), the others to the GEMV path
-// (active list).  gemm_min <= 0 or hot == nullptr: every expert is GEMV.
-struct HotSplit {
-  int gemm_min;
-  int32_t* hot;      // [E+1]: hot[0] = n_hot, hot[1..] = experts in ascending order
-  int32_t* hot_blk;  // [E+1]: exclusive prefix over hot experts of ceil(N_e / 128); hot_blk[n_hot] = total
-};
-
 struct BucketArgs {
   const int32_t* topk_idx;
   int T, k, E;
@@ -153,7 +162,6 @@ struct BucketArgs {
   int32_t* offsets;
   int32_t* pair_ids;
   int32_t* active;  // [E+1] workspace: active[0] = n_active, active[1..] = experts in ascending order
-  HotSplit split;
   int* err;
 };
 cudaError_t launch_bucket(const BucketArgs& a, bool pdl, cudaStream_t s);
@@ -198,8 +206,7 @@ struct FfnArgs {
   float* partial;         // RVQ3 only: K-slice partial sums (workspace)
   int* err;
 };
-cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, const HotSplit& split, bool pdl,
-                                       cudaStream_t s);
+cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s);
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 // The FFN on the block-scaled tensor-core MMA (mxfp4_bs.cu): every expert
 // with tokens (active[] lists them all), bf16 activations, d and ff multiples
@@ -226,28 +233,6 @@ cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float*
 cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 size_t rvq3_partial_floats(int T, int k, int d, int ff);
 
-// Tensor-core path for the hot experts (mxfp4_gemm.cu): gathers their
-// activations into slot order, then gate/up and down grouped GEMMs.
-struct GemmArgs {
-  const uint8_t* const* records;
-  int d, ff, k, T, act;
-  const void* x;        // [T][d] bf16
-  const float* max_x;   // [T] max_i |x_t[i]|
-  const int32_t* offsets;
-  const int32_t* pair_ids;
-  const int32_t* hot;
-  const int32_t* hot_blk;
-  uint16_t* xs;         // [T*k][d] f16 workspace, slot order (hot slots): x * 2^-s_t
-  float* xscale;        // [T*k] 2^s_t per hot slot
-  float* h;             // [T*k][ff] workspace; a hot slot's row holds h (fp32), then f16 hi[ff] | lo[ff] of h * 2^-s
-  float* hscale;        // [T*k] that 2^s per hot slot
-  uint8_t* row_ref;     // [E][2 ff + d] workspace: largest scale byte per row of the hot experts' Wg, Wu, Wd
-  float* y_pairs;       // [T*k][d] by pair id
-  int* err;
-};
-bool mxfp4_gemm_supported(int d, int ff, int x_dtype);
-cudaError_t launch_mxfp4_gemm(const GemmArgs& a, int num_sms, bool pdl, cudaStream_t s);
-
 struct CombineArgs {
   const void* x;
   int x_dtype;
@@ -265,6 +250,14 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 int records_crc_units(size_t record_bytes);
 cudaError_t launch_records_check(const uint8_t* const* records, int n, size_t record_bytes, const uint32_t* expected,
                                  uint32_t* crc_out, uint32_t* unit_ws, int* err, int num_sms, cudaStream_t s);
+
+// A wait that nothing completes, for testing the timeout path (selftest.cu).
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
+
+// Row-major to position-major RVQ3 records (rvq3_repack.cu): n records of
+// moe_rvq3_record_bytes(d, ff) bytes; src[i] and dst[i] device pointers.
+cudaError_t launch_rvq3_repack(const uint8_t* const* src, uint8_t* const* dst, int n, int d, int ff, int* err,
+                               int num_sms, cudaStream_t s);
 
 // ABI-layer helpers (abi.cu) shared with other translation units' entry points.
 moe_status check_expert_ffn_call(const moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int k, int d, int ff,
@@ -286,6 +279,16 @@ struct Profiler;
 extern thread_local Profiler* tl_profiler;
 void profiler_begin(Profiler* p, const char* name, cudaStream_t s);
 void profiler_end(Profiler* p, cudaStream_t s);
+Profiler* ctx_profiler(const moe_ctx* ctx);
+
+// Makes the context's profiler current for the launches of one entry point.
+struct ProfScope {
+  Profiler* prev;
+  explicit ProfScope(const moe_ctx* c) : prev(tl_profiler) { tl_profiler = c ? ctx_profiler(c) : nullptr; }
+  ~ProfScope() { tl_profiler = prev; }
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+};
 
 // Launch helper: optional programmatic dependent launch; `name` labels the
 // launch for the profiler.

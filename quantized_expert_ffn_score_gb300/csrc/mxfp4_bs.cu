@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0)  // never leave with copies in flight
       for (int j = (it > G.stages ? it - G.stages : 0); j < it; ++j)
-        mbar_wait(&full[j % G.stages], (j / G.stages) & 1, a.err);
+        mbar_wait_drain(&full[j % G.stages], (j / G.stages) & 1, a.err);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // (one thread: ring positions and descriptors advance incrementally, so
@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc::mma_commit(done);  // every MMA issued above has completed before teardown
-      mbar_wait(done, 0, a.err);
+      mbar_wait_drain(done, 0, a.err);
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ scale factors into TMEM

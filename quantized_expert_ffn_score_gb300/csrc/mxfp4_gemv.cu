@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(16 * 32, 1) mxfp4_gemv_kernel(const FfnArgs a,
       }
       // never leave the CTA with copies in flight: wait for the last fills
       for (int j = (it > g.stages ? it - g.stages : 0); j < it; ++j)
-        mbar_wait(&full[j % g.stages], (j / g.stages) & 1, a.err);
+        mbar_wait_drain(&full[j % g.stages], (j / g.stages) & 1, a.err);
     }
     return;
   }

@@ -294,7 +294,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
     // never leave with copies in flight
     if (lane == 0)
       for (int j = (it > g.stages ? it - g.stages : 0); j < it; ++j)
-        mbar_wait(&full[j % g.stages], (j / g.stages) & 1, a.err);
+        mbar_wait_drain(&full[j % g.stages], (j / g.stages) & 1, a.err);
     return;
   }
 

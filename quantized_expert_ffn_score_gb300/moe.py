@@ -21,19 +21,19 @@ MOE_F32, MOE_BF16 = 0, 1
 ACT = {"swiglu": 0, "situ": 1}
 QUANT = {"mxfp4": 0, "rvq3": 1}
 BIAS_MODE = {"logit": 0, "select": 1}
-MXFP4_KERNEL = {"block_scaled": 0, "gemv_gemm": 1, "auto": 2}
+MXFP4_KERNEL = {"block_scaled": 0, "gemv": 1, "auto": 2}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy", "moe_ctx_check", "moe_ctx_num_sms",
-           "moe_ctx_set_gemm_min_tokens", "moe_ctx_gemm_min_tokens",
            "moe_ctx_set_mxfp4_kernel", "moe_ctx_mxfp4_kernel",
            "moe_ctx_profile", "moe_ctx_profile_read", "moe_ctx_stats",
            "moe_mxfp4_record_bytes", "moe_rvq3_record_bytes", "moe_route_topk_ws_bytes", "moe_bucket_tokens_ws_bytes",
            "moe_expert_ffn_ws_bytes", "moe_layer_forward_ws_bytes", "moe_stack_forward_ws_bytes", "moe_route_topk",
            "moe_route_topk_ex",
            "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
-           "moe_stack_forward", "moe_expert_ffn_mxfp4_static", "moe_expert_ffn_mxfp4_static_max_bytes",
-           "moe_records_check_ws_bytes", "moe_records_check"]
+           "moe_stack_forward", "moe_stack_forward_ex", "moe_expert_ffn_mxfp4_static",
+           "moe_expert_ffn_mxfp4_static_max_bytes", "moe_records_check_ws_bytes", "moe_records_check",
+           "moe_ctx_set_wait_limit_ns", "moe_ctx_wait_selftest", "moe_rvq3_repack"]
 
 
 class MoeError(RuntimeError):
@@ -110,13 +110,17 @@ def lib():
         L.moe_layer_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), vp, i32, i32, vp, i32, vp, vp, vp, vp, sz,
                                         vp]
         L.moe_stack_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), i32, vp, i32, i32, vp, i32, vp, sz, vp]
+        L.moe_stack_forward_ex.argtypes = [vp, ctypes.POINTER(LayerStruct), i32, vp, i32, i32, vp, i32, vp, vp, vp, vp,
+                                           sz, vp]
+        L.moe_ctx_set_wait_limit_ns.argtypes = [vp, ctypes.c_ulonglong]
+        L.moe_ctx_wait_selftest.argtypes = [vp, vp]
+        L.moe_rvq3_repack.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         for f in ("moe_ctx_create", "moe_ctx_check", "moe_route_topk", "moe_route_topk_ex", "moe_bucket_tokens",
                   "moe_expert_ffn_mxfp4",
-                  "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward", "moe_stack_forward"):
+                  "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward", "moe_stack_forward", "moe_stack_forward_ex",
+                  "moe_ctx_set_wait_limit_ns", "moe_ctx_wait_selftest", "moe_rvq3_repack"):
             getattr(L, f).restype = i32
         L.moe_ctx_num_sms.restype = i32
-        L.moe_ctx_set_gemm_min_tokens.argtypes, L.moe_ctx_set_gemm_min_tokens.restype = [vp, i32], i32
-        L.moe_ctx_gemm_min_tokens.argtypes, L.moe_ctx_gemm_min_tokens.restype = [vp], i32
         L.moe_ctx_set_mxfp4_kernel.argtypes, L.moe_ctx_set_mxfp4_kernel.restype = [vp, i32], i32
         L.moe_ctx_mxfp4_kernel.argtypes, L.moe_ctx_mxfp4_kernel.restype = [vp], i32
         _lib = L
@@ -177,23 +181,23 @@ class Context:
         return a.value, b.value
 
     @property
-    def gemm_min_tokens(self):
-        """Experts with at least this many tokens take the tensor-core GEMM path (0: never)."""
-        return lib().moe_ctx_gemm_min_tokens(self.handle)
-
-    @gemm_min_tokens.setter
-    def gemm_min_tokens(self, n):
-        _check(lib().moe_ctx_set_gemm_min_tokens(self.handle, int(n)), "moe_ctx_set_gemm_min_tokens")
-
-    @property
     def mxfp4_kernel(self):
-        """'auto' (default), 'block_scaled' (tensor-core MMA on the stored codes and scales) or 'gemv_gemm'."""
+        """'auto' (default), 'block_scaled' (tensor-core MMA on the stored codes and scales) or 'gemv'."""
         v = lib().moe_ctx_mxfp4_kernel(self.handle)
         return {k: n for n, k in MXFP4_KERNEL.items()}.get(v, v)
 
     @mxfp4_kernel.setter
     def mxfp4_kernel(self, name):
         _check(lib().moe_ctx_set_mxfp4_kernel(self.handle, MXFP4_KERNEL[name]), "moe_ctx_set_mxfp4_kernel")
+
+    def set_wait_limit_ns(self, ns):
+        """Limit of the kernels' pipeline waits in ns (0: the default, 2 s)."""
+        _check(lib().moe_ctx_set_wait_limit_ns(self.handle, int(ns)), "moe_ctx_set_wait_limit_ns")
+
+    def wait_selftest(self, stream=None):
+        """Launches a wait that nothing completes; it times out after the wait
+        limit and the next check() raises MOE_ERR_TIMEOUT."""
+        _check(lib().moe_ctx_wait_selftest(self.handle, _stream(stream)), "moe_ctx_wait_selftest")
 
     def profile(self, capacity):
         """Turns per-launch event timing on (capacity launches between reads) or off (0)."""
@@ -376,3 +380,21 @@ def moe_stack_forward(ctx, layers, x, out, ws, stream=None):
     arr = (LayerStruct * len(layers))(*[l.struct for l in layers])
     _check(lib().moe_stack_forward(ctx.handle, arr, len(layers), _ptr(x), _dt(x), T, _ptr(out), _dt(out), _ptr(ws),
                                    ws.numel(), _stream(stream)), "moe_stack_forward")
+
+
+def moe_stack_forward_ex(ctx, layers, x, out, ws, topk_trace=None, gates_trace=None, counts_trace=None, stream=None):
+    """moe_stack_forward that also writes every layer's routing (device
+    tensors, layer after layer: [n_layers][T][k + n_shared] and
+    [n_layers][E + n_shared] when all layers have one shape)."""
+    T = x.shape[0]
+    arr = (LayerStruct * len(layers))(*[l.struct for l in layers])
+    _check(lib().moe_stack_forward_ex(ctx.handle, arr, len(layers), _ptr(x), _dt(x), T, _ptr(out), _dt(out),
+                                      _ptr(topk_trace), _ptr(gates_trace), _ptr(counts_trace), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "moe_stack_forward_ex")
+
+
+def moe_rvq3_repack(ctx, src_records, dst_records, n, d, ff, stream=None):
+    """Row-major RVQ3 records -> position-major (src_records, dst_records:
+    device int64 tensors of n record pointers)."""
+    _check(lib().moe_rvq3_repack(ctx.handle, _ptr(src_records), _ptr(dst_records), n, d, ff, _stream(stream)),
+           "moe_rvq3_repack")

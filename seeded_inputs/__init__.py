@@ -141,6 +141,21 @@ def layer_record(r: "LayerRecipe", expert):
     return rvq3_record(r.seed, expert, r.d, r.ff)
 
 
+def layer_records(r: "LayerRecipe", experts, n_total=None, nthreads=None):
+    """A list of n_total (default E + n_shared) entries: the record of each
+    expert in `experts`, None elsewhere; the records are generated on
+    `nthreads` host threads (the C filler runs without the GIL)."""
+    import concurrent.futures as cf
+    n_total = r.E + r.n_shared if n_total is None else n_total
+    want = sorted(set(int(e) for e in experts))
+    out = [None] * n_total
+    nthreads = nthreads or min(32, os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=max(1, nthreads)) as ex:
+        for e, rec in zip(want, ex.map(lambda e: layer_record(r, e), want)):
+            out[e] = rec
+    return out
+
+
 def record_size(r: "LayerRecipe"):
     return mxfp4_record_size(r.d, r.ff) if r.quant == "mxfp4" else rvq3_record_size(r.d, r.ff)
 

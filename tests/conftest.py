@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Writes the parity margins the GPU tests recorded (tests/gpu_util.py) to
+    the file named by MOE_PARITY_MARGINS, when set."""
+    path = os.environ.get("MOE_PARITY_MARGINS")
+    if not path:
+        return
+    mod = sys.modules.get("tests.gpu_util")
+    margins = getattr(mod, "MARGINS", None) if mod is not None else None
+    if not margins:
+        return
+    import json
+    os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+    with open(path, "w") as f:
+        json.dump(margins, f, indent=1, sort_keys=True)

@@ -15,6 +15,16 @@ import seeded_inputs as si
 TOL = 2e-3
 NTHREADS = max(1, min(32, os.cpu_count() or 1))
 
+# Achieved parity margins of this session: case name -> (max|err| / RMS,
+# max|err|, RMS, tokens compared).  conftest.py writes them to the JSON file
+# named by MOE_PARITY_MARGINS at the end of the session.
+MARGINS = {}
+
+
+def record_margin(name, err, rms, tokens):
+    MARGINS[name] = {"max_err_over_rms": err / rms if rms > 0 else float("inf"), "max_abs_err": err, "rms": rms,
+                     "tokens_compared": int(tokens)}
+
 
 def rms_err(y_gpu, y_ref):
     rms = float(np.sqrt(np.mean(np.asarray(y_ref, dtype=np.float64) ** 2)))
@@ -50,7 +60,7 @@ def oracle_layer(r, x_host, tokens=None, nthreads=NTHREADS, records=None):
         mask[sel] = 1
     if records is None:
         needed = set(int(e) for e in idx[sel].reshape(-1)) | set(range(r.E, r.E + r.n_shared))
-        records = [si.layer_record(r, e) if e in needed else None for e in range(r.E + r.n_shared)]
+        records = si.layer_records(r, needed, nthreads=nthreads)
     cbs = None
     if r.quant == "rvq3":
         cb = si.layer_codebooks(r)
@@ -118,5 +128,7 @@ def full_check(moe, ctx, r, tokens=None):
     np.testing.assert_array_equal(counts[:r.E], np.bincount(idx.reshape(-1), minlength=r.E))
     sel = np.arange(r.T) if tokens is None else np.asarray(tokens)
     delta = out[sel].astype(np.float64) - x_host_f64(xh)[sel]
+    err, rms = rms_err(delta, y[sel])
+    record_margin(r.name, err, rms, len(sel))
     rel = assert_rms_close(delta, y[sel], what=r.name)
     return rel, counts

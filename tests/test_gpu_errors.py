@@ -2,11 +2,14 @@
 device generator against the host generator.  Nothing here faults a GPU: a
 missing expert is a NULL entry the kernel checks, a bad expert index is a value
 the bucketing kernel range-checks."""
+import time
+
 import numpy as np
 import pytest
 import torch
 
 import seeded_inputs as si
+from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
@@ -186,3 +189,34 @@ def test_zero_gate_experts_with_nan_records_contribute_nothing(moe, ctx):
     recs = [si.layer_record(r, e) for e in range(r.E)]
     _, _, y, _ = oracle.layer_forward(xh, si.layer_router_w(r), bias.cpu().numpy(), r.d, r.ff, r.E, r.k, recs)
     gu.assert_rms_close(out2.cpu().numpy().astype(np.float64) - xh, y)
+
+
+def test_wait_that_runs_out_is_reported_and_the_context_stays_usable(moe):
+    ctx = moe.Context(0)
+    try:
+        ctx.set_wait_limit_ns(2_000_000)  # 2 ms
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ctx.wait_selftest()  # a barrier nothing completes
+        with pytest.raises(moe.MoeError) as ei:
+            ctx.check()
+        elapsed = time.perf_counter() - t0
+        assert ei.value.name == "MOE_ERR_TIMEOUT" and ei.value.detail == -1
+        assert elapsed < 1.0, f"the 2 ms limit was not applied ({elapsed:.3f} s)"
+        ctx.check()  # the error word was cleared
+        # the same context still runs the layer, with the short limit in force
+        gu.full_check(moe, ctx, si.get_workload("tiny"))
+        gu.full_check(moe, ctx, si.LayerRecipe("mid_wait_limit", d=1024, ff=576, E=40, k=6, T=37, seed=11,
+                                               scale_lo=118, scale_hi=121))
+        # 0 restores the default limit of 2 s
+        ctx.set_wait_limit_ns(0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ctx.wait_selftest()
+        with pytest.raises(moe.MoeError) as ei:
+            ctx.check()
+        elapsed = time.perf_counter() - t0
+        assert ei.value.name == "MOE_ERR_TIMEOUT" and 1.9 <= elapsed < 10.0
+        ctx.check()
+    finally:
+        ctx.close()

@@ -96,9 +96,10 @@ def test_k3_mxfp4_decode_shared2(lib, ctx):
 
 
 @pytest.mark.slow
-def test_k3_mxfp4_prefill_shared2_e64_sampled(lib, ctx):
-    # 40 tokens: routing and counts of all tokens, outputs of a sample
-    gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_prefill_shared2_e64"), tokens=[0, 7, 19, 39])
+def test_k3_mxfp4_prefill_shared2_e64(lib, ctx):
+    # 40 tokens over 64 experts plus the 2 shared ones (40 tokens each): every
+    # token's routing, counts and output
+    gu.full_check(lib, ctx, si.get_workload("k3_mxfp4_prefill_shared2_e64"))
 
 
 @pytest.mark.slow
@@ -113,13 +114,18 @@ def test_k3_rvq3_decode_b1(lib, ctx):
 
 @pytest.mark.slow
 def test_k3_rvq3_decode_b8(lib, ctx):
-    gu.full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b8"), tokens=[0, 3, 7])
+    gu.full_check(lib, ctx, si.get_workload("k3_rvq3_decode_b8"))
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["k3_mxfp4_prefill_zipf", "k3_mxfp4_prefill_uniform"])
-def test_k3_prefill_routing_all_tokens_outputs_sampled(lib, ctx, name):
-    gu.full_check(lib, ctx, si.get_workload(name), tokens=[0, 201, 511])
+def test_k3_prefill_all_tokens(lib, ctx, name):
+    # 512 tokens, 8,192 pairs: every token's routing, counts and output against
+    # the oracle (Zipf: hot buckets of hundreds of tokens in several 48/40-token
+    # n-tiles with ragged tails; uniform: ~9 tokens on each of ~896 experts)
+    _, counts = gu.full_check(lib, ctx, si.get_workload(name))
+    if name.endswith("zipf"):
+        assert counts.max() > 3 * 48 and np.any((counts > 48) & (counts % 48 != 0))
 
 
 def test_route_topk_and_bucket_standalone_match_oracle(lib, ctx):

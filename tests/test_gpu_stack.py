@@ -12,7 +12,8 @@ the input difference can cause (Cauchy-Schwarz: |dl_e| <= ||W_e|| ||dx||);
 that token is then no longer compared.  Layer 0 (identical inputs) is held to
 the parity tolerance; later layers' deviations are reported (and guarded
 against gross errors only), since the two chains' inputs legitimately differ.
-Each layer's own parity at full size is the first test."""
+Each layer's own parity at full size, on all 64 tokens, is the first test; the
+stack call's routing trace must equal the layer-by-layer routing."""
 import numpy as np
 import pytest
 import torch
@@ -52,6 +53,8 @@ def _bf16_bits(a32):
 
 
 def test_each_stack_layer_on_its_own_input(moe):
+    # every one of the 64 tokens of every layer: routing bit-exact, outputs
+    # within 2e-3 x RMS of the oracle's
     from quantized_expert_ffn_score_gb300 import synthetic
     ctx = moe.Context(0)
     for l in range(STACK_LAYERS):
@@ -60,10 +63,12 @@ def test_each_stack_layer_on_its_own_input(moe):
         x = synthetic.device_x(r)
         out, topk, gates = _gpu_layer(moe, ctx, layer, x, torch.float32)
         xh = si.layer_x(r)
-        logits, idx, g, y, _ = gu.oracle_layer(r, xh, tokens=SAMPLE)
+        logits, idx, g, y, _ = gu.oracle_layer(r, xh)
         gu.check_routing(topk, gates, idx, g, gu.gate_tolerance(r, xh, logits))
-        delta = out.cpu().numpy().astype(np.float64)[SAMPLE] - gu.x_host_f64(xh)[SAMPLE]
-        gu.assert_rms_close(delta, y[SAMPLE], what=f"stack layer {l}")
+        delta = out.cpu().numpy().astype(np.float64) - gu.x_host_f64(xh)
+        err, rms = gu.rms_err(delta, y)
+        gu.record_margin(r.name, err, rms, r.T)
+        gu.assert_rms_close(delta, y, what=f"stack layer {l}")
         del layer
         torch.cuda.empty_cache()
     ctx.close()
@@ -75,16 +80,22 @@ def test_chained_stack_against_the_oracle_chain(moe):
     recipes = [stack_layer(l) for l in range(STACK_LAYERS)]
     layers = [synthetic.device_layer(r) for r in recipes]
     x0 = synthetic.device_x(recipes[0])
-    # the library's stack call and the same chain layer by layer agree bit for bit
+    # the library's stack call (with its routing trace) and the same chain
+    # layer by layer agree bit for bit
     out_stack = torch.empty((STACK_T, recipes[0].d), dtype=torch.float32, device="cuda")
-    moe.moe_stack_forward(ctx, layers, x0, out_stack, moe.workspace(moe.stack_forward_ws_bytes(layers, STACK_T)))
+    k = recipes[0].k
+    trace = torch.full((STACK_LAYERS, STACK_T, k), -1, dtype=torch.int32, device="cuda")
+    moe.moe_stack_forward_ex(ctx, layers, x0, out_stack, moe.workspace(moe.stack_forward_ws_bytes(layers, STACK_T)),
+                             topk_trace=trace)
     ctx.check()
+    trace = trace.cpu().numpy()
     x = x0
     gpu_in, gpu_topk, gpu_out = [], [], []
     for l, layer in enumerate(layers):
         last = l == STACK_LAYERS - 1
         gpu_in.append(x.view(torch.int16).cpu().numpy().view(np.uint16)[SAMPLE])
         out, topk, _ = _gpu_layer(moe, ctx, layer, x, torch.float32)
+        np.testing.assert_array_equal(trace[l], topk)
         gpu_topk.append(topk[SAMPLE])
         gpu_out.append(out.cpu().numpy()[SAMPLE])
         x = out if last else out.to(torch.bfloat16)
