@@ -51,9 +51,13 @@ def lib():
                                           vp, vp, vp, i32, vp, vp, vp, vp]
         L.or_partial_delta.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
                                        vp]
+        L.or_project.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp]
+        L.or_round_bf16.argtypes, L.or_round_bf16.restype = [ctypes.c_double], ctypes.c_uint16
+        L.or_latent_forward.argtypes = [vp, i32, vp, vp, i32, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, i32, vp, vp, vp, vp, i32, vp, vp]
         for f in ("or_router", "or_topk_gates", "or_bucket", "or_expert_mxfp4", "or_expert_rvq3",
                   "or_expert_rvq3_rowmajor", "or_combine",
-                  "or_layer_forward", "or_partial_delta"):
+                  "or_layer_forward", "or_partial_delta", "or_project", "or_latent_forward"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -271,3 +275,44 @@ def partial_delta(x, topk_idx, gates, d, ff, k, records, e_begin, e_end, quant="
     del keep
     _check(rc, "partial_delta")
     return delta
+
+
+def project(x, W):
+    """y[t][n] = sum_k W[n][k] x[t][k] in fp64 (x [T][K], W [N][K]; float32 or
+    bf16 bit patterns in uint16)."""
+    x = np.ascontiguousarray(x)
+    W = np.ascontiguousarray(W)
+    T, K = x.shape
+    N = W.shape[0]
+    y = np.empty((T, N), dtype=np.float64)
+    _check(lib().or_project(_p(x), _dt(x), _p(W), _dt(W), T, K, N, _p(y)), "project")
+    return y
+
+
+def round_bf16(v):
+    """bf16 bit patterns (uint16) of the values in v, rounded to nearest even."""
+    a = np.asarray(v, dtype=np.float64)
+    f = lib().or_round_bf16
+    return np.array([f(float(t)) for t in a.reshape(-1)], dtype=np.uint16).reshape(a.shape)
+
+
+def latent_forward(x, w_in, w_out, router_w, bias, d, ff, E, k, records, quant="mxfp4", act_kind="swiglu",
+                   codebooks=None, nthreads=1, n_shared=0, bias_mode="logit"):
+    """(z bf16 bits [T][d], out [T][D]) of the layer run in the latent space:
+    z = bf16(W_in x), out = x + W_out (MoE delta of z)."""
+    x = np.ascontiguousarray(x)
+    w_in = np.ascontiguousarray(w_in)
+    w_out = np.ascontiguousarray(w_out)
+    assert _dt(w_in) == _dt(w_out)
+    T, D = x.shape
+    z = np.empty((T, d), dtype=np.uint16)
+    out = np.empty((T, D), dtype=np.float64)
+    recs, keep = _records_array(records, E + n_shared)
+    cbs = codebooks if codebooks is not None else (None, None, None)
+    rw = np.ascontiguousarray(router_w)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    _check(lib().or_latent_forward(_p(x), _dt(x), _p(w_in), _p(w_out), _dt(w_in), D, _p(rw), _dt(rw), _p(b),
+                                   BIAS_MODE[bias_mode], T, d, ff, E, k, n_shared, ACT[act_kind], QUANT[quant], recs,
+                                   _p(cbs[0]), _p(cbs[1]), _p(cbs[2]), int(nthreads), _p(z), _p(out)),
+           "latent_forward")
+    return z, out

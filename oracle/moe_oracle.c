@@ -49,6 +49,7 @@ double or_f16(uint16_t bits) {
 
 static double load_val(const void* p, int dtype, size_t i) {
   if (dtype == OR_BF16) return or_bf16(((const uint16_t*)p)[i]);
+  if (dtype == OR_F64) return ((const double*)p)[i];
   return (double)((const float*)p)[i];
 }
 
@@ -444,5 +445,83 @@ int or_partial_delta(const void* x, int x_dtype, const int32_t* topk_idx, const 
                         NULL, e_begin, e_end, 1, yp);
   if (!rc) or_combine(NULL, yp, gates, T, k, d, delta);
   free(yp);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Latent projections                                                        */
+/* ------------------------------------------------------------------------ */
+
+int or_project(const void* x, int x_dtype, const void* w, int w_dtype, int T, int K, int N, double* y) {
+  if (T < 0 || K <= 0 || N <= 0 || !x || !w || !y) return -1;
+  for (int t = 0; t < T; ++t) {
+    for (int n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int k = 0; k < K; ++k) s += load_val(w, w_dtype, (size_t)n * K + k) * load_val(x, x_dtype, (size_t)t * K + k);
+      y[(size_t)t * N + n] = s;
+    }
+  }
+  return 0;
+}
+
+/* bf16 keeps the sign, the 8 exponent bits and 7 fraction bits of a float:
+ * the representable values around v are found from v's binary exponent, and
+ * the nearer one is taken, the one with an even last bit on a tie. */
+uint16_t or_round_bf16(double v) {
+  if (v != v) return 0x7FC0;
+  const int neg = v < 0 || (v == 0 && 1.0 / v < 0);
+  double a = neg ? -v : v;
+  uint16_t bits;
+  if (a == 0.0) {
+    bits = 0;
+  } else {
+    int e;
+    frexp(a, &e);                    /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 8;                   /* 8 significant bits: the spacing is 2^(e-8) */
+    if (q < -133) q = -133;          /* below the normal range: the subnormal spacing 2^-133 */
+    const double ulp = ldexp(1.0, q);
+    double m = floor(a / ulp);       /* a / ulp is exact (a power of two divides) */
+    const double rem = a - m * ulp;  /* exact */
+    if (rem > 0.5 * ulp || (rem == 0.5 * ulp && fmod(m, 2.0) != 0.0)) m += 1.0;
+    const double r = m * ulp;        /* the rounded magnitude */
+    if (r >= ldexp(1.0, 128)) {
+      bits = 0x7F80;                 /* infinity */
+    } else {
+      float f = (float)r;            /* r has at most 8 significant bits and is in range: exact */
+      uint32_t u;
+      memcpy(&u, &f, sizeof u);
+      bits = (uint16_t)(u >> 16);
+    }
+  }
+  return (uint16_t)(bits | (neg ? 0x8000 : 0));
+}
+
+int or_latent_forward(const void* x, int x_dtype, const void* w_in, const void* w_out, int w_dtype, int D,
+                      const void* router_w, int router_dtype, const float* bias, int bias_mode, int T, int d, int ff,
+                      int E, int k, int n_shared, int act, int quant, const uint8_t* const* records,
+                      const uint16_t* cb_gate, const uint16_t* cb_up, const uint16_t* cb_down, int nthreads,
+                      uint16_t* z_bits, double* out) {
+  if (T < 0 || D <= 0 || d <= 0) return -1;
+  const size_t nz = (size_t)(T ? T : 1) * d, nd = (size_t)(T ? T : 1) * D;
+  double* z = (double*)malloc(sizeof(double) * nz);
+  uint16_t* zb = (uint16_t*)malloc(sizeof(uint16_t) * nz);
+  double* u = (double*)malloc(sizeof(double) * nz);
+  double* back = (double*)malloc(sizeof(double) * nd);
+  int rc = -1;
+  if (!z || !zb || !u || !back) goto done;
+  if ((rc = or_project(x, x_dtype, w_in, w_dtype, T, D, d, z)) != 0) goto done;
+  for (size_t i = 0; i < (size_t)T * d; ++i) zb[i] = or_round_bf16(z[i]);
+  if (z_bits) memcpy(z_bits, zb, sizeof(uint16_t) * (size_t)T * d);
+  rc = or_layer_forward_ex(zb, OR_BF16, router_w, router_dtype, bias, bias_mode, T, d, ff, E, k, n_shared, act, quant,
+                           records, cb_gate, cb_up, cb_down, NULL, nthreads, NULL, NULL, u, NULL);
+  if (rc) goto done;
+  if ((rc = or_project(u, OR_F64, w_out, w_dtype, T, d, D, back)) != 0) goto done;
+  if (out)
+    for (size_t i = 0; i < (size_t)T * D; ++i) out[i] = load_val(x, x_dtype, i) + back[i];
+done:
+  free(z);
+  free(zb);
+  free(u);
+  free(back);
   return rc;
 }

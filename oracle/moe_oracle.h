@@ -34,7 +34,7 @@
 extern "C" {
 #endif
 
-enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
 enum { OR_ACT_SWIGLU = 0, OR_ACT_SITU = 1 };
 
 /* ---- element decodes ---------------------------------------------------- */
@@ -138,6 +138,28 @@ int or_layer_forward_ex(const void* x, int x_dtype, const void* router_w, int w_
 int or_partial_delta(const void* x, int x_dtype, const int32_t* topk_idx, const double* gates, int T, int d,
                      int ff, int k, int act, int quant, const uint8_t* const* records, const uint16_t* cb_gate,
                      const uint16_t* cb_up, const uint16_t* cb_down, int e_begin, int e_end, double* delta);
+
+/* ---- latent projections ---------------------------------------------------
+ * LazyLoRA README, "The engine": the routed experts work in a latent space of
+ * width d = 3584, entered by a projection from the model's hidden width and
+ * left by a projection back; the page does not state K3's model width, so D
+ * is a parameter.
+ *   or_project: y[t][n] = sum_k W[n][k] * x[t][k], summed in ascending k in
+ *     fp64 (W row-major [N][K]).
+ *   or_round_bf16: the bf16 value nearest to v, ties to the even significand
+ *     (bit pattern); overflow to infinity, NaN kept NaN.
+ *   or_latent_forward: z = bf16(W_in x) (the latent activation enters the
+ *     experts in bf16, as every layer input does), u = the MoE delta of z
+ *     (or_layer_forward_ex without the residual), out = x + W_out u, for
+ *     W_in [d][D] and W_out [D][d].  z_bits (nullable) receives z's bf16
+ *     bits [T][d], out (nullable) the result [T][D]. */
+int or_project(const void* x, int x_dtype, const void* w, int w_dtype, int T, int K, int N, double* y);
+uint16_t or_round_bf16(double v);
+int or_latent_forward(const void* x, int x_dtype, const void* w_in, const void* w_out, int w_dtype, int D,
+                      const void* router_w, int router_dtype, const float* bias, int bias_mode, int T, int d, int ff,
+                      int E, int k, int n_shared, int act, int quant, const uint8_t* const* records,
+                      const uint16_t* cb_gate, const uint16_t* cb_up, const uint16_t* cb_down, int nthreads,
+                      uint16_t* z_bits, double* out);
 
 #ifdef __cplusplus
 }

@@ -43,6 +43,11 @@ MUTANTS = [
     ("shared experts dropped", "0, E + n_shared, nthreads, yp);", "0, E, nthreads, yp);"),
     ("shared expert reads a routed record", ": E + (j - k);", ": (j - k);"),
     ("shared expert weighted like a routed one", ": 1.0;", ": g[(size_t)t * k];"),
+    ("projection W transposed", "load_val(w, w_dtype, (size_t)n * K + k)", "load_val(w, w_dtype, (size_t)k * N + n)"),
+    ("latent residual dropped", "out[i] = load_val(x, x_dtype, i) + back[i];", "out[i] = back[i];"),
+    ("latent input not rounded to bf16", "zb[i] = or_round_bf16(z[i]);", "zb[i] = or_round_bf16(z[i] * 1.001);"),
+    ("bf16 ties rounded up", "fmod(m, 2.0) != 0.0", "1"),
+    ("latent delta projected with the input matrix", "or_project(u, OR_F64, w_out,", "or_project(u, OR_F64, w_in,"),
     ("CRC generator not reflected", "reg ^= 0xEDB88320u;", "reg ^= 0x04C11DB7u;"),
     ("CRC register starts at zero", "uint32_t reg = 0xFFFFFFFFu;", "uint32_t reg = 0u;"),
     ("CRC result not complemented", "return reg ^ 0xFFFFFFFFu;", "return reg;"),

@@ -514,3 +514,86 @@ def test_partial_deltas_over_expert_ranges_sum_to_full():
     a = oracle.partial_delta(x, idx, g, r.d, r.ff, r.k, recs, 0, 5)
     b = oracle.partial_delta(x, idx, g, r.d, r.ff, r.k, recs, 5, 12)
     np.testing.assert_allclose(a + b, y, rtol=0, atol=1e-12 * np.max(np.abs(y)))
+
+
+# ---- latent projections (LazyLoRA README, "The engine": the experts work in a
+# 3584-wide latent space between projections from and back to the model width)
+
+def _bf16_of(a32):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a32, dtype=np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("xdt,wdt", [("bf16", "bf16"), ("f32", "bf16"), ("f32", "f32")])
+def test_project_matches_numpy(xdt, wdt):
+    T, K, N = 3, 160, 96
+    x = si.normal(21, 1, 1.0, T * K, xdt).reshape(T, K)
+    W = si.normal(21, 2, 0.05, N * K, wdt).reshape(N, K)
+    y = oracle.project(x, W)
+    xf = npref.to_f64(x) if xdt == "bf16" else x.astype(np.float64)
+    wf = npref.to_f64(W) if wdt == "bf16" else W.astype(np.float64)
+    ref = xf @ wf.T
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.max(np.abs(xf)) * np.max(np.abs(wf)) * K
+    # row n of W against token t, element by element: a transposed W would differ
+    assert y.shape == (T, N) and abs(y[1, 7] - sum(wf[7] * xf[1])) <= 1e-12
+
+
+def test_round_bf16_is_round_to_nearest_even():
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.normal(0, 1, 2000), rng.normal(0, 1e-38, 200), rng.normal(0, 1e38, 200)]).astype(np.float32)
+    # exact ties: a bf16 value plus half its spacing, with even and odd last bits
+    base = np.array([1.0, 1.0078125, 3.0, 255.0, -1.0078125], dtype=np.float32)
+    ties = (base.astype(np.float64) + np.abs(base).astype(np.float64) * 2.0 ** -8).astype(np.float32)
+    v = np.concatenate([v, ties, np.array([0.0, -0.0, 3.4e38, -3.4e38, 1e-45], dtype=np.float32)])
+    got = oracle.round_bf16(v.astype(np.float64))
+    np.testing.assert_array_equal(got, _bf16_of(v))
+    assert oracle.round_bf16(np.array([np.nan]))[0] & 0x7FFF > 0x7F80
+    assert list(oracle.round_bf16(np.array([1.00390625, 1.01171875]))) == [0x3F80, 0x3F82]  # ties to even
+
+
+def _latent_case(D, seed, perm=None, identity=False):
+    r = si.LayerRecipe("latent_tiny", d=64, ff=64, E=8, k=2, T=3, seed=seed, x_dtype="bf16", w_dtype="bf16",
+                       scale_lo=119, scale_hi=125)
+    recs = [si.layer_record(r, e) for e in range(r.E)]
+    W = si.layer_router_w(r)
+    x = si.normal(seed, 90, 1.0, r.T * D, "bf16").reshape(r.T, D)
+    if identity:
+        w_in = np.zeros((r.d, D), dtype=np.uint16)
+        w_in[np.arange(r.d), np.arange(r.d) if perm is None else perm] = 0x3F80  # 1.0
+        w_out = np.ascontiguousarray(w_in.T)
+    else:
+        w_in = si.normal(seed, 91, 1.0 / np.sqrt(D), r.d * D, "bf16").reshape(r.d, D)
+        w_out = si.normal(seed, 92, 1.0 / np.sqrt(r.d), D * r.d, "bf16").reshape(D, r.d)
+    return r, recs, W, x, w_in, w_out
+
+
+def test_latent_identity_projection_is_the_plain_layer():
+    r, recs, W, x, w_in, w_out = _latent_case(64, 31, identity=True)
+    z, out = oracle.latent_forward(x, w_in, w_out, W, None, r.d, r.ff, r.E, r.k, recs)
+    np.testing.assert_array_equal(z, x)
+    _, _, _, o = oracle.layer_forward(x, W, None, r.d, r.ff, r.E, r.k, recs)
+    np.testing.assert_array_equal(out, o)
+
+
+def test_latent_one_hot_projection_selects_inputs():
+    D = 96
+    perm = np.random.default_rng(3).permutation(D)[:64]
+    r, recs, W, x, w_in, w_out = _latent_case(D, 32, perm=perm, identity=True)
+    z, out = oracle.latent_forward(x, w_in, w_out, W, None, r.d, r.ff, r.E, r.k, recs)
+    np.testing.assert_array_equal(z, x[:, perm])  # z[t][n] = x[t][perm[n]]
+    _, _, y, _ = oracle.layer_forward(z, W, None, r.d, r.ff, r.E, r.k, recs)
+    want = npref.to_f64(x).copy()
+    want[:, perm] += y  # W_out scatters the latent delta back to the selected inputs
+    np.testing.assert_array_equal(out, want)
+
+
+def test_latent_layer_matches_numpy_chain():
+    D = 80
+    r, recs, W, x, w_in, w_out = _latent_case(D, 33)
+    z, out = oracle.latent_forward(x, w_in, w_out, W, None, r.d, r.ff, r.E, r.k, recs)
+    zr = npref.to_f64(x) @ npref.to_f64(w_in).T
+    np.testing.assert_array_equal(z, _bf16_of(zr.astype(np.float32)))  # no value sits at a rounding tie here
+    _, _, y, _ = oracle.layer_forward(z, W, None, r.d, r.ff, r.E, r.k, recs)
+    ref = npref.to_f64(x) + y @ npref.to_f64(w_out).T
+    assert np.max(np.abs(out - ref)) <= 1e-12 * np.max(np.abs(ref))
