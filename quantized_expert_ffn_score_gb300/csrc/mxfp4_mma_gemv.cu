@@ -114,15 +114,19 @@ __device__ __forceinline__ int shift_for(float mx) {
 }
 
 // The activations of one pass as B fragments: for each of the warp's blocks,
-// token g's columns 8t..8t+7 as four f16 pairs (MODE 1: hi and lo).
-template <int MODE, int BPW>
+// token g's columns 8t..8t+7 as four f16 pairs (MODE 1: hi and lo).  PAIR
+// (MODE 1, at most 4 tokens per pass): column 2n holds token n's hi part and
+// column 2n + 1 its lo part, so one MMA forms both partial sums (lane group g
+// holds token g / 2, part g % 2) and the lo array is not needed.
+template <int MODE, int BPW, bool PAIR>
 struct Frags {
   uint32_t hi[BPW][4];
-  uint32_t lo[MODE == 1 ? BPW : 1][4];
-  float unscale;  // MODE 1: 2^s of this warp's rescale for token g (MODE 0: unused)
+  uint32_t lo[(MODE == 1 && !PAIR) ? BPW : 1][4];
+  float unscale;  // MODE 1: 2^s of this warp's rescale for the lane's token (MODE 0: unused)
 
   __device__ void load(const FfnArgs& a, int slot0, int nt, int b0, int nblk, int lane) {
-    const int g = lane >> 2, t = lane & 3;
+    const int g0 = lane >> 2, t = lane & 3;
+    const int g = PAIR ? g0 >> 1 : g0;  // the lane's token in the pass
     const bool live = g < nt;
     unscale = 1.f;
     if (MODE == 0) {
@@ -177,8 +181,14 @@ struct Frags {
         for (int i = 0; i < 4; ++i) {
           const float x0 = v[2 * i] * inv, x1 = v[2 * i + 1] * inv;
           const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-          hi[j][i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-          lo[j][i] = pack_f16x2(x0 - __half2float(h0), x1 - __half2float(h1));
+          const uint32_t hv = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+          const uint32_t lv = pack_f16x2(x0 - __half2float(h0), x1 - __half2float(h1));
+          if (PAIR) {
+            hi[j][i] = (g0 & 1) ? lv : hv;
+          } else {
+            hi[j][i] = hv;
+            lo[(MODE == 1 && !PAIR) ? j : 0][i] = lv;
+          }
         }
       }
     }
@@ -207,7 +217,7 @@ __device__ __forceinline__ void note_tokens(const FfnArgs& a, int slot0, int nt,
 // partial sums go to a double-buffered shared array whose fill is counted by an
 // mbarrier, and a reducer warp (warp 0, which computes nothing else) adds them
 // and writes the pass's outputs.  Every wait is bounded.
-template <int MODE, int BPW>
+template <int MODE, int BPW, bool PAIR>
 __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gemv_kernel(const FfnArgs a, const GeomM g) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)g.stages * g.stage_bytes);
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
   const int cw = warp - 1;
   const int gq = lane >> 2, tq = lane & 3;
   const int b0 = cw * BPW;
-  Frags<MODE, BPW> fr;
+  Frags<MODE, BPW, PAIR> fr;
   int it = 0, pc = 0, cur_a = -1, s0 = 0, ne = 0;
   bool rec_good = false;
   for (int tile = t_begin; tile < t_end; ++tile) {
@@ -427,27 +437,40 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
             const uint32_t A1[4] = {pa[2], pb[2], pa[3], pb[3]};
             mma16816(d, A0, fr.hi[j][0], fr.hi[j][1]);
             mma16816(d, A1, fr.hi[j][2], fr.hi[j][3]);
-            if (MODE == 1) {
-              mma16816(d, A0, fr.lo[MODE == 1 ? j : 0][0], fr.lo[MODE == 1 ? j : 0][1]);
-              mma16816(d, A1, fr.lo[MODE == 1 ? j : 0][2], fr.lo[MODE == 1 ? j : 0][3]);
+            if (MODE == 1 && !PAIR) {
+              constexpr bool kLo = MODE == 1 && !PAIR;
+              mma16816(d, A0, fr.lo[kLo ? j : 0][0], fr.lo[kLo ? j : 0][1]);
+              mma16816(d, A1, fr.lo[kLo ? j : 0][2], fr.lo[kLo ? j : 0][3]);
             }
             float sa, sb;
             {  // bytes j of rows ra and rb as one 16-bit pair
               const uint32_t wa2 = j < 4 ? sra[m].x : sra[m].y, wb2 = j < 4 ? srb[m].x : srb[m].y;
               e8m0x2_to_f32(__byte_perm(wa2, wb2, (uint32_t)(j & 3) | ((uint32_t)((j & 3) + 4) << 4)), sa, sb);
             }
-            acc[m][0] = fmaf(sa, d[0], acc[m][0]);
-            acc[m][2] = fmaf(sb, d[2], acc[m][2]);
-            if (!ONE) {  // token columns 2 tq + 1 (all zero when the pass holds one token)
-              acc[m][1] = fmaf(sa, d[1], acc[m][1]);
-              acc[m][3] = fmaf(sb, d[3], acc[m][3]);
+            if (PAIR) {  // columns 2 tq and 2 tq + 1: token tq's hi and lo sums
+              acc[m][0] = fmaf(sa, d[0] + d[1], acc[m][0]);
+              acc[m][2] = fmaf(sb, d[2] + d[3], acc[m][2]);
+            } else {
+              acc[m][0] = fmaf(sa, d[0], acc[m][0]);
+              acc[m][2] = fmaf(sb, d[2], acc[m][2]);
+              if (!ONE) {  // token columns 2 tq + 1 (all zero when the pass holds one token)
+                acc[m][1] = fmaf(sa, d[1], acc[m][1]);
+                acc[m][3] = fmaf(sb, d[3], acc[m][3]);
+              }
             }
           }
         }
       };
       if (nt == 1) blocks(std::true_type{});
       else blocks(std::false_type{});
-      if (MODE == 1) {  // undo this warp's rescale for tokens 2t, 2t+1
+      if (MODE == 1 && PAIR) {  // undo this warp's rescale for token t (lane groups 2t, 2t + 1 hold it)
+        const float u0 = __shfl_sync(0xffffffffu, fr.unscale, (2 * tq) * 4);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          acc[m][0] *= u0;
+          acc[m][2] *= u0;
+        }
+      } else if (MODE == 1) {  // undo this warp's rescale for tokens 2t, 2t+1
         const float u0 = __shfl_sync(0xffffffffu, fr.unscale, (2 * tq) * 4);
         const float u1 = __shfl_sync(0xffffffffu, fr.unscale, (2 * tq + 1) * 4);
 #pragma unroll
@@ -465,10 +488,15 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int ra = 16 * m + gq;
-        rb[ra * kTok + 2 * tq] = acc[m][0];
-        rb[ra * kTok + 2 * tq + 1] = acc[m][1];
-        rb[(ra + 8) * kTok + 2 * tq] = acc[m][2];
-        rb[(ra + 8) * kTok + 2 * tq + 1] = acc[m][3];
+        if (PAIR) {  // token tq (columns >= nt are never read)
+          rb[ra * kTok + tq] = acc[m][0];
+          rb[(ra + 8) * kTok + tq] = acc[m][2];
+        } else {
+          rb[ra * kTok + 2 * tq] = acc[m][0];
+          rb[ra * kTok + 2 * tq + 1] = acc[m][1];
+          rb[(ra + 8) * kTok + 2 * tq] = acc[m][2];
+          rb[(ra + 8) * kTok + 2 * tq + 1] = acc[m][3];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_full[bi]);
@@ -478,11 +506,11 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
   }
 }
 
-template <int MODE, int BPW>
+template <int MODE, int BPW, bool PAIR>
 cudaError_t launch_m(const FfnArgs& a, const GeomM& g, int num_sms, bool pdl, cudaStream_t s, const char* name) {
-  ensure_smem(mxfp4_mma_gemv_kernel<MODE, BPW>, g.smem);
-  return launch(name, mxfp4_mma_gemv_kernel<MODE, BPW>, dim3(num_sms), dim3((g.warps + 2) * 32), g.smem, s, pdl, a,
-                g);
+  ensure_smem(mxfp4_mma_gemv_kernel<MODE, BPW, PAIR>, g.smem);
+  return launch(name, mxfp4_mma_gemv_kernel<MODE, BPW, PAIR>, dim3(num_sms), dim3((g.warps + 2) * 32), g.smem, s, pdl,
+                a, g);
 }
 
 }  // namespace
@@ -499,9 +527,11 @@ cudaError_t launch_mxfp4_ffn_mma(const FfnArgs& a, int num_sms, bool pdl, cudaSt
   const GeomM g0 = make_geom_m(0, a.d, a.ff), g1 = make_geom_m(1, a.d, a.ff);
   if (g0.stages < 2 || g1.stages < 2 || g0.warps > kMaxConsumerWarps || g1.warps > kMaxConsumerWarps)
     return cudaErrorInvalidValue;
-  cudaError_t err = launch_m<0, 8>(a, g0, num_sms, pdl, s, "mxfp4_gate_up");
+  cudaError_t err = launch_m<0, 8, false>(a, g0, num_sms, pdl, s, "mxfp4_gate_up");
   if (err != cudaSuccess) return err;
-  return launch_m<1, 8>(a, g1, num_sms, true, s, "mxfp4_down");
+  // an expert gets at most T tokens, so with T <= 4 every pass fits the paired columns
+  if (a.T <= 4) return launch_m<1, 8, true>(a, g1, num_sms, true, s, "mxfp4_down");
+  return launch_m<1, 8, false>(a, g1, num_sms, true, s, "mxfp4_down");
 }
 
 }  // namespace moe
