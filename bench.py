@@ -46,7 +46,11 @@ METRIC = "MoE-layer tokens/s on 1 GB300; achieved HBM GB/s (decode) / TC util vs
 DEFAULT_WORKLOAD = "k3_mxfp4_decode"
 STACK_WORKLOAD = "k3_mxfp4_stack"
 CONFIG_WORKLOADS = ("k3_rvq3_decode_b1", "k3_rvq3_decode_b8", "k3_mxfp4_prefill_zipf", "k3_mxfp4_prefill_uniform",
-                    STACK_WORKLOAD)
+                    STACK_WORKLOAD, "k3_mxfp4_decode_tier50", "k3_mxfp4_decode_tier25")
+# experts beyond HBM: the decode layer with this share of its experts resident
+# in HBM slots (the hottest over the input pool), the others read from
+# page-locked host memory over NVLink-C2C by the same kernels
+TIER_WORKLOADS = {"k3_mxfp4_decode_tier50": ("k3_mxfp4_decode", 0.5), "k3_mxfp4_decode_tier25": ("k3_mxfp4_decode", 0.25)}
 X_POOL = 64
 FLUSH_BYTES = 512 << 20
 
@@ -168,6 +172,8 @@ def workload_recipes(name):
     import seeded_inputs as si
     if name == STACK_WORKLOAD:
         return stack_recipes()
+    if name in TIER_WORKLOADS:
+        return [si.get_workload(TIER_WORKLOADS[name][0])]
     return [si.get_workload(name)]
 
 
@@ -289,6 +295,37 @@ class Target:
             self.ws = moe.workspace(moe.stack_forward_ws_bytes(self.layers, self.T), device=dev)
         else:
             self.ws = moe.workspace(moe.layer_forward_ws_bytes(self.layers[0], self.T), device=dev)
+        self.tier = None
+        if name in TIER_WORKLOADS:
+            self._make_tier(TIER_WORKLOADS[name][1], dev)
+
+    def _make_tier(self, frac, dev):
+        """Moves the layer's bank to page-locked host memory behind a tier of
+        frac x E HBM slots holding the experts most routed over the input pool."""
+        import torch
+
+        import seeded_inputs as si
+        moe, dl, r = self.moe, self.layers[0], self.r0
+        n = r.E + r.n_shared
+        host = torch.empty(n * dl.stride, dtype=torch.uint8, pin_memory=True)
+        host.copy_(dl.bank.cpu())
+        n_slots = int(round(frac * r.E))
+        slots = torch.empty(max(n_slots, 1) * dl.stride, dtype=torch.uint8, device=dev)
+        table = torch.zeros(n, dtype=torch.int64, device=dev)
+        self.tier = moe.Tier(self.ctx, n, si.record_size(r), dl.stride, host, slots, n_slots, table)
+        layer = moe.Layer(r.d, r.ff, r.E, r.k, dl.router_w, table, quant=r.quant, act=r.act,
+                          router_bias=dl.router_bias, codebooks=dl.codebooks, keep=[host, slots],
+                          n_shared=r.n_shared, bias_mode=r.bias_mode)
+        layer.recipe = r
+        self.layers = [layer]
+        del dl
+        torch.cuda.empty_cache()
+        for i in range(X_POOL):  # the heat of the input pool's routing, then the hottest into HBM
+            self.step(i, counts=True)
+            self.tier.observe(self.counts)
+        self.tier.rebalance()
+        self.ctx.check()
+        self.slot_of, _ = self.tier.residency()
 
     def step(self, i, counts=False, x=None):
         x = self.x_pool[i % X_POOL] if x is None else x
@@ -431,6 +468,19 @@ def workload_line(t, m, K, peaks, cpu_seconds, rank, world, with_cpu):
          "gpu_launches": int(round(launches_per_step * K)), "clocks": m["clocks"], "wall_s": m["wall_s"],
          "router_fp64_recheck": {"tokens": m["fp64_tokens"], "sequential_logits": m["seq_logits"],
                                  "of_tokens": K * t.T * n_layers}}
+    if t.tier is not None:  # the records read from host memory per step, and their rate
+        import numpy as np
+        resident = t.slot_of[:t.r0.E] >= 0
+        host_rec = [float(((sc[0][:t.r0.E] > 0) & ~resident).sum()) for sc in m["step_counts"]]
+        host_bytes = float(np.mean(host_rec)) * rec_bytes
+        d["tier"] = {"resident_experts": int(resident.sum()), "of_experts": t.r0.E,
+                     "host_records_per_step": float(np.mean(host_rec)),
+                     "hbm_records_per_step": mean_distinct - float(np.mean(host_rec)),
+                     "host_bytes_per_step": host_bytes,
+                     "host_read_gbs": host_bytes / (m["dev_ms"] / K / 1e3) / 1e9,
+                     "note": "records not resident are read in place from page-locked host memory over "
+                             "NVLink-C2C by the expert kernels; resident set = the hottest experts over the "
+                             "64-token input pool"}
     if rank == 0 and world == 1 and with_cpu:
         tokens, secs, threads = oracle_sample(t.recipes, target_s=cpu_seconds)
         d["cpu_baseline"] = {"value": tokens / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -513,7 +563,9 @@ def run_ours(args):
         tc = Target(name, ctx, dev)
         mc = measure(tc, args.config_steps, max(3, min(args.warmup, 5)), flush_l2, world, dev)
         configs[name] = workload_line(tc, mc, args.config_steps, peaks, args.config_cpu_seconds, rank, world,
-                                      not args.no_cpu_baseline)
+                                      not args.no_cpu_baseline and name not in TIER_WORKLOADS)
+        if tc.tier is not None:
+            tc.tier.close()
         del tc
         torch.cuda.empty_cache()
     if configs:

@@ -398,6 +398,114 @@ MOE_API moe_status moe_rvq3_repack(moe_ctx* ctx, const uint8_t* const* src, uint
                                    cudaStream_t stream);
 
 /*
+ * Experts beyond HBM ("Running a 2.78-Trillion-Parameter Model Across Two
+ * Desks", Act II: experts split into tiers ranked by how often they are used;
+ * Act III: an expert in no tier comes back as missing, never substituted;
+ * WASTE README, "How it works": a bounded expert cache in front of the slow
+ * store).  A tier owns one layer's record table: the hottest experts sit in
+ * HBM slots, the others are read in place from page-locked host (Grace)
+ * memory over NVLink-C2C by the same expert kernels (direct_host = 1), or
+ * their table entry is NULL and a layer that routes to them reports
+ * MOE_ERR_MISSING_EXPERT (direct_host = 0).
+ *   E            records in the bank (a layer's E + n_shared)
+ *   record_bytes bytes per record (a multiple of 16)
+ *   host_records HOST array [E] of pointers to each expert's record in
+ *                page-locked, mapped host memory (cudaHostAlloc, or
+ *                cudaHostRegister with cudaHostRegisterMapped), 256-byte
+ *                aligned; NULL: the expert has no host copy (it can only be
+ *                resident if it is already in a slot -- it never is, so it
+ *                is absent)
+ *   slots        device memory for n_slots records, slot_stride bytes apart
+ *                (a multiple of 256 >= record_bytes; 256-byte aligned)
+ *   records      DEVICE array [E] the tier writes: the layer's record table
+ *                (moe_mxfp4_experts.records / moe_rvq3_experts.records)
+ *   direct_host  1: a non-resident expert's entry is its host copy; 0: NULL
+ *   decay        heat[e] <- decay * heat[e] + counts[e] per observation, 0 < decay <= 1
+ * All of this memory is the caller's and must outlive the tier.  moe_tier_create
+ * allocates the tier's own bookkeeping (a device heat array [E] and page-locked
+ * host staging), and writes the initial table (nothing resident).
+ */
+typedef struct moe_tier moe_tier;
+typedef struct {
+  int E;
+  size_t record_bytes;
+  const uint8_t* const* host_records;
+  uint8_t* slots;
+  int n_slots;
+  size_t slot_stride;
+  const uint8_t** records;
+  int direct_host;
+  float decay;
+} moe_tier_desc;
+
+MOE_API moe_status moe_tier_create(moe_ctx* ctx, const moe_tier_desc* desc, moe_tier** tier);
+MOE_API void moe_tier_destroy(moe_tier* tier);
+
+/* Adds one step's tokens per expert (device counts [E], as moe_layer_forward's
+ * counts_out) into the decayed heat.  Asynchronous on `stream`. */
+MOE_API moe_status moe_tier_observe(moe_tier* tier, const int32_t* counts, cudaStream_t stream);
+
+/* Ranks the experts by heat (ties: an already resident expert, then the lower
+ * id; see moe_tier_plan), keeps the n_slots hottest that have a host copy or
+ * are resident, copies the newcomers into slots (evicting the coldest) and
+ * rewrites the table.  Synchronises `stream` to read the heat, then enqueues
+ * on it: the table entries of moved experts switched away from their slots,
+ * one cudaMemcpyAsync per newcomer, the final table.  Run it on the stream the
+ * layer runs on (or order the two with events): the copies overwrite evicted
+ * slots.  *n_moved (nullable) receives the number of records copied. */
+MOE_API moe_status moe_tier_rebalance(moe_tier* tier, cudaStream_t stream, int* n_moved);
+
+/* Makes the n <= n_slots listed experts (host array) resident ahead of any
+ * heat, in list order (a warm start, e.g. from an earlier run's counts);
+ * experts already in other slots stay where those slots are free.
+ * Synchronises `stream`, then enqueues as moe_tier_rebalance. */
+MOE_API moe_status moe_tier_pin(moe_tier* tier, const int32_t* experts, int n, cudaStream_t stream);
+
+/* Host copies of the residency (slot of each expert or -1; host [E], nullable)
+ * and of the heat (host [E] floats, nullable; synchronous). */
+MOE_API moe_status moe_tier_residency(const moe_tier* tier, int32_t* slot_of_expert, float* heat);
+
+/* The ranking moe_tier_rebalance applies, as a pure host function: experts
+ * that have a host copy (has_host[e] != 0) or a slot (slot_of[e] in [0,
+ * n_slots)) are ordered by heat descending, then resident first, then id
+ * ascending; the first n_slots are kept.  Kept residents stay in their slot;
+ * the others take the free slots in ascending order.  Writes new_slot_of [E]
+ * (slot or -1) and returns the number of experts that move into a slot, or -1
+ * for a bad argument.  No GPU is used. */
+MOE_API int moe_tier_plan(int E, int n_slots, const float* heat, const uint8_t* has_host, const int32_t* slot_of,
+                          int32_t* new_slot_of);
+
+/*
+ * Latent projections (LazyLoRA README, "The engine": the routed experts work
+ * in a latent space of width d = 3584, entered by a projection from the
+ * model's hidden width D and left by a projection back; the page does not
+ * state K3's hidden width, so D is a parameter).
+ *
+ * moe_project: y[t][n] = resid[t][n] + sum_k W[n][k] x[t][k] for t < T, n < N.
+ *   x [T][K] (x_dtype), W [N][K] row-major (w_dtype), resid [T][N] (nullable,
+ *   resid_dtype), y [T][N] (fp32, or bf16 rounded to nearest even).  Sums in
+ *   fp32 (bf16 x bf16 products are exact in fp32).  K a multiple of 32; x and W
+ *   16-byte aligned.  K, N <= 65536.
+ *
+ * moe_latent_layer_forward: the layer L run in its latent space (L->d is the
+ * latent width) for a hidden-width input:
+ *   z   = bf16(W_in x)                       W_in [d][D], the experts' input
+ *   u   = the MoE delta of z: sum_j g_j y_j(z) + the shared experts (fp32)
+ *   out = x + W_out u                        W_out [D][d]
+ * x and out [T][D]; w_dtype bf16 or fp32 for both matrices; latent_out
+ * (nullable, 16-byte aligned) receives z's bf16 bits [T][d].  ws:
+ * moe_latent_layer_forward_ws_bytes(L, D, T) bytes.  D a multiple of 32.
+ */
+MOE_API moe_status moe_project(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int K, const void* w,
+                               moe_dtype w_dtype, int N, const void* resid, moe_dtype resid_dtype, void* y,
+                               moe_dtype y_dtype, cudaStream_t stream);
+MOE_API size_t moe_latent_layer_forward_ws_bytes(const moe_layer* L, int D, int T);
+MOE_API moe_status moe_latent_layer_forward(moe_ctx* ctx, const moe_layer* L, const void* w_in, const void* w_out,
+                                            moe_dtype w_dtype, int D, const void* x, moe_dtype x_dtype, int T,
+                                            void* out, moe_dtype out_dtype, uint16_t* latent_out, void* ws,
+                                            size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Record check (WASTE README, "How it works": every expert record carries a
  * CRC32 of its payload, verified on request, so that a truncated or spliced
  * bank names the bad record instead of answering from wrong bytes).

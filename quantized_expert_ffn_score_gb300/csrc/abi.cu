@@ -323,9 +323,10 @@ moe::FfnArgs ffn_args(const moe_ctx* ctx, const void* x, moe_dtype x_dtype, int 
   return a;
 }
 
+// residual = false: out is the MoE delta alone (the latent layer projects it back).
 moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, moe_dtype x_dtype, int T, void* out,
                               moe_dtype out_dtype, int32_t* topk_out, float* gates_out, int32_t* counts_out,
-                              const LayerWs& w, cudaStream_t s) {
+                              const LayerWs& w, cudaStream_t s, bool residual = true) {
   if (T == 0) return MOE_OK;
   const int ks = layer_pairs_per_token(L), Es = layer_experts(L);
   const int32_t* topk = topk_out ? topk_out : w.topk;
@@ -342,7 +343,10 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   }
   moe_status st = cuda_status(moe::launch_route_topk(ra, ctx->num_sms, s));
   if (st != MOE_OK) return st;
-  if (T != 1) {
+  // the RVQ3 kernels work from the routing itself (pairs in token order); the
+  // buckets are then only needed for the caller's counts
+  const bool need_buckets = L->quant == MOE_QUANT_MXFP4 || counts_out != nullptr;
+  if (T != 1 && need_buckets) {
     st = cuda_status(moe::launch_bucket(ba, true, s));
     if (st != MOE_OK) return st;
   }
@@ -357,10 +361,15 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   } else {
     fa.records = L->rvq3.records;
     for (int m = 0; m < 3; ++m) fa.cb[m] = L->rvq3.codebooks[m];
-    st = cuda_status(moe::launch_rvq3_ffn(fa, ctx->num_sms, true, s));
+    st = cuda_status(moe::launch_rvq3_ffn(fa, topk, false, ctx->num_sms, true, s));
+    if (st != MOE_OK) return st;
+    // the combine adds the down kernel's per-slice sums of each pair
+    moe::CombineArgs ca{residual ? x : nullptr, x_dtype, moe::rvq3_down_partials(fa), gates, T, ks, L->d, out,
+                        out_dtype, moe::rvq3_down_parts(L->d, L->ff)};
+    return cuda_status(moe::launch_combine(ca, true, s));
   }
   if (st != MOE_OK) return st;
-  moe::CombineArgs ca{x, x_dtype, w.y_pairs, gates, T, ks, L->d, out, out_dtype};
+  moe::CombineArgs ca{residual ? x : nullptr, x_dtype, w.y_pairs, gates, T, ks, L->d, out, out_dtype, 1};
   return cuda_status(moe::launch_combine(ca, true, s));
 }
 
@@ -733,10 +742,7 @@ moe_status moe_expert_ffn_rvq3(moe_ctx* ctx, const void* x, moe_dtype x_dtype, i
   if (st != MOE_OK || T == 0) return st;
   a.records = experts->records;
   for (int m = 0; m < 3; ++m) a.cb[m] = experts->codebooks[m];
-  st = cuda_status(
-      moe::launch_active_from_offsets(offsets, experts->E, const_cast<int32_t*>(a.active), false, stream));
-  if (st != MOE_OK) return st;
-  return cuda_status(moe::launch_rvq3_ffn(a, ctx->num_sms, true, stream));
+  return cuda_status(moe::launch_rvq3_ffn(a, nullptr, true, ctx->num_sms, false, stream));
 }
 
 moe_status moe_combine(moe_ctx* ctx, const void* x_resid, moe_dtype x_dtype, const float* y_pairs,
@@ -749,7 +755,7 @@ moe_status moe_combine(moe_ctx* ctx, const void* x_resid, moe_dtype x_dtype, con
   if (T == 0) return MOE_OK;
   if (!y_pairs || !gates || !out) return MOE_ERR_INVALID_ARG;
   if (!al16(y_pairs) || !al16(out)) return MOE_ERR_INVALID_ARG;
-  moe::CombineArgs ca{x_resid, x_dtype, y_pairs, gates, T, k, d, out, out_dtype};
+  moe::CombineArgs ca{x_resid, x_dtype, y_pairs, gates, T, k, d, out, out_dtype, 1};
   return cuda_status(moe::launch_combine(ca, false, stream));
 }
 
@@ -820,6 +826,63 @@ moe_status moe_stack_forward_ex(moe_ctx* ctx, const moe_layer* layers, int n_lay
     exp_off += (size_t)layer_experts(&layers[l]);
   }
   return MOE_OK;
+}
+
+size_t moe_latent_layer_forward_ws_bytes(const moe_layer* L, int D, int T) {
+  if (D <= 0 || D % 32 || D > 65536) return 0;
+  const size_t lw = moe_layer_forward_ws_bytes(L, T);
+  if (lw == 0) return 0;
+  return lw + align_up((size_t)T * L->d * sizeof(uint16_t)) + align_up((size_t)T * L->d * sizeof(float));
+}
+
+moe_status moe_project(moe_ctx* ctx, const void* x, moe_dtype x_dtype, int T, int K, const void* w, moe_dtype w_dtype,
+                       int N, const void* resid, moe_dtype resid_dtype, void* y, moe_dtype y_dtype,
+                       cudaStream_t stream) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  ProfScope prof_scope(ctx);
+  if (T < 0 || K <= 0 || N <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (K > 65536 || N > 65536 || (long long)T * (K > N ? K : N) > (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!dtype_ok(x_dtype) || !dtype_ok(w_dtype) || !dtype_ok(y_dtype) || (resid && !dtype_ok(resid_dtype)))
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w || !y || !al16(x) || !al16(w)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_project(x, x_dtype, w, w_dtype, resid, resid_dtype, y, y_dtype, T, K, N, false,
+                                         stream));
+}
+
+moe_status moe_latent_layer_forward(moe_ctx* ctx, const moe_layer* L, const void* w_in, const void* w_out,
+                                    moe_dtype w_dtype, int D, const void* x, moe_dtype x_dtype, int T, void* out,
+                                    moe_dtype out_dtype, uint16_t* latent_out, void* ws, size_t ws_bytes,
+                                    cudaStream_t stream) {
+  moe_status st = ctx_ok(ctx);
+  if (st != MOE_OK) return st;
+  ProfScope prof_scope(ctx);
+  if ((st = check_layer(L)) != MOE_OK) return st;
+  if ((st = check_route_shape(T, L->d, layer_experts(L), layer_pairs_per_token(L))) != MOE_OK) return st;
+  if (D <= 0 || D % 32) return MOE_ERR_INVALID_ARG;
+  if (D > 65536) return MOE_ERR_UNSUPPORTED;
+  if (!dtype_ok(x_dtype) || !dtype_ok(out_dtype) || !dtype_ok(w_dtype)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out || x == out || !w_in || !w_out) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(out) || !al16(w_in) || !al16(w_out) || !al16(L->router_w)) return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(ws, ws_bytes, moe_latent_layer_forward_ws_bytes(L, D, T))) != MOE_OK) return st;
+  const size_t lw = moe_layer_forward_ws_bytes(L, T);
+  char* base = static_cast<char*>(ws);
+  uint16_t* z = latent_out ? latent_out : reinterpret_cast<uint16_t*>(base + lw);
+  float* u = reinterpret_cast<float*>(base + lw + align_up((size_t)T * L->d * sizeof(uint16_t)));
+  if (latent_out && !al16(latent_out)) return MOE_ERR_INVALID_ARG;
+  // z = bf16(W_in x): the latent input of the experts
+  st = cuda_status(moe::launch_project(x, x_dtype, w_in, w_dtype, nullptr, 0, z, MOE_BF16, T, D, L->d, false, stream));
+  if (st != MOE_OK) return st;
+  // u = the MoE delta of z (no residual)
+  Carver c(ws);
+  LayerWs w = carve_layer(c, L, T);
+  st = layer_forward_impl(ctx, L, z, MOE_BF16, T, u, MOE_F32, nullptr, nullptr, nullptr, w, stream, false);
+  if (st != MOE_OK) return st;
+  // out = x + W_out u
+  return cuda_status(moe::launch_project(u, MOE_F32, w_out, w_dtype, x, x_dtype, out, out_dtype, T, L->d, D, true,
+                                         stream));
 }
 
 }  // extern "C"

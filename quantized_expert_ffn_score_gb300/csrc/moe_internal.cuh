@@ -190,6 +190,17 @@ struct RouteArgs {
 };
 cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s);
 
+struct CombineArgs {
+  const void* x;
+  int x_dtype;
+  const float* y_pairs;  // [T*k][d], or with nparts > 1 [T*k][nparts][d] partial sums added in ascending order
+  const float* gates;
+  int T, k, d;
+  void* out;
+  int out_dtype;
+  int nparts;
+};
+
 struct FfnArgs {
   const uint8_t* const* records;
   const uint16_t* cb[3];  // RVQ3 codebooks
@@ -230,18 +241,17 @@ cudaError_t launch_mxfp4_bs(const BsLaunch& L, int num_sms, bool pdl, cudaStream
 bool mxfp4_mma_gemv_supported(int d, int ff, int x_dtype);
 cudaError_t launch_mxfp4_ffn_mma(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
 cudaError_t launch_token_absmax(const void* x, int x_dtype, int T, int d, float* max_x, bool pdl, cudaStream_t s);
-cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);
+// RVQ3 FFN (rvq3_gemv.cu).  a.partial: rvq3_partial_floats(T, k, d, ff)
+// floats.  pair_expert: the expert of each pair p = t * k + j ([T][k], e.g. the
+// routing), or null to derive it from a.offsets / a.pair_ids.  y_out: also sum
+// the down kernel's slice partials into a.y_pairs; otherwise they stay in
+// rvq3_down_partials(a) as [T*k][rvq3_down_parts(d, ff)][d] for the combine.
+cudaError_t launch_rvq3_ffn(const FfnArgs& a, const int32_t* pair_expert, bool y_out, int num_sms, bool pdl,
+                            cudaStream_t s);
 size_t rvq3_partial_floats(int T, int k, int d, int ff);
+int rvq3_down_parts(int d, int ff);
+float* rvq3_down_partials(const FfnArgs& a);
 
-struct CombineArgs {
-  const void* x;
-  int x_dtype;
-  const float* y_pairs;
-  const float* gates;
-  int T, k, d;
-  void* out;
-  int out_dtype;
-};
 cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 
 // CRC-32 of n records of record_bytes (a multiple of 16) each; checks them
@@ -250,6 +260,11 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s);
 int records_crc_units(size_t record_bytes);
 cudaError_t launch_records_check(const uint8_t* const* records, int n, size_t record_bytes, const uint32_t* expected,
                                  uint32_t* crc_out, uint32_t* unit_ws, int* err, int num_sms, cudaStream_t s);
+
+// y[t][n] = resid[t][n] (optional) + sum_k W[n][k] x[t][k] (project.cu); W
+// [N][K] bf16 or fp32 with K a multiple of 32, every pointer 16-byte aligned.
+cudaError_t launch_project(const void* x, int x_dtype, const void* w, int w_dtype, const void* resid, int resid_dtype,
+                           void* y, int y_dtype, int T, int K, int N, bool pdl, cudaStream_t s);
 
 // A wait that nothing completes, for testing the timeout path (selftest.cu).
 cudaError_t launch_wait_selftest(int* err, cudaStream_t s);

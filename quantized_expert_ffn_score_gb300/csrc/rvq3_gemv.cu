@@ -3,120 +3,421 @@
 // over 8-dim vectors, 3.00 bits per weight; a weight is the sum of its three
 // stage codewords).
 //
-// The weights are never materialised.  For one input vector x and one K-slice
-// of 32 vector positions (256 columns) the kernel builds, in shared memory,
-//   LUT[s][c][v] = <codebook_s[c], x[8v .. 8v+8)>      (fp32, 3 x 256 x 32)
+// The weights are never materialised.  For one input vector a (a token's x for
+// gate/up, a pair's h for down) and one K-slice of 32 vector positions (256
+// columns) the kernel builds, in shared memory,
+//   LUT[s][c][v] = <codebook_s[c], a[8v .. 8v+8)>      (fp32, 3 stages x 256 x 32)
 // so that a row's partial dot product over the slice is
 //   sum_v  LUT[0][code0[v][r]][v] + LUT[1][code1[v][r]][v] + LUT[2][code2[v][r]][v].
-// Lane l of every warp owns vector position v = l, so the 32 lanes of a lookup
-// hit 32 different banks whatever the codes are.  Codes are stored
-// position-major (rows contiguous for a fixed position), so lane l reads 32
-// consecutive rows' codes of its position with two 16-byte loads per stage.
-// A 32-lane reduce-scatter leaves row r0 + l's slice partial on lane l; the
-// slice partials go to a workspace buffer and a finalize kernel sums them in
-// ascending slice order (then applies the activation, or scatters y).
+// One table serves every matrix applied to the same vector: all of a token's
+// experts' gate and up rows (the codebooks are per layer), or a pair's down rows.
+//
+// Codes are stored position-major (rows contiguous for one position and
+// stage).  A producer warp stages the codes of one 512-row group into a
+// double-buffered ring of shared memory, a group ahead of the lookups: four TMA
+// boxes of [3 stages][32 positions][128 rows] (12 KB each, one instruction
+// apiece) with the 128-byte swizzle, so that each (stage, position) run of
+// 128 rows is one contiguous DRAM read and the 16-byte reads of 8 lanes fall
+// in 8 different bank groups.  The boxes' tensor map is the matrix's; its
+// address is patched on the device whenever the matrix changes.
+//
+// Lookups.  Lane l of a consumer warp owns position l of the slice: the 32
+// lanes of a lookup read 32 different banks whatever the codes are.  The
+// table sits at a 64 KB-aligned shared address L and keeps stages 0 and 1 in
+// the two halves of 256-byte rows -- entry (s, c, l) at L + c * 256 + 128 s +
+// 4 l, stage 2 at L + 65,536 + c * 256 + 4 l -- so one byte permute that puts
+// code c into byte 1 of the lane's base address (L + 4 l, byte 1 zero) is
+// already the entry's shared address.  The code ring's twelve-kilobyte boxes
+// fill the space either side of the table.
+// Each of the 16 consumer warps takes 32 rows of the staged group and
+// reduces its 32 per-lane row values over the lanes with a reduce-scatter.
+// Lane l accumulates in register j the row j XOR (a lane-dependent mask):
+// the code word it loads, the half of the word and the byte it picks are
+// chosen by its own lane bits, so four of the five halving steps swap no
+// registers before their shuffle; lane l ends with one row's slice sum.
+//
+// Work: units are (vector, slice, matrix, 256-row group) in this order; each
+// persistent CTA takes one contiguous range of units and rebuilds the table
+// when the (vector, slice) changes (about once or twice per CTA at decode
+// sizes) while the producer keeps staging codes.  Slice sums go to
+// pair-indexed partial buffers; the down kernel finishes h (the slice sums of
+// gate and up, then the activation) while it loads its vector, and the
+// combine adds the down kernel's slice sums, so no separate reduction pass
+// runs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 #include <utility>
 
 #include "moe_internal.cuh"
+#include "tc_ops.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRvqThreads = 256;
-constexpr int kRvqWarps = kRvqThreads / 32;
-constexpr int kSlicePos = 32;       // vector positions per K-slice
-constexpr int kChunkRowsMax = 1536; // rows per work unit
+constexpr int kConsumerWarps = 16;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kPos = 32;                              // vector positions per slice
+constexpr int kGroupRows = 512;                       // rows per staged group
+constexpr int kBoxRows = 128;                         // rows per TMA box (one 128-byte swizzle line)
+constexpr int kBoxesPerGroup = kGroupRows / kBoxRows;  // 4
+constexpr int kRowsPerWarp = kGroupRows / kConsumerWarps;  // 32
+constexpr int kBoxBytes = 3 * kPos * kBoxRows;        // 12,288
+constexpr int kBufs = 2;
+constexpr int kMapSlots = 8;  // per-CTA global tensor maps: a slot is reused after 8 matrix changes
+constexpr uint32_t kLutBytes = 131072;  // stages 0 and 1 interleaved (64 KB), stage 2 (64 KB, half used)
+constexpr uint32_t kVecBytes = 8 * kPos * sizeof(float);  // 1,024: the vector's slice
+constexpr uint32_t kUpOff = kVecBytes;                    // down: the up half's slice sums while h is formed
+constexpr uint32_t kMapOff = kUpOff + kVecBytes;          // 128-byte tensor map being patched
+constexpr uint32_t kBarOff = kMapOff + 128;
+constexpr uint32_t kValidOff = kBarOff + 2 * kBufs * sizeof(uint64_t);  // [kBufs] the staged group has a record
+constexpr uint32_t kMiscBytes = kValidOff + kBufs * sizeof(int);
+constexpr int kMaxPartsInFlight = 8;  // down: gate/up slice sums loaded at once per element of h
+constexpr int kBoxes = kBufs * kBoxesPerGroup;  // 8 boxes of 12 KB, 1024-byte aligned (128-byte swizzle atoms)
+constexpr size_t kSmem = 232448;                // all of it: the table, the boxes and the rest are placed at run time
+static_assert(kLutBytes + kBoxes * kBoxBytes + kMiscBytes <= kSmem, "shared memory per CTA");  // placement checked at run time
+constexpr int kMaxSmsRvq = 160;
 
-struct RGeom {
-  int K, rows, kinds, ns, nchunks, chunk_rows, upe;
-  size_t mat_bytes;   // one matrix: 3 * rows * K / 8
+// Where the table, the boxes and the small items go in this CTA's shared
+// window [s0, s0 + kSmem): the table at the first 64 KB boundary, boxes in
+// 1024-byte aligned runs before and after it, the small items in what is left
+// of either gap.  Offsets are from the start of the dynamic shared memory.
+struct SmemPlan {
+  uint32_t lut;
+  uint32_t box1, n1, box2;  // boxes n < n1 at box1 + n * kBoxBytes, the rest from box2
+  uint32_t misc;
+  bool ok;
+  __device__ uint32_t box(int n) const {
+    return n < (int)n1 ? box1 + n * kBoxBytes : box2 + (n - n1) * kBoxBytes;
+  }
 };
 
-RGeom make_rgeom(int mode, int d, int ff) {
+__device__ SmemPlan plan_smem(uint32_t s0) {
+  SmemPlan p;
+  const uint32_t end = s0 + (uint32_t)kSmem;
+  const uint32_t t = (s0 + 65535u) & ~65535u;
+  p.lut = t - s0;
+  const uint32_t a1 = (s0 + 1023u) & ~1023u;
+  p.n1 = t >= a1 ? min((uint32_t)kBoxes, (t - a1) / kBoxBytes) : 0u;
+  p.box1 = a1 - s0;
+  p.box2 = t + kLutBytes - s0;
+  const uint32_t after1 = a1 + p.n1 * kBoxBytes;          // first byte after the boxes before the table
+  const uint32_t after2 = t + kLutBytes + (kBoxes - p.n1) * kBoxBytes;
+  bool misc_ok = true;
+  if (after1 + kMiscBytes <= t)
+    p.misc = after1 - s0;
+  else if (after2 + kMiscBytes <= end)
+    p.misc = after2 - s0;
+  else
+    misc_ok = false;
+  p.ok = misc_ok && after2 <= end;
+  return p;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f32_128(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+128];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+// The codebooks (one or two of 3 x 256 codewords, 16 bytes each) sit in the
+// unused upper halves of the table's stage-2 rows: codeword i at table byte
+// 65,536 + (i / 8) * 256 + 128 + (i % 8) * 16.
+__device__ __forceinline__ uint32_t cb_offset(int i) {
+  return 65536u + (uint32_t)(i >> 3) * 256u + 128u + (uint32_t)(i & 7) * 16u;
+}
+__device__ __forceinline__ uint4 lds_u128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
+struct RGeom {
+  int K;         // contraction length of the matrices
+  int rows;      // rows of one matrix
+  int kv;        // K / 8 vector positions
+  int ns;        // slices: ceil(kv / 32)
+  int nvec;      // vectors: tokens (gate/up) or pairs (down)
+  int kcombo;    // gate/up: 1 when gate and up share a codebook (one table serves both), else 2
+  int nseg;      // matrices per (vector, table): gate/up ks * 2 / kcombo, down 1
+  int gpm;       // 512-row groups per matrix
+  int ks;        // pairs per token
+  int ns_gu;     // down: the gate/up kernel's slice count (its partials per row)
+  size_t mat_bytes;  // one matrix: 3 * rows * K / 8 (gate and up: ff x d; down: d x ff)
+};
+
+RGeom make_geom(int mode, const FfnArgs& a) {
   RGeom g;
-  g.K = mode == 0 ? d : ff;
-  g.rows = mode == 0 ? ff : d;
-  g.kinds = mode == 0 ? 2 : 1;
-  g.ns = (g.K / 8 + kSlicePos - 1) / kSlicePos;
-  g.chunk_rows = g.rows < kChunkRowsMax ? g.rows : kChunkRowsMax;
-  g.nchunks = (g.rows + g.chunk_rows - 1) / g.chunk_rows;
-  g.upe = g.kinds * g.ns * g.nchunks;
-  g.mat_bytes = (size_t)3 * ff * d / 8;
+  g.K = mode == 0 ? a.d : a.ff;
+  g.rows = mode == 0 ? a.ff : a.d;
+  g.kv = g.K / 8;
+  g.ns = (g.kv + kPos - 1) / kPos;
+  g.ks = a.k;
+  g.nvec = mode == 0 ? a.T : a.T * a.k;
+  g.kcombo = mode == 0 ? (a.cb[0] == a.cb[1] ? 1 : 2) : 1;
+  g.nseg = mode == 0 ? a.k * (2 / g.kcombo) : 1;
+  g.gpm = (g.rows + kGroupRows - 1) / kGroupRows;
+  g.ns_gu = (a.d / 8 + kPos - 1) / kPos;
+  g.mat_bytes = (size_t)3 * a.ff * a.d / 8;
   return g;
 }
 
-constexpr size_t kRvqSmem = (size_t)3 * 256 * kSlicePos * sizeof(float)  // LUT
-                            + 256 * sizeof(float)                        // x slice
-                            + 3 * 256 * sizeof(uint4);                   // codebooks
+// One unit: its table (vector, kind-of-table, slice) and its rows.
+struct Unit {
+  long long combo;
+  int vi, kc, slice;
+  int p, kind;  // pair and matrix (0 gate, 1 up, 2 down)
+  int r0, nrows;
+};
 
-template <int NV>
-__device__ __forceinline__ void reduce_scatter32(float (&v)[NV], int lane) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < m; ++i) {
-      const float send = upper ? v[i] : v[i + m];
-      const float keep = upper ? v[i + m] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-    }
+// Walks the units of a CTA's range in order without divisions (one set of
+// divisions at the start).
+struct UnitIter {
+  long long combo;
+  int slice, kc, vi, seg, grp;
+  __device__ void init(const RGeom& g, long long u) {
+    const long long per_combo = (long long)g.nseg * g.gpm;
+    combo = u / per_combo;
+    const int rem = (int)(u - combo * per_combo);
+    seg = rem / g.gpm;
+    grp = rem % g.gpm;
+    slice = (int)(combo % g.ns);
+    kc = (int)((combo / g.ns) % g.kcombo);
+    vi = (int)(combo / ((long long)g.ns * g.kcombo));
   }
+  __device__ void next(const RGeom& g) {
+    if (++grp < g.gpm) return;
+    grp = 0;
+    if (++seg < g.nseg) return;
+    seg = 0;
+    ++combo;
+    if (++slice < g.ns) return;
+    slice = 0;
+    if (++kc < g.kcombo) return;
+    kc = 0;
+    ++vi;
+  }
+  template <int MODE>
+  __device__ Unit unit(const RGeom& g) const {
+    Unit t;
+    t.combo = combo;
+    t.slice = slice;
+    t.kc = kc;
+    t.vi = vi;
+    if (MODE == 0) {
+      const int kpc = 2 / g.kcombo;  // kinds per table
+      t.p = vi * g.ks + seg / kpc;
+      t.kind = g.kcombo == 1 ? seg % kpc : kc;
+    } else {
+      t.p = vi;
+      t.kind = 2;
+    }
+    t.r0 = grp * kGroupRows;
+    t.nrows = min(kGroupRows, g.rows - t.r0);
+    return t;
+  }
+};
+
+// The record of pair p, or null (reported) when it is unusable.
+__device__ __forceinline__ const uint8_t* pair_record(const FfnArgs& a, const int32_t* pair_expert, int p,
+                                                     bool report) {
+  const int e = pair_expert[p];
+  const uint8_t* rec = (e >= 0 && e < a.E) ? a.records[e] : nullptr;
+  if (rec == nullptr || (reinterpret_cast<uintptr_t>(rec) & 15u)) {
+    if (report)
+      dev_error(a.err, (e < 0 || e >= a.E) ? MOE_ERR_BAD_EXPERT_INDEX
+                                           : (rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG), e);
+    return nullptr;
+  }
+  return rec;
 }
 
-__device__ __forceinline__ uint32_t byte_of(const uint4& q, int r) {  // r static after unrolling
-  const uint32_t w = (r >> 2) == 0 ? q.x : (r >> 2) == 1 ? q.y : (r >> 2) == 2 ? q.z : q.w;
-  return (w >> (8 * (r & 3))) & 0xFFu;
+// Shared address of the entry for the code in byte (sel >> 4 & 3) of w: that
+// byte replaces byte 1 of the lane's base address (L + 4 l, whose byte 1 is
+// zero) -> L + c * 256 + 4 l.
+__device__ __forceinline__ uint32_t lut_addr(uint32_t w, uint32_t base, uint32_t sel) {
+  return __byte_perm(w, base, sel);
 }
 
+// Sum over the 32 lanes of 32 values whose registers are XOR-permuted by the
+// lane bits 4..1 (register j of lane l holds row j ^ mask(l)): four halving
+// steps add the partner's upper half straight into the lower half; the last
+// (lane bit 0) swaps as usual.  Lane l ends with row mask(l)'s sum in v[0].
+__device__ __forceinline__ void reduce_scatter32_xor(float (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 16; m >= 2; m >>= 1) {
+#pragma unroll
+    for (int i = 0; i < m; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + m], m);
+  }
+  const bool upper = (lane & 1) != 0;
+  const float send = upper ? v[0] : v[1];
+  const float keep = upper ? v[1] : v[0];
+  v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+
+// MODE 0: gate/up (vectors = tokens; a table of kind kc, or of both kinds when
+// they share a codebook); MODE 1: down (vectors = pairs).
+//   gpart[((p * 2 + kind) * ns_gu + slice) * ff + row]
+//   dpart[(p * ns + slice) * d + row]
 template <int MODE>
-__global__ void __launch_bounds__(kRvqThreads, 2) rvq3_unit_kernel(const FfnArgs a, const RGeom g) {
-  extern __shared__ __align__(16) float rsm[];
-  float* lut = rsm;                                         // [3][256][32]
-  float* xs = lut + 3 * 256 * kSlicePos;                    // [256]
-  uint4* cbs = reinterpret_cast<uint4*>(xs + 256);          // [3][256]
+__global__ void __launch_bounds__(kThreads, 1)
+    rvq3_kernel(const FfnArgs a, const RGeom g, const int32_t* pair_expert, float* gpart, float* dpart,
+                const __grid_constant__ CUtensorMap tmpl, CUtensorMap* gmaps) {
+  extern __shared__ __align__(1024) uint8_t rsm[];
+  const uint32_t s0 = tc::saddr(rsm);
+  const SmemPlan plan = plan_smem(s0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (!plan.ok) {  // the shared window cannot hold the layout: nothing was touched
+    if (tid == 0) dev_error(a.err, MOE_ERR_UNSUPPORTED, (int)s0);
+    return;
+  }
+  uint8_t* lut = rsm + plan.lut;                                   // the table (layout above)
+  float* vec = reinterpret_cast<float*>(rsm + plan.misc);          // [256] the vector's slice
+  uint8_t* smap = rsm + plan.misc + kMapOff;                       // the tensor map being patched
+  uint64_t* full = reinterpret_cast<uint64_t*>(rsm + plan.misc + kBarOff);  // [kBufs]
+  uint64_t* empty = full + kBufs;                                           // [kBufs]
+  volatile int* bvalid = reinterpret_cast<volatile int*>(rsm + plan.misc + kValidOff);  // [kBufs]
+  // box i of buffer b: rsm + plan.box(b * kBoxesPerGroup + i), [3][32][128] bytes
+  if (tid == 0) {
+    for (int b = 0; b < kBufs; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kConsumerWarps) reinterpret_cast<uint32_t*>(smap)[lane] = reinterpret_cast<const uint32_t*>(&tmpl)[lane];
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
-  const int n_act = a.active[0];
-  const int total = n_act * g.upe;
-  for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
-    const int e = a.active[1 + unit / g.upe];
-    const uint8_t* rec = a.records[e];
-    if (rec == nullptr || (reinterpret_cast<uintptr_t>(rec) & 15u)) {
-      if (tid == 0) dev_error(a.err, rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG, e);
-      continue;
-    }
-    int u = unit % g.upe;
-    const int kind = u / (g.ns * g.nchunks);
-    u %= g.ns * g.nchunks;
-    const int slice = u / g.nchunks, chunk = u % g.nchunks;
-    const uint16_t* cb = a.cb[MODE == 0 ? kind : 2];
-    const uint8_t* mat = rec + (size_t)(MODE == 0 ? kind : 2) * g.mat_bytes;
-    const int v0 = slice * kSlicePos;
-    const int nv = min(kSlicePos, g.K / 8 - v0);
-    const int r_begin = chunk * g.chunk_rows, r_end = min(g.rows, r_begin + g.chunk_rows);
-    const int s0 = a.offsets[e], ne = a.offsets[e + 1] - s0;
-    __syncthreads();  // previous unit's readers of cbs / lut are done
-    for (int i = tid; i < 3 * 256; i += kRvqThreads) cbs[i] = reinterpret_cast<const uint4*>(cb)[i];
-    for (int q = 0; q < ne; ++q) {
-      const int slot = s0 + q;
-      __syncthreads();
-      for (int i = tid; i < 256; i += kRvqThreads) {
-        float v = 0.f;
-        if (i < 8 * nv) {
-          const int col = 8 * v0 + i;
-          v = MODE == 0 ? load_act(a.x, a.x_dtype, (size_t)(a.pair_ids[slot] / a.k) * a.d + col)
-                        : a.h[(size_t)slot * a.ff + col];
-        }
-        xs[i] = v;
+  const long long total = (long long)g.nvec * g.kcombo * g.ns * g.nseg * g.gpm;
+  const long long ub = total * blockIdx.x / gridDim.x, ue = total * (blockIdx.x + 1) / gridDim.x;
+  const int nu = (int)(ue - ub);
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer
+    int cur_p = -1, cur_kind = -1, slot = -1;
+    const uint8_t* rec = nullptr;
+    CUtensorMap* my_maps = gmaps + (size_t)blockIdx.x * kMapSlots;
+    int issued = 0;
+    UnitIter it;
+    it.init(g, ub);
+    for (int n = 0; n < nu; ++n, it.next(g)) {
+      const Unit t = it.unit<MODE>(g);
+      if (t.p != cur_p) {
+        rec = pair_record(a, pair_expert, t.p, lane == 0);
+        cur_p = t.p;
+        cur_kind = -1;
       }
-      __syncthreads();
-      {  // LUT build: warp w takes entries (s, c) = w, w + 8, ...; lane = position
+      const int b = n % kBufs;
+      int ok = 1;
+      if (lane == 0 && n >= kBufs && !mbar_wait(&empty[b], ((n / kBufs) - 1) & 1, a.err)) ok = 0;
+      if (__shfl_sync(0xffffffffu, ok, 0) == 0) break;
+      if (lane == 0) bvalid[b] = rec != nullptr;  // published by the arrival below
+      if (rec == nullptr) {  // nothing to stage: complete the phase without bytes
+        if (lane == 0) mbar_arrive(&full[b]);
+      } else {
+        if (t.kind != cur_kind) {  // the matrix's tensor map, in a slot no copy in flight still uses
+          cur_kind = t.kind;
+          slot = (slot + 1) % kMapSlots;
+          if (lane == 0) tc::tensormap_set_address(smap, rec + (size_t)t.kind * g.mat_bytes);
+          __syncwarp();
+          tc::tensormap_publish(my_maps + slot, smap);
+          if (lane == 0) tc::tensormap_acquire(my_maps + slot);
+          __syncwarp();
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[b], (uint32_t)(kBoxesPerGroup * kBoxBytes));
+          // boxes at (row r0 + 128 i, position v0, stage 0); rows past the matrix read zeros
+#pragma unroll
+          for (int i = 0; i < kBoxesPerGroup; ++i)
+            tc::tma_load_3d(rsm + plan.box(b * kBoxesPerGroup + i), my_maps + slot, t.r0 + i * kBoxRows,
+                            t.slice * kPos, 0, &full[b]);
+        }
+      }
+      issued = n + 1;
+    }
+    // never leave with copies in flight
+    if (lane == 0)
+      for (int j = (issued > kBufs ? issued - kBufs : 0); j < issued; ++j)
+        mbar_wait_drain(&full[j % kBufs], (j / kBufs) & 1, a.err);
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  long long lut_combo = -1;
+  bool alive = true;  // false after a wait ran out: the remaining units are skipped, barriers still met
+  {  // the codebooks this kernel's tables use, into the table's spare bytes (read after the first build's barrier)
+    const int ncb = MODE == 0 ? g.kcombo : 1;
+    for (int i = tid; i < ncb * 3 * 256; i += kConsumerWarps * 32) {
+      const int kc = i / (3 * 256);
+      const uint4* src = reinterpret_cast<const uint4*>(MODE == 0 ? a.cb[kc] : a.cb[2]);
+      *reinterpret_cast<uint4*>(lut + cb_offset(i)) = __ldg(src + (i - kc * 3 * 256));
+    }
+  }
+  const uint32_t lut_s = s0 + plan.lut;
+  const uint32_t base01 = s0 + plan.lut + 4u * (uint32_t)lane;  // stages 0 and 1 (+128)
+  const uint32_t base2 = base01 + 65536u;                         // stage 2
+  // the lane's register permutation: bit 4 of the row picks the 16-row chunk,
+  // bit 3 the 8-byte half of it, bits 1-0 the byte (lane bits 4, 3, 2-1)
+  const int l4 = (lane >> 4) & 1, l3 = (lane >> 3) & 1;
+  const uint32_t jx = ((uint32_t)lane >> 1) & 3u;
+  uint32_t sel[4];
+#pragma unroll
+  for (int J = 0; J < 4; ++J) sel[J] = 0x7604u | (((uint32_t)J ^ jx) << 4);
+  const int r_local = warp * kRowsPerWarp;
+  const int c0 = (r_local % kBoxRows) / 16;  // the warp's first 16-row chunk in its box
+  static_assert(kBufs == 2, "two buffers");
+  const uint32_t box_s0 = s0 + plan.box(r_local / kBoxRows), box_s1 = s0 + plan.box(kBoxesPerGroup + r_local / kBoxRows);
+  const int row_of_lane = 16 * l4 + 8 * l3 + 4 * (lane & 1) + (int)jx;
+  UnitIter uit;
+  uit.init(g, ub);
+  for (int n = 0; n < nu; ++n, uit.next(g)) {
+    const Unit t = uit.unit<MODE>(g);
+    const int v0 = t.slice * kPos, nv = min(kPos, g.kv - v0);  // positions past kv: zero vector, zero entries
+    if (t.combo != lut_combo) {  // a new (vector, slice): rebuild the table (uniform over the consumer warps)
+      named_bar_sync(1, kConsumerWarps * 32);  // the previous table's readers are done
+      if (MODE == 0) {
+        if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? load_act(a.x, a.x_dtype, (size_t)t.vi * a.d + 8 * v0 + tid) : 0.f;
+      } else {  // h of pair vi: each thread sums one gate or up element's slice sums (ascending), then the activation
+        float* up = reinterpret_cast<float*>(rsm + plan.misc + kUpOff);
+        const int i = tid & (8 * kPos - 1), kind = tid >> 8;
+        float sum = 0.f;
+        if (i < 8 * nv) {
+          const float* gp = gpart + ((size_t)t.vi * 2 + kind) * g.ns_gu * a.ff + 8 * v0 + i;
+          for (int q0 = 0; q0 < g.ns_gu; q0 += kMaxPartsInFlight) {  // loads in flight together, added in order
+            float pv[kMaxPartsInFlight];
+#pragma unroll
+            for (int q = 0; q < kMaxPartsInFlight; ++q)
+              if (q0 + q < g.ns_gu) pv[q] = gp[(size_t)(q0 + q) * a.ff];
+#pragma unroll
+            for (int q = 0; q < kMaxPartsInFlight; ++q)
+              if (q0 + q < g.ns_gu) sum += pv[q];
+          }
+        }
+        (kind == 0 ? vec : up)[i] = sum;
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? act_fn(vec[tid], up[tid], a.act) : 0.f;
+      }
+      named_bar_sync(1, kConsumerWarps * 32);
+      {  // table build: thread (eg, v) computes entries eg, eg + 16, ... of position v
+        const int v = tid & (kPos - 1), eg = tid >> 5;
         float xv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) xv[i] = xs[8 * lane + i];
-        for (int p = warp; p < 3 * 256; p += kRvqWarps) {
-          const uint4 c8 = cbs[p];
+        for (int i = 0; i < 8; ++i) xv[i] = vec[8 * v + i];
+#pragma unroll 4
+        for (int e = eg; e < 3 * 256; e += kConsumerWarps) {
+          const uint4 c8 = lds_u128(lut_s + cb_offset((MODE == 0 ? t.kc * 3 * 256 : 0) + e));  // one broadcast per warp
           const uint32_t hw[4] = {c8.x, c8.y, c8.z, c8.w};
           float acc = 0.f;
 #pragma unroll
@@ -125,226 +426,177 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq3_unit_kernel(const FfnArgs
             acc = fmaf(f.x, xv[2 * j], acc);
             acc = fmaf(f.y, xv[2 * j + 1], acc);
           }
-          lut[p * kSlicePos + lane] = acc;
+          const int st = e >> 8, c = e & 255;  // entry (stage, code)
+          const uint32_t off = st < 2 ? (uint32_t)(c * 256 + 128 * st + 4 * v) : (uint32_t)(65536 + c * 256 + 4 * v);
+          *reinterpret_cast<float*>(lut + off) = acc;
         }
       }
-      __syncthreads();
-      const bool vl = lane < nv;
-      const float* l0 = lut + lane;
-      const float* l1 = lut + 256 * kSlicePos + lane;
-      const float* l2 = lut + 2 * 256 * kSlicePos + lane;
-      for (int rg = r_begin + 32 * warp; rg < r_end; rg += 32 * kRvqWarps) {
-        float acc[32];
-        if (vl) {
-          uint4 c[3][2];
+      named_bar_sync(1, kConsumerWarps * 32);
+      lut_combo = t.combo;
+    }
+    const int b = n % kBufs;
+    if (alive && !mbar_wait(&full[b], (n / kBufs) & 1, a.err)) alive = false;
+    const bool mine = alive && bvalid[b] != 0 && r_local < t.nrows;  // no record: the producer reported it
+    uint2 q[3][2][2];  // stage s, chunk h, half hf (words 2 hf, 2 hf + 1) of the lane's permuted view
+    if (mine) {
+      const uint32_t box_s = b ? box_s1 : box_s0;
+      // line (stage s, position lane) of the box; its 16-byte chunks are swizzled by the line index
 #pragma unroll
-          for (int s = 0; s < 3; ++s) {
-            const uint4* p = reinterpret_cast<const uint4*>(mat + ((size_t)s * (g.K / 8) + v0 + lane) * g.rows + rg);
-            c[s][0] = __ldg(p);
-            c[s][1] = __ldg(p + 1);
-          }
+      for (int st = 0; st < 3; ++st) {
+        const int line = st * kPos + lane;
 #pragma unroll
-          for (int r = 0; r < 32; ++r) {
-            const uint32_t k0 = byte_of(c[0][r >> 4], r & 15);
-            const uint32_t k1 = byte_of(c[1][r >> 4], r & 15);
-            const uint32_t k2 = byte_of(c[2][r >> 4], r & 15);
-            acc[r] = l0[k0 * kSlicePos] + l1[k1 * kSlicePos] + l2[k2 * kSlicePos];
-          }
-        } else {
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int r = 0; r < 32; ++r) acc[r] = 0.f;
-        }
-        reduce_scatter32<32>(acc, lane);
-        a.partial[(((size_t)slot * g.kinds + kind) * g.ns + slice) * g.rows + rg + lane] = acc[0];
+          for (int hf = 0; hf < 2; ++hf)
+            q[st][h][hf] = lds_u64(box_s + (uint32_t)(line * kBoxRows + (((c0 + (h ^ l4)) ^ (line & 7)) * 16) +
+                                                         8 * (hf ^ l3)));
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[b]);  // the codes are in registers: the buffer can be refilled
+    if (!mine) continue;
+    // register j = 16 h + 8 hf + 2 J + wd holds row 16 (h ^ l4) + 8 (hf ^ l3) + 4 wd + (J ^ jx);
+    // positions past the matrix have all-zero table entries, so every lane adds
+    float acc[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int wd = 0; wd < 2; ++wd) {
+          const uint32_t w0 = wd ? q[0][h][hf].y : q[0][h][hf].x;
+          const uint32_t w1 = wd ? q[1][h][hf].y : q[1][h][hf].x;
+          const uint32_t w2 = wd ? q[2][h][hf].y : q[2][h][hf].x;
+#pragma unroll
+          for (int J = 0; J < 4; ++J)
+            acc[16 * h + 8 * hf + 2 * J + wd] = lds_f32(lut_addr(w0, base01, sel[J])) +
+                                                lds_f32_128(lut_addr(w1, base01, sel[J])) +
+                                                lds_f32(lut_addr(w2, base2, sel[J]));
+        }
+    reduce_scatter32_xor(acc, lane);
+    const int r = t.r0 + r_local + row_of_lane;
+    if (MODE == 0)
+      gpart[(((size_t)t.p * 2 + t.kind) * g.ns + t.slice) * a.ff + r] = acc[0];
+    else
+      dpart[((size_t)t.p * g.ns + t.slice) * a.d + r] = acc[0];
   }
 }
 
-// The same lookups with the table shared by every expert of a token (gate/up:
-// the codebooks are per layer and the experts of a token see the same x) or
-// of a slot (down: h is per slot).  Work units, in this order:
-//   (group g, kind, slice, slot of the group, 1536-row chunk)
-// with g = token (MODE 0, the token's k slots) or slot (MODE 1, one slot);
-// each unit streams one expert's rows of the slice (long contiguous runs per
-// vector position), persistent CTAs take contiguous unit ranges and rebuild
-// the table only when (g, kind, slice) changes.  For at most kLutMaxPairs pairs.
-constexpr int kLutChunk = 1536;
-constexpr int kLutMaxPairs = 512;
-constexpr size_t kLutSmem = kRvqSmem + 2 * kLutMaxPairs * sizeof(uint16_t);  // two CTAs per SM
-
-template <int MODE>
-__global__ void __launch_bounds__(kRvqThreads, 2) rvq3_lut_kernel(const FfnArgs a, const RGeom g) {
-  extern __shared__ __align__(16) float rsm[];
-  float* lut = rsm;                                         // [3][256][32]
-  float* xs = lut + 3 * 256 * kSlicePos;                    // [256]
-  uint4* cbs = reinterpret_cast<uint4*>(xs + 256);          // [3][256]
-  uint16_t* slot_of_pair = reinterpret_cast<uint16_t*>(cbs + 3 * 256);  // [P]
-  uint16_t* expert_of_slot = slot_of_pair + kLutMaxPairs;                // [P]
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// pair_expert[pair_ids[s]] = the expert whose bucket holds slot s (the
+// standalone expert call, which gets buckets instead of the routing).
+__global__ void pair_expert_kernel(const int32_t* offsets, const int32_t* pair_ids, int E, int32_t* pair_expert) {
   pdl_wait();
   pdl_launch_dependents();
+  for (int e = blockIdx.x; e < E; e += gridDim.x)
+    for (int s = offsets[e] + threadIdx.x; s < offsets[e + 1]; s += blockDim.x) pair_expert[pair_ids[s]] = e;
+}
+
+// y_pairs[p][i] = sum over slices of the down kernel's partial sums (ascending).
+__global__ void sum_parts_kernel(const float* dpart, int ns, int d, long long n, float* y_pairs) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const long long p = i / d, r = i % d;
+    const float* src = dpart + (size_t)p * ns * d + r;
+    float s = 0.f;
+    for (int k = 0; k < ns; ++k) s += src[(size_t)k * d];
+    y_pairs[i] = s;
+  }
+}
+
+struct Parts {
+  CUtensorMap* maps;
+  float* gpart;
+  float* dpart;
+  int32_t* pair_expert;
+};
+
+// The partial area: per-CTA tensor-map slots (64-byte aligned), then the
+// gate/up and down partial sums and the pair -> expert list.
+constexpr size_t kMapFloats = (size_t)kMaxSmsRvq * kMapSlots * sizeof(CUtensorMap) / sizeof(float);
+
+Parts carve_parts(const FfnArgs& a) {
   const int P = a.T * a.k;
-  for (int i = tid; i < P; i += kRvqThreads) slot_of_pair[a.pair_ids[i]] = (uint16_t)i;
-  const int n_act = a.active[0];
-  for (int ai = warp; ai < n_act; ai += kRvqWarps) {
-    const int e = a.active[1 + ai];
-    for (int sl = a.offsets[e] + lane; sl < a.offsets[e + 1]; sl += 32) expert_of_slot[sl] = (uint16_t)e;
-  }
-  const int ngroups = MODE == 0 ? a.T : P;
-  const int nchunks = (g.rows + kLutChunk - 1) / kLutChunk;
-  const int nslots = MODE == 0 ? a.k : 1;
-  const long long total = (long long)ngroups * g.kinds * g.ns * nslots * nchunks;
-  const int ub = (int)(total * blockIdx.x / gridDim.x), ue = (int)(total * (blockIdx.x + 1) / gridDim.x);
-  int cur_key = -1, cur_kind = -1;
-  for (int unit = ub; unit < ue; ++unit) {
-    int u = unit;
-    const int chunk = u % nchunks;
-    u /= nchunks;
-    const int j = u % nslots;
-    u /= nslots;
-    const int slice = u % g.ns;
-    u /= g.ns;
-    const int kind = u % g.kinds;
-    const int grp = u / g.kinds;
-    const int key = (grp * g.kinds + kind) * g.ns + slice;
-    const int v0 = slice * kSlicePos;
-    const int nv = min(kSlicePos, g.K / 8 - v0);
-    __syncthreads();  // the prologue's tables; the previous unit's readers of lut / cbs / xs
-    if (key != cur_key) {
-      if (kind != cur_kind) {
-        const uint16_t* cb = a.cb[MODE == 0 ? kind : 2];
-        for (int i = tid; i < 3 * 256; i += kRvqThreads) cbs[i] = reinterpret_cast<const uint4*>(cb)[i];
-        cur_kind = kind;
-      }
-      for (int i = tid; i < 256; i += kRvqThreads) {
-        float v = 0.f;
-        if (i < 8 * nv) {
-          const int col = 8 * v0 + i;
-          v = MODE == 0 ? load_act(a.x, a.x_dtype, (size_t)grp * a.d + col) : a.h[(size_t)grp * a.ff + col];
-        }
-        xs[i] = v;
-      }
-      __syncthreads();
-      float xv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xv[i] = xs[8 * lane + i];
-      for (int p = warp; p < 3 * 256; p += kRvqWarps) {
-        const uint4 c8 = cbs[p];
-        const uint32_t hw[4] = {c8.x, c8.y, c8.z, c8.w};
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
-          acc = fmaf(f.x, xv[2 * j], acc);
-          acc = fmaf(f.y, xv[2 * j + 1], acc);
-        }
-        lut[p * kSlicePos + lane] = acc;
-      }
-      cur_key = key;
-      __syncthreads();
-    }
-    const bool vl = lane < nv;
-    const float* l0 = lut + lane;
-    const float* l1 = lut + 256 * kSlicePos + lane;
-    const float* l2 = lut + 2 * 256 * kSlicePos + lane;
-    const int r_begin = chunk * kLutChunk, r_end = min(g.rows, r_begin + kLutChunk);
-    const int ngrp = (r_end - r_begin + 31) / 32;
-    // 32-row groups of the unit's expert rows; warp w takes groups w, w + 8, ...
-    const int slot = MODE == 0 ? slot_of_pair[grp * a.k + j] : grp;
-    for (int task = warp; task < ngrp; task += kRvqWarps) {
-      const int rg = r_begin + 32 * task;
-      const int e = expert_of_slot[slot];
-      const uint8_t* rec = a.records[e];
-      if (rec == nullptr || (reinterpret_cast<uintptr_t>(rec) & 15u)) {
-        if (lane == 0) dev_error(a.err, rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG, e);
-        continue;
-      }
-      const uint8_t* mat = rec + (size_t)(MODE == 0 ? kind : 2) * g.mat_bytes;
-      float acc[32];
-      if (vl) {
-        uint4 c[3][2];
-#pragma unroll
-        for (int st = 0; st < 3; ++st) {
-          const uint4* q = reinterpret_cast<const uint4*>(mat + ((size_t)st * (g.K / 8) + v0 + lane) * g.rows + rg);
-          c[st][0] = __ldg(q);
-          c[st][1] = __ldg(q + 1);
-        }
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const uint32_t k0 = byte_of(c[0][r >> 4], r & 15);
-          const uint32_t k1 = byte_of(c[1][r >> 4], r & 15);
-          const uint32_t k2 = byte_of(c[2][r >> 4], r & 15);
-          acc[r] = l0[k0 * kSlicePos] + l1[k1 * kSlicePos] + l2[k2 * kSlicePos];
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < 32; ++r) acc[r] = 0.f;
-      }
-      reduce_scatter32<32>(acc, lane);
-      a.partial[(((size_t)slot * g.kinds + kind) * g.ns + slice) * g.rows + rg + lane] = acc[0];
-    }
-  }
+  const int ns_gu = (a.d / 8 + kPos - 1) / kPos, ns_dn = (a.ff / 8 + kPos - 1) / kPos;
+  Parts pt;
+  pt.maps = reinterpret_cast<CUtensorMap*>(a.partial);
+  pt.gpart = a.partial + kMapFloats;
+  pt.dpart = pt.gpart + (size_t)P * 2 * ns_gu * a.ff;
+  pt.pair_expert = reinterpret_cast<int32_t*>(pt.dpart + (size_t)P * ns_dn * a.d);
+  return pt;
 }
 
-// Sums the slice partials in ascending slice order.
-template <int MODE>
-__global__ void rvq3_finalize_kernel(const FfnArgs a, const RGeom g, int P) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  if (idx >= (size_t)P * g.rows) return;
-  const int slot = (int)(idx / g.rows), r = (int)(idx % g.rows);
-  const float* base = a.partial + (size_t)slot * g.kinds * g.ns * g.rows + r;
-  float s0 = 0.f;
-  for (int s = 0; s < g.ns; ++s) s0 += base[(size_t)s * g.rows];
-  if (MODE == 0) {
-    float s1 = 0.f;
-    for (int s = 0; s < g.ns; ++s) s1 += base[(size_t)(g.ns + s) * g.rows];
-    a.h[(size_t)slot * a.ff + r] = act_fn(s0, s1, a.act);
-  } else {
-    a.y_pairs[(size_t)a.pair_ids[slot] * a.d + r] = s0;
-  }
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// One matrix's codes as a 3-D byte tensor (row, position, stage): strides
+// `rows` bytes (position) and kv * rows bytes (stage); one box = 128 rows x 32
+// positions x 3 stages with the 128-byte swizzle.  The address is replaced
+// per matrix on the device.
+bool make_code_map(CUtensorMap* m, const void* any_base, const RGeom& g) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)g.rows, (cuuint64_t)g.kv, 3};
+  cuuint64_t strides[2] = {(cuuint64_t)g.rows, (cuuint64_t)g.kv * g.rows};
+  cuuint32_t box[3] = {kBoxRows, kPos, 3};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(any_base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 size_t rvq3_partial_floats(int T, int k, int d, int ff) {
-  const RGeom g0 = make_rgeom(0, d, ff), g1 = make_rgeom(1, d, ff);
-  const size_t per0 = (size_t)g0.kinds * g0.ns * g0.rows, per1 = (size_t)g1.kinds * g1.ns * g1.rows;
-  return (size_t)T * k * (per0 > per1 ? per0 : per1);
+  const size_t P = (size_t)T * k;
+  const size_t ns_gu = (d / 8 + kPos - 1) / kPos, ns_dn = (ff / 8 + kPos - 1) / kPos;
+  return kMapFloats + P * (2 * ns_gu * ff + ns_dn * d + 1);  // tensor maps, partials, pair -> expert
 }
 
-cudaError_t launch_rvq3_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s) {
+int rvq3_down_parts(int d, int ff) {
+  (void)d;
+  return (ff / 8 + kPos - 1) / kPos;
+}
+
+float* rvq3_down_partials(const FfnArgs& a) { return carve_parts(a).dpart; }
+
+cudaError_t launch_rvq3_ffn(const FfnArgs& a, const int32_t* pair_expert, bool y_out, int num_sms, bool pdl,
+                            cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  const int P = a.T * a.k;
-  const RGeom g0 = make_rgeom(0, a.d, a.ff), g1 = make_rgeom(1, a.d, a.ff);
-  const dim3 grid(2 * num_sms);
-  const bool lut_shared = P <= kLutMaxPairs && a.E <= 65536 && g0.rows % 32 == 0 && g1.rows % 32 == 0;
-  // down tables are per slot: sharing saves nothing at one token, where the per-expert units are faster
-  // (K3 shape: 59 against 64 us); gate/up tables are shared by the token's experts (93 -> 90 us)
-  const bool lut_down = lut_shared && a.T >= 2;
+  const Parts pt = carve_parts(a);
   cudaError_t err;
-  if (lut_shared) {
-    ensure_smem(rvq3_lut_kernel<0>, kLutSmem);
-    err = launch("rvq3_gate_up", rvq3_lut_kernel<0>, grid, dim3(kRvqThreads), kLutSmem, s, pdl, a, g0);
-  } else {
-    ensure_smem(rvq3_unit_kernel<0>, kRvqSmem);
-    err = launch("rvq3_gate_up", rvq3_unit_kernel<0>, grid, dim3(kRvqThreads), kRvqSmem, s, pdl, a, g0);
+  if (pair_expert == nullptr) {  // from the buckets
+    err = launch("rvq3_pair_expert", pair_expert_kernel, dim3(num_sms), dim3(128), 0, s, pdl, a.offsets, a.pair_ids,
+                 a.E, pt.pair_expert);
+    if (err != cudaSuccess) return err;
+    pair_expert = pt.pair_expert;
+    pdl = true;
   }
+  if (num_sms > kMaxSmsRvq) return cudaErrorInvalidValue;  // the map slots are sized for this many CTAs
+  const RGeom g0 = make_geom(0, a), g1 = make_geom(1, a);
+  CUtensorMap m0, m1;
+  if (!make_code_map(&m0, pt.gpart, g0) || !make_code_map(&m1, pt.gpart, g1)) return cudaErrorInvalidValue;
+  ensure_smem(rvq3_kernel<0>, kSmem);
+  ensure_smem(rvq3_kernel<1>, kSmem);
+  err = launch("rvq3_gate_up", rvq3_kernel<0>, dim3(num_sms), dim3(kThreads), kSmem, s, pdl, a, g0, pair_expert,
+               pt.gpart, pt.dpart, m0, pt.maps);
   if (err != cudaSuccess) return err;
-  const size_t n0 = (size_t)P * g0.rows, n1 = (size_t)P * g1.rows;
-  err = launch("rvq3_gate_up_sum", rvq3_finalize_kernel<0>, dim3((unsigned)((n0 + 255) / 256)), dim3(256), 0, s, true, a, g0, P);
-  if (err != cudaSuccess) return err;
-  if (lut_down) {
-    ensure_smem(rvq3_lut_kernel<1>, kLutSmem);
-    err = launch("rvq3_down", rvq3_lut_kernel<1>, grid, dim3(kRvqThreads), kLutSmem, s, true, a, g1);
-  } else {
-    ensure_smem(rvq3_unit_kernel<1>, kRvqSmem);
-    err = launch("rvq3_down", rvq3_unit_kernel<1>, grid, dim3(kRvqThreads), kRvqSmem, s, true, a, g1);
-  }
-  if (err != cudaSuccess) return err;
-  return launch("rvq3_down_sum", rvq3_finalize_kernel<1>, dim3((unsigned)((n1 + 255) / 256)), dim3(256), 0, s, true, a, g1, P);
+  err = launch("rvq3_down", rvq3_kernel<1>, dim3(num_sms), dim3(kThreads), kSmem, s, true, a, g1, pair_expert,
+               pt.gpart, pt.dpart, m1, pt.maps);
+  if (err != cudaSuccess || !y_out) return err;
+  const long long n = (long long)a.T * a.k * a.d;
+  return launch("rvq3_sum_parts", sum_parts_kernel, dim3(2 * num_sms), dim3(256), 0, s, true, pt.dpart, g1.ns, a.d, n,
+                a.y_pairs);
 }
 
 }  // namespace moe

@@ -238,6 +238,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(mbar))
       : "memory");
 }
+// 3-D tiled load of one box at element coordinates (c0 innermost, c1, c2),
+// completing its bytes on `mbar`.  c0 * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          saddr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(saddr(mbar))
+      : "memory");
+}
 // 4-D tiled load of one box at element coordinates (c0 innermost .. c3),
 // completing its bytes on `mbar`.  c0 * element size must be a multiple of 16.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,

@@ -33,7 +33,9 @@ EXPORTS = ["moe_status_str", "moe_version", "moe_ctx_create", "moe_ctx_destroy",
            "moe_bucket_tokens", "moe_expert_ffn_mxfp4", "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward",
            "moe_stack_forward", "moe_stack_forward_ex", "moe_expert_ffn_mxfp4_static",
            "moe_expert_ffn_mxfp4_static_max_bytes", "moe_records_check_ws_bytes", "moe_records_check",
-           "moe_ctx_set_wait_limit_ns", "moe_ctx_wait_selftest", "moe_rvq3_repack"]
+           "moe_ctx_set_wait_limit_ns", "moe_ctx_wait_selftest", "moe_rvq3_repack", "moe_tier_create",
+           "moe_tier_destroy", "moe_tier_observe", "moe_tier_rebalance", "moe_tier_pin", "moe_tier_residency",
+           "moe_tier_plan", "moe_project", "moe_latent_layer_forward_ws_bytes", "moe_latent_layer_forward"]
 
 
 class MoeError(RuntimeError):
@@ -51,6 +53,12 @@ class MxExperts(ctypes.Structure):
 class RvqExperts(ctypes.Structure):
     _fields_ = [("records", ctypes.c_void_p), ("codebooks", ctypes.c_void_p * 3), ("d", ctypes.c_int),
                 ("ff", ctypes.c_int), ("E", ctypes.c_int)]
+
+
+class TierDesc(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("record_bytes", ctypes.c_size_t), ("host_records", ctypes.c_void_p),
+                ("slots", ctypes.c_void_p), ("n_slots", ctypes.c_int), ("slot_stride", ctypes.c_size_t),
+                ("records", ctypes.c_void_p), ("direct_host", ctypes.c_int), ("decay", ctypes.c_float)]
 
 
 class LayerStruct(ctypes.Structure):
@@ -115,10 +123,24 @@ def lib():
         L.moe_ctx_set_wait_limit_ns.argtypes = [vp, ctypes.c_ulonglong]
         L.moe_ctx_wait_selftest.argtypes = [vp, vp]
         L.moe_rvq3_repack.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.moe_tier_create.argtypes = [vp, ctypes.POINTER(TierDesc), ctypes.POINTER(vp)]
+        L.moe_tier_destroy.argtypes, L.moe_tier_destroy.restype = [vp], None
+        L.moe_tier_observe.argtypes = [vp, vp, vp]
+        L.moe_tier_rebalance.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        L.moe_tier_pin.argtypes = [vp, vp, i32, vp]
+        L.moe_tier_residency.argtypes = [vp, vp, vp]
+        L.moe_tier_plan.argtypes, L.moe_tier_plan.restype = [i32, i32, vp, vp, vp, vp], i32
+        L.moe_project.argtypes = [vp, vp, i32, i32, i32, vp, i32, i32, vp, i32, vp, i32, vp]
+        L.moe_latent_layer_forward_ws_bytes.argtypes = [ctypes.POINTER(LayerStruct), i32, i32]
+        L.moe_latent_layer_forward_ws_bytes.restype = sz
+        L.moe_latent_layer_forward.argtypes = [vp, ctypes.POINTER(LayerStruct), vp, vp, i32, i32, vp, i32, i32, vp,
+                                               i32, vp, vp, sz, vp]
         for f in ("moe_ctx_create", "moe_ctx_check", "moe_route_topk", "moe_route_topk_ex", "moe_bucket_tokens",
                   "moe_expert_ffn_mxfp4",
                   "moe_expert_ffn_rvq3", "moe_combine", "moe_layer_forward", "moe_stack_forward", "moe_stack_forward_ex",
-                  "moe_ctx_set_wait_limit_ns", "moe_ctx_wait_selftest", "moe_rvq3_repack"):
+                  "moe_ctx_set_wait_limit_ns", "moe_ctx_wait_selftest", "moe_rvq3_repack", "moe_tier_create",
+                  "moe_tier_observe", "moe_tier_rebalance", "moe_tier_pin", "moe_tier_residency", "moe_project",
+                  "moe_latent_layer_forward"):
             getattr(L, f).restype = i32
         L.moe_ctx_num_sms.restype = i32
         L.moe_ctx_set_mxfp4_kernel.argtypes, L.moe_ctx_set_mxfp4_kernel.restype = [vp, i32], i32
@@ -398,3 +420,100 @@ def moe_rvq3_repack(ctx, src_records, dst_records, n, d, ff, stream=None):
     device int64 tensors of n record pointers)."""
     _check(lib().moe_rvq3_repack(ctx.handle, _ptr(src_records), _ptr(dst_records), n, d, ff, _stream(stream)),
            "moe_rvq3_repack")
+
+
+# ----------------------------------------------------------------------------- experts beyond HBM
+
+def tier_plan(heat, has_host, slot_of, n_slots):
+    """moe_tier_plan (host only): (new slot of each expert or -1, experts moved)."""
+    import numpy as np
+    heat = np.ascontiguousarray(heat, dtype=np.float32)
+    has = np.ascontiguousarray(has_host, dtype=np.uint8)
+    cur = np.ascontiguousarray(slot_of, dtype=np.int32)
+    out = np.empty(heat.size, dtype=np.int32)
+    n = lib().moe_tier_plan(heat.size, n_slots, heat.ctypes.data, has.ctypes.data, cur.ctypes.data, out.ctypes.data)
+    if n < 0:
+        raise MoeError(1, "moe_tier_plan")
+    return out, n
+
+
+class Tier:
+    """A moe_tier over one layer's bank.  host_bank: page-locked uint8 CPU
+    tensor holding E records stride bytes apart (None entries in `present`
+    mark experts without a host copy); slots: CUDA uint8 tensor of n_slots x
+    stride bytes; records: CUDA int64 tensor [E], the table the layer reads."""
+
+    def __init__(self, ctx, E, record_bytes, stride, host_bank, slots, n_slots, records, direct_host=True,
+                 decay=1.0, present=None):
+        self.ctx = ctx
+        base = host_bank.data_ptr()
+        ptrs = [base + e * stride if (present is None or present[e]) else None for e in range(E)]
+        self._host_ptrs = (ctypes.c_void_p * E)(*ptrs)
+        self._keep = (host_bank, slots, records)
+        d = TierDesc()
+        d.E, d.record_bytes, d.host_records = E, record_bytes, ctypes.cast(self._host_ptrs, ctypes.c_void_p)
+        d.slots, d.n_slots, d.slot_stride = _ptr(slots), n_slots, stride
+        d.records, d.direct_host, d.decay = _ptr(records), 1 if direct_host else 0, decay
+        self._desc = d
+        h = ctypes.c_void_p()
+        _check(lib().moe_tier_create(ctx.handle, ctypes.byref(d), ctypes.byref(h)), "moe_tier_create")
+        self.handle = h
+        self.E = E
+
+    def observe(self, counts, stream=None):
+        _check(lib().moe_tier_observe(self.handle, _ptr(counts), _stream(stream)), "moe_tier_observe")
+
+    def rebalance(self, stream=None):
+        n = ctypes.c_int(0)
+        _check(lib().moe_tier_rebalance(self.handle, _stream(stream), ctypes.byref(n)), "moe_tier_rebalance")
+        return n.value
+
+    def pin(self, experts, stream=None):
+        import numpy as np
+        a = np.ascontiguousarray(experts, dtype=np.int32)
+        _check(lib().moe_tier_pin(self.handle, a.ctypes.data if a.size else None, a.size, _stream(stream)),
+               "moe_tier_pin")
+
+    def residency(self):
+        """(slot of each expert or -1, heat) as numpy arrays."""
+        import numpy as np
+        slot = np.empty(self.E, dtype=np.int32)
+        heat = np.empty(self.E, dtype=np.float32)
+        _check(lib().moe_tier_residency(self.handle, slot.ctypes.data, heat.ctypes.data), "moe_tier_residency")
+        return slot, heat
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().moe_tier_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ----------------------------------------------------------------------------- latent projections
+
+def moe_project(ctx, x, w, y, resid=None, stream=None):
+    """y[t][n] = resid[t][n] + sum_k w[n][k] x[t][k] (x [T][K], w [N][K], y [T][N])."""
+    T, K = x.shape
+    N = w.shape[0]
+    rdt = _dt(resid) if resid is not None else MOE_F32
+    _check(lib().moe_project(ctx.handle, _ptr(x), _dt(x), T, K, _ptr(w), _dt(w), N, _ptr(resid), rdt, _ptr(y), _dt(y),
+                             _stream(stream)), "moe_project")
+
+
+def latent_layer_forward_ws_bytes(layer, D, T):
+    return int(lib().moe_latent_layer_forward_ws_bytes(ctypes.byref(layer.struct), D, T))
+
+
+def moe_latent_layer_forward(ctx, layer, w_in, w_out, x, out, ws, latent_out=None, stream=None):
+    """The layer in its latent space for hidden-width x [T][D]: out = x + w_out (MoE delta of bf16(w_in x));
+    latent_out (int16/bf16 [T][d], optional) receives bf16(w_in x)."""
+    T, D = x.shape
+    assert _dt(w_in) == _dt(w_out)
+    _check(lib().moe_latent_layer_forward(ctx.handle, ctypes.byref(layer.struct), _ptr(w_in), _ptr(w_out), _dt(w_in), D,
+                                          _ptr(x), _dt(x), T, _ptr(out), _dt(out), _ptr(latent_out), _ptr(ws),
+                                          ws.numel(), _stream(stream)), "moe_latent_layer_forward")

@@ -5,7 +5,7 @@ it also takes buckets of up to a few hundred tokens, which it serves in passes
 of 8 tokens (the warp-level MMA's N) over each staged weight tile.
 
 Cases: a Zipf-skewed router (one bucket of many 8-token passes with a ragged
-last pass, many buckets of one token), every bucket about 50 tokens with the
+last pass, small buckets of one pass), every bucket about 50 tokens with the
 last expert's bucket reaching the end of the slot range, SiTU, the standalone
 expert call against the oracle's per-pair outputs, and a missing expert
 reported on the error word."""
@@ -43,7 +43,7 @@ def test_zipf_buckets_in_many_passes(lib, ctx):
     _, counts = gu.full_check(lib, ctx, ZIPF)
     assert counts.max() > 16 * 8, "needs a bucket of many 8-token passes"
     assert np.any((counts > 8) & (counts % 8 != 0)), "needs a ragged last pass"
-    assert np.any(counts == 1), "needs one-token buckets too"
+    assert np.any((counts > 0) & (counts <= 8)), "needs one-pass buckets too"
 
 
 def test_uniform_buckets_last_expert_at_end_of_slots(lib, ctx):
