@@ -230,20 +230,24 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
 
   // warp 0 reduces, warps 1 .. W compute (warp w owns blocks [BPW (w-1), BPW w)), warp W + 1 loads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int W = g.warps;
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], W);
+      mbar_init(&empty[s], g.warps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&red_full[b], W);
+      mbar_init(&red_full[b], g.warps);
       mbar_init(&red_empty[b], 1);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();
+  // The down pass's producer stages weights only, and the routing it follows
+  // was written two launches earlier (complete before the gate/up pass passed
+  // its own wait, which precedes this launch): it starts streaming while the
+  // gate/up pass finishes.  Everything that reads h or writes outputs waits.
+  const int W = g.warps;
+  if (MODE == 0 || warp != W + 1) pdl_wait();
   pdl_launch_dependents();
 
   const long long total = (long long)a.active[0] * g.tpe;

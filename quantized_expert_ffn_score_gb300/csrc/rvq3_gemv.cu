@@ -298,7 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kConsumerWarps) reinterpret_cast<uint32_t*>(smap)[lane] = reinterpret_cast<const uint32_t*>(&tmpl)[lane];
   __syncthreads();
-  pdl_wait();
+  // The down kernel's producer stages codes only, for routing written before
+  // the gate/up kernel passed its own wait (which precedes this launch), into
+  // tensor-map slots of its own: it starts while the gate/up kernel finishes.
+  // The consumers read the gate/up sums, so they wait.
+  if (MODE == 0 || warp != kConsumerWarps) pdl_wait();
   pdl_launch_dependents();
   const long long total = (long long)g.nvec * g.kcombo * g.ns * g.nseg * g.gpm;
   const long long ub = total * blockIdx.x / gridDim.x, ue = total * (blockIdx.x + 1) / gridDim.x;
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- producer
     int cur_p = -1, cur_kind = -1, slot = -1;
     const uint8_t* rec = nullptr;
-    CUtensorMap* my_maps = gmaps + (size_t)blockIdx.x * kMapSlots;
+    CUtensorMap* my_maps = gmaps + ((size_t)MODE * kMaxSmsRvq + blockIdx.x) * kMapSlots;  // per kernel and CTA
     int issued = 0;
     UnitIter it;
     it.init(g, ub);
@@ -513,7 +517,7 @@ struct Parts {
 
 // The partial area: per-CTA tensor-map slots (64-byte aligned), then the
 // gate/up and down partial sums and the pair -> expert list.
-constexpr size_t kMapFloats = (size_t)kMaxSmsRvq * kMapSlots * sizeof(CUtensorMap) / sizeof(float);
+constexpr size_t kMapFloats = (size_t)2 * kMaxSmsRvq * kMapSlots * sizeof(CUtensorMap) / sizeof(float);
 
 Parts carve_parts(const FfnArgs& a) {
   const int P = a.T * a.k;

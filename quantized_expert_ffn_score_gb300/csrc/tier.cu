@@ -183,8 +183,13 @@ moe_status moe_tier_create(moe_ctx* ctx, const moe_tier_desc* d, moe_tier** out)
       st = MOE_ERR_INVALID_ARG;  // the kernels read records with aligned bulk copies
       break;
     }
+    // page-locked memory only: where the GPU can also reach pageable memory
+    // through the host's page tables, the device-pointer query alone would
+    // accept pageable memory too
+    cudaPointerAttributes pa;
     void* p = nullptr;
-    if (cudaHostGetDevicePointer(&p, const_cast<uint8_t*>(h), 0) != cudaSuccess) {
+    if (cudaPointerGetAttributes(&pa, h) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
+        cudaHostGetDevicePointer(&p, const_cast<uint8_t*>(h), 0) != cudaSuccess) {
       cudaGetLastError();
       st = MOE_ERR_INVALID_ARG;  // not page-locked, mapped host memory
       break;
