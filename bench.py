@@ -382,13 +382,13 @@ def expert_rooflines(t, prof, step_counts, peaks):
         sec = ms / n / 1e3
         hb = {"bound": "hbm", "kernel": "mxfp4_bs_gate_up", "achieved": bs_bytes / sec / 1e9, "peak": peaks["hbm_gbs"],
               "unit": "GB/s", "frac": bs_bytes / sec / 1e9 / peaks["hbm_gbs"], "peak_source": peaks["source"],
-              "bytes_per_launch": bs_bytes, "mean_launch_us": 1e3 * sec,
+              "bytes_per_launch": bs_bytes, "mean_launch_us": 1e6 * sec,
               "traffic": ncu_traffic("mxfp4_bs_gate_up", t.name)}
         fp8_peak = 2 * peaks["bf16_tflops"]
         tc_ = {"bound": "tensor", "kernel": "mxfp4_bs_gate_up", "achieved": bs_flops / sec / 1e12, "peak": fp8_peak,
                "unit": "TFLOP/s", "frac": bs_flops / sec / 1e12 / fp8_peak,
                "peak_source": peaks["source"] + " bf16 x 2 (E2M1 x E4M3 MMA)", "flops_per_launch": bs_flops,
-               "mean_launch_us": 1e3 * sec, "traffic": hb["traffic"]}
+               "mean_launch_us": 1e6 * sec, "traffic": hb["traffic"]}
         rooflines["mxfp4_bs_gate_up"] = hb if hb["frac"] >= tc_["frac"] else tc_
         rooflines["mxfp4_bs_gate_up_other_bound"] = tc_ if hb["frac"] >= tc_["frac"] else hb
     roofline = max((v for k_, v in rooflines.items() if not k_.endswith("_other_bound")),
