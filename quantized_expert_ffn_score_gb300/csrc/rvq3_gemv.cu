@@ -137,9 +137,9 @@ __device__ __forceinline__ uint2 lds_u64(uint32_t a) {
 __device__ __forceinline__ uint32_t cb_offset(int i) {
   return 65536u + (uint32_t)(i >> 3) * 256u + 128u + (uint32_t)(i & 7) * 16u;
 }
-__device__ __forceinline__ uint4 lds_u128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 
@@ -264,6 +264,92 @@ __device__ __forceinline__ void reduce_scatter32_xor(float (&v)[32], int lane) {
   const float send = upper ? v[0] : v[1];
   const float keep = upper ? v[1] : v[0];
   v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// fp32 2^e for -126 <= e <= 127.
+__device__ __forceinline__ float pow2_i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Power-of-two shift s with mx * 2^-s in [2^14, 2^15) (0 for mx 0 or not finite).
+__device__ __forceinline__ int f16_shift(float mx) {
+  int sh = 0;
+  if (mx > 0.f && mx < INFINITY) sh = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 - 14;
+  return max(-100, min(100, sh));
+}
+
+// The table of one (vector, slice) on the tensor cores: per stage, LUT = P C^T
+// with P [32 positions][8 dims] the slice of the vector and C [256 codes][8]
+// the codebook, as mma.sync.m16n8k8 (M = 16 positions, N = 8 codes, K = 8
+// dims).  A position's 8 elements are rescaled by a power of two (its largest
+// magnitude into [2^14, 2^15)) and split into an f16 pair hi + lo, so every
+// product is exact and the two MMAs' fp32 sum carries about 22 significant
+// bits of the elements; the codewords are exact f16.  Warp w takes the 8-code
+// N tiles w, w + 16, ... (96 per table) for both position halves.  The lane
+// holding an entry is not the lane that owns its position in the lookups, so
+// the stores pair up lanes: store q writes position half q ^ (t >> 1), which
+// puts 16 different positions (banks) into every store instruction.
+//   cb_base: shared address of codeword 0 of the table's codebook, holes
+//   addressed by cb_offset() relative to it.
+__device__ __forceinline__ void build_table(uint8_t* lut, uint32_t cb_base, const float* vec, int warp, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t ahi[2][2], alo[2][2];  // [position half][row g, row g + 8]
+  float unscale[2][2];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int pos = 16 * mt + 8 * h + g;
+      const float2 e = *reinterpret_cast<const float2*>(vec + 8 * pos + 2 * t);
+      float mx = fmaxf(fabsf(e.x), fabsf(e.y));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));  // the 4 lanes holding the position
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const int sh = f16_shift(mx);
+      const float inv = pow2_i(-sh);
+      unscale[mt][h] = pow2_i(sh);
+      const float x0 = e.x * inv, x1 = e.y * inv;
+      const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+      ahi[mt][h] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+      const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
+      alo[mt][h] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    }
+  const int up = t >> 1;
+#pragma unroll 2
+  for (int j = warp; j < 3 * 32; j += kConsumerWarps) {
+    const int st = j >> 5, c0 = (j & 31) * 8;  // stage and first code of the N tile
+    // B: codeword c0 + g, elements 2t, 2t + 1
+    const uint32_t bf = lds_u32(cb_base + cb_offset(st * 256 + c0 + g) + 4u * (uint32_t)t);
+    float d[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[mt][i] = 0.f;
+      mma1688(d[mt], ahi[mt][0], ahi[mt][1], bf);
+      mma1688(d[mt], alo[mt][0], alo[mt][1], bf);
+      d[mt][0] *= unscale[mt][0];
+      d[mt][1] *= unscale[mt][0];
+      d[mt][2] *= unscale[mt][1];
+      d[mt][3] *= unscale[mt][1];
+    }
+    // entry (stage st, code c, position p) at st < 2 ? c * 256 + 128 st + 4 p : 65536 + c * 256 + 4 p
+    uint8_t* row = lut + (st < 2 ? 128 * st : 65536) + (size_t)(c0 + 2 * t) * 256;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int mt = q ^ up;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const float v = mt ? d[1][2 * h + b] : d[0][2 * h + b];
+          *reinterpret_cast<float*>(row + b * 256 + 4 * (16 * mt + 8 * h + g)) = v;
+        }
+    }
+  }
 }
 
 // MODE 0: gate/up (vectors = tokens; a table of kind kc, or of both kinds when
@@ -414,27 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? act_fn(vec[tid], up[tid], a.act) : 0.f;
       }
       named_bar_sync(1, kConsumerWarps * 32);
-      {  // table build: thread (eg, v) computes entries eg, eg + 16, ... of position v
-        const int v = tid & (kPos - 1), eg = tid >> 5;
-        float xv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xv[i] = vec[8 * v + i];
-#pragma unroll 4
-        for (int e = eg; e < 3 * 256; e += kConsumerWarps) {
-          const uint4 c8 = lds_u128(lut_s + cb_offset((MODE == 0 ? t.kc * 3 * 256 : 0) + e));  // one broadcast per warp
-          const uint32_t hw[4] = {c8.x, c8.y, c8.z, c8.w};
-          float acc = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
-            acc = fmaf(f.x, xv[2 * j], acc);
-            acc = fmaf(f.y, xv[2 * j + 1], acc);
-          }
-          const int st = e >> 8, c = e & 255;  // entry (stage, code)
-          const uint32_t off = st < 2 ? (uint32_t)(c * 256 + 128 * st + 4 * v) : (uint32_t)(65536 + c * 256 + 4 * v);
-          *reinterpret_cast<float*>(lut + off) = acc;
-        }
-      }
+      // the table's codebook: kind kc's codewords start kc * 768 / 8 holes further
+      build_table(lut, lut_s + (uint32_t)(MODE == 0 ? t.kc * 3 * 256 / 8 * 256 : 0), vec, warp, lane);
       named_bar_sync(1, kConsumerWarps * 32);
       lut_combo = t.combo;
     }
