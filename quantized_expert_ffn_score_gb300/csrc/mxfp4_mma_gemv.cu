@@ -30,10 +30,20 @@
 // The producer warp copies each tile row by row (bulk async copies, one per
 // lane) into shared memory rows padded by 16 bytes, so that the fragment
 // loads (32-bit words of 8 rows at the same column) hit distinct banks.
+//
+// One-token launches (T = 1) keep the B fragments in shared memory instead of
+// registers: only the lanes of the token's column (gate/up: lanes 0-3; down,
+// whose hi and lo parts fill two columns: lanes 0-7) hold non-zero values, so
+// a block's fragments are 64 or 128 bytes, read back once per block with one
+// 16-byte load (the other lanes read a zeroed slot), and the warps' partial
+// sums keep one token column.  Measured against the register form on one
+// GB300: gate/up 49.2 -> 47.7 us, decode step 91.9 -> 90.7 us; with the
+// registers freed, 4 blocks per warp and 28 compute warps were slower (57 us).
 #include <type_traits>
 #include <utility>
 
 #include "moe_internal.cuh"
+#include "tc_ops.cuh"
 
 namespace moe {
 namespace {
@@ -42,10 +52,13 @@ constexpr int kTok = 8;  // tokens per pass (MMA N)
 constexpr int kRows = 32;  // weight rows per tile (two 16-row M tiles)
 constexpr int kMaxStagesM = 4;
 constexpr int kSmemBudgetM = 224 * 1024;
-constexpr int kMaxConsumerWarps = 14;  // compute warps (plus one reducer and one producer warp)
+constexpr int kMaxConsumerWarps = 14;  // compute warps of 8 blocks (plus one reducer and one producer warp)
+constexpr int kMaxBlocks = kMaxConsumerWarps * 8;  // K / 32 at most (d, ff <= 3584)
 
 struct GeomM {
   int K;            // contraction length
+  uint32_t sb_lane_bytes;  // one-token launches: bytes of B fragments per block (0: fragments in registers)
+  uint32_t sb_off;         // their offset in shared memory (then a zeroed 16-byte slot)
   int nblk;         // K / 32
   int bpw;          // blocks per consumer warp
   int warps;        // consumer warps
@@ -54,25 +67,28 @@ struct GeomM {
   uint32_t scales;  // bytes of scales per stage: 32 rows x K / 32
   uint32_t stage_bytes;
   int stages;
-  size_t red_floats;  // one reduction buffer: warps x 32 rows x 8 tokens
+  size_t red_floats;  // one reduction buffer: warps x 32 rows x 8 tokens (1 token for one-token launches)
   size_t smem;
 };
 
-GeomM make_geom_m(int mode, int d, int ff) {
+GeomM make_geom_m(int mode, int d, int ff, int bpw, bool staged_b) {
   GeomM g;
   g.K = mode == 0 ? d : ff;
+  g.sb_lane_bytes = staged_b ? (mode == 0 ? 64u : 128u) : 0u;
   g.nblk = g.K / 32;
-  g.bpw = 8;
+  g.bpw = bpw;
   g.warps = (g.nblk + g.bpw - 1) / g.bpw;
   g.tpe = mode == 0 ? ff / 16 : d / 32;
   g.pitch = (uint32_t)g.K / 2 + 16;
   g.scales = (uint32_t)kRows * (uint32_t)g.K / 32;
   g.stage_bytes = (uint32_t)kRows * g.pitch + ((g.scales + 15) & ~15u);
-  g.red_floats = (size_t)g.warps * kRows * kTok;
-  const size_t fixed = (2 * kMaxStagesM + 4) * sizeof(uint64_t) + (2 * g.red_floats + 2 * kTok) * sizeof(float);
+  g.red_floats = (size_t)g.warps * kRows * (staged_b ? 1 : kTok);
+  const size_t sb = staged_b ? (size_t)g.nblk * g.sb_lane_bytes + 16 : 0;
+  const size_t fixed = (2 * kMaxStagesM + 4) * sizeof(uint64_t) + (2 * g.red_floats + 2 * kTok) * sizeof(float) + sb;
   g.stages = (int)((kSmemBudgetM - fixed) / g.stage_bytes);
   if (g.stages > kMaxStagesM) g.stages = kMaxStagesM;
   g.smem = (size_t)g.stages * g.stage_bytes + fixed;
+  g.sb_off = (uint32_t)(g.smem - sb);
   return g;
 }
 
@@ -118,11 +134,22 @@ __device__ __forceinline__ int shift_for(float mx) {
 // (MODE 1, at most 4 tokens per pass): column 2n holds token n's hi part and
 // column 2n + 1 its lo part, so one MMA forms both partial sums (lane group g
 // holds token g / 2, part g % 2) and the lo array is not needed.
-template <int MODE, int BPW, bool PAIR>
+template <int MODE, int BPW, bool PAIR, bool SB>
 struct Frags {
-  uint32_t hi[BPW][4];
-  uint32_t lo[(MODE == 1 && !PAIR) ? BPW : 1][4];
+  uint32_t hi[SB ? 1 : BPW][4];
+  uint32_t lo[(MODE == 1 && !PAIR && !SB) ? BPW : 1][4];
   float unscale;  // MODE 1: 2^s of this warp's rescale for the lane's token (MODE 0: unused)
+  uint8_t* sb;    // SB: the blocks' fragments in shared memory, lane_bytes per block
+  uint32_t lane_bytes;
+
+  // SB: lanes below lane_bytes / 16 keep block b's fragment at sb + b * lane_bytes + 16 lane
+  __device__ __forceinline__ void put(int j, int b, int i, uint32_t v, int lane) {
+    if (SB) {
+      if ((uint32_t)lane * 16u < lane_bytes) reinterpret_cast<uint32_t*>(sb + (size_t)b * lane_bytes + 16 * lane)[i] = v;
+    } else {
+      hi[j][i] = v;
+    }
+  }
 
   __device__ void load(const FfnArgs& a, int slot0, int nt, int b0, int nblk, int lane) {
     const int g0 = lane >> 2, t = lane & 3;
@@ -143,9 +170,10 @@ struct Frags {
         uint4 w = make_uint4(0, 0, 0, 0);
         if (live && b < nblk) w = *reinterpret_cast<const uint4*>(xrow + 32 * b + 8 * t);
         const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+        if (SB && b >= nblk) continue;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          hi[j][i] = pack_f16x2(__uint_as_float(v[i] << 16) * inv, __uint_as_float(v[i] & 0xFFFF0000u) * inv);
+          put(j, b, i, pack_f16x2(__uint_as_float(v[i] << 16) * inv, __uint_as_float(v[i] & 0xFFFF0000u) * inv), lane);
       }
     } else {
       // two passes over the (cached) rows: the token's max over this warp's
@@ -177,6 +205,7 @@ struct Frags {
           v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
           v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
         }
+        if (SB && b >= nblk) continue;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float x0 = v[2 * i] * inv, x1 = v[2 * i + 1] * inv;
@@ -184,14 +213,15 @@ struct Frags {
           const uint32_t hv = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
           const uint32_t lv = pack_f16x2(x0 - __half2float(h0), x1 - __half2float(h1));
           if (PAIR) {
-            hi[j][i] = (g0 & 1) ? lv : hv;
+            put(j, b, i, (g0 & 1) ? lv : hv, lane);
           } else {
-            hi[j][i] = hv;
-            lo[(MODE == 1 && !PAIR) ? j : 0][i] = lv;
+            hi[SB ? 0 : j][i] = hv;
+            lo[(MODE == 1 && !PAIR && !SB) ? j : 0][i] = lv;
           }
         }
       }
     }
+    if (SB) __syncwarp();
   }
 };
 
@@ -217,8 +247,10 @@ __device__ __forceinline__ void note_tokens(const FfnArgs& a, int slot0, int nt,
 // partial sums go to a double-buffered shared array whose fill is counted by an
 // mbarrier, and a reducer warp (warp 0, which computes nothing else) adds them
 // and writes the pass's outputs.  Every wait is bounded.
-template <int MODE, int BPW, bool PAIR>
-__global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gemv_kernel(const FfnArgs a, const GeomM g) {
+template <int MODE, int BPW, bool PAIR, bool SB>
+__global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv_kernel(const FfnArgs a, const GeomM g) {
+  static_assert(!SB || MODE == 0 || PAIR, "one-token fragments in shared memory: gate/up, or down with paired columns");
+  constexpr int kRedTok = SB ? 1 : kTok;  // token columns of a reduction buffer row
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)g.stages * g.stage_bytes);
   uint64_t* empty = full + kMaxStagesM;
@@ -241,6 +273,8 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
     }
     fence_mbar_init();
   }
+  if (SB && threadIdx.x < 4)  // the zeroed slot after the fragments
+    reinterpret_cast<uint32_t*>(smem + g.sb_off + (size_t)g.nblk * g.sb_lane_bytes)[threadIdx.x] = 0u;
   __syncthreads();
   // The down pass's producer stages weights only, and the routing it follows
   // was written two launches earlier (complete before the gate/up pass passed
@@ -339,10 +373,10 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
             float sum0 = 0.f, sum1 = 0.f;
             int w = 0;
             for (; w + 1 < W; w += 2) {
-              sum0 += rbase[((size_t)w * kRows + lane) * kTok + n];
-              sum1 += rbase[((size_t)(w + 1) * kRows + lane) * kTok + n];
+              sum0 += rbase[((size_t)w * kRows + lane) * kRedTok + n];
+              sum1 += rbase[((size_t)(w + 1) * kRows + lane) * kRedTok + n];
             }
-            if (w < W) sum0 += rbase[((size_t)w * kRows + lane) * kTok + n];
+            if (w < W) sum0 += rbase[((size_t)w * kRows + lane) * kRedTok + n];
             const float sum = sum0 + sum1;
             const float us = __shfl_down_sync(0xffffffffu, sum, 16);
             if (lane < 16) {
@@ -354,7 +388,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
           for (int idx = lane; idx < kRows * nt; idx += 32) {
             const int r = idx & 31, n = idx >> 5;
             float ys = 0.f;
-            for (int w = 0; w < W; ++w) ys += rbase[((size_t)w * kRows + r) * kTok + n];
+            for (int w = 0; w < W; ++w) ys += rbase[((size_t)w * kRows + r) * kRedTok + n];
             a.y_pairs[(size_t)tok_i[n] * a.d + (size_t)rt * kRows + r] = ys;
           }
         }
@@ -369,7 +403,13 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
   const int cw = warp - 1;
   const int gq = lane >> 2, tq = lane & 3;
   const int b0 = cw * BPW;
-  Frags<MODE, BPW, PAIR> fr;
+  Frags<MODE, BPW, PAIR, SB> fr;
+  fr.sb = smem + g.sb_off;
+  fr.lane_bytes = g.sb_lane_bytes;
+  // SB: this lane's fragment of block b at sb_lane + b * lane_bytes, or the zeroed slot
+  const uint32_t sb_zero = tc::saddr(smem + g.sb_off + (size_t)g.nblk * g.sb_lane_bytes);
+  const bool sb_live = (uint32_t)lane * 16u < g.sb_lane_bytes;
+  const uint32_t sb_lane = tc::saddr(smem + g.sb_off) + 16u * (uint32_t)lane;
   int it = 0, pc = 0, cur_a = -1, s0 = 0, ne = 0;
   bool rec_good = false;
   for (int tile = t_begin; tile < t_end; ++tile) {
@@ -428,6 +468,11 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
         for (int j = 0; j < BPW; ++j) {
           const int b = b0 + j;
           if (b >= g.nblk) continue;  // (fully unrolled: the fragments stay in registers)
+          uint4 bj = make_uint4(0u, 0u, 0u, 0u);
+          if (SB) {
+            const uint32_t ad = sb_live ? sb_lane + (uint32_t)b * g.sb_lane_bytes : sb_zero;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(bj.x), "=r"(bj.y), "=r"(bj.z), "=r"(bj.w) : "r"(ad));
+          }
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             const int ra = 16 * m + gq, rb = ra + 8;
@@ -439,8 +484,13 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
             float d[4] = {0.f, 0.f, 0.f, 0.f};
             const uint32_t A0[4] = {pa[0], pb[0], pa[1], pb[1]};
             const uint32_t A1[4] = {pa[2], pb[2], pa[3], pb[3]};
-            mma16816(d, A0, fr.hi[j][0], fr.hi[j][1]);
-            mma16816(d, A1, fr.hi[j][2], fr.hi[j][3]);
+            if (SB) {
+              mma16816(d, A0, bj.x, bj.y);
+              mma16816(d, A1, bj.z, bj.w);
+            } else {
+              mma16816(d, A0, fr.hi[SB ? 0 : j][0], fr.hi[SB ? 0 : j][1]);
+              mma16816(d, A1, fr.hi[SB ? 0 : j][2], fr.hi[SB ? 0 : j][3]);
+            }
             if (MODE == 1 && !PAIR) {
               constexpr bool kLo = MODE == 1 && !PAIR;
               mma16816(d, A0, fr.lo[kLo ? j : 0][0], fr.lo[kLo ? j : 0][1]);
@@ -488,11 +538,16 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
       const int bi = pc & 1, use = pc >> 1;
       ++pc;
       if (use > 0 && !mbar_wait(&red_empty[bi], (use - 1) & 1, a.err)) return;
-      float* rb = red + bi * g.red_floats + (size_t)cw * kRows * kTok;
+      float* rb = red + bi * g.red_floats + (size_t)cw * kRows * kRedTok;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int ra = 16 * m + gq;
-        if (PAIR) {  // token tq (columns >= nt are never read)
+        if (SB) {  // the one token: column 0, held by the lanes with tq = 0
+          if (tq == 0) {
+            rb[ra] = acc[m][0];
+            rb[ra + 8] = acc[m][2];
+          }
+        } else if (PAIR) {  // token tq (columns >= nt are never read)
           rb[ra * kTok + tq] = acc[m][0];
           rb[(ra + 8) * kTok + tq] = acc[m][2];
         } else {
@@ -510,11 +565,12 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 2) * 32, 1) mxfp4_mma_gem
   }
 }
 
-template <int MODE, int BPW, bool PAIR>
+template <int MODE, int BPW, bool PAIR, bool SB>
 cudaError_t launch_m(const FfnArgs& a, const GeomM& g, int num_sms, bool pdl, cudaStream_t s, const char* name) {
-  ensure_smem(mxfp4_mma_gemv_kernel<MODE, BPW, PAIR>, g.smem);
-  return launch(name, mxfp4_mma_gemv_kernel<MODE, BPW, PAIR>, dim3(num_sms), dim3((g.warps + 2) * 32), g.smem, s, pdl,
-                a, g);
+  if (g.bpw != BPW || g.warps > kMaxBlocks / BPW || g.stages < 2) return cudaErrorInvalidValue;
+  ensure_smem(mxfp4_mma_gemv_kernel<MODE, BPW, PAIR, SB>, g.smem);
+  return launch(name, mxfp4_mma_gemv_kernel<MODE, BPW, PAIR, SB>, dim3(num_sms), dim3((g.warps + 2) * 32), g.smem, s,
+                pdl, a, g);
 }
 
 }  // namespace
@@ -528,14 +584,18 @@ bool mxfp4_mma_gemv_supported(int d, int ff, int x_dtype) {
 
 cudaError_t launch_mxfp4_ffn_mma(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  const GeomM g0 = make_geom_m(0, a.d, a.ff), g1 = make_geom_m(1, a.d, a.ff);
-  if (g0.stages < 2 || g1.stages < 2 || g0.warps > kMaxConsumerWarps || g1.warps > kMaxConsumerWarps)
-    return cudaErrorInvalidValue;
-  cudaError_t err = launch_m<0, 8, false>(a, g0, num_sms, pdl, s, "mxfp4_gate_up");
+  if (a.T == 1) {  // one token: fragments in shared memory, 8 blocks per warp
+    const GeomM g0 = make_geom_m(0, a.d, a.ff, 8, true), g1 = make_geom_m(1, a.d, a.ff, 8, true);
+    cudaError_t err = launch_m<0, 8, false, true>(a, g0, num_sms, pdl, s, "mxfp4_gate_up");
+    if (err != cudaSuccess) return err;
+    return launch_m<1, 8, true, true>(a, g1, num_sms, true, s, "mxfp4_down");
+  }
+  const GeomM g0 = make_geom_m(0, a.d, a.ff, 8, false), g1 = make_geom_m(1, a.d, a.ff, 8, false);
+  cudaError_t err = launch_m<0, 8, false, false>(a, g0, num_sms, pdl, s, "mxfp4_gate_up");
   if (err != cudaSuccess) return err;
   // an expert gets at most T tokens, so with T <= 4 every pass fits the paired columns
-  if (a.T <= 4) return launch_m<1, 8, true>(a, g1, num_sms, true, s, "mxfp4_down");
-  return launch_m<1, 8, false>(a, g1, num_sms, true, s, "mxfp4_down");
+  if (a.T <= 4) return launch_m<1, 8, true, false>(a, g1, num_sms, true, s, "mxfp4_down");
+  return launch_m<1, 8, false, false>(a, g1, num_sms, true, s, "mxfp4_down");
 }
 
 }  // namespace moe
