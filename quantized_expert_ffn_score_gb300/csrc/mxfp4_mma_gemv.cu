@@ -151,7 +151,8 @@ struct Frags {
     }
   }
 
-  __device__ void load(const FfnArgs& a, int slot0, int nt, int b0, int nblk, int lane) {
+  // tok_fixed >= 0: the pass's one token is that token (no routing read)
+  __device__ void load(const FfnArgs& a, int slot0, int nt, int b0, int nblk, int lane, int tok_fixed = -1) {
     const int g0 = lane >> 2, t = lane & 3;
     const int g = PAIR ? g0 >> 1 : g0;  // the lane's token in the pass
     const bool live = g < nt;
@@ -160,7 +161,7 @@ struct Frags {
       float inv = 1.f;
       const uint16_t* xrow = nullptr;
       if (live) {
-        const int tok = a.pair_ids[slot0 + g] / a.k;
+        const int tok = tok_fixed >= 0 ? tok_fixed : a.pair_ids[slot0 + g] / a.k;
         inv = pow2i(-shift_for(a.max_x[tok]));
         xrow = static_cast<const uint16_t*>(a.x) + (size_t)tok * a.d;
       }
@@ -280,7 +281,21 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
   // was written two launches earlier (complete before the gate/up pass passed
   // its own wait, which precedes this launch): it starts streaming while the
   // gate/up pass finishes.  Everything that reads h or writes outputs waits.
+  // One-token gate/up: the compute warps stage the token's B fragments first
+  // (the layer input and the router's max |x| were complete before the top-k
+  // kernel ran) and the producer pulls the record table into L2 while the
+  // routing is made.  Dependents are released only after the wait: the down
+  // pass's producer reads the routing without waiting, which is safe only
+  // because this pass's wait has returned before that launch.
   const int W = g.warps;
+  if (SB && MODE == 0 && warp >= 1 && warp <= W) {
+    Frags<MODE, BPW, PAIR, SB> f0;
+    f0.sb = smem + g.sb_off;
+    f0.lane_bytes = g.sb_lane_bytes;
+    f0.load(a, 0, 1, (warp - 1) * BPW, g.nblk, lane, 0);
+  }
+  if (MODE == 0 && warp == W + 1)
+    for (int i = 16 * lane; i < a.E; i += 16 * 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.records + i));
   if (MODE == 0 || warp != W + 1) pdl_wait();
   pdl_launch_dependents();
 
@@ -420,7 +435,8 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
       rec_good = rec_ok(a.records[e]);
       s0 = a.offsets[e];
       ne = a.offsets[e + 1] - s0;
-      if (rec_good && ne <= kTok) fr.load(a, s0, ne, b0, g.nblk, lane);
+      // (one-token gate/up: staged before the wait)
+      if (rec_good && ne <= kTok && !(SB && MODE == 0)) fr.load(a, s0, ne, b0, g.nblk, lane);
     }
     if (!rec_good) continue;
     const int stage = it % g.stages;

@@ -384,18 +384,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kConsumerWarps) reinterpret_cast<uint32_t*>(smap)[lane] = reinterpret_cast<const uint32_t*>(&tmpl)[lane];
   __syncthreads();
-  // The down kernel's producer stages codes only, for routing written before
-  // the gate/up kernel passed its own wait (which precedes this launch), into
-  // tensor-map slots of its own: it starts while the gate/up kernel finishes.
-  // The consumers read the gate/up sums, so they wait.
-  if (MODE == 0 || warp != kConsumerWarps) pdl_wait();
-  pdl_launch_dependents();
+  // Work that depends on nothing the previous kernel writes runs before the
+  // wait on it: the codebooks, the gate/up kernel's first table (the layer
+  // input was complete before the routing kernels ran), and the down kernel's
+  // whole producer, which stages codes for routing written before the gate/up
+  // kernel passed its own wait (into tensor-map slots of its own).  Each role
+  // waits where it first needs the previous kernel's output, and releases the
+  // dependent launch only after that wait: the down kernel's producer relies
+  // on the gate/up kernel's wait having returned before it starts.
   const long long total = (long long)g.nvec * g.kcombo * g.ns * g.nseg * g.gpm;
   const long long ub = total * blockIdx.x / gridDim.x, ue = total * (blockIdx.x + 1) / gridDim.x;
   const int nu = (int)(ue - ub);
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer
+    for (int i = 16 * lane; i < a.E; i += 16 * 32)  // the record table into L2 while the routing is made
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.records + i));
+    if (MODE == 0) pdl_wait();
+    pdl_launch_dependents();
     int cur_p = -1, cur_kind = -1, slot = -1;
     const uint8_t* rec = nullptr;
     CUtensorMap* my_maps = gmaps + ((size_t)MODE * kMaxSmsRvq + blockIdx.x) * kMapSlots;  // per kernel and CTA
@@ -470,39 +476,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kBufs == 2, "two buffers");
   const uint32_t box_s0 = s0 + plan.box(r_local / kBoxRows), box_s1 = s0 + plan.box(kBoxesPerGroup + r_local / kBoxRows);
   const int row_of_lane = 16 * l4 + 8 * l3 + 4 * (lane & 1) + (int)jx;
+  // a new (vector, slice): rebuild the table (uniform over the consumer warps)
+  auto rebuild = [&](const Unit& t) {
+    const int v0 = t.slice * kPos, nv = min(kPos, g.kv - v0);  // positions past kv: zero vector, zero entries
+    named_bar_sync(1, kConsumerWarps * 32);  // the previous table's readers are done
+    if (MODE == 0) {
+      if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? load_act(a.x, a.x_dtype, (size_t)t.vi * a.d + 8 * v0 + tid) : 0.f;
+    } else {  // h of pair vi: each thread sums one gate or up element's slice sums (ascending), then the activation
+      float* up = reinterpret_cast<float*>(rsm + plan.misc + kUpOff);
+      const int i = tid & (8 * kPos - 1), kind = tid >> 8;
+      float sum = 0.f;
+      if (i < 8 * nv) {
+        const float* gp = gpart + ((size_t)t.vi * 2 + kind) * g.ns_gu * a.ff + 8 * v0 + i;
+        for (int q0 = 0; q0 < g.ns_gu; q0 += kMaxPartsInFlight) {  // loads in flight together, added in order
+          float pv[kMaxPartsInFlight];
+#pragma unroll
+          for (int q = 0; q < kMaxPartsInFlight; ++q)
+            if (q0 + q < g.ns_gu) pv[q] = gp[(size_t)(q0 + q) * a.ff];
+#pragma unroll
+          for (int q = 0; q < kMaxPartsInFlight; ++q)
+            if (q0 + q < g.ns_gu) sum += pv[q];
+        }
+      }
+      (kind == 0 ? vec : up)[i] = sum;
+      named_bar_sync(1, kConsumerWarps * 32);
+      if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? act_fn(vec[tid], up[tid], a.act) : 0.f;
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+    // the table's codebook: kind kc's codewords start kc * 768 / 8 holes further
+    build_table(lut, lut_s + (uint32_t)(MODE == 0 ? t.kc * 3 * 256 / 8 * 256 : 0), vec, warp, lane);
+    named_bar_sync(1, kConsumerWarps * 32);
+  };
   UnitIter uit;
   uit.init(g, ub);
+  if (MODE == 0 && nu > 0) {  // the first table needs only the layer input
+    const Unit t0 = uit.unit<MODE>(g);
+    rebuild(t0);
+    lut_combo = t0.combo;
+  }
+  pdl_wait();
+  pdl_launch_dependents();
   for (int n = 0; n < nu; ++n, uit.next(g)) {
     const Unit t = uit.unit<MODE>(g);
-    const int v0 = t.slice * kPos, nv = min(kPos, g.kv - v0);  // positions past kv: zero vector, zero entries
-    if (t.combo != lut_combo) {  // a new (vector, slice): rebuild the table (uniform over the consumer warps)
-      named_bar_sync(1, kConsumerWarps * 32);  // the previous table's readers are done
-      if (MODE == 0) {
-        if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? load_act(a.x, a.x_dtype, (size_t)t.vi * a.d + 8 * v0 + tid) : 0.f;
-      } else {  // h of pair vi: each thread sums one gate or up element's slice sums (ascending), then the activation
-        float* up = reinterpret_cast<float*>(rsm + plan.misc + kUpOff);
-        const int i = tid & (8 * kPos - 1), kind = tid >> 8;
-        float sum = 0.f;
-        if (i < 8 * nv) {
-          const float* gp = gpart + ((size_t)t.vi * 2 + kind) * g.ns_gu * a.ff + 8 * v0 + i;
-          for (int q0 = 0; q0 < g.ns_gu; q0 += kMaxPartsInFlight) {  // loads in flight together, added in order
-            float pv[kMaxPartsInFlight];
-#pragma unroll
-            for (int q = 0; q < kMaxPartsInFlight; ++q)
-              if (q0 + q < g.ns_gu) pv[q] = gp[(size_t)(q0 + q) * a.ff];
-#pragma unroll
-            for (int q = 0; q < kMaxPartsInFlight; ++q)
-              if (q0 + q < g.ns_gu) sum += pv[q];
-          }
-        }
-        (kind == 0 ? vec : up)[i] = sum;
-        named_bar_sync(1, kConsumerWarps * 32);
-        if (tid < 8 * kPos) vec[tid] = tid < 8 * nv ? act_fn(vec[tid], up[tid], a.act) : 0.f;
-      }
-      named_bar_sync(1, kConsumerWarps * 32);
-      // the table's codebook: kind kc's codewords start kc * 768 / 8 holes further
-      build_table(lut, lut_s + (uint32_t)(MODE == 0 ? t.kc * 3 * 256 / 8 * 256 : 0), vec, warp, lane);
-      named_bar_sync(1, kConsumerWarps * 32);
+    if (t.combo != lut_combo) {
+      rebuild(t);
       lut_combo = t.combo;
     }
     const int b = n % kBufs;
