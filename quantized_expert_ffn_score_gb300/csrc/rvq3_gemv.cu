@@ -215,10 +215,9 @@ struct UnitIter {
     t.slice = slice;
     t.kc = kc;
     t.vi = vi;
-    if (MODE == 0) {
-      const int kpc = 2 / g.kcombo;  // kinds per table
-      t.p = vi * g.ks + seg / kpc;
-      t.kind = g.kcombo == 1 ? seg % kpc : kc;
+    if (MODE == 0) {  // one table serves both kinds (segments alternate gate, up) or one kind (kc)
+      t.p = vi * g.ks + (g.kcombo == 1 ? seg >> 1 : seg);
+      t.kind = g.kcombo == 1 ? seg & 1 : kc;
     } else {
       t.p = vi;
       t.kind = 2;
@@ -476,6 +475,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kBufs == 2, "two buffers");
   const uint32_t box_s0 = s0 + plan.box(r_local / kBoxRows), box_s1 = s0 + plan.box(kBoxesPerGroup + r_local / kBoxRows);
   const int row_of_lane = 16 * l4 + 8 * l3 + 4 * (lane & 1) + (int)jx;
+  // byte offsets in a box of the lane's code words for stage 0: line lane (the
+  // stage adds 32 lines, 4096 bytes, and leaves line & 7 unchanged), 16-byte
+  // chunk (c0 + h ^ l4) swizzled by the line, half hf ^ l3 of it
+  uint32_t qo[2][2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+      qo[h][hf] = (uint32_t)(lane * kBoxRows + (((c0 + (h ^ l4)) ^ (lane & 7)) * 16) + 8 * (hf ^ l3));
   // a new (vector, slice): rebuild the table (uniform over the consumer warps)
   auto rebuild = [&](const Unit& t) {
     const int v0 = t.slice * kPos, nv = min(kPos, g.kv - v0);  // positions past kv: zero vector, zero entries
@@ -530,15 +538,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t box_s = b ? box_s1 : box_s0;
       // line (stage s, position lane) of the box; its 16-byte chunks are swizzled by the line index
 #pragma unroll
-      for (int st = 0; st < 3; ++st) {
-        const int line = st * kPos + lane;
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t ad = box_s + qo[h][hf];
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-            q[st][h][hf] = lds_u64(box_s + (uint32_t)(line * kBoxRows + (((c0 + (h ^ l4)) ^ (line & 7)) * 16) +
-                                                         8 * (hf ^ l3)));
-      }
+          for (int st = 0; st < 3; ++st) q[st][h][hf] = lds_u64(ad + (uint32_t)(st * kPos * kBoxRows));
+        }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[b]);  // the codes are in registers: the buffer can be refilled
