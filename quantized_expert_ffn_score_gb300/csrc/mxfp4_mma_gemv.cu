@@ -310,8 +310,14 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
     int it = 0, cur_a = -1;
     const uint8_t* rec = nullptr;
     bool alive = true;
+    // tile = ai * tpe + rt and the ring position advance without divisions
+    int ai = t_begin / g.tpe, rt = t_begin - ai * g.tpe - 1, stage = -1;
+    uint32_t rph = 1;  // parity of the current round over the stage ring
     for (int tile = t_begin; tile < t_end && alive; ++tile) {
-      const int ai = tile / g.tpe;
+      if (++rt == g.tpe) {
+        rt = 0;
+        ++ai;
+      }
       if (ai != cur_a) {
         cur_a = ai;
         const int e = a.active[1 + ai];
@@ -320,10 +326,11 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
           dev_error(a.err, rec == nullptr ? MOE_ERR_MISSING_EXPERT : MOE_ERR_INVALID_ARG, e);
       }
       if (!rec_ok(rec)) continue;
-      const int stage = it % g.stages, n = it / g.stages;
+      if (++stage == g.stages) stage = 0;
+      if (stage == 0) rph ^= 1u;
       int ok = 1;
       if (lane == 0) {
-        if (n > 0 && !mbar_wait(&empty[stage], (n - 1) & 1, a.err)) ok = 0;
+        if (it >= g.stages && !mbar_wait(&empty[stage], rph ^ 1u, a.err)) ok = 0;
         if (ok) mbar_arrive_expect_tx(&full[stage], (uint32_t)kRows * (uint32_t)(K / 2) + g.scales);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -332,7 +339,6 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
         break;
       }
       uint8_t* dst = smem + (size_t)stage * g.stage_bytes;
-      const int rt = tile % g.tpe;
       // lane l copies staged row l: MODE 0 rows 0..15 = Wg rows, 16..31 = Wu rows
       const uint8_t* src;
       if (MODE == 0) {
@@ -365,8 +371,12 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
     // -------------------------------------------------------------- reducer
     int pc = 0, cur_a = -1, s0 = 0, ne = 0;
     bool rec_good = false;
+    int ai = t_begin / g.tpe, rt = t_begin - ai * g.tpe - 1;
     for (int tile = t_begin; tile < t_end; ++tile) {
-      const int ai = tile / g.tpe;
+      if (++rt == g.tpe) {
+        rt = 0;
+        ++ai;
+      }
       if (ai != cur_a) {
         cur_a = ai;
         const int e = a.active[1 + ai];
@@ -375,7 +385,6 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
         ne = a.offsets[e + 1] - s0;
       }
       if (!rec_good) continue;
-      const int rt = tile % g.tpe;
       for (int c0 = 0; c0 < ne; c0 += kTok) {
         const int nt = min(kTok, ne - c0);
         const int bi = pc & 1, use = pc >> 1;
@@ -427,8 +436,13 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
   const uint32_t sb_lane = tc::saddr(smem + g.sb_off) + 16u * (uint32_t)lane;
   int it = 0, pc = 0, cur_a = -1, s0 = 0, ne = 0;
   bool rec_good = false;
+  int ai = t_begin / g.tpe, rt_ = t_begin - ai * g.tpe - 1, stage = -1;
+  uint32_t cph = 1;  // parity of the current round over the stage ring
   for (int tile = t_begin; tile < t_end; ++tile) {
-    const int ai = tile / g.tpe;
+    if (++rt_ == g.tpe) {
+      rt_ = 0;
+      ++ai;
+    }
     if (ai != cur_a) {  // a new expert: its slots, and its activations if one pass holds them
       cur_a = ai;
       const int e = a.active[1 + ai];
@@ -439,8 +453,9 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
       if (rec_good && ne <= kTok && !(SB && MODE == 0)) fr.load(a, s0, ne, b0, g.nblk, lane);
     }
     if (!rec_good) continue;
-    const int stage = it % g.stages;
-    if (!mbar_wait(&full[stage], (it / g.stages) & 1, a.err)) return;
+    if (++stage == g.stages) stage = 0;
+    if (stage == 0) cph ^= 1u;
+    if (!mbar_wait(&full[stage], cph, a.err)) return;
     ++it;
     const uint8_t* st = smem + (size_t)stage * g.stage_bytes;
     const uint8_t* sc = st + (size_t)kRows * g.pitch;
