@@ -234,7 +234,7 @@ __device__ __forceinline__ void note_tokens(const FfnArgs& a, int slot0, int nt,
   if (lane < nt) {
     const int slot = slot0 + lane;
     if (MODE == 0) {
-      tok_f[lane] = pow2i(shift_for(a.max_x[a.pair_ids[slot] / a.k]));
+      tok_f[lane] = pow2i(shift_for(a.max_x[a.T == 1 ? 0 : a.pair_ids[slot] / a.k]));
       tok_i[lane] = slot;
     } else {
       tok_i[lane] = a.pair_ids[slot];
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
 
   if (warp == 0) {
     // -------------------------------------------------------------- reducer
-    int pc = 0, cur_a = -1, s0 = 0, ne = 0;
+    int pc = 0, cur_a = -1, s0 = 0, ne = 0, noted = -1;
     bool rec_good = false;
     int ai = t_begin / g.tpe, rt = t_begin - ai * g.tpe - 1;
     for (int tile = t_begin; tile < t_end; ++tile) {
@@ -389,7 +389,10 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
         const int nt = min(kTok, ne - c0);
         const int bi = pc & 1, use = pc >> 1;
         ++pc;
-        note_tokens<MODE>(a, s0 + c0, nt, lane, tok_f, tok_i);
+        if (ne > kTok || noted != cur_a) {  // a one-pass expert's tokens are noted once
+          note_tokens<MODE>(a, s0 + c0, nt, lane, tok_f, tok_i);
+          noted = cur_a;
+        }
         if (!mbar_wait(&red_full[bi], use & 1, a.err)) return;
         const float* rbase = red + bi * g.red_floats;
         if (MODE == 0) {  // lane = (half, row): gate rows on lanes 0-15, up rows on lanes 16-31
