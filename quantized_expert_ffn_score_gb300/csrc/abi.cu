@@ -340,6 +340,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   if (T == 1) {  // one token: the top-k kernel buckets its pairs itself
     ra.fuse_bucket = 1;
     ra.bucket = ba;
+    ra.bucket.counts = counts_out;  // no later step reads the counts: only the caller's copy is written
   }
   moe_status st = cuda_status(moe::launch_route_topk(ra, ctx->num_sms, s));
   if (st != MOE_OK) return st;

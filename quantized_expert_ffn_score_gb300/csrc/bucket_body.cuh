@@ -140,9 +140,13 @@ __device__ __forceinline__ void bucket_block(const BucketArgs& a, int nw, int* b
 // The same result for a single token (T = 1, k <= 32 distinct experts): no
 // histogram or scan.  With the k selected ids sel[j], an expert's offset is the
 // number of selected ids below it, pair j lands at the rank of sel[j], and
-// every selected expert has one token.  Every thread of the block calls it.
+// every selected expert has one token.  The offsets come from a bit mask of
+// the selected ids and its per-word population-count prefix.  a.counts may be
+// null (not wanted).  Every thread of the block calls it.
 __device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_smem, bool preloaded = false) {
-  const int E = a.E, k = a.k;
+  __shared__ uint32_t sel_mask[kMaxE / 32 + 1];
+  __shared__ int mask_prefix[kMaxE / 32 + 1];
+  const int E = a.E, k = a.k, nw = (E >> 5) + 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x < k) {
     int e = preloaded ? sel_smem[threadIdx.x] : a.topk_idx[threadIdx.x];
@@ -152,6 +156,10 @@ __device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_s
     }
     sel_smem[threadIdx.x] = e;
   }
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) sel_mask[w] = 0u;
+  __syncthreads();
+  if (threadIdx.x < k && sel_smem[threadIdx.x] < E)
+    atomicOr(&sel_mask[sel_smem[threadIdx.x] >> 5], 1u << (sel_smem[threadIdx.x] & 31));
   __syncthreads();
   if (warp == 0) {
     const int e = lane < k ? sel_smem[lane] : 0x7fffffff;
@@ -166,16 +174,27 @@ __device__ __forceinline__ void bucket_one_token(const BucketArgs& a, int* sel_s
       a.active[1 + rank] = e;
     }
     if (lane == 0) a.active[0] = nvalid;
-  }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    int below = 0, is_sel = 0;
-    for (int j = 0; j < k; ++j) {
-      const int o = sel_smem[j];
-      below += (o < e) ? 1 : 0;
-      is_sel += (o == e) ? 1 : 0;
+    // exclusive prefix of the words' population counts, 32 words at a time
+    int carry = 0;
+    for (int w0 = 0; w0 < nw; w0 += 32) {
+      const int w = w0 + lane;
+      const int c = w < nw ? __popc(sel_mask[w]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (w < nw) mask_prefix[w] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    a.offsets[e] = below;
-    if (e < E) a.counts[e] = is_sel;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    const int w = e >> 5, b = e & 31;
+    const uint32_t m = sel_mask[w];
+    a.offsets[e] = mask_prefix[w] + __popc(m & ((1u << b) - 1u));
+    if (e < E && a.counts) a.counts[e] = (int)((m >> b) & 1u);
   }
 }
 

@@ -145,7 +145,9 @@ cudaError_t launch_combine(const CombineArgs& a, bool pdl, cudaStream_t s) {
     return launch("combine", combine_parts_kernel, grid, dim3(32 * kPartsWarps), smem, s, pdl, a);
   }
   const int n4 = a.d / 4;
-  const int threads = n4 < 256 ? ((n4 + 31) / 32) * 32 : 256;
+  // few tokens: small blocks, so that the gathers of one token spread over many SMs
+  const int tmax = a.T <= 4 ? 64 : 256;
+  const int threads = n4 < tmax ? ((n4 + 31) / 32) * 32 : tmax;
   const dim3 grid((n4 + threads - 1) / threads, a.T);
   return launch("combine", combine_kernel, grid, dim3(threads), 0, s, pdl, a);
 }
