@@ -17,9 +17,15 @@
 // double-buffered ring of shared memory, a group ahead of the lookups: four TMA
 // boxes of [3 stages][32 positions][128 rows] (12 KB each, one instruction
 // apiece) with the 128-byte swizzle, so that each (stage, position) run of
-// 128 rows is one contiguous DRAM read and the 16-byte reads of 8 lanes fall
-// in 8 different bank groups.  The boxes' tensor map is the matrix's; its
-// address is patched on the device whenever the matrix changes.
+// 128 rows is one contiguous DRAM read and the lanes' 8-byte code reads
+// (lane l reads line l of a stage) spread over the banks.  The boxes' tensor
+// map is the matrix's; its address is patched on the device whenever the
+// matrix changes.
+//
+// Tables are built on the tensor cores (build_table): per stage the product
+// of the slice's 32 x 8 elements and the 256 x 8 codebook, one
+// mma.sync.m16n8k8 per 16 positions x 8 codes, the elements split into f16
+// hi + lo pairs after a power-of-two rescale.
 //
 // Lookups.  Lane l of a consumer warp owns position l of the slice: the 32
 // lanes of a lookup read 32 different banks whatever the codes are.  The
@@ -36,10 +42,11 @@
 // chosen by its own lane bits, so four of the five halving steps swap no
 // registers before their shuffle; lane l ends with one row's slice sum.
 //
-// Work: units are (vector, slice, matrix, 256-row group) in this order; each
+// Work: units are (vector, slice, matrix, 512-row group) in this order; each
 // persistent CTA takes one contiguous range of units and rebuilds the table
 // when the (vector, slice) changes (about once or twice per CTA at decode
-// sizes) while the producer keeps staging codes.  Slice sums go to
+// sizes) while the producer keeps staging codes; the gate/up kernel builds its
+// first table before it waits for the routing kernels.  Slice sums go to
 // pair-indexed partial buffers; the down kernel finishes h (the slice sums of
 // gate and up, then the activation) while it loads its vector, and the
 // combine adds the down kernel's slice sums, so no separate reduction pass
