@@ -195,6 +195,7 @@ moe::RouteArgs route_args(const void* x, moe_dtype x_dtype, const void* w, moe_d
   ra.absdot = ws.absdot;
   ra.comp = T <= kCompensatedMaxT ? 1 : 0;
   ra.gamma = ra.comp ? router_gamma_comp(d) : router_gamma(d, x_dtype, w_dtype);
+  ra.gamma_comp = router_gamma_comp(d);
   ra.topk_idx = topk;
   ra.gates = gates;
   ra.err = err;

@@ -182,6 +182,7 @@ struct RouteArgs {
   float* absdot;  // [T][E]   workspace: sum_i |W[e][i] x[t][i]| (compensated logits only)
   int comp;       // logits by compensated (Dot2) sums; bounds from absdot
   float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
+  float gamma_comp;  // the compensated sums' coefficient (router_gamma_comp), for the top-k's recheck
   int32_t* topk_idx;  // [T][k + n_shared]
   float* gates;       // [T][k + n_shared]
   int* err;

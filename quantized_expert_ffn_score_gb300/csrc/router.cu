@@ -538,6 +538,84 @@ __device__ void logit_fp64_warp(const RouteArgs& a, int t, int e, double* val, d
   *abs_sum = sa;
 }
 
+// Warp-parallel compensated fp32 logit, summed exactly as router_logits_comp_kernel
+// sums one token (lane chunks of N elements, two Dot2 chains per lane merged
+// by TwoSum, then a TwoSum butterfly over the lanes), so the same coefficient
+// bounds it: |val - l_ref| <= gamma_comp * sum|p|, where val = s + c is kept
+// unrounded in fp64 (its last addition and the bias add at most 2^-52 |val|).
+// fp32 arithmetic at the full rate, where the fp64 form runs at the GPU's far
+// lower fp64 rate.
+template <typename WT>
+__device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, double* abs_sum) {
+  constexpr int N = Vec16<WT>::N;
+  const int lane = threadIdx.x & 31;
+  const int d = a.d, nch = d / (32 * N), rem = d - nch * 32 * N;
+  const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)e * d);
+  float s[2] = {0.f, 0.f}, c[2] = {0.f, 0.f}, sa = 0.f;
+  auto consume = [&](const uint4 raw, int col) {
+    float w[N], xr[N];
+    Vec16<WT>::unpack(raw, w);
+    const size_t xo = (size_t)t * d + col;  // N consecutive activations, 16-byte aligned
+    if (a.x_dtype == MOE_BF16) {
+      const uint16_t* xb = static_cast<const uint16_t*>(a.x) + xo;
+#pragma unroll
+      for (int q = 0; q < N / 8; ++q) Vec16<uint16_t>::unpack(__ldg(reinterpret_cast<const uint4*>(xb) + q), xr + 8 * q);
+      if (N == 4) {
+        const uint2 h = __ldg(reinterpret_cast<const uint2*>(xb));
+        xr[0] = __uint_as_float(h.x << 16);
+        xr[1] = __uint_as_float(h.x & 0xFFFF0000u);
+        xr[2] = __uint_as_float(h.y << 16);
+        xr[3] = __uint_as_float(h.y & 0xFFFF0000u);
+      }
+    } else {
+      const float4* xf = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + xo);
+#pragma unroll
+      for (int q = 0; q < N / 4; ++q) {
+        const float4 v = __ldg(xf + q);
+        xr[4 * q] = v.x;
+        xr[4 * q + 1] = v.y;
+        xr[4 * q + 2] = v.z;
+        xr[4 * q + 3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < N; ++m) {
+      const float xv = xr[m];
+      const int ch = m & 1;
+      const float p = __fmul_rn(w[m], xv);
+      const float ep = __fmaf_rn(w[m], xv, -p);
+      float t2, es;
+      two_sum(s[ch], p, t2, es);
+      s[ch] = t2;
+      c[ch] = __fadd_rn(c[ch], __fadd_rn(es, ep));
+      sa = __fadd_rn(sa, fabsf(p));
+    }
+  };
+  for (int u = 0; u < nch; ++u) consume(__ldg(wrow + u * 32 + lane), (u * 32 + lane) * N);
+  if (lane * N < rem) consume(__ldg(wrow + nch * 32 + lane), (nch * 32 + lane) * N);
+  float st, ct;
+  {
+    float es;
+    two_sum(s[0], s[1], st, es);
+    ct = __fadd_rn(__fadd_rn(c[0], c[1]), es);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, st, o);
+    const float c2 = __shfl_xor_sync(0xffffffffu, ct, o);
+    sa = __fadd_rn(sa, __shfl_xor_sync(0xffffffffu, sa, o));
+    float t2, es;
+    two_sum(st, s2, t2, es);
+    st = t2;
+    ct = __fadd_rn(__fadd_rn(ct, c2), es);
+  }
+  double v = (double)st + (double)ct;
+  const float* kb = a.bias ? a.bias : a.sel_bias;
+  if (kb) v += (double)kb[e];
+  *val = v;
+  *abs_sum = (double)sa;
+}
+
 __device__ __forceinline__ double gamma64(int n) {
   const double u = 1.1102230246251565e-16;  // 2^-53
   return n * u / (1.0 - n * u);
@@ -578,8 +656,10 @@ __device__ float block_max(float v, float* scratch) {
 // Recheck path of one token's top-k (the fp32 bounds did not certify the
 // selection): every expert that could be in the top k (selected, or upper
 // bound at least m, the lowest selected lower bound) gets an interval; those
-// meeting another one's are recomputed in fp64 (warp-parallel, with its own
-// bound) and, if still undecided, by the reference's sequential fp64 sum.
+// meeting another one's are recomputed with compensated fp32 sums (warp-
+// parallel, about u^2 relative), those still undecided in fp64 (warp-parallel,
+// with its own bound) and, if still undecided, by the reference's sequential
+// fp64 sum.
 __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float* sv, const float* sb,
                                           const unsigned char* insel, float m, double* clo, double* chi, int* cand,
                                           unsigned char* cflag, int* out_sel) {
@@ -603,7 +683,29 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
   }
   __syncthreads();
   const int n = n_cand;
-  // pass 1: candidates whose interval meets another one's get a warp-parallel fp64 value
+  // candidates whose interval meets another one's get a tighter value below
+  for (int c = tid; c < n; c += blockDim.x) {
+    unsigned char f = 0;
+    for (int c2 = 0; c2 < n; ++c2)
+      if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
+    cflag[c] = f;
+  }
+  __syncthreads();
+  // pass 1: compensated fp32 sums, the bound of the compensated router kernel
+  for (int c = warp; c < n; c += kTopkThreads / 32) {
+    if (!cflag[c]) continue;
+    double val, sa;
+    if (a.w_dtype == MOE_BF16)
+      logit_dot2_warp<uint16_t>(a, t, cand[c], &val, &sa);
+    else
+      logit_dot2_warp<float>(a, t, cand[c], &val, &sa);
+    if (lane == 0) {
+      const double bd = (double)a.gamma_comp * sa * 1.0001 + 2.3e-16 * fabs(val) + 1e-300;
+      clo[c] = val - bd;
+      chi[c] = val + bd;
+    }
+  }
+  __syncthreads();
   for (int c = tid; c < n; c += blockDim.x) {
     unsigned char f = 0;
     for (int c2 = 0; c2 < n; ++c2)
@@ -627,7 +729,7 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
     }
   }
   __syncthreads();
-  // pass 2: still undecided -> the reference's own sequential fp64 sum
+  // pass 3: still undecided -> the reference's own sequential fp64 sum
   for (int c = tid; c < n; c += blockDim.x) {
     unsigned char f = 0;
     for (int c2 = 0; c2 < n; ++c2)
@@ -761,7 +863,7 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   // the search: the selection is then every key whose masked value is at or
   // above the prefix (usually after two of the four passes).
   for (int shift = 24; shift >= 0; shift -= 8) {
-    hist[tid] = 0;
+    if (tid < 256) hist[tid] = 0;
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kSlicePerLane; ++i)
