@@ -56,6 +56,25 @@ def test_mid_mxfp4_all_experts_selected(lib, ctx):
     gu.full_check(lib, ctx, MID_MX.with_(E=8, k=8, T=3, seed=15))
 
 
+@pytest.mark.parametrize("quant", ["mxfp4", "rvq3"])
+def test_one_token_layer_without_optional_outputs(lib, ctx, quant):
+    # one token with no routing outputs asked for: the top-k kernel buckets the
+    # pairs and writes no per-expert counts; the output must still match the oracle
+    moe = lib
+    from quantized_expert_ffn_score_gb300 import synthetic
+    r = (MID_MX if quant == "mxfp4" else MID_RVQ).with_(T=1, seed=33)
+    layer = synthetic.device_layer(r)
+    x = synthetic.device_x(r)
+    out = torch.empty((1, r.d), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(moe.layer_forward_ws_bytes(layer, 1))
+    moe.moe_layer_forward(ctx, layer, x, out, ws)
+    ctx.check()
+    xh = si.layer_x(r)
+    _, _, _, y, _ = gu.oracle_layer(r, xh)
+    delta = out.cpu().numpy().astype(np.float64) - gu.x_host_f64(xh)
+    gu.assert_rms_close(delta, y, what=f"one token, {quant}, no optional outputs")
+
+
 def test_mid_rvq3(lib, ctx):
     gu.full_check(lib, ctx, MID_RVQ)
 
