@@ -354,6 +354,7 @@ moe_status layer_forward_impl(moe_ctx* ctx, const moe_layer* L, const void* x, m
   }
   moe::FfnArgs fa = ffn_args(ctx, x, x_dtype, T, ks, L->d, L->ff, Es, L->act, w.offsets, w.pairs, w.y_pairs, w.ffn);
   fa.max_x = w.route.max_x;  // computed by the router kernel
+  fa.x_early = 1;            // two launches before the expert kernels
   if (L->quant == MOE_QUANT_MXFP4 && bs) {
     fa.records = L->mxfp4.records;
     st = cuda_status(moe::launch_mxfp4_bs(bs_launch(fa, w.ffn), ctx->num_sms, true, s));

@@ -217,6 +217,11 @@ struct FfnArgs {
   float* y_pairs;         // [T*k][d] by pair id
   float* partial;         // RVQ3 only: K-slice partial sums (workspace)
   int* err;
+  // 1 when x and max_x were complete before the kernel launched just ahead of
+  // the expert kernels started (the layer path: the router wrote max_x two
+  // launches earlier), so that the one-token GEMV may stage x before its wait;
+  // 0 when the launch just ahead writes them (the standalone expert calls)
+  int x_early;
 };
 cudaError_t launch_active_from_offsets(const int32_t* offsets, int E, int32_t* active, bool pdl, cudaStream_t s);
 cudaError_t launch_mxfp4_ffn(const FfnArgs& a, int num_sms, bool pdl, cudaStream_t s);

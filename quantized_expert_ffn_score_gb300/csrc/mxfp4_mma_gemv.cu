@@ -281,14 +281,16 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
   // was written two launches earlier (complete before the gate/up pass passed
   // its own wait, which precedes this launch): it starts streaming while the
   // gate/up pass finishes.  Everything that reads h or writes outputs waits.
-  // One-token gate/up: the compute warps stage the token's B fragments first
-  // (the layer input and the router's max |x| were complete before the top-k
-  // kernel ran) and the producer pulls the record table into L2 while the
+  // One-token gate/up: when x and max |x| were complete before the kernel just
+  // ahead of this one (a.x_early: the layer path, where the router wrote max |x|
+  // two launches earlier), the compute warps stage the token's B fragments
+  // before the wait; the producer pulls the record table into L2 while the
   // routing is made.  Dependents are released only after the wait: the down
   // pass's producer reads the routing without waiting, which is safe only
   // because this pass's wait has returned before that launch.
   const int W = g.warps;
-  if (SB && MODE == 0 && warp >= 1 && warp <= W) {
+  const bool x_staged = SB && MODE == 0 && a.x_early;
+  if (x_staged && warp >= 1 && warp <= W) {
     Frags<MODE, BPW, PAIR, SB> f0;
     f0.sb = smem + g.sb_off;
     f0.lane_bytes = g.sb_lane_bytes;
@@ -452,8 +454,8 @@ __global__ void __launch_bounds__((kMaxBlocks / BPW + 2) * 32, 1) mxfp4_mma_gemv
       rec_good = rec_ok(a.records[e]);
       s0 = a.offsets[e];
       ne = a.offsets[e + 1] - s0;
-      // (one-token gate/up: staged before the wait)
-      if (rec_good && ne <= kTok && !(SB && MODE == 0)) fr.load(a, s0, ne, b0, g.nblk, lane);
+      // (one-token gate/up of the layer path: staged before the wait)
+      if (rec_good && ne <= kTok && !x_staged) fr.load(a, s0, ne, b0, g.nblk, lane);
     }
     if (!rec_good) continue;
     if (++stage == g.stages) stage = 0;

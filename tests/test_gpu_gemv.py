@@ -86,6 +86,39 @@ def test_standalone_expert_call_matches_oracle_pairs(lib, ctx):
     gu.assert_rms_close(y, ref, what="GEMV expert call")
 
 
+@pytest.mark.parametrize("static", [False, True])
+def test_standalone_one_token_expert_call_matches_oracle(lib, ctx, static):
+    # one token through the expert call itself: the per-token max |x| comes from
+    # the launch just ahead of the expert kernels (not from a router two launches
+    # earlier), so the one-token kernel must not stage x before its wait
+    import oracle
+    from quantized_expert_ffn_score_gb300 import synthetic
+    r = ZIPF.with_(T=1, seed=41)
+    layer = synthetic.device_layer(r)
+    for call, offset in enumerate((0, 7)):  # two calls: the second must not see the first token's scale
+        x = synthetic.device_x(r, token_offset=offset)
+        topk = torch.empty((1, r.k), dtype=torch.int32, device="cuda")
+        gates = torch.empty((1, r.k), dtype=torch.float32, device="cuda")
+        lib.moe_route_topk(ctx, x, layer.router_w, layer.router_bias, r.k, topk, gates,
+                           lib.workspace(lib.route_topk_ws_bytes(1, r.d, r.E, r.k)))
+        counts = torch.empty(r.E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(r.E + 1, dtype=torch.int32, device="cuda")
+        pairs = torch.empty(r.k, dtype=torch.int32, device="cuda")
+        lib.moe_bucket_tokens(ctx, topk, r.E, counts, offsets, pairs,
+                              lib.workspace(lib.bucket_tokens_ws_bytes(1, r.k, r.E)))
+        y = torch.full((r.k, r.d), float("nan"), dtype=torch.float32, device="cuda")
+        if static:
+            lib.moe_expert_ffn_mxfp4_static(ctx, x, r.k, layer, offsets, pairs, y)
+        else:
+            lib.moe_expert_ffn_mxfp4(ctx, x, r.k, layer, offsets, pairs, y,
+                                     lib.workspace(lib.expert_ffn_ws_bytes(1, r.k, r.d, r.ff, r.E)))
+        ctx.check()
+        xh = gu.x_host_f64(si.layer_x(r, T=1, token_offset=offset))
+        idx = topk.cpu().numpy().reshape(-1)
+        ref = np.stack([oracle.expert_mxfp4(xh[0], si.layer_record(r, int(e)), r.d, r.ff, act_kind=r.act) for e in idx])
+        gu.assert_rms_close(y.cpu().numpy().astype(np.float64), ref, what=f"one-token expert call {call + 1}")
+
+
 def test_missing_expert_is_reported(lib, ctx):
     from quantized_expert_ffn_score_gb300 import synthetic
     r = ZIPF
