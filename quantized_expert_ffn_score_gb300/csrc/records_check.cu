@@ -13,7 +13,11 @@
 //   * the standard value is CRC(M) = R(M) xor (0xFFFFFFFF * x^(8|M|)) xor 0xFFFFFFFF.
 // A record of B bytes is read as if preceded by zeros up to a whole number of
 // 4 KiB units.  Every warp takes one unit at a time, independently of the
-// other warps: each lane folds its 128 contiguous bytes through byte tables
+// other warps: it reads the unit with coalesced 16-byte loads (each load
+// instruction covers 512 contiguous bytes) into its own 4 KiB of shared
+// memory, XOR-swizzled by 16-byte slot so that both the stores and the
+// per-lane reads below are free of bank conflicts, while the loads of its next
+// unit are in flight; each lane then folds its 128 contiguous bytes through byte tables
 // (four bytes per step, the four tables giving a byte's effect after 4, 3, 2
 // and 1 more bytes), multiplies the result by x to the number of bits that
 // follow it in the unit, and the warp xors the lanes into the unit's raw CRC.
@@ -30,15 +34,23 @@ namespace moe {
 namespace {
 
 constexpr uint32_t kCrcPoly = 0xEDB88320u;
-constexpr int kCrcWarps = 32;
+constexpr int kCrcWarps = 16;
 constexpr int kCrcThreads = kCrcWarps * 32;
 constexpr int kCrcLaneBytes = 128;             // contiguous bytes per lane and unit
 constexpr int kCrcUnit = 32 * kCrcLaneBytes;   // 4 KiB per warp unit
-// shared memory: byte tables [4][256][32] (128 KiB), then the per-lane nibble
-// tables of the lane's power of x [8][16][32] (16 KiB)
+// shared memory: byte tables [4][256][32] (128 KiB), the per-lane nibble
+// tables of the lane's power of x [8][16][32] (16 KiB), then one unit per warp
+// (64 KiB)
 constexpr int kByteTabWords = 4 * 256 * 32;
 constexpr int kNibTabWords = 8 * 16 * 32;
-constexpr size_t kCrcSmemBytes = (size_t)(kByteTabWords + kNibTabWords) * sizeof(uint32_t);
+constexpr int kStageWords = kCrcWarps * kCrcUnit / 4;
+constexpr size_t kCrcSmemBytes = (size_t)(kByteTabWords + kNibTabWords + kStageWords) * sizeof(uint32_t);
+
+// Shared-memory slot of a unit's 16-byte piece k (0..255): the low three bits
+// are xored with bits 3..5, so that 8 consecutive lanes touch 8 distinct
+// 16-byte bank groups both when lane l stores pieces l + 32 j and when it
+// reads pieces 8 l + i.
+__device__ __forceinline__ int crc_slot(int k) { return k ^ ((k >> 3) & 7); }
 
 // a * b modulo the generator: sum over the coefficients a_k of x^k * b.
 __host__ __device__ inline uint32_t gf2_mulmod(uint32_t a, uint32_t b) {
@@ -113,19 +125,36 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_units_kernel(const CrcArgs
   // n * units < 2^31 (checked by the launcher): 32-bit work indices
   const unsigned total = (unsigned)a.n * (unsigned)a.units;
   const unsigned nwarps = gridDim.x * kCrcWarps;
-  for (unsigned w = blockIdx.x * kCrcWarps + warp; w < total; w += nwarps) {
+  uint4* stage = reinterpret_cast<uint4*>(nib + kNibTabWords) + warp * (kCrcUnit / 16);
+  // the coalesced loads of unit w: lane l's pieces l + 32 j (zeros where the
+  // piece lies in the virtual leading zeros; nothing for an unusable record)
+  auto fetch = [&](unsigned w, uint4 (&g)[8]) {
     const unsigned rec = w / (unsigned)a.units;
     const long long unit = (long long)(w - rec * (unsigned)a.units);
     const uint8_t* base = a.records[rec];
-    uint32_t part = 0;
-    if (record_usable(base)) {
-      const long long o = unit * kCrcUnit + lane * kCrcLaneBytes - a.pad;  // real offset of the lane's piece
-      uint4 q[kCrcLaneBytes / 16];
+    const bool usable = record_usable(base);
 #pragma unroll
-      for (int j = 0; j < kCrcLaneBytes / 16; ++j) {
-        const long long oj = o + 16 * j;  // 16-byte chunks lie wholly in the padding or in the record
-        q[j] = oj >= 0 ? __ldg(reinterpret_cast<const uint4*>(base + oj)) : make_uint4(0u, 0u, 0u, 0u);
-      }
+    for (int j = 0; j < 8; ++j) {
+      const long long o = unit * kCrcUnit + 16 * (lane + 32 * j) - a.pad;  // pieces lie wholly in the padding or the record
+      g[j] = usable && o >= 0 ? __ldg(reinterpret_cast<const uint4*>(base + o)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    return usable;
+  };
+  uint4 g[8];
+  unsigned w = blockIdx.x * kCrcWarps + warp;
+  bool usable = w < total && fetch(w, g);
+  for (; w < total; w += nwarps) {
+    __syncwarp();  // the previous unit's reads are done
+#pragma unroll
+    for (int j = 0; j < 8; ++j) stage[crc_slot(lane + 32 * j)] = g[j];
+    __syncwarp();
+    uint4 q[kCrcLaneBytes / 16];
+#pragma unroll
+    for (int i = 0; i < kCrcLaneBytes / 16; ++i) q[i] = stage[crc_slot(8 * lane + i)];
+    const bool cur_usable = usable;
+    if (w + nwarps < total) usable = fetch(w + nwarps, g);  // in flight during the folding below
+    uint32_t part = 0;
+    if (cur_usable) {
       uint32_t reg = 0;
 #pragma unroll
       for (int j = 0; j < kCrcLaneBytes / 16; ++j) {

@@ -200,21 +200,39 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_kernel(RouteAr
   pdl_launch_dependents();
 }
 
-// Tiled form of the same sums for bf16 x and W with d a multiple of 256 (the
-// prefill router): 8 tokens staged per CTA as fp32 with the two halves of
-// every 8-element chunk stored apart (xs[(2t + h) * d/8 + c] holds elements
-// 8c + 4h .. 8c + 4h + 3 of token t), so that lane l's loads of chunk
-// c = 32u + l are conflict-free; each warp takes 4 expert rows, two at a time,
-// against 4 tokens at a time.  Every logit is summed exactly as in
-// router_logits_kernel (lane chunks, one accumulator per element position, the
-// same tree), so the error bound and the values are unchanged.
-constexpr int kTiledTok = 8;       // tokens staged per CTA
-constexpr int kTiledPass = 4;      // tokens per accumulator pass
-constexpr int kTiledRows = 4;      // expert rows per warp
-constexpr int kTiledBatch = 2;     // chunks of both rows loaded ahead
+// Tiled form for bf16 x and W with d a multiple of 256 (the prefill router):
+// 8 tokens staged per CTA as fp32 with the two halves of every 8-element chunk
+// stored apart (xs[(2t + h) * d/8 + c] holds elements 8c + 4h .. 8c + 4h + 3
+// of token t), so that lane l's loads of chunk c = 32u + l are conflict-free;
+// each warp takes 4 expert rows against all 8 tokens, one accumulator per
+// (row, token) and lane, so that a staged token feeds 4 rows and a loaded
+// weight chunk 8 tokens.  Per chunk the lane sums each half's 4 products as an
+// fma chain started by an exact product (bf16 x bf16 fits fp32) and adds the
+// two halves, then adds the chunk sum to its accumulator in ascending chunk
+// order; the lanes join in a 5-level tree.  A product thus passes through at
+// most 3 + 1 + (d/256 - 1) + 5 = d/256 + 8 roundings, the depth of
+// router_logits_kernel's tree that the error bound assumes.
+constexpr int kTiledTok = 8;   // tokens staged per CTA
+constexpr int kTiledRows = 4;  // expert rows per warp
 constexpr int kTiledExperts = kLogitWarps * kTiledRows;
 
 __host__ __device__ inline size_t tiled_smem_bytes(int d) { return (size_t)kTiledTok * d * sizeof(float); }
+
+// Sum over the 32 lanes of each of v[0..31]: lane l ends with the sum of v[l]
+// (a 5-level tree per value, one shuffle per value and level halved each time).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = upper ? v[i] : v[i + m];
+      const float keep = upper ? v[i + m] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return v[0];
+}
 
 __global__ void __launch_bounds__(kLogitWarps * 32, 2) router_logits_tiled_kernel(RouteArgs a) {
   extern __shared__ float4 xs4[];  // [kTiledTok][2][d/8]
@@ -222,6 +240,17 @@ __global__ void __launch_bounds__(kLogitWarps * 32, 2) router_logits_tiled_kerne
   const int d = a.d, nc = d / 8, nch = d / 256;
   const int t0 = blockIdx.y * kTiledTok;
   const int nt = min(kTiledTok, a.T - t0);
+  // the warp's rows (clamped to the last expert; those sums are not written)
+  const int e_first = blockIdx.x * kTiledExperts + warp * kTiledRows;
+  const uint4* wrow[kTiledRows];
+#pragma unroll
+  for (int r = 0; r < kTiledRows; ++r)
+    wrow[r] = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.w) +
+                                             (size_t)min(e_first + r, a.E - 1) * d);
+  // the first chunk's weights do not depend on the previous kernel
+  uint4 wq[kTiledRows];
+#pragma unroll
+  for (int r = 0; r < kTiledRows; ++r) wq[r] = __ldg(wrow[r] + lane);
   pdl_wait();
   {  // stage the tokens (zeros past T)
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)t0 * d);
@@ -255,85 +284,63 @@ __global__ void __launch_bounds__(kLogitWarps * 32, 2) router_logits_tiled_kerne
       a.max_x[t0 + warp] = m;
     }
   }
-  const int e_first = blockIdx.x * kTiledExperts + warp * kTiledRows;
-  const uint16_t* wbase = static_cast<const uint16_t*>(a.w);
-  for (int rp = 0; rp < kTiledRows; rp += 2) {
-    const int e0 = e_first + rp, e1 = e0 + 1;
-    if (e0 >= a.E) break;
-    const bool has1 = e1 < a.E;
-    const uint4* w0 = reinterpret_cast<const uint4*>(wbase + (size_t)e0 * d);
-    const uint4* w1 = reinterpret_cast<const uint4*>(wbase + (size_t)(has1 ? e1 : e0) * d);
-    float sq0 = 0.f, sq1 = 0.f;
-    for (int tp = 0; tp < nt; tp += kTiledPass) {
-      float acc[kTiledPass][2][8];
+  if (e_first >= a.E) {
+    pdl_launch_dependents();
+    return;
+  }
+  const bool norms = blockIdx.y == 0;
+  float acc[kTiledRows * kTiledTok];  // [row][token]
+  float sq[kTiledRows];
 #pragma unroll
-      for (int t = 0; t < kTiledPass; ++t)
+  for (int i = 0; i < kTiledRows * kTiledTok; ++i) acc[i] = 0.f;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc[t][0][m] = acc[t][1][m] = 0.f;
-      for (int cb = 0; cb < nch; cb += kTiledBatch) {
-        uint4 wa[kTiledBatch], wb[kTiledBatch];
+  for (int r = 0; r < kTiledRows; ++r) sq[r] = 0.f;
+  for (int u = 0; u < nch; ++u) {
+    const int c = u * 32 + lane;
+    float w[kTiledRows][8];
 #pragma unroll
-        for (int u = 0; u < kTiledBatch; ++u)
-          if (cb + u < nch) {
-            wa[u] = __ldg(w0 + (cb + u) * 32 + lane);
-            wb[u] = __ldg(w1 + (cb + u) * 32 + lane);
-          }
+    for (int r = 0; r < kTiledRows; ++r) Vec16<uint16_t>::unpack(wq[r], w[r]);
+    if (u + 1 < nch) {  // the next chunk's weights, in flight during this one
 #pragma unroll
-        for (int u = 0; u < kTiledBatch; ++u) {
-          if (cb + u >= nch) break;
-          const int c = (cb + u) * 32 + lane;
-          float fa[8], fb[8];
-          Vec16<uint16_t>::unpack(wa[u], fa);
-          Vec16<uint16_t>::unpack(wb[u], fb);
-          if (tp == 0 && blockIdx.y == 0) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              sq0 = fmaf(fa[m], fa[m], sq0);
-              sq1 = fmaf(fb[m], fb[m], sq1);
-            }
-          }
-#pragma unroll
-          for (int t = 0; t < kTiledPass; ++t) {
-            const float4 x0 = xs4[(2 * (tp + t)) * nc + c], x1 = xs4[(2 * (tp + t) + 1) * nc + c];
-            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              acc[t][0][m] = fmaf(fa[m], xv[m], acc[t][0][m]);
-              acc[t][1][m] = fmaf(fb[m], xv[m], acc[t][1][m]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kTiledPass; ++t) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-          for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-            for (int m = 0; m < w; ++m) acc[t][r][m] += acc[t][r][m + w];
-          float s = acc[t][r][0];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          const int e = r == 0 ? e0 : e1;
-          if (lane == 0 && tp + t < nt && (r == 0 || has1))
-            a.logits[(size_t)(t0 + tp + t) * a.E + e] = s + (a.bias ? a.bias[e] : 0.f);
-        }
-      }
+      for (int r = 0; r < kTiledRows; ++r) wq[r] = __ldg(wrow[r] + c + 32);
     }
-    if (blockIdx.y == 0) {
+    if (norms) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sq0 += __shfl_xor_sync(0xffffffffu, sq0, o);
-        sq1 += __shfl_xor_sync(0xffffffffu, sq1, o);
-      }
-      if (lane == 0) {
-        a.nrm_w[e0] = sqrtf(sq0);
-        if (has1) a.nrm_w[e1] = sqrtf(sq1);
+      for (int r = 0; r < kTiledRows; ++r)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) sq[r] = fmaf(w[r][m], w[r][m], sq[r]);
+    }
+#pragma unroll
+    for (int t = 0; t < kTiledTok; ++t) {
+      const float4 x0 = xs4[(2 * t) * nc + c], x1 = xs4[(2 * t + 1) * nc + c];
+#pragma unroll
+      for (int r = 0; r < kTiledRows; ++r) {
+        float h0 = __fmul_rn(w[r][0], x0.x);
+        h0 = __fmaf_rn(w[r][1], x0.y, h0);
+        h0 = __fmaf_rn(w[r][2], x0.z, h0);
+        h0 = __fmaf_rn(w[r][3], x0.w, h0);
+        float h1 = __fmul_rn(w[r][4], x1.x);
+        h1 = __fmaf_rn(w[r][5], x1.y, h1);
+        h1 = __fmaf_rn(w[r][6], x1.z, h1);
+        h1 = __fmaf_rn(w[r][7], x1.w, h1);
+        acc[r * kTiledTok + t] = __fadd_rn(acc[r * kTiledTok + t], __fadd_rn(h0, h1));  // first add exact (acc = 0)
       }
     }
   }
   pdl_launch_dependents();
+  const float s = reduce_scatter32(acc, lane);
+  {
+    const int r = lane / kTiledTok, t = lane % kTiledTok, e = e_first + r;
+    if (t < nt && e < a.E) a.logits[(size_t)(t0 + t) * a.E + e] = s + (a.bias ? a.bias[e] : 0.f);
+  }
+  if (norms) {
+#pragma unroll
+    for (int r = 0; r < kTiledRows; ++r) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
+      if (lane == 0 && e_first + r < a.E) a.nrm_w[e_first + r] = sqrtf(sq[r]);
+    }
+  }
 }
 
 // Compensated variant (used for small T; TT tokens per CTA, 1 when T = 1 so
