@@ -155,6 +155,16 @@ float router_gamma_comp(int d) {
   return (float)((gn * gn * (1.0 + gn) + g64) * 1.01);
 }
 
+// Bound coefficient of the top-k recheck's warp-parallel fp64 logits against the
+// reference's sequential fp64 sum: gamma64(d/32 + 6) for the warp sum (lane
+// chains of d/32 products plus a 5-level butterfly and the bias), gamma64(d + 1)
+// for the reference, 1 % for the fp64 evaluation of sum|p|.
+double router_gamma_fp64(int d) {
+  const double u = 1.1102230246251565e-16;  // 2^-53
+  auto g = [u](double n) { return n * u / (1.0 - n * u); };
+  return (g(d / 32 + 6) + g(d + 1.0)) * 1.01;
+}
+
 struct RouteWs {
   float* logits;
   float* nrm_w;
@@ -196,6 +206,7 @@ moe::RouteArgs route_args(const void* x, moe_dtype x_dtype, const void* w, moe_d
   ra.comp = T <= kCompensatedMaxT ? 1 : 0;
   ra.gamma = ra.comp ? router_gamma_comp(d) : router_gamma(d, x_dtype, w_dtype);
   ra.gamma_comp = router_gamma_comp(d);
+  ra.gamma_fp64 = router_gamma_fp64(d);
   ra.topk_idx = topk;
   ra.gates = gates;
   ra.err = err;

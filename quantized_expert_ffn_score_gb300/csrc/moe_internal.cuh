@@ -183,6 +183,7 @@ struct RouteArgs {
   int comp;       // logits by compensated (Dot2) sums; bounds from absdot
   float gamma;    // error-bound coefficient (see router_gamma / router_gamma_comp)
   float gamma_comp;  // the compensated sums' coefficient (router_gamma_comp), for the top-k's recheck
+  double gamma_fp64;  // the warp-parallel fp64 sums' coefficient (router_gamma_fp64), for the recheck
   int32_t* topk_idx;  // [T][k + n_shared]
   float* gates;       // [T][k + n_shared]
   int* err;

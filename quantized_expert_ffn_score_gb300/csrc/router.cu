@@ -449,10 +449,6 @@ __global__ void __launch_bounds__(kLogitWarps * 32) router_logits_comp_kernel(Ro
 // ---------------------------------------------------------------- top-k
 constexpr int kTopkThreads = 256;
 
-__device__ __forceinline__ bool better(double v1, int e1, double v2, int e2) {
-  return v1 > v2 || (v1 == v2 && e1 < e2);
-}
-
 // Eight consecutive elements i0 .. i0+7 (i0 a multiple of 8) of a bf16 or fp32
 // row as doubles, with one or two 16-byte loads.
 __device__ __forceinline__ void load8_d(const void* p, int dtype, size_t i0, double (&v)[8]) {
@@ -555,14 +551,14 @@ __device__ void logit_fp64_warp(const RouteArgs& a, int t, int e, double* val, d
 template <typename WT>
 __device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, double* abs_sum) {
   constexpr int N = Vec16<WT>::N;
+  constexpr int B = 4;  // chunks whose loads are in flight together (the sums still run in chunk order)
   const int lane = threadIdx.x & 31;
   const int d = a.d, nch = d / (32 * N), rem = d - nch * 32 * N;
   const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const WT*>(a.w) + (size_t)e * d);
   float s[2] = {0.f, 0.f}, c[2] = {0.f, 0.f}, sa = 0.f;
-  auto consume = [&](const uint4 raw, int col) {
-    float w[N], xr[N];
-    Vec16<WT>::unpack(raw, w);
-    const size_t xo = (size_t)t * d + col;  // N consecutive activations, 16-byte aligned
+  // the N activations of the chunk at column col (16-byte aligned)
+  auto load_x = [&](int col, float (&xr)[N]) {
+    const size_t xo = (size_t)t * d + col;
     if (a.x_dtype == MOE_BF16) {
       const uint16_t* xb = static_cast<const uint16_t*>(a.x) + xo;
 #pragma unroll
@@ -585,6 +581,10 @@ __device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, d
         xr[4 * q + 3] = v.w;
       }
     }
+  };
+  auto consume = [&](const uint4 raw, const float (&xr)[N]) {
+    float w[N];
+    Vec16<WT>::unpack(raw, w);
 #pragma unroll
     for (int m = 0; m < N; ++m) {
       const float xv = xr[m];
@@ -598,8 +598,25 @@ __device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, d
       sa = __fadd_rn(sa, fabsf(p));
     }
   };
-  for (int u = 0; u < nch; ++u) consume(__ldg(wrow + u * 32 + lane), (u * 32 + lane) * N);
-  if (lane * N < rem) consume(__ldg(wrow + nch * 32 + lane), (nch * 32 + lane) * N);
+  for (int u0 = 0; u0 < nch; u0 += B) {
+    uint4 wq[B];
+    float xr[B][N];
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      if (u0 + j < nch) {
+        wq[j] = __ldg(wrow + (u0 + j) * 32 + lane);
+        load_x(((u0 + j) * 32 + lane) * N, xr[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < B; ++j)
+      if (u0 + j < nch) consume(wq[j], xr[j]);
+  }
+  if (lane * N < rem) {
+    float xr[N];
+    load_x((nch * 32 + lane) * N, xr);
+    consume(__ldg(wrow + nch * 32 + lane), xr);
+  }
   float st, ct;
   {
     float es;
@@ -623,9 +640,59 @@ __device__ void logit_dot2_warp(const RouteArgs& a, int t, int e, double* val, d
   *abs_sum = (double)sa;
 }
 
-__device__ __forceinline__ double gamma64(int n) {
-  const double u = 1.1102230246251565e-16;  // 2^-53
-  return n * u / (1.0 - n * u);
+// Order-preserving integer image of a double that is not NaN (-0 maps with
+// +0): the recheck path compares and orders its fp64 interval ends on the
+// integer units, since fp64 arithmetic runs at a small fraction of the fp32
+// rate on this GPU.
+__device__ __forceinline__ long long ord64(double v) {
+  long long b = __double_as_longlong(v);
+  if (b == (long long)0x8000000000000000ull) b = 0;
+  return b < 0 ? (b ^ 0x7fffffffffffffffll) : b;
+}
+
+// Whether candidate c's interval [lo, hi] meets candidate c2's.
+__device__ __forceinline__ bool meets(const double* lo, const double* hi, int c, int c2) {
+  return !(ord64(lo[c]) > ord64(hi[c2]) || ord64(hi[c]) < ord64(lo[c2]));
+}
+
+// The recheck path runs in few CTAs, so its code is rarely in the instruction
+// caches: it is kept small, and the steps it repeats (or shares with the
+// certified path) are out-of-line functions fetched once.
+
+// flag[c] = whether candidate c's interval meets another candidate's (the
+// whole CTA; followed by a barrier).
+__device__ __noinline__ void mark_meeting(const double* lo, const double* hi, unsigned char* flag, int n) {
+  for (int c = threadIdx.x; c < n; c += blockDim.x) {
+    unsigned char f = 0;
+    for (int c2 = 0; c2 < n && !f; ++c2)
+      if (c2 != c && meets(lo, hi, c, c2)) f = 1;
+    flag[c] = f;
+  }
+  __syncthreads();
+}
+
+// One warp: the gates of a token's k selected experts, lane j < k holding
+// expert e and its gate logit lj (others lj = -inf): exp(lj - max) over their
+// sum, written with the indices to the routing rows and to out_sel.  lj - max
+// is formed exactly in fp64 and rounded once to fp32.
+__device__ __noinline__ void write_gates(const RouteArgs& a, int t, double lj, int e, int* out_sel) {
+  const int lane = threadIdx.x & 31, k = a.k;
+  double lm = lj;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // the largest, compared on the integer units
+    const double ov = __shfl_xor_sync(0xffffffffu, lm, o);
+    if (ord64(ov) > ord64(lm)) lm = ov;
+  }
+  const float g = lane < k ? expf((float)(lj - lm)) : 0.f;
+  float den = g;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane < k) {
+    const size_t r = (size_t)t * (k + a.n_shared) + lane;
+    a.topk_idx[r] = e;
+    a.gates[r] = g / den;
+    out_sel[lane] = e;
+  }
 }
 
 constexpr int kTopkWarps = kTopkThreads / 32;
@@ -672,7 +739,7 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
                                           unsigned char* cflag, int* out_sel) {
   __shared__ int n_cand;
   __shared__ int order[kMaxK];
-  __shared__ double oval[kMaxK];
+  __shared__ int order_c[kMaxK];
   const int E = a.E, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -691,13 +758,7 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
   __syncthreads();
   const int n = n_cand;
   // candidates whose interval meets another one's get a tighter value below
-  for (int c = tid; c < n; c += blockDim.x) {
-    unsigned char f = 0;
-    for (int c2 = 0; c2 < n; ++c2)
-      if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
-    cflag[c] = f;
-  }
-  __syncthreads();
+  mark_meeting(clo, chi, cflag, n);
   // pass 1: compensated fp32 sums, the bound of the compensated router kernel
   for (int c = warp; c < n; c += kTopkThreads / 32) {
     if (!cflag[c]) continue;
@@ -713,18 +774,12 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
     }
   }
   __syncthreads();
-  for (int c = tid; c < n; c += blockDim.x) {
-    unsigned char f = 0;
-    for (int c2 = 0; c2 < n; ++c2)
-      if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
-    cflag[c] = f;
-  }
-  __syncthreads();
-  // bound of the warp-parallel fp64 sum against the reference's sequential one:
-  // its own error gamma64(d/32 + 6) * sum|p| (sum|p| itself within
-  // gamma64(d/32 + 5), absorbed by the factor), the reference's gamma64(d + 1) * sum|p|,
-  // and the rounding of the bias additions
-  const double bound_scale = (gamma64(a.d / 32 + 6) + gamma64(a.d + 1)) * 1.01;
+  mark_meeting(clo, chi, cflag, n);
+  // bound of the warp-parallel fp64 sum against the reference's sequential one
+  // (a.gamma_fp64, host computed): its own error gamma64(d/32 + 6) * sum|p|
+  // (sum|p| itself within gamma64(d/32 + 5), absorbed by the factor), the
+  // reference's gamma64(d + 1) * sum|p|, and the rounding of the bias additions
+  const double bound_scale = a.gamma_fp64;
   for (int c = warp; c < n; c += kTopkThreads / 32) {
     if (!cflag[c]) continue;
     double val, sa;
@@ -737,13 +792,7 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
   }
   __syncthreads();
   // pass 3: still undecided -> the reference's own sequential fp64 sum
-  for (int c = tid; c < n; c += blockDim.x) {
-    unsigned char f = 0;
-    for (int c2 = 0; c2 < n; ++c2)
-      if (c2 != c && !(clo[c] > chi[c2] || chi[c] < clo[c2])) f = 1;
-    cflag[c] = f;
-  }
-  __syncthreads();
+  mark_meeting(clo, chi, cflag, n);
   for (int c = tid; c < n; c += blockDim.x) {
     if (!cflag[c]) continue;
     atomicAdd(a.err + 3, 1);
@@ -752,58 +801,35 @@ __device__ __noinline__ void topk_recheck(const RouteArgs& a, int t, const float
     chi[c] = val;
   }
   __syncthreads();
-  // order the candidates: disjoint intervals order by midpoint; overlapping
-  // ones are now exact and order by value, ties by expert index
+  // order the candidates: every two intervals are now disjoint or both exact
+  // (any two that met were both recomputed exactly), so the lower ends order
+  // them as their values do; equal values (exact) order by expert index.  Rank
+  // by counting; the midpoint of a chosen interval is its gate logit.
+  for (int c = tid; c < n; c += blockDim.x) {
+    const long long kc = ord64(clo[c]);
+    const int ec = cand[c];
+    int r = 0;
+    for (int c2 = 0; c2 < n && r < k; ++c2) {
+      const long long k2 = ord64(clo[c2]);
+      r += k2 > kc || (k2 == kc && cand[c2] < ec);
+    }
+    if (r < k) {
+      order[r] = ec;
+      order_c[r] = c;
+    }
+  }
+  __syncthreads();
   if (warp == 0) {
-    for (int j = 0; j < k; ++j) {
-      double bvv = -INFINITY;
-      int be = 0x7fffffff, bc = -1;
-      for (int c = lane; c < n; c += 32) {
-        if (cflag[c] == 2) continue;
-        const double mid = 0.5 * (clo[c] + chi[c]);
-        if (bc < 0 || better(mid, cand[c], bvv, be)) {
-          bvv = mid;
-          be = cand[c];
-          bc = c;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bvv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-        if (oc >= 0 && (bc < 0 || better(ov, oe, bvv, be))) {
-          bvv = ov;
-          be = oe;
-          bc = oc;
-        }
-      }
-      if (lane == 0) {
-        order[j] = be;
-        oval[j] = bvv;
-        cflag[bc] = 2;
-      }
-      __syncwarp();
-    }
-    // gate logits: the keys, or (selection-only bias) the router's fp32 logits
-    // without the bias, as on the certified path (a key that was not
-    // recomputed is an fp32 sum rounded once more by the bias addition); the
-    // largest of them is subtracted before exp
+    // gate logits: the midpoints, or (selection-only bias) the router's fp32
+    // logits without the bias, as on the certified path (a key that was not
+    // recomputed is an fp32 sum rounded once more by the bias addition)
     double lj = -INFINITY;
-    if (lane < k) lj = a.sel_bias ? (double)a.logits[(size_t)t * E + order[lane]] : oval[lane];
-    double lm = lj;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lm = fmax(lm, __shfl_xor_sync(0xffffffffu, lm, o));
-    const float g = lane < k ? expf((float)(lj - lm)) : 0.f;
-    float den = g;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    int e = 0;
     if (lane < k) {
-      const size_t r = (size_t)t * (k + a.n_shared) + lane;
-      a.topk_idx[r] = order[lane];
-      a.gates[r] = g / den;
-      out_sel[lane] = order[lane];
+      e = order[lane];
+      lj = a.sel_bias ? (double)a.logits[(size_t)t * E + e] : 0.5 * (clo[order_c[lane]] + chi[order_c[lane]]);
     }
+    write_gates(a, t, lj, e, out_sel);
   }
 }
 
@@ -967,22 +993,11 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   if (certified) {
     if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum
       // gate logits: the keys, or (selection-only bias) the router's logits
-      // without the bias; the largest of them is subtracted before exp
+      // without the bias (lj - max is the fp32 difference: exact in fp64,
+      // rounded once)
       float lj = -INFINITY;
       if (lane < k) lj = a.sel_bias ? a.logits[(size_t)t * E + sel[lane]] : sv[sel[lane]];
-      float lm = lj;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, o));
-      const float g = lane < k ? expf(lj - lm) : 0.f;
-      float den = g;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      if (lane < k) {
-        const size_t r = (size_t)t * (k + a.n_shared) + lane;
-        a.topk_idx[r] = sel[lane];
-        a.gates[r] = g / den;
-        out_sel[lane] = sel[lane];
-      }
+      write_gates(a, t, (double)lj, lane < k ? sel[lane] : 0, out_sel);
     }
     return;
   }
@@ -990,7 +1005,12 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   topk_recheck(a, t, sv, sb, insel, m, clo, chi, cand, cflag, out_sel);
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
+// MINB CTAs per SM at least: 1 where every token's CTA is resident at once
+// anyway; 4 for calls of more tokens than SMs, which then run in one wave
+// instead of four (the fp64 recheck path, rarely taken, spills a little
+// under the 64-register cap).
+template <int MINB>
+__global__ void __launch_bounds__(kTopkThreads, MINB) topk_kernel(RouteArgs a) {
   __shared__ int sel_smem[kMaxK];
   topk_token(a, sel_smem);
   if (a.fuse_bucket) {  // one token: bucket its k pairs right here (no further launch)
@@ -1002,7 +1022,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(RouteArgs a) {
 }  // namespace
 
 cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s) {
-  (void)num_sms;
   if (a.T == 0) return cudaSuccess;
   const dim3 grid((a.E + kLogitWarps - 1) / kLogitWarps, (a.T + kTokTile - 1) / kTokTile);
   const size_t smem = (size_t)kTokTile * a.d * sizeof(float);
@@ -1047,8 +1066,12 @@ cudaError_t launch_route_topk(const RouteArgs& a, int num_sms, cudaStream_t s) {
   }
   if (err != cudaSuccess) return err;
   const size_t tsm = topk_smem_bytes(a.E);
-  ensure_smem(topk_kernel, tsm);
-  return launch("topk", topk_kernel, dim3(a.T), dim3(kTopkThreads), tsm, s, true, a);
+  if (a.T > num_sms) {
+    ensure_smem(topk_kernel<4>, tsm);
+    return launch("topk", topk_kernel<4>, dim3(a.T), dim3(kTopkThreads), tsm, s, true, a);
+  }
+  ensure_smem(topk_kernel<1>, tsm);
+  return launch("topk", topk_kernel<1>, dim3(a.T), dim3(kTopkThreads), tsm, s, true, a);
 }
 
 }  // namespace moe
