@@ -252,12 +252,15 @@ def test_route_topk_ex_forced_selection_gates_ignore_the_bias(lib, ctx, T):
     gu.check_routing(topk.cpu().numpy(), gates.cpu().numpy(), idx, g, np.full(T, 2e-5))
 
 
-def test_router_certifies_exact_ties_and_near_ties(lib, ctx):
+@pytest.mark.parametrize("T", [16, 300])
+def test_router_certifies_exact_ties_and_near_ties(lib, ctx, T):
     # duplicated router rows give exactly equal logits (ties must go to the lower
     # index); rows differing in one low bit give near-ties the fp32 bound cannot
-    # separate, forcing the fp64 and sequential-fp64 recomputation paths
+    # separate, forcing the fp64 and sequential-fp64 recomputation paths.  16
+    # tokens: compensated logits, one top-k CTA per SM; 300 tokens (more than
+    # the SMs): the tiled fp32 logits and the top-k launched 4 CTAs per SM
     moe = lib
-    d, E, k, T = 256, 64, 8, 16
+    d, E, k = 256, 64, 8
     rng = np.random.default_rng(0)
     Wf = (rng.standard_normal((E, d)) / 16).astype(np.float32)
     Wb = torch.from_numpy(Wf).to(torch.bfloat16)
