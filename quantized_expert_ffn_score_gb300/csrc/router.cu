@@ -656,8 +656,8 @@ __device__ __forceinline__ bool meets(const double* lo, const double* hi, int c,
 }
 
 // The recheck path runs in few CTAs, so its code is rarely in the instruction
-// caches: it is kept small, and the steps it repeats (or shares with the
-// certified path) are out-of-line functions fetched once.
+// caches: it is kept small, and the steps it repeats are out-of-line functions
+// fetched once.
 
 // flag[c] = whether candidate c's interval meets another candidate's (the
 // whole CTA; followed by a barrier).
@@ -991,13 +991,25 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int* out_sel) {
   if (tid == 0) certified = (!nbad && hi_out < m) ? 1 : 0;
   __syncthreads();
   if (certified) {
-    if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum
+    if (warp == 0) {  // gates from the fp32 logits, fixed-order warp sum (inline: the decode path)
       // gate logits: the keys, or (selection-only bias) the router's logits
-      // without the bias (lj - max is the fp32 difference: exact in fp64,
-      // rounded once)
+      // without the bias; the largest of them is subtracted before exp (the
+      // fp32 difference, as write_gates forms it for the recheck path)
       float lj = -INFINITY;
       if (lane < k) lj = a.sel_bias ? a.logits[(size_t)t * E + sel[lane]] : sv[sel[lane]];
-      write_gates(a, t, (double)lj, lane < k ? sel[lane] : 0, out_sel);
+      float lm = lj;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+      const float g = lane < k ? expf(lj - lm) : 0.f;
+      float den = g;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (lane < k) {
+        const size_t r = (size_t)t * (k + a.n_shared) + lane;
+        a.topk_idx[r] = sel[lane];
+        a.gates[r] = g / den;
+        out_sel[lane] = sel[lane];
+      }
     }
     return;
   }
