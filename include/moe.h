@@ -337,7 +337,8 @@ MOE_API size_t moe_expert_ffn_mxfp4_static_max_bytes(void);
  * Combine: out[t][i] = x_resid[t][i] + sum over j ascending with gates[t][j] != 0
  * of gates[t][j] * y_pairs[t*k + j][i].  x_resid [T][d] (x_dtype) may be NULL
  * (out is then the MoE delta alone).  out [T][d] in out_dtype (bf16: the fp32
- * sum rounded to nearest even).  A pair with gate 0 is never read.
+ * sum rounded to nearest even).  A pair with gate 0 never enters the sum, whatever
+ * its row of y_pairs holds (NaN included); every row of y_pairs [T*k][d] may be read.
  */
 MOE_API moe_status moe_combine(moe_ctx* ctx, const void* x_resid, moe_dtype x_dtype, const float* y_pairs,
                        const float* gates, int T, int k, int d, void* out, moe_dtype out_dtype, cudaStream_t stream);
